@@ -1,0 +1,384 @@
+"""Benchmark of the GB300 Leyline AMORTIZE splice.
+
+Workload (default): the DeepSeek-V2-Lite-shaped paged MLA cache -- 27 layers,
+32768 tokens, block size 16, latent 512 + rope 64 bf16 -- and one directive that
+replaces [20000, 26000) by 12 rows (Delta = -5988): 6768 downstream slots, each
+moved and rotated in all 27 layers.  A step is one leyline_splice call (plan,
+move+rotate, commit kernels) on one request.  Each timed step splices a
+different, pre-filled request, so every step reads 0.42 GB that no earlier step
+touched (inputs larger than L2; no reset inside the timed region).
+
+Metric: downstream slots spliced per second (each slot covers all layers), plus
+HBM GB/s of the move+rotate kernel against the measured copy bandwidth.
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference] [--workload cfg2]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+# Per-launch DRAM traffic (read + write bytes) of the move+rotate kernel on this
+# workload, from an ncu capture, valid only for the kernel source it was taken on.
+NCU_TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    p = os.path.join(ROOT, "rope_rotation_gb300", "csrc", "leyline_kernels.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(tempfile.gettempdir(), f"leyline_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workload --
+
+def workload(name: str):
+    from synth import configs
+    w = configs.by_name(name)
+    if len(w.steps) != 1:
+        raise SystemExit(f"workload {name} is a multi-step chain; bench runs single-call workloads")
+    return w
+
+
+def per_request_counts(w):
+    """Downstream and replacement slots of one call of the workload (oracle-free: planner dry run)."""
+    from rope_rotation_gb300 import leyline
+    desc = leyline.pool_desc(w.num_layers, w.block_size, 1, w.latent_dim, w.rope_dim, w.theta)
+    dirs = [leyline.directive(d.req, d.s_start, d.s_end, None, n_repl=0) for d in w.steps[0]]
+    nb = max(-(-(L + 64 * 3) // w.block_size) for L in w.lengths)
+    st, _ = leyline.leyline_splice_plan(desc, np.array(w.lengths, dtype=np.int64), nb, dirs)
+    return st
+
+
+# ---------------------------------------------------------------- our arm ---
+
+def run_ours(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    from rope_rotation_gb300 import leyline
+    from rope_rotation_gb300.runtime import PagedCache
+    from synth import fill
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = workload(args.workload)
+    K, W = args.steps, args.warmup
+    C = w.num_reqs
+    legs = 1 if args.no_e2e else 2
+    groups = (W + K) * legs  # every step and warm-up splices its own copy of the workload's requests
+    B = w.block_size
+    max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
+    pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
+    cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta)
+    seed = w.seed + 1000 * rank
+    for g in range(groups):
+        for r, L in enumerate(w.lengths):
+            cache.add_request(g * C + r, L)
+            fill.fill_request(cache, seed, g * C + r, L)
+    # replacement rows: device copies (value leg) and pinned host copies (e2e leg)
+    repl_dev, repl_host = {}, {}
+    for d in w.steps[0]:
+        if d.n_repl:
+            t = fill.repl_tensor(seed, d.req, d.key, w.num_layers, d.n_repl, cache.row, dev)
+            repl_dev[d.key] = t
+            repl_host[d.key] = t.cpu().pin_memory()
+
+    def dirs_for(g, repl_map):
+        return [leyline.directive(g * C + d.req, d.s_start, d.s_end, repl_map.get(d.key), n_repl=d.n_repl)
+                for d in w.steps[0]]
+
+    stream = torch.cuda.current_stream()
+    # warm-up
+    for g in range(W):
+        cache.splice(dirs_for(g, repl_dev))
+    torch.cuda.synchronize()
+    cache.check_status()
+    st = cache.last_stats()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    leyline.leyline_kernel_timing_enable(cache.pool, True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for k in range(K):
+        cache.splice(dirs_for(W + k, repl_dev))
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
+    leyline.leyline_kernel_timing_enable(cache.pool, False)
+    cache.check_status()
+
+    e2e = None
+    if not args.no_e2e:
+        # End to end through the public API: each step copies its replacement rows from
+        # pinned host memory, splices, and reads back the request's new lengths and table row.
+        base = W + K
+        rbuf = {k: torch.empty_like(v) for k, v in repl_dev.items()}
+        out_tab = torch.empty((K, C, max_blocks), dtype=torch.int32).pin_memory()
+        out_len = torch.empty((K, C), dtype=torch.int32).pin_memory()
+        for g in range(W):  # warm the copy path
+            for k2, v in repl_host.items():
+                rbuf[k2].copy_(v, non_blocking=True)
+            cache.splice(dirs_for(base + g, rbuf))
+        torch.cuda.synchronize()
+        h2d = sum(v.numel() * v.element_size() for v in repl_host.values())
+        d2h = C * max_blocks * 4 + C * 4
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(K):
+            g = base + W + k
+            for k2, v in repl_host.items():
+                rbuf[k2].copy_(v, non_blocking=True)
+            cache.splice(dirs_for(g, rbuf))
+            out_tab[k].copy_(cache.table[g * C:(g + 1) * C], non_blocking=True)
+            out_len[k].copy_(cache.seq_lens_dev[g * C:(g + 1) * C], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        cache.check_status()
+        exp_len = cache.seq_lens_host[(base + W) * C:(base + W + K) * C].reshape(K, C)
+        assert np.array_equal(out_len.numpy(), exp_len), "e2e read-back lengths differ"
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+    clocks = sampler.stop()
+
+    # max over ranks
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms, e2e["ms"] if e2e else 0.0], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, e2e_ms_max = float(t[0]), float(t[1])
+        if e2e:
+            e2e["ms"] = e2e_ms_max
+    slots = st["downstream_slots"] * K * world
+    value = slots / (elapsed_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    k2_avg_s = (k2_ms / max(k2_n, 1)) / 1e3
+    achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
+    traffic = None
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "slots/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": elapsed_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.num_layers, "tokens": w.lengths if C > 1 else w.lengths[0],
+                   "block_size": B, "latent_dim": w.latent_dim, "rope_dim": w.rope_dim, "storage": "bf16",
+                   "directives": [[d.s_start, d.s_end, d.n_repl] for d in w.steps[0]],
+                   "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
+                   "algorithmic_bytes_per_step": st["algorithmic_bytes"],
+                   "l2": "inputs larger than L2: each step splices its own pre-filled request",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
+        "clocks": clocks,
+        "gpu_launches": K * st["kernels_launched"],
+        "roofline": {"kernel": "move_rotate_mla", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "launch_ms": k2_avg_s * 1e3, "launches_timed": k2_n,
+                     "algorithmic_bytes_per_launch": st["algorithmic_bytes"]},
+    }
+    if e2e:
+        line["e2e"] = {"value": slots / (e2e["ms"] / 1e3), "unit": "slots/s", "h2d_bytes_per_step": e2e["h2d"],
+                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"] / K}
+    cache.close()
+    return line, w
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle (single thread, as it stands) on whole calls of the workload,
+    repeated until about budget_s seconds of CPU work."""
+    import oracle
+    import synth
+    st = per_request_counts(w)
+    caches = [synth.cache_request(seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)]
+    reps = {d.key: synth.repl_rows(seed, d.req, d.key, w.num_layers, d.n_repl, w.row_elems) for d in w.steps[0]}
+    calls, t_total = 0, 0.0
+    while t_total < budget_s or calls == 0:
+        t0 = time.perf_counter()
+        for r in range(w.num_reqs):
+            ds = [d for d in w.steps[0] if d.req == r]
+            if ds:
+                oracle.splice_request(caches[r], [(d.s_start, d.s_end, d.n_repl) for d in ds],
+                                      [reps[d.key] for d in ds], w.latent_dim, w.theta)
+        t_total += time.perf_counter() - t0
+        calls += 1
+    value = st.downstream_slots * calls / t_total
+    return {"value": value, "unit": "slots/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} whole call(s) of {w.name} ({w.num_layers} layers) through the fp64 C oracle, "
+                      f"single thread, {t_total:.1f} s"}, t_total / calls
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 CPU oracle timed as it stands on the same workload."""
+    if rank != 0:
+        return None
+    w = workload(args.workload)
+    import oracle
+    import synth
+    st = per_request_counts(w)
+    seed = w.seed
+    caches = [synth.cache_request(seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)]
+    reps = {d.key: synth.repl_rows(seed, d.req, d.key, w.num_layers, d.n_repl, w.row_elems) for d in w.steps[0]}
+
+    def one_call():
+        for r in range(w.num_reqs):
+            ds = [d for d in w.steps[0] if d.req == r]
+            if ds:
+                oracle.splice_request(caches[r], [(d.s_start, d.s_end, d.n_repl) for d in ds],
+                                      [reps[d.key] for d in ds], w.latent_dim, w.theta)
+    for _ in range(args.warmup):
+        one_call()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_call()
+    dt = time.perf_counter() - t0
+    value = st.downstream_slots * args.steps / dt
+    return {"metric": METRIC, "value": value, "unit": "slots/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.num_layers, "block_size": w.block_size, "storage": "bf16"},
+            "cpu_baseline": {"value": value, "unit": "slots/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} timed whole call(s) of {w.name} through the fp64 C oracle, "
+                                       "single thread"},
+            "e2e": {"value": value, "unit": "slots/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line, w = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            cb, _ = cpu_oracle_sample(w, args.cpu_seconds)
+            line["cpu_baseline"] = cb
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

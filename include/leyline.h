@@ -1,0 +1,230 @@
+/*
+ * leyline.h -- C ABI of the GB300 Leyline AMORTIZE splice library (libleyline.so).
+ *
+ * The operation: "Leyline: KV Cache Directives for Agentic Inference"
+ * (technical summary of arXiv 2606.01065).
+ *   section 2.1  A directive D = (s_start, s_end, R, m) replaces the token span
+ *                [s_start, s_end) of a sequence by the token sequence R.  Mode
+ *                AMORTIZE splices in place: R is inserted, downstream positions
+ *                are re-indexed, and the downstream tokens keep their position-
+ *                free KV content (K_nope and V).  Mode FORGET routes the edit to
+ *                a prefix-trimming re-prefill instead.
+ *   section 2.2  With |S| = s_end - s_start, every downstream token moves by
+ *                Delta = |R| - |S|, and its cached RoPE band is corrected in
+ *                closed form: K_pe_new = R(Delta) K_pe.  Because R(a)R(b) =
+ *                R(a+b), this equals encoding the token from scratch at its new
+ *                position.  In MLA the key splits into K_nope (position-free, from
+ *                the compressed latent) and K_pe (RoPE-rotated).
+ *   section 2.3  Serving integration: match the prefix [0, s_start), prefill R
+ *                into new slots, then a rotation kernel delta-rotates and
+ *                re-indexes every downstream slot.  This library is that last
+ *                step plus the slot writes; matching and prefill stay with the
+ *                caller.
+ *   section 3    The directive interface sits above block-level (paged) storage.
+ *   section 4.3  bf16 storage makes delta-rotation drift; computing the rotation
+ *                in fp32 mitigates it.  The library rotates in fp32 and stores bf16.
+ *
+ * Storage model.  A pool holds num_pages pages per layer.  One page stores
+ * block_size consecutive token slots of one request.  A slot row is
+ * latent_dim + rope_dim bf16 values: the compressed latent first (moved bit for
+ * bit, never recomputed), the RoPE band k_pe last.  The pool memory is laid out
+ *     kv[layer][page][slot][latent_dim + rope_dim]      (bf16, row-major)
+ * and one block table, shared by all layers, maps block b of request r to a page:
+ *     table[r * max_blocks + b] = page id, for b < ceil(seq_len[r] / block_size).
+ *
+ * How a splice is carried out.  Every block from floor(s_min / block_size) on
+ * (s_min = the smallest s_start of the request's directives) is rewritten into
+ * fresh pages taken from the pool's free-page stack; the request's old pages from
+ * that block on go back onto the stack when the rewrite is committed.  Source
+ * rows are never written, so the call has no read/write hazard whatever the sign
+ * of Delta, and a call that fails validation changes nothing.  The prefix rows
+ * of the first rewritten block are copied unchanged.
+ *
+ * Conventions.  All functions return LEYLINE_OK (0) or a negative
+ * LEYLINE_ERR_* code, and never throw or abort.  leyline_last_error() gives a
+ * message for the calling thread.  Device pointers are CUDA global-memory
+ * pointers on the device that was current at leyline_pool_create; every bf16
+ * buffer must be 16-byte aligned.  "stream" is a cudaStream_t (NULL = legacy
+ * default stream).  Work is enqueued asynchronously; host-side state (the
+ * seq_lens_host mirror and the free-page count) is updated at enqueue time.
+ * Calls on one pool must not run concurrently from several host threads.
+ */
+#ifndef LEYLINE_H
+#define LEYLINE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ errors ---- */
+#define LEYLINE_OK 0
+#define LEYLINE_ERR_INVALID_ARG (-1)       /* null / misaligned pointer, bad size or descriptor */
+#define LEYLINE_ERR_INVALID_DIRECTIVE (-2) /* s_start > s_end, s_end > seq_len, bad req, n_repl < 0 */
+#define LEYLINE_ERR_OVERLAP (-3)           /* two spans of one request overlap or share s_start */
+#define LEYLINE_ERR_NO_PAGES (-4)          /* not enough free pages for the rewritten blocks */
+#define LEYLINE_ERR_UNSUPPORTED_MODE (-5)  /* FORGET (caller re-prefills) or unknown mode */
+#define LEYLINE_ERR_CUDA (-6)              /* a CUDA runtime call failed */
+#define LEYLINE_ERR_CAPACITY (-7)          /* new length exceeds max_blocks * block_size */
+#define LEYLINE_ERR_DEVICE_CHECK (-8)      /* a device-side bounds check fired (leyline_sync_status) */
+
+/* --------------------------------------------------------------- types ---- */
+typedef struct leyline_pool leyline_pool_t; /* opaque, owned by the library */
+
+/* RoPE pair layout of the rope band (the pages fix none; half-split is the
+ * rotate_half convention, pair j = (j, j + rope_dim/2)). */
+typedef enum { LEYLINE_PAIRS_HALF_SPLIT = 0, LEYLINE_PAIRS_INTERLEAVED = 1 } leyline_pair_layout_t;
+
+/* Arithmetic of the delta-rotation.  FP32 is the product path (section 4.3).
+ * BF16_NAIVE rounds cos, sin, each product and each sum to bf16; it exists only
+ * as the comparison arm of drift studies. */
+typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_rotate_precision_t;
+
+typedef struct {
+    int32_t num_layers;       /* >= 1 */
+    int32_t latent_dim;       /* multiple of 8 (512 for DeepSeek-V2/V3 MLA) */
+    int32_t rope_dim;         /* multiple of 16 (64 for DeepSeek-V2/V3 MLA) */
+    int32_t block_size;       /* tokens per page, >= 1 (16: vLLM-style blocks; 1: per-token) */
+    int64_t num_pages;        /* pages per layer, 1 .. 2^31 - 1 */
+    double rope_theta;        /* RoPE base, > 0 (10000) */
+    int32_t pair_layout;      /* leyline_pair_layout_t */
+    int32_t rotate_precision; /* leyline_rotate_precision_t */
+} leyline_pool_desc_t;
+
+/* Block tables of num_reqs requests.  Caller-owned; the library borrows them for
+ * the duration of enqueued work.  table and seq_lens_dev are device int32 arrays
+ * ([num_reqs][max_blocks] and [num_reqs]); seq_lens_host is the host mirror of
+ * the lengths, read to validate directives and updated by leyline_splice when
+ * the work is enqueued.  Unused table entries should hold -1. */
+typedef struct {
+    int32_t* table;
+    int32_t* seq_lens_dev;
+    int64_t* seq_lens_host;
+    int32_t num_reqs;
+    int32_t max_blocks;
+} leyline_block_table_t;
+
+typedef enum { LEYLINE_AMORTIZE = 0, LEYLINE_FORGET = 1 } leyline_mode_t;
+
+/* One directive D = (s_start, s_end, R, m) for request `req` (section 2.1).
+ * [s_start, s_end) is half-open, in the request's coordinates before the call;
+ * several directives of one request must not overlap and must have distinct
+ * s_start.  repl_rows: device bf16 [num_layers][n_repl][latent_dim + rope_dim],
+ * the rows of R already encoded at their final positions s_start + D_before + i
+ * (D_before = the summed Delta of the request's directives left of this one),
+ * as prefill writes them (section 2.3); they are copied bit for bit and must stay
+ * live until the enqueued work has finished.  May be NULL when n_repl == 0. */
+typedef struct {
+    int32_t req;
+    int32_t mode; /* leyline_mode_t */
+    int64_t s_start;
+    int64_t s_end;
+    int32_t n_repl;
+    int32_t reserved; /* must be 0 */
+    const void* repl_rows;
+} leyline_directive_t;
+
+/* Work accounting of one splice call. */
+typedef struct {
+    int64_t downstream_slots;  /* surviving tokens at or after each request's first s_end, summed */
+    int64_t repl_slots;        /* rows of R written */
+    int64_t head_slots;        /* unchanged prefix rows copied into the first rewritten block */
+    int64_t algorithmic_bytes; /* 2 * row_bytes * num_layers * (downstream_slots + repl_slots) */
+    int64_t moved_bytes;       /* 2 * row_bytes * num_layers * (downstream + repl + head slots) */
+    int64_t pages_popped;      /* fresh pages taken for the rewritten blocks */
+    int64_t pages_pushed;      /* old pages returned to the free stack */
+    int32_t requests_touched;
+    int32_t kernels_launched;  /* kernels this call enqueued */
+} leyline_stats_t;
+
+/* -------------------------------------------------------------- pool ---- */
+
+/* Create a pool over caller-owned device memory kv_dev (bf16
+ * [num_layers][num_pages][block_size][latent_dim + rope_dim], 16-byte aligned).
+ * All pages start free.  The library allocates the free-page stack and a small
+ * plan buffer on the current device.  Synchronous.
+ * Errors: INVALID_ARG (bad descriptor, null/misaligned kv_dev), CUDA. */
+int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_pool_t** out);
+
+/* Wait for the pool's enqueued work and free what the library allocated (never kv_dev). */
+int leyline_pool_destroy(leyline_pool_t* pool);
+
+/* Take n pages off the free stack, for the caller's initial fill or prefill.
+ * Synchronous (waits for the pool's enqueued work).  page_ids_host receives n ids
+ * (the k-th id taken first).  Errors: INVALID_ARG, NO_PAGES, CUDA. */
+int leyline_alloc_pages(leyline_pool_t* pool, int32_t n, int32_t* page_ids_host);
+
+/* Return n pages (ids from page_ids_host) to the free stack.  Synchronous.
+ * Errors: INVALID_ARG (id out of range, more pages than the pool holds), CUDA. */
+int leyline_free_pages(leyline_pool_t* pool, int32_t n, const int32_t* page_ids_host);
+
+/* Number of free pages as seen at enqueue time (negative code on a NULL pool). */
+int64_t leyline_free_page_count(const leyline_pool_t* pool);
+
+/* -------------------------------------------------------------- splice ---- */
+
+/* Apply n AMORTIZE directives (any mix of requests) as one composed pass per
+ * request (section 2.2 / 2.3): for each request with at least one effective
+ * directive, drop its spans, write the rows of R, move every downstream slot to
+ * its new position (latent bit for bit) and rotate its rope band by the
+ * accumulated Delta in fp32, storing bf16.  Directives with s_start == s_end and
+ * n_repl == 0 are no-ops.  On return the work is enqueued on `stream`, the
+ * seq_lens_host entries hold the new lengths and the pages are accounted; the
+ * table and seq_lens_dev change when the enqueued work runs.  Enqueues at most
+ * three kernels and one host-to-device copy of the plan (a few KB).
+ * Errors (nothing is enqueued or changed): INVALID_ARG, INVALID_DIRECTIVE,
+ * OVERLAP, UNSUPPORTED_MODE (FORGET: the caller re-prefills, section 2.1),
+ * CAPACITY, NO_PAGES.  CUDA: a launch failed after validation; the pool must
+ * then be considered inconsistent. */
+int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
+                   int32_t n, void* stream);
+
+/* Host-only dry run of leyline_splice: validates the directives against
+ * seq_lens_host (length num_reqs) and the pool geometry in desc, and reports the
+ * work and the page demand in *stats without touching any device.  If
+ * new_seq_lens is not NULL it receives the length of every request after the
+ * splice.  free_pages: pages available (pass a negative value to skip the page
+ * check).  Returns the same error codes as leyline_splice. */
+int leyline_splice_plan(const leyline_pool_desc_t* desc, const int64_t* seq_lens_host, int32_t num_reqs,
+                        int32_t max_blocks, const leyline_directive_t* dirs, int32_t n, int64_t free_pages,
+                        leyline_stats_t* stats, int64_t* new_seq_lens);
+
+/* Statistics of the last successful leyline_splice on this pool. */
+int leyline_last_stats(const leyline_pool_t* pool, leyline_stats_t* out);
+
+/* -------------------------------------------------------------- gather ---- */
+
+/* Copy the logical rows [t0, t1) of request `req`, layer `layer` into out_dev
+ * (device bf16 [t1 - t0][latent_dim + rope_dim], 16-byte aligned), reading
+ * through the block table.  Asynchronous on `stream`.
+ * Errors: INVALID_ARG (range outside [0, seq_lens_host[req]], bad layer/req). */
+int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, int32_t layer,
+                   int64_t t0, int64_t t1, void* out_dev, void* stream);
+
+/* ----------------------------------------------------------- checking ---- */
+
+/* Wait for the pool's enqueued work and read its device status word.  Returns
+ * LEYLINE_OK, LEYLINE_ERR_DEVICE_CHECK if a kernel met a page id or position
+ * outside the pool or table (it then skipped that row; the status is cleared by
+ * this call), or LEYLINE_ERR_CUDA. */
+int leyline_sync_status(leyline_pool_t* pool);
+
+/* Kernel timing for benchmarks.  While enabled, each splice records CUDA events
+ * on its stream around its move+rotate kernel.  leyline_kernel_timing_read waits
+ * for them and returns the summed kernel time (ms) and the number of timed
+ * launches since the last enable, then keeps timing. */
+int leyline_kernel_timing_enable(leyline_pool_t* pool, int32_t enable);
+int leyline_kernel_timing_read(leyline_pool_t* pool, double* total_ms, int32_t* launches);
+
+/* Message of the last error on the calling thread ("" if none). */
+const char* leyline_last_error(void);
+
+/* Library version, e.g. "leyline-gb300 0.1.0 sm_103a". */
+const char* leyline_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LEYLINE_H */

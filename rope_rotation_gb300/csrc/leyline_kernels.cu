@@ -1,0 +1,535 @@
+// leyline_kernels.cu -- device side of the GB300 Leyline AMORTIZE splice (sm_103a).
+//
+// "Leyline: KV Cache Directives for Agentic Inference":
+//   section 2.2  every downstream slot's RoPE band gets K_pe_new = R(Delta) K_pe
+//                (one 2x2 rotation per pair); K_nope and V (here: the compressed
+//                latent they derive from) are kept.
+//   section 2.3  the rotation kernel re-indexes and rotates every downstream slot.
+//   section 4.3  the rotation is computed in fp32 and stored in bf16.
+//
+// Kernels of one splice, in stream order:
+//   plan kernel      cos/sin of Delta * theta_j per rotated segment (fp64 angle,
+//                    rounded to fp32) and the fresh page ids popped off the stack;
+//   move+rotate      every rewritten row x layer is read once and written once:
+//                    latent and R rows copied as 16-byte vectors, rope band turned
+//                    in fp32 and rounded to bf16 (the HBM-bound hot loop);
+//   commit           new block-table entries, new lengths, old pages pushed back.
+// The path is bandwidth-bound (about 64 fp32 FMAs per 2304 bytes moved), so it
+// uses no tensor cores: the point is coalesced 16-byte streaming at HBM speed.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "leyline_internal.h"
+
+namespace leyline {
+namespace {
+
+constexpr int kMoveThreads = 256;  // 8 warps x 2 rows = one 16-row tile
+constexpr int kRowsPerWarp = 2;
+static_assert(kTileRows == (kMoveThreads / 32) * kRowsPerWarp, "tile shape");
+
+// device status bits (leyline_sync_status)
+enum : int32_t { ST_BAD_PAGE = 1, ST_BAD_BLOCK = 2, ST_BAD_FRESH = 4, ST_BAD_OLD = 8, ST_BAD_RANGE = 16 };
+
+__device__ __forceinline__ void raise_status(int32_t* status, int32_t bit) { atomicOr(status, bit); }
+
+// 16-byte streaming load through the non-coherent path, not kept in L1: every
+// source row is read exactly once and is never written during the kernel.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// 16-byte store with the evict-first (streaming) policy.
+__device__ __forceinline__ void st_stream(uint4* p, const uint4& v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// One pair turned by (c, s):  x' = x c - y s,  y' = x s + y c.
+__device__ __forceinline__ void turn_fp32(float x, float y, float c, float s, float& xo, float& yo)
+{
+    xo = fmaf(x, c, -(y * s));
+    yo = fmaf(x, s, y * c);
+}
+
+// The naive all-bf16 arm: products and sums each rounded to bf16 (c, s are bf16 values).
+__device__ __forceinline__ void turn_bf16(float x, float y, float c, float s, float& xo, float& yo)
+{
+    const float xc = round_bf16(x * c), ys = round_bf16(y * s);
+    const float xs = round_bf16(x * s), yc = round_bf16(y * c);
+    xo = xc - ys;
+    yo = xs + yc;
+}
+
+// Half-split layout: xv holds x of pairs j0..j0+7, yv holds y of the same pairs.
+template <bool kBf16>
+__device__ __forceinline__ void rotate_half_split(uint4& xv, uint4& yv, const float* c, const float* s)
+{
+    uint32_t* xw = reinterpret_cast<uint32_t*>(&xv);
+    uint32_t* yw = reinterpret_cast<uint32_t*>(&yv);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float x0 = bf16_lo(xw[w]), x1 = bf16_hi(xw[w]);
+        float y0 = bf16_lo(yw[w]), y1 = bf16_hi(yw[w]);
+        float a0, b0, a1, b1;
+        if (kBf16) {
+            turn_bf16(x0, y0, c[2 * w], s[2 * w], a0, b0);
+            turn_bf16(x1, y1, c[2 * w + 1], s[2 * w + 1], a1, b1);
+        } else {
+            turn_fp32(x0, y0, c[2 * w], s[2 * w], a0, b0);
+            turn_fp32(x1, y1, c[2 * w + 1], s[2 * w + 1], a1, b1);
+        }
+        xw[w] = pack_bf16x2(a0, a1);
+        yw[w] = pack_bf16x2(b0, b1);
+    }
+}
+
+// Interleaved layout: word w of v holds pair (x, y) of pair j0 + w.
+template <bool kBf16>
+__device__ __forceinline__ void rotate_interleaved(uint4& v, const float* c, const float* s)
+{
+    uint32_t* vw = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float x = bf16_lo(vw[w]), y = bf16_hi(vw[w]);
+        float a, b;
+        if (kBf16) turn_bf16(x, y, c[w], s[w], a, b);
+        else turn_fp32(x, y, c[w], s[w], a, b);
+        vw[w] = pack_bf16x2(a, b);
+    }
+}
+
+// Where one destination row of a tile comes from and goes to (layer 0).
+struct RowDesc {
+    const uint4* src;       // nullptr: row is not written
+    uint4* dst;
+    long long src_lstride;  // 16-byte vectors between consecutive layers of the source
+    int trig;               // trig entry, -1: no rotation
+    int pad;
+};
+
+__device__ __forceinline__ int find_req_by_tile(const SpliceArgs& a, long long tile)
+{
+    int lo = 0, hi = a.n_reqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.reqs[mid].tile_begin <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Slot map of destination row i of a tile: segment lookup, then the source row
+// through the old block table (or the rows of R), the destination row in its
+// fresh page.  Every page id and block index is checked; a bad one is recorded
+// in the status word and the row is skipped.
+__device__ RowDesc make_desc(const SpliceArgs& a, long long tile, int i)
+{
+    RowDesc d{nullptr, nullptr, 0, -1, 0};
+    const ReqPlan& rp = a.reqs[find_req_by_tile(a, tile)];
+    const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + i;
+    if (p >= rp.new_len) return d;
+    const Seg* sg = a.segs + rp.seg_begin;
+    int k = 0;
+    for (int q = 1; q < rp.seg_count; ++q)
+        if (sg[q].new_start <= p) k = q;
+    const Seg s = sg[k];
+    const long long off = p - s.new_start;
+    const long long B = a.g.block_size;
+    const long long rv = a.g.row_vecs;
+    uint4* kv = static_cast<uint4*>(a.kv);
+    const uint4* src;
+    long long lstride;
+    int trig = -1;
+    if (s.kind == SEG_REPL) {
+        src = static_cast<const uint4*>(s.repl) + (s.src_start + off) * rv;
+        lstride = (long long)s.n_repl * rv;
+    } else {
+        const long long t = s.src_start + off;
+        const long long blk = t / B;
+        if (t < 0 || blk >= a.max_blocks) {
+            raise_status(a.status, ST_BAD_BLOCK);
+            return d;
+        }
+        const int page = a.table[(long long)rp.req * a.max_blocks + blk];
+        if (page < 0 || page >= a.g.num_pages) {
+            raise_status(a.status, ST_BAD_PAGE);
+            return d;
+        }
+        src = kv + ((long long)page * B + (t - blk * B)) * rv;
+        lstride = a.g.layer_vecs;
+        if (s.kind == SEG_ROT) trig = s.trig;
+    }
+    const long long dblk = p / B;
+    const int fresh = a.staged[rp.pop_off + (dblk - rp.b0)];
+    if (fresh < 0 || fresh >= a.g.num_pages) {
+        raise_status(a.status, ST_BAD_FRESH);
+        return d;
+    }
+    d.src = src;
+    d.dst = kv + ((long long)fresh * B + (p - dblk * B)) * rv;
+    d.src_lstride = lstride;
+    d.trig = trig;
+    return d;
+}
+
+// Contiguous share [u0, u1) of `units` for this CTA (sizes differ by at most one).
+__device__ __forceinline__ void my_units(long long units, long long& u0, long long& u1)
+{
+    const long long per = units / gridDim.x, rem = units % gridDim.x;
+    const long long b = blockIdx.x;
+    u0 = b * per + (b < rem ? b : rem);
+    u1 = u0 + per + (b < rem ? 1 : 0);
+}
+
+// -------------------------------------------------------------------------
+// Move+rotate, MLA shape (latent 512 = 64 vectors, rope 64 = 8 vectors).
+// Work unit = (16-row tile, layer); a CTA takes a contiguous run of units, so it
+// walks the layers of one tile and computes the tile's slot map once.  Warp w
+// owns rows 2w and 2w+1: each lane moves 4 latent vectors (a warp instruction
+// covers 512 contiguous bytes), and 8 (half-split) or 16 (interleaved) lanes
+// move the rope band with the pair's cos/sin held in registers.
+template <int kLatentVecs, int kRopeVecs, int kLayout, bool kBf16>
+__global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const SpliceArgs a, long long units)
+{
+    static_assert(kLatentVecs == 64 && kRopeVecs == 8, "MLA shape");
+    __shared__ RowDesc desc[kTileRows];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = a.g.num_layers;
+    const long long layer_vecs = a.g.layer_vecs;
+    const int half = 4 * kRopeVecs;  // pairs per row
+    // rope role of this lane
+    constexpr int kRopeLanesPerRow = kLayout == 0 ? kRopeVecs / 2 : kRopeVecs;  // 4 or 8
+    const bool rope_lane = lane < kRowsPerWarp * kRopeLanesPerRow;
+    const int rope_row = warp * kRowsPerWarp + lane / kRopeLanesPerRow;
+    const int rope_q = lane % kRopeLanesPerRow;
+    float cs[8], sn[8];
+    int trig = -1;
+
+    long long u0, u1;
+    my_units(units, u0, u1);
+    long long cur_tile = -1;
+    for (long long u = u0; u < u1; ++u) {
+        const long long tile = u / L;
+        const long long layer = u - tile * L;
+        if (tile != cur_tile) {
+            __syncthreads();
+            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, tile, threadIdx.x);
+            __syncthreads();
+            cur_tile = tile;
+            trig = rope_lane ? desc[rope_row].trig : -1;
+            if (trig >= 0) {
+                // pairs covered by this lane: 8 (half-split) or 4 (interleaved)
+                const int j0 = kLayout == 0 ? 8 * rope_q : 4 * rope_q;
+                const float4* tp = reinterpret_cast<const float4*>(a.trig + 2 * ((long long)trig * half + j0));
+#pragma unroll
+                for (int w = 0; w < (kLayout == 0 ? 4 : 2); ++w) {
+                    const float4 v = tp[w];
+                    cs[2 * w] = v.x;
+                    sn[2 * w] = v.y;
+                    cs[2 * w + 1] = v.z;
+                    sn[2 * w + 1] = v.w;
+                }
+            }
+        }
+        const RowDesc d0 = desc[warp * kRowsPerWarp];
+        const RowDesc d1 = desc[warp * kRowsPerWarp + 1];
+        uint4 v[4];
+        const uint4* s0 = d0.src + layer * d0.src_lstride;
+        const uint4* s1 = d1.src + layer * d1.src_lstride;
+        if (d0.src) {
+            v[0] = ld_stream(s0 + lane);
+            v[1] = ld_stream(s0 + lane + 32);
+        }
+        if (d1.src) {
+            v[2] = ld_stream(s1 + lane);
+            v[3] = ld_stream(s1 + lane + 32);
+        }
+        const RowDesc dr = rope_lane ? desc[rope_row] : d0;
+        const bool do_rope = rope_lane && dr.src != nullptr;
+        uint4 rx, ry;
+        const uint4* rs = dr.src + layer * dr.src_lstride + kLatentVecs;
+        if (do_rope) {
+            rx = ld_stream(rs + rope_q);
+            if (kLayout == 0) ry = ld_stream(rs + rope_q + kRopeVecs / 2);
+        }
+        if (d0.src) {
+            uint4* t0 = d0.dst + layer * layer_vecs;
+            st_stream(t0 + lane, v[0]);
+            st_stream(t0 + lane + 32, v[1]);
+        }
+        if (d1.src) {
+            uint4* t1 = d1.dst + layer * layer_vecs;
+            st_stream(t1 + lane, v[2]);
+            st_stream(t1 + lane + 32, v[3]);
+        }
+        if (do_rope) {
+            uint4* rd = dr.dst + layer * layer_vecs + kLatentVecs;
+            if (kLayout == 0) {
+                if (trig >= 0) rotate_half_split<kBf16>(rx, ry, cs, sn);
+                st_stream(rd + rope_q, rx);
+                st_stream(rd + rope_q + kRopeVecs / 2, ry);
+            } else {
+                if (trig >= 0) rotate_interleaved<kBf16>(rx, cs, sn);
+                st_stream(rd + rope_q, rx);
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------------------
+// Move+rotate for any latent_dim (multiple of 8) and rope_dim (multiple of 16):
+// the same slot map, with plain strided loops over the vectors of the tile.
+template <bool kBf16>
+__global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const SpliceArgs a, long long units)
+{
+    __shared__ RowDesc desc[kTileRows];
+    const int L = a.g.num_layers;
+    const int lv = a.g.latent_vecs, rvv = a.g.rope_vecs, half = a.g.rope_dim / 2;
+    const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
+    const int rope_items = split ? rvv / 2 : rvv;
+    long long u0, u1;
+    my_units(units, u0, u1);
+    long long cur_tile = -1;
+    for (long long u = u0; u < u1; ++u) {
+        const long long tile = u / L;
+        const long long layer = u - tile * L;
+        if (tile != cur_tile) {
+            __syncthreads();
+            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, tile, threadIdx.x);
+            __syncthreads();
+            cur_tile = tile;
+        }
+        for (int it = threadIdx.x; it < kTileRows * lv; it += blockDim.x) {
+            const RowDesc d = desc[it / lv];
+            if (!d.src) continue;
+            const int c = it % lv;
+            st_stream(d.dst + layer * a.g.layer_vecs + c, ld_stream(d.src + layer * d.src_lstride + c));
+        }
+        for (int it = threadIdx.x; it < kTileRows * rope_items; it += blockDim.x) {
+            const RowDesc d = desc[it / rope_items];
+            if (!d.src) continue;
+            const int q = it % rope_items;
+            const uint4* rs = d.src + layer * d.src_lstride + lv;
+            uint4* rd = d.dst + layer * a.g.layer_vecs + lv;
+            float cs[8], sn[8];
+            const int j0 = split ? 8 * q : 4 * q;
+            const int np = split ? 8 : 4;
+            if (d.trig >= 0) {
+                for (int w = 0; w < np; ++w) {
+                    cs[w] = a.trig[2 * ((long long)d.trig * half + j0 + w)];
+                    sn[w] = a.trig[2 * ((long long)d.trig * half + j0 + w) + 1];
+                }
+            }
+            if (split) {
+                uint4 x = ld_stream(rs + q), y = ld_stream(rs + q + rvv / 2);
+                if (d.trig >= 0) rotate_half_split<kBf16>(x, y, cs, sn);
+                st_stream(rd + q, x);
+                st_stream(rd + q + rvv / 2, y);
+            } else {
+                uint4 x = ld_stream(rs + q);
+                if (d.trig >= 0) rotate_interleaved<kBf16>(x, cs, sn);
+                st_stream(rd + q, x);
+            }
+        }
+    }
+}
+
+// -------------------------------------------------------------------------
+// Plan kernel: cos/sin of Delta * theta_j for every rotated segment, and the
+// fresh page ids (the i-th page taken is stack[pop_top - 1 - i]).
+// The angle is formed and reduced in fp64: Delta * theta_0 reaches 1e5 rad, where
+// an fp32 angle would be off by ~1e-2 rad, more than a bf16 step.
+__global__ void plan_kernel(const SpliceArgs a)
+{
+    const int half = a.g.rope_dim / 2;
+    const long long n_trig = (long long)a.n_trig * half;
+    const long long n = n_trig > a.total_pop ? n_trig : a.total_pop;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        if (i < n_trig) {
+            const long long t = i / half;
+            const int j = (int)(i - t * half);
+            const double theta_j = pow(a.g.theta, -2.0 * (double)j / (double)a.g.rope_dim);
+            const double phi = (double)a.trig_delta[t] * theta_j;
+            double s, c;
+            sincos(phi, &s, &c);
+            float cf, sf;
+            if (a.g.precision == LEYLINE_ROTATE_BF16_NAIVE) {
+                cf = __bfloat162float(__double2bfloat16(c));
+                sf = __bfloat162float(__double2bfloat16(s));
+            } else {
+                cf = (float)c;
+                sf = (float)s;
+            }
+            a.trig[2 * i] = cf;
+            a.trig[2 * i + 1] = sf;
+        }
+        if (i < a.total_pop) {
+            int page = a.free_stack[a.pop_top - 1 - i];
+            if (page < 0 || page >= a.g.num_pages) {
+                raise_status(a.status, ST_BAD_FRESH);
+                page = -1;
+            }
+            a.staged[i] = page;
+        }
+    }
+}
+
+__device__ __forceinline__ int find_req_by_commit(const SpliceArgs& a, long long i)
+{
+    int lo = 0, hi = a.n_reqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.reqs[mid].commit_begin <= i) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Commit: block-table entries [b0, b0 + n_new) take the fresh pages, entries
+// [b0 + n_new, b0 + n_old) become -1, the old pages of [b0, b0 + n_old) go back
+// onto the free stack, and seq_lens_dev takes the new length.  One thread owns
+// one table entry, so reading the old id and writing the new one cannot race.
+__global__ void commit_kernel(const SpliceArgs a)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_commit;
+         i += (long long)gridDim.x * blockDim.x) {
+        const ReqPlan& rp = a.reqs[find_req_by_commit(a, i)];
+        const long long k = i - rp.commit_begin;
+        int32_t* row = a.table_w + (long long)rp.req * a.max_blocks + rp.b0;
+        if (k == 0) a.seq_lens_dev[rp.req] = (int32_t)rp.new_len;
+        int old = -1;
+        if (k < rp.n_old) old = row[k];
+        if (k < rp.n_new) row[k] = a.staged[rp.pop_off + k];
+        else if (k < rp.n_old) row[k] = -1;
+        if (k < rp.n_old) {
+            const long long slot = a.push_base + rp.push_off + k;
+            if (old < 0 || old >= a.g.num_pages) {
+                raise_status(a.status, ST_BAD_OLD);
+                old = -1;
+            }
+            if (slot < a.g.num_pages) a.free_stack[slot] = old;
+            else raise_status(a.status, ST_BAD_RANGE);
+        }
+    }
+}
+
+__global__ void init_stack_kernel(int32_t* stack, long long n)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        stack[i] = (int32_t)(n - 1 - i);
+}
+
+// Gather logical rows [t0, t1) of one request and layer into a contiguous buffer.
+__global__ void gather_kernel(const uint4* kv, const int32_t* table_row, long long B, long long row_vecs,
+                              long long layer_off, long long num_pages, long long t0, long long n, uint4* out,
+                              int32_t* status)
+{
+    const long long total = n * row_vecs;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / row_vecs, c = i - r * row_vecs;
+        const long long t = t0 + r;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= num_pages) {
+            raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        out[i] = kv[layer_off + ((long long)page * B + t % B) * row_vecs + c];
+    }
+}
+
+int grid_for(long long items, int threads, int cap)
+{
+    long long g = (items + threads - 1) / threads;
+    if (g < 1) g = 1;
+    if (g > cap) g = cap;
+    return (int)g;
+}
+
+bool mla_shape(const Geometry& g) { return g.latent_vecs == 64 && g.rope_vecs == 8; }
+
+}  // namespace
+
+int launch_init_stack(int32_t* stack, int64_t num_pages, void* stream)
+{
+    init_stack_kernel<<<grid_for(num_pages, 256, 4096), 256, 0, (cudaStream_t)stream>>>(stack, num_pages);
+    return (int)cudaGetLastError();
+}
+
+int launch_plan_kernel(const SpliceArgs& a, void* stream)
+{
+    const long long items = std::max<long long>((long long)a.n_trig * (a.g.rope_dim / 2), a.total_pop);
+    if (items == 0) return 0;
+    plan_kernel<<<grid_for(items, 256, 2048), 256, 0, (cudaStream_t)stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_move_rotate(const SpliceArgs& a, int grid, void* stream)
+{
+    const long long units = a.total_tiles * a.g.num_layers;
+    if (units == 0) return 0;
+    if ((long long)grid > units) grid = (int)units;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    if (mla_shape(a.g)) {
+        if (a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT) {
+            if (bf16) move_rotate_mla<64, 8, 0, true><<<grid, kMoveThreads, 0, s>>>(a, units);
+            else move_rotate_mla<64, 8, 0, false><<<grid, kMoveThreads, 0, s>>>(a, units);
+        } else {
+            if (bf16) move_rotate_mla<64, 8, 1, true><<<grid, kMoveThreads, 0, s>>>(a, units);
+            else move_rotate_mla<64, 8, 1, false><<<grid, kMoveThreads, 0, s>>>(a, units);
+        }
+    } else {
+        if (bf16) move_rotate_generic<true><<<grid, kMoveThreads, 0, s>>>(a, units);
+        else move_rotate_generic<false><<<grid, kMoveThreads, 0, s>>>(a, units);
+    }
+    return (int)cudaGetLastError();
+}
+
+int launch_commit(const SpliceArgs& a, void* stream)
+{
+    if (a.total_commit == 0) return 0;
+    commit_kernel<<<grid_for(a.total_commit, 256, 4096), 256, 0, (cudaStream_t)stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
+                  int64_t t1, void* out, int32_t* status, void* stream)
+{
+    const long long n = t1 - t0;
+    if (n <= 0) return 0;
+    gather_kernel<<<grid_for(n * g.row_vecs, 256, 8192), 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint4*>(kv), table_row, g.block_size, g.row_vecs, (long long)layer * g.layer_vecs,
+        g.num_pages, t0, n, static_cast<uint4*>(out), status);
+    return (int)cudaGetLastError();
+}
+
+int move_rotate_blocks_per_sm(int* blocks)
+{
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, move_rotate_mla<64, 8, 0, false>,
+                                                              kMoveThreads, 0);
+}
+
+}  // namespace leyline

@@ -1,0 +1,67 @@
+// leyline_plan.h -- the splice plan: what the host planner hands to the kernels.
+//
+// A splice of one request ("Leyline: KV Cache Directives for Agentic
+// Inference", sections 2.1-2.3) is described in the request's NEW coordinates as
+// a short list of segments that tile the rewritten range [b0 * B, new_len):
+//   HEAD   prefix rows of the first rewritten block, copied unchanged (Delta 0)
+//   REPL   rows of a directive's R, copied bit for bit
+//   COPY   a surviving run whose accumulated Delta is 0, moved unchanged
+//   ROT    a surviving run moved by Delta != 0; its rope band is turned by R(Delta)
+// The kernels look up the segment of a destination row, read the source row
+// through the old block table (or from R), and write it into a fresh page.
+#pragma once
+
+#include <cstdint>
+
+namespace leyline {
+
+constexpr int kTileRows = 16;  // destination rows per move+rotate tile
+
+enum SegKind : int32_t { SEG_HEAD = 0, SEG_REPL = 1, SEG_COPY = 2, SEG_ROT = 3 };
+
+struct Geometry {
+    int32_t num_layers;
+    int32_t latent_dim;
+    int32_t rope_dim;
+    int32_t block_size;
+    int32_t row_elems;    // latent_dim + rope_dim
+    int32_t row_vecs;     // row_elems / 8 (16-byte vectors)
+    int32_t latent_vecs;  // latent_dim / 8
+    int32_t rope_vecs;    // rope_dim / 8
+    int64_t num_pages;
+    int64_t layer_vecs;   // num_pages * block_size * row_vecs
+    double theta;
+    int32_t pair_layout;
+    int32_t precision;
+};
+
+struct ReqPlan {
+    int32_t req;           // table row
+    int32_t b0;            // first rewritten block
+    int32_t n_new;         // fresh pages: ceil(new_len / B) - b0
+    int32_t n_old;         // pages returned: ceil(old_len / B) - b0
+    int64_t row0;          // b0 * B, first rewritten destination row
+    int64_t new_len;
+    int64_t old_len;
+    int64_t tile_begin;    // first flat move+rotate tile of this request
+    int64_t commit_begin;  // first flat commit index of this request
+    int32_t seg_begin;
+    int32_t seg_count;
+    int32_t pop_off;       // into the staged fresh pages
+    int32_t push_off;      // into the push region of the free stack
+};
+
+struct Seg {
+    int64_t new_start;     // first destination row of the segment
+    int64_t src_start;     // source position (HEAD/COPY/ROT) or row index in R (REPL)
+    const void* repl;      // R rows [num_layers][n_repl][row] (REPL only)
+    int32_t kind;          // SegKind
+    int32_t trig;          // trig table entry (ROT only), else -1
+    int32_t n_repl;        // rows of R per layer (REPL only)
+    int32_t pad;
+};
+
+static_assert(sizeof(ReqPlan) == 72, "ReqPlan layout");
+static_assert(sizeof(Seg) == 40, "Seg layout");
+
+}  // namespace leyline

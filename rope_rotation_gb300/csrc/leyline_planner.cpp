@@ -1,0 +1,232 @@
+// leyline_planner.cpp -- host-side validation and planning of a splice call.
+//
+// "Leyline: KV Cache Directives for Agentic Inference":
+//   section 2.1  D = (s_start, s_end, R, m); AMORTIZE splices in place; FORGET is
+//                routed to a re-prefill, which this library does not do.
+//   section 2.2  Delta = |R| - |S| for every downstream token.
+//   section 2.3  prefix [0, s_start) kept, R written to new slots, downstream
+//                slots re-indexed and rotated.
+//
+// Several directives of one request are composed into one pass: with the spans
+// sorted, directive k's rows of R start at s_k + D_{k-1} and the surviving run
+// [e_k, s_{k+1}) moves by D_k, where D_k is the summed Delta of directives 1..k.
+// This equals applying the directives one at a time, right to left.
+#include <algorithm>
+#include <climits>
+#include <cstdio>
+#include <cstring>
+
+#include "leyline_internal.h"
+
+namespace leyline {
+
+namespace {
+thread_local std::string g_last_error;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+}  // namespace
+
+int set_error(int code, const std::string& msg)
+{
+    g_last_error = msg;
+    return code;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+const char* last_error_cstr() { return g_last_error.c_str(); }
+
+int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
+{
+    if (!d) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool descriptor");
+    if (d->num_layers < 1) return set_error(LEYLINE_ERR_INVALID_ARG, "num_layers must be >= 1");
+    if (d->latent_dim < 0 || d->latent_dim % 8 != 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "latent_dim must be a non-negative multiple of 8");
+    if (d->rope_dim < 16 || d->rope_dim % 16 != 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "rope_dim must be a positive multiple of 16");
+    if (d->block_size < 1) return set_error(LEYLINE_ERR_INVALID_ARG, "block_size must be >= 1");
+    if (d->num_pages < 1 || d->num_pages > INT32_MAX)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "num_pages must be in [1, 2^31 - 1]");
+    if (!(d->rope_theta > 0.0)) return set_error(LEYLINE_ERR_INVALID_ARG, "rope_theta must be > 0");
+    if (d->pair_layout != LEYLINE_PAIRS_HALF_SPLIT && d->pair_layout != LEYLINE_PAIRS_INTERLEAVED)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pair_layout");
+    if (d->rotate_precision != LEYLINE_ROTATE_FP32 && d->rotate_precision != LEYLINE_ROTATE_BF16_NAIVE)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "unknown rotate_precision");
+    g->num_layers = d->num_layers;
+    g->latent_dim = d->latent_dim;
+    g->rope_dim = d->rope_dim;
+    g->block_size = d->block_size;
+    g->row_elems = d->latent_dim + d->rope_dim;
+    g->row_vecs = g->row_elems / 8;
+    g->latent_vecs = d->latent_dim / 8;
+    g->rope_vecs = d->rope_dim / 8;
+    g->num_pages = d->num_pages;
+    g->layer_vecs = d->num_pages * (int64_t)d->block_size * g->row_vecs;
+    g->theta = d->rope_theta;
+    g->pair_layout = d->pair_layout;
+    g->precision = d->rotate_precision;
+    return LEYLINE_OK;
+}
+
+int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs, int32_t max_blocks,
+               const leyline_directive_t* dirs, int32_t n, int64_t free_pages, Plan* plan)
+{
+    char msg[256];
+    *plan = Plan{};
+    if (n < 0) return set_error(LEYLINE_ERR_INVALID_ARG, "negative directive count");
+    if (n > 0 && !dirs) return set_error(LEYLINE_ERR_INVALID_ARG, "null directive array");
+    if (num_reqs < 0 || max_blocks < 0) return set_error(LEYLINE_ERR_INVALID_ARG, "negative table size");
+    if (n > 0 && !seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null seq_lens_host");
+    const int64_t B = g.block_size;
+
+    // 1. each directive on its own
+    for (int32_t k = 0; k < n; ++k) {
+        const leyline_directive_t& d = dirs[k];
+        if (d.req < 0 || d.req >= num_reqs) {
+            snprintf(msg, sizeof msg, "directive %d: request %d out of range [0, %d)", k, d.req, num_reqs);
+            return set_error(LEYLINE_ERR_INVALID_DIRECTIVE, msg);
+        }
+        if (d.mode == LEYLINE_FORGET) {
+            snprintf(msg, sizeof msg, "directive %d: FORGET is served by a re-prefill, not by the splice", k);
+            return set_error(LEYLINE_ERR_UNSUPPORTED_MODE, msg);
+        }
+        if (d.mode != LEYLINE_AMORTIZE) {
+            snprintf(msg, sizeof msg, "directive %d: unknown mode %d", k, d.mode);
+            return set_error(LEYLINE_ERR_UNSUPPORTED_MODE, msg);
+        }
+        if (d.reserved != 0) {
+            snprintf(msg, sizeof msg, "directive %d: reserved field must be 0", k);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+        const int64_t L = seq_lens_host[d.req];
+        if (d.s_start < 0 || d.s_start > d.s_end || d.s_end > L) {
+            snprintf(msg, sizeof msg, "directive %d: need 0 <= s_start <= s_end <= seq_len, got [%lld, %lld) of %lld",
+                     k, (long long)d.s_start, (long long)d.s_end, (long long)L);
+            return set_error(LEYLINE_ERR_INVALID_DIRECTIVE, msg);
+        }
+        if (d.n_repl < 0) {
+            snprintf(msg, sizeof msg, "directive %d: n_repl < 0", k);
+            return set_error(LEYLINE_ERR_INVALID_DIRECTIVE, msg);
+        }
+        if (d.n_repl > 0 && (!d.repl_rows || (reinterpret_cast<uintptr_t>(d.repl_rows) & 15) != 0)) {
+            snprintf(msg, sizeof msg, "directive %d: repl_rows must be a 16-byte aligned device pointer", k);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+    }
+
+    // 2. group by request, sort by s_start, check non-overlap
+    std::vector<int32_t> order(n);
+    for (int32_t k = 0; k < n; ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+        if (dirs[a].req != dirs[b].req) return dirs[a].req < dirs[b].req;
+        return dirs[a].s_start < dirs[b].s_start;
+    });
+    for (int32_t i = 0; i + 1 < n; ++i) {
+        const leyline_directive_t& a = dirs[order[i]];
+        const leyline_directive_t& b = dirs[order[i + 1]];
+        if (a.req != b.req) continue;
+        if (a.s_start == b.s_start || a.s_end > b.s_start) {
+            snprintf(msg, sizeof msg, "request %d: spans [%lld, %lld) and [%lld, %lld) overlap or share s_start",
+                     a.req, (long long)a.s_start, (long long)a.s_end, (long long)b.s_start, (long long)b.s_end);
+            return set_error(LEYLINE_ERR_OVERLAP, msg);
+        }
+    }
+
+    // 3. plan each touched request
+    int64_t tiles = 0, commit = 0, pops = 0, pushes = 0;
+    leyline_stats_t& st = plan->stats;
+    for (int32_t i = 0; i < n;) {
+        const int32_t req = dirs[order[i]].req;
+        int32_t j = i;
+        std::vector<const leyline_directive_t*> eff;
+        for (; j < n && dirs[order[j]].req == req; ++j) {
+            const leyline_directive_t* d = &dirs[order[j]];
+            if (d->s_start == d->s_end && d->n_repl == 0) continue;  // no-op
+            eff.push_back(d);
+        }
+        i = j;
+        if (eff.empty()) continue;
+
+        const int64_t L = seq_lens_host[req];
+        int64_t delta_total = 0;
+        for (const auto* d : eff) delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
+        const int64_t Lp = L + delta_total;
+        if (Lp > (int64_t)max_blocks * B || Lp > INT32_MAX) {
+            snprintf(msg, sizeof msg, "request %d: new length %lld exceeds the table capacity %lld", req,
+                     (long long)Lp, (long long)max_blocks * B);
+            return set_error(LEYLINE_ERR_CAPACITY, msg);
+        }
+        ReqPlan rp{};
+        rp.req = req;
+        rp.b0 = (int32_t)(eff.front()->s_start / B);
+        rp.row0 = (int64_t)rp.b0 * B;
+        rp.old_len = L;
+        rp.new_len = Lp;
+        rp.n_new = (int32_t)(ceil_div(Lp, B) - rp.b0);
+        rp.n_old = (int32_t)(ceil_div(L, B) - rp.b0);
+        rp.seg_begin = (int32_t)plan->segs.size();
+        rp.pop_off = (int32_t)pops;
+        rp.push_off = (int32_t)pushes;
+        rp.tile_begin = tiles;
+        rp.commit_begin = commit;
+
+        // segments in new coordinates
+        const int64_t s1 = eff.front()->s_start;
+        if (rp.row0 < s1) {
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0};
+            plan->segs.push_back(s);
+            st.head_slots += s1 - rp.row0;
+        }
+        int64_t D = 0;  // accumulated Delta left of the current position
+        for (size_t k = 0; k < eff.size(); ++k) {
+            const leyline_directive_t* d = eff[k];
+            if (d->n_repl > 0) {
+                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, 0};
+                plan->segs.push_back(s);
+                st.repl_slots += d->n_repl;
+            }
+            D += (int64_t)d->n_repl - (d->s_end - d->s_start);
+            const int64_t run_end = (k + 1 < eff.size()) ? eff[k + 1]->s_start : L;
+            if (run_end > d->s_end) {
+                Seg s{d->s_end + D, d->s_end, nullptr, D == 0 ? SEG_COPY : SEG_ROT, -1, 0, 0};
+                if (D != 0) {
+                    s.trig = (int32_t)plan->trig_delta.size();
+                    plan->trig_delta.push_back(D);
+                }
+                plan->segs.push_back(s);
+                st.downstream_slots += run_end - d->s_end;
+            }
+        }
+        rp.seg_count = (int32_t)plan->segs.size() - rp.seg_begin;
+        if (rp.seg_count == 0) {  // nothing left to write (pure truncation at a block boundary)
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0};
+            plan->segs.push_back(s);
+            rp.seg_count = 1;
+        }
+        const int64_t rows = Lp - rp.row0;
+        tiles += ceil_div(rows, kTileRows);
+        commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
+        pops += rp.n_new;
+        pushes += rp.n_old;
+        plan->reqs.push_back(rp);
+    }
+
+    if (free_pages >= 0 && pops > free_pages) {
+        snprintf(msg, sizeof msg, "splice needs %lld fresh pages, %lld free", (long long)pops, (long long)free_pages);
+        return set_error(LEYLINE_ERR_NO_PAGES, msg);
+    }
+    plan->total_tiles = tiles;
+    plan->total_commit = commit;
+    plan->total_pop = pops;
+    plan->total_push = pushes;
+    const int64_t row_bytes = (int64_t)g.row_elems * 2;
+    st.algorithmic_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots);
+    st.moved_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots + st.head_slots);
+    st.pages_popped = pops;
+    st.pages_pushed = pushes;
+    st.requests_touched = (int32_t)plan->reqs.size();
+    st.kernels_launched = plan->reqs.empty() ? 0 : 3;
+    return LEYLINE_OK;
+}
+
+}  // namespace leyline

@@ -1,0 +1,438 @@
+// leyline_pool.cpp -- pool, free-page stack, splice / gather entry points (C ABI).
+//
+// The pool borrows the caller's KV memory and block tables.  It owns the
+// free-page stack (device int32 [num_pages], top counted on the host), a device
+// plan buffer and a pinned host staging buffer for the plan, a status word and
+// a few events.  A splice call:
+//   1. validates and plans on the host (leyline_planner.cpp) -- on error nothing
+//      is enqueued and nothing changes;
+//   2. uploads the plan (a few KB) with one async host-to-device copy;
+//   3. enqueues the plan, move+rotate and commit kernels on the caller's stream;
+//   4. updates the host mirrors (lengths, free-page count) at enqueue time.
+// Source pages are only read and fresh pages only written, so a splice whose
+// spans shift downstream rows left (Delta < 0) or right (Delta > 0) has no
+// read/write overlap; the old pages are recycled by the commit kernel.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "leyline_internal.h"
+
+namespace leyline {
+const char* last_error_cstr();
+}
+
+using namespace leyline;
+
+struct leyline_pool {
+    leyline_pool_desc_t desc{};
+    Geometry g{};
+    void* kv = nullptr;
+    int device = 0;
+    int sm_count = 0;
+    int move_blocks_per_sm = 1;
+    int32_t* d_stack = nullptr;
+    int64_t free_top = 0;
+    int32_t* d_status = nullptr;
+    char* d_plan = nullptr;
+    size_t d_plan_cap = 0;
+    char* h_plan = nullptr;  // pinned
+    size_t h_plan_cap = 0;
+    cudaEvent_t plan_uploaded = nullptr;  // staging buffer reusable once this completes
+    cudaEvent_t done = nullptr;           // last enqueued work of the pool
+    bool has_work = false;
+    cudaStream_t last_stream = nullptr;
+    leyline_stats_t last_stats{};
+    bool timing = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;
+    size_t tev_used = 0;
+};
+
+namespace {
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess) ok = true;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+int cuda_error(cudaError_t e, const char* what)
+{
+    char msg[256];
+    snprintf(msg, sizeof msg, "%s: %s", what, cudaGetErrorString(e));
+    return set_error(LEYLINE_ERR_CUDA, msg);
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int wait_pool(leyline_pool_t* p)
+{
+    if (p->has_work) {
+        cudaError_t e = cudaEventSynchronize(p->done);
+        if (e != cudaSuccess) return cuda_error(e, "waiting for the pool's work");
+    }
+    return LEYLINE_OK;
+}
+
+// Make `stream` wait for the pool's previous work when it came from another stream.
+int order_after_previous(leyline_pool_t* p, cudaStream_t stream)
+{
+    if (p->has_work && p->last_stream != stream) {
+        cudaError_t e = cudaStreamWaitEvent(stream, p->done, 0);
+        if (e != cudaSuccess) return cuda_error(e, "ordering after the previous splice");
+    }
+    return LEYLINE_OK;
+}
+
+int mark_done(leyline_pool_t* p, cudaStream_t stream)
+{
+    cudaError_t e = cudaEventRecord(p->done, stream);
+    if (e != cudaSuccess) return cuda_error(e, "recording completion event");
+    p->has_work = true;
+    p->last_stream = stream;
+    return LEYLINE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* leyline_last_error(void) { return last_error_cstr(); }
+
+const char* leyline_version(void) { return "leyline-gb300 0.1.0 sm_103a"; }
+
+int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_pool_t** out)
+{
+    clear_error();
+    if (!out) return set_error(LEYLINE_ERR_INVALID_ARG, "null output pointer");
+    *out = nullptr;
+    Geometry g;
+    int rc = make_geometry(desc, &g);
+    if (rc != LEYLINE_OK) return rc;
+    if (!kv_dev || (reinterpret_cast<uintptr_t>(kv_dev) & 15) != 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "kv_dev must be a non-null 16-byte aligned device pointer");
+    leyline_pool_t* p = new (std::nothrow) leyline_pool();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "out of host memory");
+    p->desc = *desc;
+    p->g = g;
+    p->kv = kv_dev;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
+    if (e == cudaSuccess) e = (cudaError_t)move_rotate_blocks_per_sm(&p->move_blocks_per_sm);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_stack, sizeof(int32_t) * (size_t)g.num_pages);
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->plan_uploaded, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = (cudaError_t)launch_init_stack(p->d_stack, g.num_pages, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        int r = cuda_error(e, "creating the pool");
+        leyline_pool_destroy(p);
+        return r;
+    }
+    if (p->move_blocks_per_sm < 1) p->move_blocks_per_sm = 1;
+    p->free_top = g.num_pages;
+    *out = p;
+    return LEYLINE_OK;
+}
+
+int leyline_pool_destroy(leyline_pool_t* p)
+{
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    DeviceGuard guard(p->device);
+    if (p->has_work) cudaEventSynchronize(p->done);
+    for (auto& ev : p->tev) {
+        cudaEventDestroy(ev.first);
+        cudaEventDestroy(ev.second);
+    }
+    if (p->plan_uploaded) cudaEventDestroy(p->plan_uploaded);
+    if (p->done) cudaEventDestroy(p->done);
+    if (p->d_plan) cudaFree(p->d_plan);
+    if (p->h_plan) cudaFreeHost(p->h_plan);
+    if (p->d_status) cudaFree(p->d_status);
+    if (p->d_stack) cudaFree(p->d_stack);
+    delete p;
+    return LEYLINE_OK;
+}
+
+int64_t leyline_free_page_count(const leyline_pool_t* p)
+{
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    return p->free_top;
+}
+
+int leyline_alloc_pages(leyline_pool_t* p, int32_t n, int32_t* ids)
+{
+    clear_error();
+    if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
+    if (n > p->free_top) return set_error(LEYLINE_ERR_NO_PAGES, "not enough free pages");
+    if (n == 0) return LEYLINE_OK;
+    DeviceGuard guard(p->device);
+    int rc = wait_pool(p);
+    if (rc != LEYLINE_OK) return rc;
+    std::vector<int32_t> top(n);
+    cudaError_t e = cudaMemcpy(top.data(), p->d_stack + (p->free_top - n), sizeof(int32_t) * (size_t)n,
+                               cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_error(e, "reading the free stack");
+    for (int32_t i = 0; i < n; ++i) ids[i] = top[n - 1 - i];
+    p->free_top -= n;
+    return LEYLINE_OK;
+}
+
+int leyline_free_pages(leyline_pool_t* p, int32_t n, const int32_t* ids)
+{
+    clear_error();
+    if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
+    if (p->free_top + n > p->g.num_pages)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "more pages returned than the pool holds");
+    for (int32_t i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= p->g.num_pages) return set_error(LEYLINE_ERR_INVALID_ARG, "page id out of range");
+    if (n == 0) return LEYLINE_OK;
+    DeviceGuard guard(p->device);
+    int rc = wait_pool(p);
+    if (rc != LEYLINE_OK) return rc;
+    std::vector<int32_t> v(ids, ids + n);
+    std::reverse(v.begin(), v.end());  // ids[0] is taken first by the next pop
+    cudaError_t e = cudaMemcpy(p->d_stack + p->free_top, v.data(), sizeof(int32_t) * (size_t)n,
+                               cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_error(e, "writing the free stack");
+    p->free_top += n;
+    return LEYLINE_OK;
+}
+
+int leyline_splice_plan(const leyline_pool_desc_t* desc, const int64_t* seq_lens_host, int32_t num_reqs,
+                        int32_t max_blocks, const leyline_directive_t* dirs, int32_t n, int64_t free_pages,
+                        leyline_stats_t* stats, int64_t* new_seq_lens)
+{
+    clear_error();
+    Geometry g;
+    int rc = make_geometry(desc, &g);
+    if (rc != LEYLINE_OK) return rc;
+    if (num_reqs > 0 && !seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null seq_lens_host");
+    Plan plan;
+    rc = build_plan(g, seq_lens_host, num_reqs, max_blocks, dirs, n, free_pages, &plan);
+    if (rc != LEYLINE_OK) return rc;
+    if (stats) *stats = plan.stats;
+    if (new_seq_lens) {
+        for (int32_t r = 0; r < num_reqs; ++r) new_seq_lens[r] = seq_lens_host[r];
+        for (const ReqPlan& rp : plan.reqs) new_seq_lens[rp.req] = rp.new_len;
+    }
+    return LEYLINE_OK;
+}
+
+int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_directive_t* dirs, int32_t n,
+                   void* stream_v)
+{
+    clear_error();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    if (!bt || !bt->table || !bt->seq_lens_dev || !bt->seq_lens_host || bt->num_reqs < 0 || bt->max_blocks < 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "incomplete block table");
+    for (int32_t r = 0; r < bt->num_reqs; ++r)
+        if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
+            return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
+    Plan plan;
+    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, p->free_top, &plan);
+    if (rc != LEYLINE_OK) return rc;
+    if (plan.reqs.empty()) {
+        p->last_stats = plan.stats;
+        return LEYLINE_OK;
+    }
+    if (p->free_top - plan.total_pop + plan.total_push > p->g.num_pages)
+        return set_error(LEYLINE_ERR_INVALID_ARG,
+                         "the rewritten requests hold more pages than the pool has free slots for: "
+                         "their tables were not filled from this pool");
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
+
+    // plan buffer layout (16-byte aligned sections): uploaded part, then device-only part
+    const int half = p->g.rope_dim / 2;
+    const size_t off_reqs = 0;
+    const size_t off_segs = align_up(off_reqs + sizeof(ReqPlan) * plan.reqs.size(), 16);
+    const size_t off_delta = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
+    const size_t upload = align_up(off_delta + sizeof(int64_t) * plan.trig_delta.size(), 16);
+    const size_t off_trig = upload;
+    const size_t off_staged = align_up(off_trig + sizeof(float) * 2 * half * plan.trig_delta.size(), 16);
+    const size_t total = align_up(off_staged + sizeof(int32_t) * (size_t)plan.total_pop, 256);
+
+    cudaError_t e;
+    if (total > p->d_plan_cap) {
+        rc = wait_pool(p);
+        if (rc != LEYLINE_OK) return rc;
+        if (p->d_plan) cudaFree(p->d_plan);
+        p->d_plan = nullptr;
+        p->d_plan_cap = 0;
+        const size_t cap = std::max<size_t>(total * 2, 1 << 16);
+        e = cudaMalloc(&p->d_plan, cap);
+        if (e != cudaSuccess) return cuda_error(e, "allocating the plan buffer");
+        p->d_plan_cap = cap;
+    }
+    if (upload > p->h_plan_cap) {
+        if (p->h_plan) {
+            e = cudaEventSynchronize(p->plan_uploaded);
+            if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
+            cudaFreeHost(p->h_plan);
+            p->h_plan = nullptr;
+            p->h_plan_cap = 0;
+        }
+        const size_t cap = std::max<size_t>(upload * 2, 1 << 16);
+        e = cudaHostAlloc((void**)&p->h_plan, cap, cudaHostAllocDefault);
+        if (e != cudaSuccess) return cuda_error(e, "allocating the pinned plan buffer");
+        p->h_plan_cap = cap;
+    } else if (p->has_work) {
+        e = cudaEventSynchronize(p->plan_uploaded);  // the staging buffer may still be in flight
+        if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
+    }
+    memcpy(p->h_plan + off_reqs, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
+    memcpy(p->h_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
+    if (!plan.trig_delta.empty())
+        memcpy(p->h_plan + off_delta, plan.trig_delta.data(), sizeof(int64_t) * plan.trig_delta.size());
+
+    rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    e = cudaMemcpyAsync(p->d_plan, p->h_plan, upload, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
+    e = cudaEventRecord(p->plan_uploaded, stream);
+    if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
+
+    SpliceArgs a{};
+    a.kv = p->kv;
+    a.table = bt->table;
+    a.table_w = bt->table;
+    a.seq_lens_dev = bt->seq_lens_dev;
+    a.free_stack = p->d_stack;
+    a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan + off_reqs);
+    a.segs = reinterpret_cast<const Seg*>(p->d_plan + off_segs);
+    a.trig_delta = reinterpret_cast<const int64_t*>(p->d_plan + off_delta);
+    a.trig = reinterpret_cast<float*>(p->d_plan + off_trig);
+    a.staged = reinterpret_cast<int32_t*>(p->d_plan + off_staged);
+    a.status = p->d_status;
+    a.pop_top = p->free_top;
+    a.push_base = p->free_top - plan.total_pop;
+    a.total_tiles = plan.total_tiles;
+    a.total_commit = plan.total_commit;
+    a.total_pop = plan.total_pop;
+    a.n_reqs = (int32_t)plan.reqs.size();
+    a.n_trig = (int32_t)plan.trig_delta.size();
+    a.max_blocks = bt->max_blocks;
+    a.g = p->g;
+
+    int err = launch_plan_kernel(a, stream);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the plan kernel");
+    cudaEvent_t t0 = nullptr, t1 = nullptr;
+    if (p->timing) {
+        if (p->tev_used == p->tev.size()) {
+            cudaEvent_t x, y;
+            if (cudaEventCreate(&x) != cudaSuccess || cudaEventCreate(&y) != cudaSuccess)
+                return set_error(LEYLINE_ERR_CUDA, "creating timing events");
+            p->tev.emplace_back(x, y);
+        }
+        t0 = p->tev[p->tev_used].first;
+        t1 = p->tev[p->tev_used].second;
+        ++p->tev_used;
+        cudaEventRecord(t0, stream);
+    }
+    const int grid = p->sm_count * p->move_blocks_per_sm;
+    err = launch_move_rotate(a, grid, stream);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the move+rotate kernel");
+    if (t1) cudaEventRecord(t1, stream);
+    err = launch_commit(a, stream);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the commit kernel");
+    rc = mark_done(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+
+    for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
+    p->free_top = p->free_top - plan.total_pop + plan.total_push;
+    p->last_stats = plan.stats;
+    return LEYLINE_OK;
+}
+
+int leyline_last_stats(const leyline_pool_t* p, leyline_stats_t* out)
+{
+    if (!p || !out) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    *out = p->last_stats;
+    return LEYLINE_OK;
+}
+
+int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t req, int32_t layer, int64_t t0,
+                   int64_t t1, void* out, void* stream_v)
+{
+    clear_error();
+    if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    if (req < 0 || req >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
+    if (layer < 0 || layer >= p->g.num_layers) return set_error(LEYLINE_ERR_INVALID_ARG, "layer out of range");
+    if (t0 < 0 || t0 > t1 || t1 > bt->seq_lens_host[req] || t1 > (int64_t)bt->max_blocks * p->g.block_size)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "rows outside [0, seq_len]");
+    if (t1 > t0 && (!out || (reinterpret_cast<uintptr_t>(out) & 15) != 0))
+        return set_error(LEYLINE_ERR_INVALID_ARG, "out must be a 16-byte aligned device pointer");
+    if (t1 == t0) return LEYLINE_OK;
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    DeviceGuard guard(p->device);
+    int rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    int err = launch_gather(p->kv, bt->table + (int64_t)req * bt->max_blocks, p->g, layer, t0, t1, out, p->d_status,
+                            stream);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the gather kernel");
+    return mark_done(p, stream);
+}
+
+int leyline_sync_status(leyline_pool_t* p)
+{
+    clear_error();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    DeviceGuard guard(p->device);
+    int rc = wait_pool(p);
+    if (rc != LEYLINE_OK) return rc;
+    int32_t st = 0;
+    cudaError_t e = cudaMemcpy(&st, p->d_status, sizeof st, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_error(e, "reading the status word");
+    if (st != 0) {
+        cudaMemset(p->d_status, 0, sizeof(int32_t));
+        char msg[128];
+        snprintf(msg, sizeof msg, "device check failed (status bits 0x%x)", st);
+        return set_error(LEYLINE_ERR_DEVICE_CHECK, msg);
+    }
+    return LEYLINE_OK;
+}
+
+int leyline_kernel_timing_enable(leyline_pool_t* p, int32_t enable)
+{
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    p->timing = enable != 0;
+    p->tev_used = 0;
+    return LEYLINE_OK;
+}
+
+int leyline_kernel_timing_read(leyline_pool_t* p, double* total_ms, int32_t* launches)
+{
+    if (!p || !total_ms || !launches) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    DeviceGuard guard(p->device);
+    double sum = 0.0;
+    for (size_t i = 0; i < p->tev_used; ++i) {
+        cudaError_t e = cudaEventSynchronize(p->tev[i].second);
+        if (e != cudaSuccess) return cuda_error(e, "waiting for timing events");
+        float ms = 0.f;
+        e = cudaEventElapsedTime(&ms, p->tev[i].first, p->tev[i].second);
+        if (e != cudaSuccess) return cuda_error(e, "reading timing events");
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = (int32_t)p->tev_used;
+    p->tev_used = 0;
+    return LEYLINE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,258 @@
+"""Thin ctypes binding of libleyline.so (C ABI in include/leyline.h).
+
+Argument marshalling only: every step of the splice runs in the library's CUDA
+kernels.  Functions carry the C names and raise ``LeylineError`` on a negative
+return code.  Device buffers are torch CUDA tensors (PyTorch provides device
+memory and streams); the library borrows their pointers.
+
+If the library is not built, importing works but the first call raises: there
+is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import _build
+
+LEYLINE_OK = 0
+LEYLINE_ERR_INVALID_ARG = -1
+LEYLINE_ERR_INVALID_DIRECTIVE = -2
+LEYLINE_ERR_OVERLAP = -3
+LEYLINE_ERR_NO_PAGES = -4
+LEYLINE_ERR_UNSUPPORTED_MODE = -5
+LEYLINE_ERR_CUDA = -6
+LEYLINE_ERR_CAPACITY = -7
+LEYLINE_ERR_DEVICE_CHECK = -8
+
+LEYLINE_PAIRS_HALF_SPLIT = 0
+LEYLINE_PAIRS_INTERLEAVED = 1
+LEYLINE_ROTATE_FP32 = 0
+LEYLINE_ROTATE_BF16_NAIVE = 1
+LEYLINE_AMORTIZE = 0
+LEYLINE_FORGET = 1
+
+
+class LeylineError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"leyline error {code}: {msg}")
+        self.code = code
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("latent_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_pages", ctypes.c_int64), ("rope_theta", ctypes.c_double),
+                ("pair_layout", ctypes.c_int32), ("rotate_precision", ctypes.c_int32)]
+
+
+class BlockTable(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("seq_lens_dev", ctypes.c_void_p), ("seq_lens_host", ctypes.c_void_p),
+                ("num_reqs", ctypes.c_int32), ("max_blocks", ctypes.c_int32)]
+
+
+class Directive(ctypes.Structure):
+    _fields_ = [("req", ctypes.c_int32), ("mode", ctypes.c_int32), ("s_start", ctypes.c_int64),
+                ("s_end", ctypes.c_int64), ("n_repl", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("repl_rows", ctypes.c_void_p)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("downstream_slots", ctypes.c_int64), ("repl_slots", ctypes.c_int64),
+                ("head_slots", ctypes.c_int64), ("algorithmic_bytes", ctypes.c_int64),
+                ("moved_bytes", ctypes.c_int64), ("pages_popped", ctypes.c_int64),
+                ("pages_pushed", ctypes.c_int64), ("requests_touched", ctypes.c_int32),
+                ("kernels_launched", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_vp = ctypes.c_void_p
+_SIGNATURES = {
+    "leyline_pool_create": (ctypes.c_int, [ctypes.POINTER(PoolDesc), _vp, ctypes.POINTER(_vp)]),
+    "leyline_pool_destroy": (ctypes.c_int, [_vp]),
+    "leyline_alloc_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "leyline_free_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
+    "leyline_free_page_count": (ctypes.c_int64, [_vp]),
+    "leyline_splice": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(Directive), ctypes.c_int32,
+                                      _vp]),
+    "leyline_splice_plan": (ctypes.c_int, [ctypes.POINTER(PoolDesc), ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.POINTER(Directive), ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.POINTER(Stats), ctypes.POINTER(ctypes.c_int64)]),
+    "leyline_last_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
+    "leyline_gather": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int64, ctypes.c_int64, _vp, _vp]),
+    "leyline_sync_status": (ctypes.c_int, [_vp]),
+    "leyline_kernel_timing_enable": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "leyline_kernel_timing_read": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double),
+                                                  ctypes.POINTER(ctypes.c_int32)]),
+    "leyline_last_error": (ctypes.c_char_p, []),
+    "leyline_version": (ctypes.c_char_p, []),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libleyline.so; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with rope_rotation_gb300.build() "
+                               "(the splice runs only in its CUDA kernels)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc < 0:
+        msg = load().leyline_last_error().decode(errors="replace")
+        raise LeylineError(rc, msg)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _tensor_ptr(t) -> int:
+    return int(t.data_ptr())
+
+
+# ------------------------------------------------------------------ pool ----
+
+def pool_desc(num_layers: int, block_size: int, num_pages: int, latent_dim: int = 512, rope_dim: int = 64,
+              rope_theta: float = 10000.0, pair_layout: int = LEYLINE_PAIRS_HALF_SPLIT,
+              rotate_precision: int = LEYLINE_ROTATE_FP32) -> PoolDesc:
+    return PoolDesc(num_layers, latent_dim, rope_dim, block_size, num_pages, rope_theta, pair_layout,
+                    rotate_precision)
+
+
+def leyline_pool_create(desc: PoolDesc, kv) -> ctypes.c_void_p:
+    """kv: torch bf16 CUDA tensor with num_layers*num_pages*block_size*(latent+rope) elements."""
+    need = desc.num_layers * desc.num_pages * desc.block_size * (desc.latent_dim + desc.rope_dim)
+    if kv.numel() != need or kv.element_size() != 2 or not kv.is_cuda or not kv.is_contiguous():
+        raise LeylineError(LEYLINE_ERR_INVALID_ARG, "kv must be a contiguous 2-byte CUDA tensor of the pool's size")
+    h = ctypes.c_void_p()
+    _check(load().leyline_pool_create(ctypes.byref(desc), _tensor_ptr(kv), ctypes.byref(h)))
+    return h
+
+
+def leyline_pool_destroy(pool) -> None:
+    _check(load().leyline_pool_destroy(pool))
+
+
+def leyline_alloc_pages(pool, n: int) -> np.ndarray:
+    ids = np.empty(max(n, 1), dtype=np.int32)
+    _check(load().leyline_alloc_pages(pool, n, ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+    return ids[:n]
+
+
+def leyline_free_pages(pool, ids) -> None:
+    a = np.ascontiguousarray(ids, dtype=np.int32)
+    _check(load().leyline_free_pages(pool, a.size, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+
+
+def leyline_free_page_count(pool) -> int:
+    n = load().leyline_free_page_count(pool)
+    _check(int(n) if n < 0 else 0)
+    return int(n)
+
+
+# ----------------------------------------------------------- block table ----
+
+class Tables:
+    """Keeps the tensors behind a BlockTable alive: table int32 [R][max_blocks] and seq_lens
+    int32 [R] on the device, and the int64 host mirror of the lengths."""
+
+    def __init__(self, table, seq_lens_dev, seq_lens_host: np.ndarray):
+        self.table = table
+        self.seq_lens_dev = seq_lens_dev
+        self.seq_lens_host = np.ascontiguousarray(seq_lens_host, dtype=np.int64)
+        self.bt = BlockTable(_tensor_ptr(table), _tensor_ptr(seq_lens_dev), self.seq_lens_host.ctypes.data,
+                             int(table.shape[0]), int(table.shape[1]))
+
+
+def directive(req: int, s_start: int, s_end: int, repl=None, n_repl: Optional[int] = None,
+              mode: int = LEYLINE_AMORTIZE) -> Directive:
+    """repl: bf16 CUDA tensor [num_layers][n_repl][row] or None."""
+    if n_repl is None:
+        n_repl = 0 if repl is None else int(repl.shape[1])
+    return Directive(req, mode, s_start, s_end, n_repl, 0, None if repl is None else _tensor_ptr(repl))
+
+
+def _dir_array(dirs: Sequence[Directive]):
+    arr = (Directive * max(len(dirs), 1))(*dirs)
+    return arr
+
+
+# ---------------------------------------------------------------- splice ----
+
+def leyline_splice(pool, tables: Tables, dirs: Sequence[Directive], stream=None) -> None:
+    arr = _dir_array(dirs)
+    _check(load().leyline_splice(pool, ctypes.byref(tables.bt), arr, len(dirs), _stream_ptr(stream)))
+
+
+def leyline_splice_plan(desc: PoolDesc, seq_lens_host, max_blocks: int, dirs: Sequence[Directive],
+                        free_pages: int = -1):
+    """Host-only dry run: returns (Stats, new lengths as int64 array)."""
+    lens = np.ascontiguousarray(seq_lens_host, dtype=np.int64)
+    out = np.empty(max(lens.size, 1), dtype=np.int64)
+    st = Stats()
+    arr = _dir_array(dirs)
+    p64 = ctypes.POINTER(ctypes.c_int64)
+    _check(load().leyline_splice_plan(ctypes.byref(desc), lens.ctypes.data_as(p64), lens.size, max_blocks, arr,
+                                      len(dirs), free_pages, ctypes.byref(st), out.ctypes.data_as(p64)))
+    return st, out[:lens.size]
+
+
+def leyline_last_stats(pool) -> Stats:
+    st = Stats()
+    _check(load().leyline_last_stats(pool, ctypes.byref(st)))
+    return st
+
+
+def leyline_gather(pool, tables: Tables, req: int, layer: int, t0: int, t1: int, out, stream=None) -> None:
+    """out: bf16 CUDA tensor [t1 - t0][row]."""
+    _check(load().leyline_gather(pool, ctypes.byref(tables.bt), req, layer, t0, t1, _tensor_ptr(out),
+                                 _stream_ptr(stream)))
+
+
+def leyline_sync_status(pool) -> None:
+    _check(load().leyline_sync_status(pool))
+
+
+def leyline_kernel_timing_enable(pool, enable: bool = True) -> None:
+    _check(load().leyline_kernel_timing_enable(pool, 1 if enable else 0))
+
+
+def leyline_kernel_timing_read(pool):
+    ms = ctypes.c_double()
+    n = ctypes.c_int32()
+    _check(load().leyline_kernel_timing_read(pool, ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
+
+
+def leyline_last_error() -> str:
+    return load().leyline_last_error().decode(errors="replace")
+
+
+def leyline_version() -> str:
+    return load().leyline_version().decode()

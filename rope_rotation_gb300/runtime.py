@@ -1,0 +1,93 @@
+"""A paged MLA KV cache in torch device memory, driven through libleyline.so.
+
+Plumbing for callers: it allocates the pool tensor (layout
+``kv[layer][page][slot][latent + rope]``, bf16), the block table and the length
+arrays, takes pages for new requests, and forwards splices and gathers to the
+C ABI.  It computes nothing itself.
+"""
+from __future__ import annotations
+
+from typing import Sequence
+
+import numpy as np
+
+from . import leyline
+
+
+class PagedCache:
+    def __init__(self, num_layers: int, block_size: int, num_pages: int, max_reqs: int, max_blocks: int,
+                 latent_dim: int = 512, rope_dim: int = 64, rope_theta: float = 10000.0,
+                 pair_layout: int = leyline.LEYLINE_PAIRS_HALF_SPLIT,
+                 rotate_precision: int = leyline.LEYLINE_ROTATE_FP32, device: str = "cuda"):
+        import torch
+        self.torch = torch
+        self.num_layers = num_layers
+        self.block_size = block_size
+        self.num_pages = num_pages
+        self.latent_dim = latent_dim
+        self.rope_dim = rope_dim
+        self.row = latent_dim + rope_dim
+        self.device = torch.device(device)
+        self.kv = torch.empty(num_layers * num_pages * block_size * self.row, dtype=torch.bfloat16,
+                              device=self.device)
+        self.desc = leyline.pool_desc(num_layers, block_size, num_pages, latent_dim, rope_dim, rope_theta,
+                                      pair_layout, rotate_precision)
+        self.pool = leyline.leyline_pool_create(self.desc, self.kv)
+        self.table = torch.full((max_reqs, max_blocks), -1, dtype=torch.int32, device=self.device)
+        self.seq_lens_dev = torch.zeros(max_reqs, dtype=torch.int32, device=self.device)
+        self.tables = leyline.Tables(self.table, self.seq_lens_dev, np.zeros(max_reqs, dtype=np.int64))
+
+    # ------------------------------------------------------------------
+    @property
+    def seq_lens_host(self) -> np.ndarray:
+        return self.tables.seq_lens_host
+
+    def kv_view(self):
+        """[layers][pages][block_size][row] view of the pool."""
+        return self.kv.view(self.num_layers, self.num_pages, self.block_size, self.row)
+
+    def add_request(self, req: int, length: int) -> np.ndarray:
+        """Take pages for a new request of `length` tokens and install its table row; returns the page ids."""
+        n = -(-length // self.block_size)
+        pages = leyline.leyline_alloc_pages(self.pool, n)
+        row = np.full(self.table.shape[1], -1, dtype=np.int32)
+        row[:n] = pages
+        self.table[req].copy_(self.torch.from_numpy(row))
+        self.seq_lens_dev[req] = length
+        self.tables.seq_lens_host[req] = length
+        return pages
+
+    def slot_index(self, req: int, tokens) -> "np.ndarray":
+        """Flat slot index page * block_size + offset of each token (host; reads the table)."""
+        t = np.asarray(tokens, dtype=np.int64)
+        row = self.table[req].cpu().numpy().astype(np.int64)
+        return row[t // self.block_size] * self.block_size + t % self.block_size
+
+    def splice(self, dirs: Sequence[leyline.Directive], stream=None) -> None:
+        leyline.leyline_splice(self.pool, self.tables, dirs, stream)
+
+    def gather(self, req: int, layer: int, t0: int, t1: int, out=None, stream=None):
+        if out is None:
+            out = self.torch.empty((t1 - t0, self.row), dtype=self.torch.bfloat16, device=self.device)
+        leyline.leyline_gather(self.pool, self.tables, req, layer, t0, t1, out, stream)
+        return out
+
+    def free_pages(self) -> int:
+        return leyline.leyline_free_page_count(self.pool)
+
+    def last_stats(self) -> dict:
+        return leyline.leyline_last_stats(self.pool).as_dict()
+
+    def check_status(self) -> None:
+        leyline.leyline_sync_status(self.pool)
+
+    def close(self) -> None:
+        if self.pool is not None:
+            leyline.leyline_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,162 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every function
+include/leyline.h declares, and its host-only planner (leyline_splice_plan)
+validates directives and computes lengths and work exactly as the oracle's
+logical splice does ("Leyline: KV Cache Directives for Agentic Inference",
+section 2.1: D = (s_start, s_end, R, m); section 2.2: Delta = |R| - |S|).
+No call here touches a device.
+"""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from synth import configs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE_DEV_PTR = 0x7F0000001000  # aligned; the dry run never dereferences it
+
+
+@pytest.fixture(scope="module")
+def L():
+    import rope_rotation_gb300
+    from rope_rotation_gb300 import leyline
+    rope_rotation_gb300.build()
+    leyline.load()
+    return leyline
+
+
+def test_exports_every_declared_symbol(L):
+    header = open(os.path.join(ROOT, "include", "leyline.h")).read()
+    names = set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**\s*(leyline_\w+)\s*\(", header, re.M))
+    assert len(names) >= 14
+    lib = L.load()
+    for n in sorted(names):
+        assert hasattr(lib, n), f"{n} declared but not exported"
+    assert "sm_103a" in L.leyline_version()
+
+
+def _d(L, req, s, e, n, mode=0, reserved=0, ptr=FAKE_DEV_PTR):
+    return L.Directive(req, mode, s, e, n, reserved, ptr if n > 0 else None)
+
+
+def _plan(L, lens, dirs, B=16, max_blocks=None, free=-1, desc=None):
+    desc = desc or L.pool_desc(4, B, 1 << 20)
+    if max_blocks is None:
+        max_blocks = max(-(-(x + 200) // B) for x in lens)
+    return L.leyline_splice_plan(desc, np.array(lens), max_blocks, dirs, free)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("forget", -5), ("unknown_mode", -5), ("s_gt_e", -2), ("e_gt_len", -2), ("neg_s", -2), ("bad_req", -2),
+    ("overlap", -3), ("shared_start", -3), ("neg_repl", -2), ("null_repl", -1), ("misaligned_repl", -1),
+    ("reserved", -1), ("capacity", -7), ("no_pages", -4),
+])
+def test_validation_errors(L, case, code):
+    lens = [100, 50]
+    dirs = {
+        "forget": [_d(L, 0, 1, 5, 0, mode=1)],
+        "unknown_mode": [_d(L, 0, 1, 5, 0, mode=7)],
+        "s_gt_e": [_d(L, 0, 9, 5, 0)],
+        "e_gt_len": [_d(L, 1, 10, 51, 0)],
+        "neg_s": [_d(L, 0, -1, 5, 0)],
+        "bad_req": [_d(L, 2, 1, 5, 0)],
+        "overlap": [_d(L, 0, 10, 20, 1), _d(L, 0, 15, 30, 1)],
+        "shared_start": [_d(L, 0, 10, 10, 1), _d(L, 0, 10, 20, 1)],
+        "neg_repl": [L.Directive(0, 0, 1, 5, -1, 0, None)],
+        "null_repl": [L.Directive(0, 0, 1, 5, 3, 0, None)],
+        "misaligned_repl": [L.Directive(0, 0, 1, 5, 3, 0, FAKE_DEV_PTR + 2)],
+        "reserved": [_d(L, 0, 1, 5, 0, reserved=1)],
+        "capacity": [_d(L, 1, 0, 0, 500)],
+        "no_pages": [_d(L, 0, 0, 10, 3)],
+    }[case]
+    kw = {"max_blocks": 10} if case == "capacity" else {}
+    if case == "no_pages":
+        kw["free"] = 2
+    with pytest.raises(L.LeylineError) as ei:
+        _plan(L, lens, dirs, **kw)
+    assert ei.value.code == code
+    assert L.leyline_last_error()
+
+
+def test_bad_descriptors(L):
+    for kw in [dict(rope_dim=8), dict(latent_dim=7), dict(block_size=0), dict(rope_theta=0.0),
+               dict(pair_layout=2), dict(rotate_precision=3), dict(num_layers=0)]:
+        args = dict(num_layers=2, block_size=16, num_pages=100)
+        args.update(kw)
+        desc = L.pool_desc(**args)
+        with pytest.raises(L.LeylineError) as ei:
+            L.leyline_splice_plan(desc, np.array([10]), 8, [_d(L, 0, 1, 2, 0)])
+        assert ei.value.code == -1
+
+
+def _expected(lens, dirs_by_req, B):
+    """Lengths, downstream slots, head slots and page counts from the oracle's logical splice."""
+    out = {"len": list(lens), "down": 0, "head": 0, "repl": 0, "pop": 0, "push": 0}
+    for r, dirs in dirs_by_req.items():
+        eff = [d for d in dirs if not (d[0] == d[1] and d[2] == 0)]
+        newlen, kind, idx, _ = oracle.splice_map(lens[r], dirs)
+        out["len"][r] = newlen
+        if not eff:
+            continue
+        first_end = min(d[1] for d in eff)
+        s_min = min(d[0] for d in eff)
+        out["down"] += int(((kind == 0) & (idx >= first_end)).sum())
+        out["repl"] += sum(d[2] for d in eff)
+        b0 = s_min // B
+        out["head"] += s_min - b0 * B
+        out["pop"] += -(-newlen // B) - b0
+        out["push"] += -(-lens[r] // B) - b0
+    return out
+
+
+@pytest.mark.parametrize("B", [1, 2, 16])
+def test_planner_matches_oracle_on_random_directives(L, B):
+    rng = np.random.default_rng(B)
+    for _ in range(300):
+        lens = [int(x) for x in rng.integers(0, 200, size=int(rng.integers(1, 5)))]
+        dirs_by_req, dirs = {}, []
+        for r, Lr in enumerate(lens):
+            k = int(rng.integers(0, 4))
+            cuts = sorted(int(x) for x in rng.integers(0, Lr + 1, size=2 * k))
+            ds = [(cuts[2 * i], cuts[2 * i + 1], int(rng.integers(0, 20))) for i in range(k)]
+            if len({d[0] for d in ds}) != len(ds):
+                continue
+            if ds:
+                dirs_by_req[r] = ds
+                dirs += [_d(L, r, s, e, n) for s, e, n in ds]
+        rng.shuffle(dirs)
+        st, newlens = _plan(L, lens, dirs, B=B)
+        want = _expected(lens, dirs_by_req, B)
+        assert list(newlens) == want["len"]
+        assert st.downstream_slots == want["down"]
+        assert st.repl_slots == want["repl"]
+        assert st.head_slots == want["head"]
+        assert st.pages_popped == want["pop"]
+        assert st.pages_pushed == want["push"]
+        row_bytes = 2 * 576
+        assert st.algorithmic_bytes == 2 * row_bytes * 4 * (want["down"] + want["repl"])
+
+
+def test_planner_matches_golden_workloads(L):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "workloads.json")))
+    for name, entry in g.items():
+        w = configs.by_name(name)
+        lens = list(w.lengths)
+        desc = L.pool_desc(w.num_layers, w.block_size, 1 << 30)
+        for step, want in zip(w.steps, entry["steps"]):
+            dirs = [_d(L, d.req, d.s_start, d.s_end, d.n_repl) for d in step]
+            st, newlens = L.leyline_splice_plan(desc, np.array(lens), max(-(-(x + 200) // w.block_size) for x in lens),
+                                                dirs)
+            assert st.downstream_slots == sum(x["downstream"] for x in want), name
+            for x in want:
+                assert newlens[x["req"]] == x["new_len"], name
+            lens = [int(v) for v in newlens]
+
+
+def test_noop_directives_touch_nothing(L):
+    st, newlens = _plan(L, [64, 10], [_d(L, 0, 5, 5, 0), _d(L, 1, 10, 10, 0)])
+    assert list(newlens) == [64, 10]
+    assert st.requests_touched == 0 and st.kernels_launched == 0 and st.pages_popped == 0

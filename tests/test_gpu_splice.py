@@ -1,0 +1,134 @@
+"""GPU splice vs the fp64 oracle, through the C ABI (needs a GB300).
+
+Edge cases of "Leyline: KV Cache Directives for Agentic Inference", section 2.1
+(spans at the start and the end of the sequence, empty spans, pure insertions
+and deletions, several directives per request, several requests per call) at
+block sizes 1, 2, 4 and 16, with ragged tails; the two RoPE pair layouts; the
+generic-shape kernel; the bf16-only comparison arm; and the 1-layer 4k and the
+27-layer 32k workloads in full.
+"""
+import numpy as np
+import pytest
+
+import splice_harness as H
+from synth import configs
+from synth.configs import Dir, Workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import rope_rotation_gb300
+    rope_rotation_gb300.build()
+
+
+EDGE = [
+    # (L, directives as (s, e, n_repl))
+    (37, [(5, 20, 3)]),
+    (37, [(0, 9, 2)]),             # s_start = 0
+    (37, [(30, 37, 5)]),           # s_end = L, grows
+    (37, [(17, 17, 6)]),           # pure insertion (Delta > 0)
+    (37, [(8, 30, 0)]),            # pure deletion
+    (37, [(0, 37, 4)]),            # everything replaced
+    (37, [(0, 37, 0)]),            # everything deleted
+    (32, [(16, 32, 0)]),           # truncation at a block boundary (B=16)
+    (48, [(3, 5, 9), (20, 33, 1), (40, 41, 0)]),  # three directives
+    (48, [(47, 48, 2), (1, 2, 0)]),  # unsorted input
+    (64, [(10, 10, 0), (20, 30, 10)]),  # a no-op directive and Delta = 0
+    (100, [(33, 71, 12)]),
+]
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 16])
+def test_edge_grid(B):
+    for i, (L, dirs) in enumerate(EDGE):
+        w = Workload(f"edge{i}-B{B}", 3, B, [L], [[Dir(0, s, e, n, k) for k, (s, e, n) in enumerate(dirs)]], seed=i)
+        cache = H.make_cache(w)
+        state = H.oracle_state(w)
+        H.splice_step_and_check(w, cache, state, w.steps[0])
+        cache.close()
+
+
+@pytest.mark.parametrize("B", [1, 16])
+def test_many_requests_one_call_and_chained_steps(B):
+    lengths = [70, 16, 0, 129, 33]
+    steps = [
+        [Dir(0, 10, 40, 3, 0), Dir(1, 0, 16, 0, 1), Dir(3, 64, 64, 20, 2), Dir(3, 100, 120, 1, 3),
+         Dir(4, 32, 33, 1, 4), Dir(2, 0, 0, 5, 5)],
+        [Dir(0, 0, 1, 0, 6), Dir(3, 1, 2, 2, 7), Dir(4, 0, 0, 0, 8)],
+        [Dir(2, 5, 5, 17, 9), Dir(0, 30, 42, 7, 10)],
+    ]
+    w = Workload(f"multi-B{B}", 2, B, lengths, steps, seed=11)
+    cache = H.make_cache(w, slack_pages=8)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step)
+    cache.close()
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_interleaved_and_half_split_layouts(layout):
+    w = Workload(f"layout{layout}", 2, 16, [300, 211], [[Dir(0, 40, 200, 7, 0), Dir(1, 3, 50, 60, 1)]], seed=3)
+    cache = H.make_cache(w, pair_layout=layout)
+    H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0], layout=layout)
+    cache.close()
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_generic_shape_kernel(layout):
+    """latent 64 + rope 16: not the MLA shape, so the generic move+rotate kernel runs."""
+    w = Workload(f"generic{layout}", 3, 4, [90, 45], [[Dir(0, 20, 60, 5, 0), Dir(1, 44, 45, 3, 1)]], seed=4,
+                 latent_dim=64, rope_dim=16)
+    cache = H.make_cache(w, pair_layout=layout)
+    H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0], layout=layout)
+    cache.close()
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_bf16_naive_arm_is_exact(layout):
+    w = Workload(f"bf16naive{layout}", 2, 16, [500], [[Dir(0, 100, 180, 12, 0)], [Dir(0, 0, 33, 1, 1)]], seed=5)
+    cache = H.make_cache(w, pair_layout=layout, precision=1)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step, layout=layout, precision=1)
+    cache.close()
+
+
+def test_delta_zero_leaves_logical_cache_unchanged():
+    """|R| = |S| with R equal to the replaced rows: every logical row keeps its bits."""
+    w = Workload("delta0", 4, 16, [777], [[]], seed=6)
+    cache = H.make_cache(w)
+    before = H.logical_rows(cache, 0, 777)
+    repl = torch.from_numpy(before[:, 100:140].copy().view(np.int16)).cuda().view(torch.bfloat16)
+    from rope_rotation_gb300 import leyline
+    cache.splice([leyline.directive(0, 100, 140, repl)])
+    torch.cuda.synchronize()
+    cache.check_status()
+    after = H.logical_rows(cache, 0, 777)
+    assert np.array_equal(before, after)
+    cache.close()
+
+
+def test_contiguous_4k_workload():
+    w = configs.contiguous_4k()
+    cache = H.make_cache(w)
+    c = H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0])
+    assert c["stats"]["downstream_slots"] == 2048 and c["stats"]["repl_slots"] == 16
+    cache.close()
+
+
+def test_dsv2_lite_32k_workload_full():
+    """27 layers x 32768 tokens, block 16: every row checked against the oracle."""
+    w = configs.dsv2_lite_32k()
+    cache = H.make_cache(w)
+    c = H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0])
+    st = c["stats"]
+    assert (st["downstream_slots"], st["repl_slots"], st["head_slots"]) == (6768, 12, 0)
+    assert st["algorithmic_bytes"] == 2304 * 27 * (6768 + 12)
+    print("cfg2 rope parity:", {k: v for k, v in c.items() if k != "stats"})
+    cache.close()
