@@ -68,6 +68,7 @@ extern "C" {
 #define LEYLINE_ERR_CUDA (-6)              /* a CUDA runtime call failed */
 #define LEYLINE_ERR_CAPACITY (-7)          /* new length exceeds max_blocks * block_size */
 #define LEYLINE_ERR_DEVICE_CHECK (-8)      /* a device-side bounds check fired (leyline_sync_status) */
+#define LEYLINE_ERR_SCRATCH (-9)           /* plan larger than the static scratch of leyline_splice_noalloc */
 
 /* --------------------------------------------------------------- types ---- */
 typedef struct leyline_pool leyline_pool_t; /* opaque, owned by the library */
@@ -179,6 +180,26 @@ int64_t leyline_free_page_count(const leyline_pool_t* pool);
  * then be considered inconsistent. */
 int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
                    int32_t n, void* stream);
+
+/* The same splice as leyline_splice, for callers that must not allocate device
+ * memory while they run: a serving framework that has reserved nearly all of the
+ * GPU's memory in its own caching allocator (a cudaMalloc behind its back fails
+ * or fragments what it manages), or a process whose device footprint must stay
+ * fixed after start-up.  The paper has no counterpart; this is an interface
+ * variant only.  It makes no device, pinned-host or torch allocation: its
+ * scratch is a static 4 MiB device array that every GPU which loads the library
+ * holds until the process exits, and the plan is staged through a static host
+ * array (the host-side planning itself uses ordinary C++ containers).  The
+ * array's device address is looked up on the first call on each device; make
+ * that first call before any stream capture.  All calls share the array:
+ * calls that overlap on the GPU without ordering (different streams, different
+ * pools) race on it.  Copying the plan from pageable memory may make the call
+ * wait for earlier work on `stream`.  Same arguments, results and error codes
+ * as leyline_splice, plus SCRATCH when the call's plan exceeds 4 MiB (roughly
+ * one million fresh pages, or tens of thousands of directives): split the
+ * directives over several calls. */
+int leyline_splice_noalloc(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
+                           int32_t n, void* stream);
 
 /* Host-only dry run of leyline_splice: validates the directives against
  * seq_lens_host (length num_reqs) and the pool geometry in desc, and reports the

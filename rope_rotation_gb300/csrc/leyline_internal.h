@@ -2,8 +2,11 @@
 // and the kernel launchers.  Not installed; the public surface is include/leyline.h.
 #pragma once
 
+#include <cuda_runtime.h>
+
 #include <cstdint>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "leyline.h"
@@ -72,3 +75,28 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
 int move_rotate_blocks_per_sm(int* blocks);
 
 }  // namespace leyline
+
+// State of one pool (opaque to callers as leyline_pool_t).
+struct leyline_pool {
+    leyline_pool_desc_t desc{};
+    leyline::Geometry g{};
+    void* kv = nullptr;
+    int device = 0;
+    int sm_count = 0;
+    int move_blocks_per_sm = 1;
+    int32_t* d_stack = nullptr;
+    int64_t free_top = 0;
+    int32_t* d_status = nullptr;
+    char* d_plan = nullptr;
+    size_t d_plan_cap = 0;
+    char* h_plan = nullptr;  // pinned
+    size_t h_plan_cap = 0;
+    cudaEvent_t plan_uploaded = nullptr;  // staging buffer reusable once this completes
+    cudaEvent_t done = nullptr;           // last enqueued work of the pool
+    bool has_work = false;
+    cudaStream_t last_stream = nullptr;
+    leyline_stats_t last_stats{};
+    bool timing = false;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;
+    size_t tev_used = 0;
+};

@@ -1,0 +1,180 @@
+// leyline_noalloc.cu -- leyline_splice_noalloc: the splice without any device or
+// pinned-memory allocation.
+//
+// Who needs it.  leyline_splice keeps its per-call plan in a buffer that the pool
+// grows with cudaMalloc / cudaHostAlloc when a call needs more room than any
+// earlier one.  Some callers must never trigger that: a serving process whose
+// framework has already reserved nearly all device memory in its own caching
+// allocator (a cudaMalloc behind its back can fail or fragment the pool it
+// manages), or a process that forbids device allocations after start-up so
+// that its memory footprint stays fixed.  This entry point runs the same three
+// kernels, but its scratch lives in a file-scope static device array of fixed
+// size, and the plan is staged through a static host array.
+//
+// The scratch.  g_splice_scratch holds kNoallocScratchBytes (4 MiB) on every GPU
+// on which this library's device code is loaded, from then until the process
+// exits.  Its device address is looked up once per device with
+// cudaGetSymbolAddress on the first call made on that device (with the device
+// current); make that first call before any stream capture.  Every call shares
+// the array: calls that overlap on the GPU (on different streams, or from
+// different pools, without ordering between them) race on it.  Calls on one pool
+// are ordered by the pool, as for leyline_splice.  Each call writes every byte
+// its kernels read (the uploaded plan, then the trig table and fresh page ids
+// written by the plan kernel), so nothing has to start at zero and what the
+// previous call left behind is never read.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "leyline_internal.h"
+
+using namespace leyline;
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = size_t(4) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_splice_scratch[kNoallocScratchBytes];
+
+// Host staging of the uploaded part of the plan (pageable, static).
+alignas(256) static unsigned char g_host_plan[kNoallocScratchBytes];
+
+std::mutex g_mutex;                     // guards g_host_plan and g_scratch_addr
+void* g_scratch_addr[kMaxDevices] = {};  // device address of g_splice_scratch, per device
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    char msg[256];
+    snprintf(msg, sizeof msg, "%s: %s", what, cudaGetErrorString(e));
+    return set_error(LEYLINE_ERR_CUDA, msg);
+}
+
+// Device address of the static scratch on `device` (which must be current).
+int scratch_address(int device, void** out)
+{
+    if (device < 0 || device >= kMaxDevices) return set_error(LEYLINE_ERR_INVALID_ARG, "device ordinal too large");
+    if (!g_scratch_addr[device]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_splice_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "looking up the static splice scratch");
+        g_scratch_addr[device] = ptr;
+    }
+    *out = g_scratch_addr[device];
+    return LEYLINE_OK;
+}
+
+}  // namespace
+
+extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_directive_t* dirs,
+                                      int32_t n, void* stream_v)
+{
+    clear_error();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    if (!bt || !bt->table || !bt->seq_lens_dev || !bt->seq_lens_host || bt->num_reqs < 0 || bt->max_blocks < 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "incomplete block table");
+    for (int32_t r = 0; r < bt->num_reqs; ++r)
+        if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
+            return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
+    Plan plan;
+    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, p->free_top, &plan);
+    if (rc != LEYLINE_OK) return rc;
+    if (plan.reqs.empty()) {
+        p->last_stats = plan.stats;
+        return LEYLINE_OK;
+    }
+    if (p->free_top - plan.total_pop + plan.total_push > p->g.num_pages)
+        return set_error(LEYLINE_ERR_INVALID_ARG,
+                         "the rewritten requests hold more pages than the pool has free slots for: "
+                         "their tables were not filled from this pool");
+
+    const int half = p->g.rope_dim / 2;
+    const size_t off_reqs = 0;
+    const size_t off_segs = align_up(off_reqs + sizeof(ReqPlan) * plan.reqs.size(), 16);
+    const size_t off_delta = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
+    const size_t upload = align_up(off_delta + sizeof(int64_t) * plan.trig_delta.size(), 16);
+    const size_t off_trig = upload;
+    const size_t off_staged = align_up(off_trig + sizeof(float) * 2 * half * plan.trig_delta.size(), 16);
+    const size_t total = off_staged + sizeof(int32_t) * (size_t)plan.total_pop;
+    if (total > kNoallocScratchBytes) {
+        char msg[256];
+        snprintf(msg, sizeof msg,
+                 "this splice needs %zu bytes of scratch; the static scratch of leyline_splice_noalloc holds %zu "
+                 "(split the directives over several calls, or use leyline_splice)",
+                 total, kNoallocScratchBytes);
+        return set_error(LEYLINE_ERR_SCRATCH, msg);
+    }
+
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(p->device) != cudaSuccess)
+        return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
+    struct Restore {
+        int dev;
+        ~Restore()
+        {
+            if (dev >= 0) cudaSetDevice(dev);
+        }
+    } restore{prev};
+
+    void* scratch_v = nullptr;
+    rc = scratch_address(p->device, &scratch_v);
+    if (rc != LEYLINE_OK) return rc;
+    char* scratch = static_cast<char*>(scratch_v);
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    cudaError_t e;
+    if (p->has_work && p->last_stream != stream) {
+        e = cudaStreamWaitEvent(stream, p->done, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "ordering after the previous splice");
+    }
+    memcpy(g_host_plan + off_reqs, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
+    memcpy(g_host_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
+    if (!plan.trig_delta.empty())
+        memcpy(g_host_plan + off_delta, plan.trig_delta.data(), sizeof(int64_t) * plan.trig_delta.size());
+    // From pageable memory: the copy is staged before the call returns, so the
+    // static host buffer may be reused by the next call.
+    e = cudaMemcpyAsync(scratch, g_host_plan, upload, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "uploading the plan");
+
+    SpliceArgs a{};
+    a.kv = p->kv;
+    a.table = bt->table;
+    a.table_w = bt->table;
+    a.seq_lens_dev = bt->seq_lens_dev;
+    a.free_stack = p->d_stack;
+    a.reqs = reinterpret_cast<const ReqPlan*>(scratch + off_reqs);
+    a.segs = reinterpret_cast<const Seg*>(scratch + off_segs);
+    a.trig_delta = reinterpret_cast<const int64_t*>(scratch + off_delta);
+    a.trig = reinterpret_cast<float*>(scratch + off_trig);
+    a.staged = reinterpret_cast<int32_t*>(scratch + off_staged);
+    a.status = p->d_status;
+    a.pop_top = p->free_top;
+    a.push_base = p->free_top - plan.total_pop;
+    a.total_tiles = plan.total_tiles;
+    a.total_commit = plan.total_commit;
+    a.total_pop = plan.total_pop;
+    a.n_reqs = (int32_t)plan.reqs.size();
+    a.n_trig = (int32_t)plan.trig_delta.size();
+    a.max_blocks = bt->max_blocks;
+    a.g = p->g;
+
+    int err = launch_plan_kernel(a, stream);
+    if (err != 0) return cuda_fail((cudaError_t)err, "launching the plan kernel");
+    err = launch_move_rotate(a, p->sm_count * p->move_blocks_per_sm, stream);
+    if (err != 0) return cuda_fail((cudaError_t)err, "launching the move+rotate kernel");
+    err = launch_commit(a, stream);
+    if (err != 0) return cuda_fail((cudaError_t)err, "launching the commit kernel");
+    e = cudaEventRecord(p->done, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "recording completion event");
+    p->has_work = true;
+    p->last_stream = stream;
+
+    for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
+    p->free_top = p->free_top - plan.total_pop + plan.total_push;
+    p->last_stats = plan.stats;
+    return LEYLINE_OK;
+}

@@ -29,30 +29,6 @@ const char* last_error_cstr();
 
 using namespace leyline;
 
-struct leyline_pool {
-    leyline_pool_desc_t desc{};
-    Geometry g{};
-    void* kv = nullptr;
-    int device = 0;
-    int sm_count = 0;
-    int move_blocks_per_sm = 1;
-    int32_t* d_stack = nullptr;
-    int64_t free_top = 0;
-    int32_t* d_status = nullptr;
-    char* d_plan = nullptr;
-    size_t d_plan_cap = 0;
-    char* h_plan = nullptr;  // pinned
-    size_t h_plan_cap = 0;
-    cudaEvent_t plan_uploaded = nullptr;  // staging buffer reusable once this completes
-    cudaEvent_t done = nullptr;           // last enqueued work of the pool
-    bool has_work = false;
-    cudaStream_t last_stream = nullptr;
-    leyline_stats_t last_stats{};
-    bool timing = false;
-    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;
-    size_t tev_used = 0;
-};
-
 namespace {
 
 struct DeviceGuard {

@@ -27,6 +27,7 @@ LEYLINE_ERR_UNSUPPORTED_MODE = -5
 LEYLINE_ERR_CUDA = -6
 LEYLINE_ERR_CAPACITY = -7
 LEYLINE_ERR_DEVICE_CHECK = -8
+LEYLINE_ERR_SCRATCH = -9
 
 LEYLINE_PAIRS_HALF_SPLIT = 0
 LEYLINE_PAIRS_INTERLEAVED = 1
@@ -79,6 +80,8 @@ _SIGNATURES = {
     "leyline_free_page_count": (ctypes.c_int64, [_vp]),
     "leyline_splice": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(Directive), ctypes.c_int32,
                                       _vp]),
+    "leyline_splice_noalloc": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(Directive),
+                                              ctypes.c_int32, _vp]),
     "leyline_splice_plan": (ctypes.c_int, [ctypes.POINTER(PoolDesc), ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
                                            ctypes.c_int32, ctypes.POINTER(Directive), ctypes.c_int32, ctypes.c_int64,
                                            ctypes.POINTER(Stats), ctypes.POINTER(ctypes.c_int64)]),
@@ -208,6 +211,12 @@ def _dir_array(dirs: Sequence[Directive]):
 def leyline_splice(pool, tables: Tables, dirs: Sequence[Directive], stream=None) -> None:
     arr = _dir_array(dirs)
     _check(load().leyline_splice(pool, ctypes.byref(tables.bt), arr, len(dirs), _stream_ptr(stream)))
+
+
+def leyline_splice_noalloc(pool, tables: Tables, dirs: Sequence[Directive], stream=None) -> None:
+    """leyline_splice with its scratch in the library's static device array (no allocation)."""
+    arr = _dir_array(dirs)
+    _check(load().leyline_splice_noalloc(pool, ctypes.byref(tables.bt), arr, len(dirs), _stream_ptr(stream)))
 
 
 def leyline_splice_plan(desc: PoolDesc, seq_lens_host, max_blocks: int, dirs: Sequence[Directive],

@@ -1,0 +1,87 @@
+"""leyline_splice_noalloc against leyline_splice, through the C ABI (needs a GPU).
+
+leyline_splice_noalloc exists for callers that must not allocate device memory
+while they serve: for example a framework that has reserved nearly all GPU
+memory in its own caching allocator, where a cudaMalloc made behind its back can
+fail or fragment the memory it manages, or a process that keeps its device
+footprint fixed after start-up.  It runs the same kernels with its scratch in a
+static device array instead of a buffer that grows with cudaMalloc.
+
+The test splices two identical caches, one through each entry point, for two
+calls in a row, and checks that the results agree within the tolerance of the
+other splice tests (latents, prefix rows, rows of R and lengths bit-exact; moved
+rope bands within one bf16 step or 2^-16 of the pair norm).  It also checks that
+a call whose plan exceeds the static scratch is refused without changing
+anything.  This file is collected last, so a run stopped at the first failure
+has already run every other test.
+"""
+import numpy as np
+import pytest
+
+import splice_harness as H
+from synth.configs import Dir, Workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import rope_rotation_gb300
+    rope_rotation_gb300.build()
+
+
+def test_noalloc_matches_splice_on_two_calls():
+    from rope_rotation_gb300 import leyline
+    steps = [
+        [Dir(0, 40, 130, 9, 0), Dir(1, 5, 700, 3, 1), Dir(1, 800, 820, 64, 2), Dir(2, 76, 77, 1, 3)],
+        [Dir(0, 0, 3, 0, 4), Dir(1, 100, 101, 30, 5), Dir(2, 10, 50, 2, 6)],
+    ]
+    w = Workload("noalloc", 4, 16, [300, 1000, 77], steps, seed=21)
+    ref = H.make_cache(w, slack_pages=16)
+    new = H.make_cache(w, slack_pages=16)
+    for step in w.steps:
+        dirs_ref, keep_ref = H.gpu_directives(w, step)
+        dirs_new, keep_new = H.gpu_directives(w, step)
+        leyline.leyline_splice(ref.pool, ref.tables, dirs_ref)
+        leyline.leyline_splice_noalloc(new.pool, new.tables, dirs_new)
+        torch.cuda.synchronize()
+        ref.check_status()
+        new.check_status()
+        assert np.array_equal(ref.seq_lens_host, new.seq_lens_host)
+        assert np.array_equal(ref.seq_lens_dev.cpu().numpy(), new.seq_lens_dev.cpu().numpy())
+        assert ref.free_pages() == new.free_pages()
+        assert ref.last_stats() == new.last_stats()
+        for r in range(w.num_reqs):
+            n = int(ref.seq_lens_host[r])
+            a = H.logical_rows(ref, r, n)
+            b = H.logical_rows(new, r, n)
+            lat = w.latent_dim
+            assert np.array_equal(a[:, :, :lat], b[:, :, :lat])
+            H.compare_kpe(b[:, :, lat:].reshape(-1, w.rope_dim), a[:, :, lat:].reshape(-1, w.rope_dim), 0)
+        del keep_ref, keep_new
+    ref.close()
+    new.close()
+
+
+def test_noalloc_refuses_a_plan_larger_than_its_scratch():
+    """Block size 1 and a 1.1M-token request: rewriting it needs 1.1M fresh page ids,
+    more than the 4 MiB static scratch holds."""
+    from rope_rotation_gb300 import leyline
+    from rope_rotation_gb300.runtime import PagedCache
+    L = 1_100_000
+    cache = PagedCache(1, 1, 2 * L + 8, 1, L + 8)
+    cache.add_request(0, L)
+    torch.cuda.synchronize()
+    before = cache.table[0, :8].cpu().numpy().copy()
+    free = cache.free_pages()
+    with pytest.raises(leyline.LeylineError) as ei:
+        leyline.leyline_splice_noalloc(cache.pool, cache.tables, [leyline.directive(0, 0, 1, None)])
+    assert ei.value.code == leyline.LEYLINE_ERR_SCRATCH
+    assert "scratch" in str(ei.value)
+    assert int(cache.seq_lens_host[0]) == L and cache.free_pages() == free
+    assert np.array_equal(cache.table[0, :8].cpu().numpy(), before)
+    cache.close()
