@@ -172,8 +172,10 @@ int64_t leyline_free_page_count(const leyline_pool_t* pool);
  * accumulated Delta in fp32, storing bf16.  Directives with s_start == s_end and
  * n_repl == 0 are no-ops.  On return the work is enqueued on `stream`, the
  * seq_lens_host entries hold the new lengths and the pages are accounted; the
- * table and seq_lens_dev change when the enqueued work runs.  Enqueues at most
- * three kernels and one host-to-device copy of the plan (a few KB).
+ * table and seq_lens_dev change when the enqueued work runs.  Enqueues two
+ * kernels (move+rotate, then commit).  The plan travels as a kernel parameter
+ * when it has at most 8 requests, 24 segments and 10 rotated segments;
+ * otherwise it is uploaded first with one host-to-device copy.
  * Errors (nothing is enqueued or changed): INVALID_ARG, INVALID_DIRECTIVE,
  * OVERLAP, UNSUPPORTED_MODE (FORGET: the caller re-prefills, section 2.1),
  * CAPACITY, NO_PAGES.  CUDA: a launch failed after validation; the pool must
@@ -195,9 +197,9 @@ int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leylin
  * calls that overlap on the GPU without ordering (different streams, different
  * pools) race on it.  Copying the plan from pageable memory may make the call
  * wait for earlier work on `stream`.  Same arguments, results and error codes
- * as leyline_splice, plus SCRATCH when the call's plan exceeds 4 MiB (roughly
- * one million fresh pages, or tens of thousands of directives): split the
- * directives over several calls. */
+ * as leyline_splice, plus SCRATCH when the call's plan exceeds 4 MiB (with a
+ * 64-wide rope band, about 12,000 directives that shift their downstream
+ * rows): split the directives over several calls. */
 int leyline_splice_noalloc(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
                            int32_t n, void* stream);
 

@@ -25,11 +25,12 @@ int make_geometry(const leyline_pool_desc_t* desc, Geometry* g);
 struct Plan {
     std::vector<ReqPlan> reqs;
     std::vector<Seg> segs;
-    std::vector<int64_t> trig_delta;  // accumulated Delta of every ROT segment
-    int64_t total_tiles = 0;          // move+rotate tiles over all requests
-    int64_t total_commit = 0;         // commit work items over all requests
-    int64_t total_pop = 0;            // fresh pages
-    int64_t total_push = 0;           // pages returned
+    std::vector<float> trig;  // per ROT segment: rope_dim / 2 pairs of (cos, sin) of Delta * theta_j
+    int32_t n_trig = 0;       // ROT segments
+    int64_t total_tiles = 0;  // move+rotate tiles over all requests
+    int64_t total_commit = 0; // commit work items over all requests
+    int64_t total_pop = 0;    // fresh pages
+    int64_t total_push = 0;   // pages returned
     leyline_stats_t stats{};
 };
 
@@ -39,24 +40,35 @@ struct Plan {
 int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs, int32_t max_blocks,
                const leyline_directive_t* dirs, int32_t n, int64_t free_pages, Plan* plan);
 
+// A plan small enough to travel as a kernel parameter (__grid_constant__): no
+// host-to-device copy and no plan buffer on the path.
+constexpr int kParamReqs = 8;
+constexpr int kParamSegs = 24;
+constexpr int kParamTrigFloats = 640;  // 10 rotated segments of a 64-wide rope band
+struct ParamPlan {
+    ReqPlan reqs[kParamReqs];
+    Seg segs[kParamSegs];
+    float trig[kParamTrigFloats];
+};
+bool plan_fits_params(const Plan& plan);
+void pack_param_plan(const Plan& plan, ParamPlan* pp);
+
 // Kernel arguments (passed by value).
 struct SpliceArgs {
-    void* kv;                      // pool base
-    const int32_t* table;          // [num_reqs][max_blocks], read by the move+rotate kernel
-    int32_t* table_w;              // same table, written by the commit kernel
+    void* kv;                 // pool base
+    const int32_t* table;     // [num_reqs][max_blocks], read by the move+rotate kernel
+    int32_t* table_w;         // same table, written by the commit kernel
     int32_t* seq_lens_dev;
-    int32_t* free_stack;           // [num_pages]
-    const ReqPlan* reqs;
+    int32_t* free_q;          // free-page ring, q_cap entries
+    int64_t q_cap;
+    int64_t pop_base;         // ring position of the first page this call takes (mod q_cap)
+    int64_t push_base;        // ring position of the first page this call returns (mod q_cap)
+    const ReqPlan* reqs;      // plan in device memory (when it is not a kernel parameter)
     const Seg* segs;
-    const int64_t* trig_delta;
-    float* trig;                   // [n_trig][rope_dim / 2][2] (cos, sin)
-    int32_t* staged;               // [total_pop] fresh page ids in pop order
-    int32_t* status;               // device status word
-    int64_t pop_top;               // free-stack top before the call
-    int64_t push_base;             // pop_top - total_pop
+    const float* trig;
+    int32_t* status;          // device status word
     int64_t total_tiles;
     int64_t total_commit;
-    int64_t total_pop;
     int32_t n_reqs;
     int32_t n_trig;
     int32_t max_blocks;
@@ -64,11 +76,13 @@ struct SpliceArgs {
     Geometry g;
 };
 
-// Launchers (leyline_kernels.cu).  Each returns the cudaError_t of the launch as int.
-int launch_init_stack(int32_t* stack, int64_t num_pages, void* stream);
-int launch_plan_kernel(const SpliceArgs& a, void* stream);
-int launch_move_rotate(const SpliceArgs& a, int grid, void* stream);
-int launch_commit(const SpliceArgs& a, void* stream);
+// Launchers (leyline_kernels.cu).  Each returns the cudaError_t of the launches as int.
+int launch_init_queue(int32_t* q, int64_t num_pages, void* stream);
+// Enqueue move+rotate then commit.  pp != nullptr: the plan travels in pp (a.reqs,
+// a.segs, a.trig unused); else it is read from a.reqs / a.segs / a.trig.  With
+// timing events, they bracket the move+rotate kernel.
+int launch_splice(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stream, cudaEvent_t t0,
+                  cudaEvent_t t1);
 int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
                   int64_t t1, void* out, int32_t* status, void* stream);
 // Resident CTAs per SM of the move+rotate kernel (occupancy query).
@@ -84,14 +98,17 @@ struct leyline_pool {
     int device = 0;
     int sm_count = 0;
     int move_blocks_per_sm = 1;
-    int32_t* d_stack = nullptr;
-    int64_t free_top = 0;
+    int32_t* d_queue = nullptr;  // free-page ring, 2 * num_pages entries
+    int64_t q_cap = 0;
+    int64_t q_head = 0;          // monotonic: next page to take is d_queue[q_head % q_cap]
+    int64_t q_tail = 0;          // monotonic: next free slot is d_queue[q_tail % q_cap]
     int32_t* d_status = nullptr;
     char* d_plan = nullptr;
     size_t d_plan_cap = 0;
     char* h_plan = nullptr;  // pinned
     size_t h_plan_cap = 0;
     cudaEvent_t plan_uploaded = nullptr;  // staging buffer reusable once this completes
+    bool uploaded_once = false;
     cudaEvent_t done = nullptr;           // last enqueued work of the pool
     bool has_work = false;
     cudaStream_t last_stream = nullptr;

@@ -8,14 +8,16 @@
 //   section 4.3  the rotation is computed in fp32 and stored in bf16.
 //
 // Kernels of one splice, in stream order:
-//   plan kernel      cos/sin of Delta * theta_j per rotated segment (fp64 angle,
-//                    rounded to fp32) and the fresh page ids popped off the stack;
-//   move+rotate      every rewritten row x layer is read once and written once:
-//                    latent and R rows copied as 16-byte vectors, rope band turned
-//                    in fp32 and rounded to bf16 (the HBM-bound hot loop);
-//   commit           new block-table entries, new lengths, old pages pushed back.
-// The path is bandwidth-bound (about 64 fp32 FMAs per 2304 bytes moved), so it
-// uses no tensor cores: the point is coalesced 16-byte streaming at HBM speed.
+//   move+rotate  every rewritten row x layer is read once and written once into a
+//                fresh page: latent and R rows copied as 16-byte vectors, the rope
+//                band turned in fp32 with the segment's cos/sin and rounded to
+//                bf16 (the HBM-bound hot loop);
+//   commit       new block-table entries, new lengths, old pages returned to the
+//                free-page ring.
+// The commit kernel is launched as a programmatic dependent of move+rotate, so its
+// launch overlaps the move; it waits (griddepcontrol.wait) for the move to finish
+// before it touches the table.  The path is bandwidth-bound (about 64 fp32 FMAs per
+// 2304 bytes moved), so it uses no tensor cores.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,9 +34,14 @@ constexpr int kRowsPerWarp = 2;
 static_assert(kTileRows == (kMoveThreads / 32) * kRowsPerWarp, "tile shape");
 
 // device status bits (leyline_sync_status)
-enum : int32_t { ST_BAD_PAGE = 1, ST_BAD_BLOCK = 2, ST_BAD_FRESH = 4, ST_BAD_OLD = 8, ST_BAD_RANGE = 16 };
+enum : int32_t { ST_BAD_PAGE = 1, ST_BAD_BLOCK = 2, ST_BAD_FRESH = 4, ST_BAD_OLD = 8 };
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bit) { atomicOr(status, bit); }
+
+// Programmatic dependent launch: wait until the preceding kernel in the stream has
+// finished and its writes are visible; allow the next kernel to be launched now.
+__device__ __forceinline__ void wait_for_previous_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // 16-byte streaming load through the non-coherent path, not kept in L1: every
 // source row is read exactly once and is never written during the kernel.
@@ -119,6 +126,28 @@ __device__ __forceinline__ void rotate_interleaved(uint4& v, const float* c, con
     }
 }
 
+// ------------------------------------------------------------- plan access --
+// The plan is either a __grid_constant__ kernel parameter (small plans) or in
+// device memory; both are read through the same three pointers.
+struct NoParamPlan {
+    int32_t unused;
+};
+
+struct PlanView {
+    const ReqPlan* reqs;
+    const Seg* segs;
+    const float* trig;
+};
+
+__device__ __forceinline__ PlanView plan_view(const SpliceArgs&, const ParamPlan& p)
+{
+    return PlanView{p.reqs, p.segs, p.trig};
+}
+__device__ __forceinline__ PlanView plan_view(const SpliceArgs& a, const NoParamPlan&)
+{
+    return PlanView{a.reqs, a.segs, a.trig};
+}
+
 // Where one destination row of a tile comes from and goes to (layer 0).
 struct RowDesc {
     const uint4* src;       // nullptr: row is not written
@@ -128,28 +157,31 @@ struct RowDesc {
     int pad;
 };
 
-__device__ __forceinline__ int find_req_by_tile(const SpliceArgs& a, long long tile)
+__device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v, bool by_tile)
 {
-    int lo = 0, hi = a.n_reqs - 1;
+    int lo = 0, hi = n - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (a.reqs[mid].tile_begin <= tile) lo = mid;
+        const long long key = by_tile ? reqs[mid].tile_begin : reqs[mid].commit_begin;
+        if (key <= v) lo = mid;
         else hi = mid - 1;
     }
     return lo;
 }
 
+__device__ __forceinline__ long long ring(long long i, long long cap) { return i % cap; }
+
 // Slot map of destination row i of a tile: segment lookup, then the source row
 // through the old block table (or the rows of R), the destination row in its
 // fresh page.  Every page id and block index is checked; a bad one is recorded
 // in the status word and the row is skipped.
-__device__ RowDesc make_desc(const SpliceArgs& a, long long tile, int i)
+__device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long tile, int i)
 {
     RowDesc d{nullptr, nullptr, 0, -1, 0};
-    const ReqPlan& rp = a.reqs[find_req_by_tile(a, tile)];
+    const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, true)];
     const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + i;
     if (p >= rp.new_len) return d;
-    const Seg* sg = a.segs + rp.seg_begin;
+    const Seg* sg = pv.segs + rp.seg_begin;
     int k = 0;
     for (int q = 1; q < rp.seg_count; ++q)
         if (sg[q].new_start <= p) k = q;
@@ -181,7 +213,7 @@ __device__ RowDesc make_desc(const SpliceArgs& a, long long tile, int i)
         if (s.kind == SEG_ROT) trig = s.trig;
     }
     const long long dblk = p / B;
-    const int fresh = a.staged[rp.pop_off + (dblk - rp.b0)];
+    const int fresh = a.free_q[ring(a.pop_base + rp.pop_off + (dblk - rp.b0), a.q_cap)];
     if (fresh < 0 || fresh >= a.g.num_pages) {
         raise_status(a.status, ST_BAD_FRESH);
         return d;
@@ -209,16 +241,19 @@ __device__ __forceinline__ void my_units(long long units, long long& u0, long lo
 // owns rows 2w and 2w+1: each lane moves 4 latent vectors (a warp instruction
 // covers 512 contiguous bytes), and 8 (half-split) or 16 (interleaved) lanes
 // move the rope band with the pair's cos/sin held in registers.
-template <int kLatentVecs, int kRopeVecs, int kLayout, bool kBf16>
-__global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const SpliceArgs a, long long units)
+template <int kLayout, bool kBf16, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const __grid_constant__ SpliceArgs a,
+                                                                const __grid_constant__ PlanSrc plan)
 {
-    static_assert(kLatentVecs == 64 && kRopeVecs == 8, "MLA shape");
+    constexpr int kLatentVecs = 64, kRopeVecs = 8;
     __shared__ RowDesc desc[kTileRows];
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = a.g.num_layers;
+    const long long L = a.g.num_layers;
     const long long layer_vecs = a.g.layer_vecs;
     const int half = 4 * kRopeVecs;  // pairs per row
-    // rope role of this lane
     constexpr int kRopeLanesPerRow = kLayout == 0 ? kRopeVecs / 2 : kRopeVecs;  // 4 or 8
     const bool rope_lane = lane < kRowsPerWarp * kRopeLanesPerRow;
     const int rope_row = warp * kRowsPerWarp + lane / kRopeLanesPerRow;
@@ -227,49 +262,46 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const SpliceArgs
     int trig = -1;
 
     long long u0, u1;
-    my_units(units, u0, u1);
+    my_units(a.total_tiles * L, u0, u1);
     long long cur_tile = -1;
     for (long long u = u0; u < u1; ++u) {
         const long long tile = u / L;
         const long long layer = u - tile * L;
         if (tile != cur_tile) {
             __syncthreads();
-            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, tile, threadIdx.x);
+            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, pv, tile, threadIdx.x);
             __syncthreads();
             cur_tile = tile;
             trig = rope_lane ? desc[rope_row].trig : -1;
             if (trig >= 0) {
                 // pairs covered by this lane: 8 (half-split) or 4 (interleaved)
                 const int j0 = kLayout == 0 ? 8 * rope_q : 4 * rope_q;
-                const float4* tp = reinterpret_cast<const float4*>(a.trig + 2 * ((long long)trig * half + j0));
+                const float* tp = pv.trig + 2 * ((long long)trig * half + j0);
 #pragma unroll
-                for (int w = 0; w < (kLayout == 0 ? 4 : 2); ++w) {
-                    const float4 v = tp[w];
-                    cs[2 * w] = v.x;
-                    sn[2 * w] = v.y;
-                    cs[2 * w + 1] = v.z;
-                    sn[2 * w + 1] = v.w;
+                for (int w = 0; w < (kLayout == 0 ? 8 : 4); ++w) {
+                    cs[w] = tp[2 * w];
+                    sn[w] = tp[2 * w + 1];
                 }
             }
         }
         const RowDesc d0 = desc[warp * kRowsPerWarp];
         const RowDesc d1 = desc[warp * kRowsPerWarp + 1];
         uint4 v[4];
-        const uint4* s0 = d0.src + layer * d0.src_lstride;
-        const uint4* s1 = d1.src + layer * d1.src_lstride;
         if (d0.src) {
+            const uint4* s0 = d0.src + layer * d0.src_lstride;
             v[0] = ld_stream(s0 + lane);
             v[1] = ld_stream(s0 + lane + 32);
         }
         if (d1.src) {
+            const uint4* s1 = d1.src + layer * d1.src_lstride;
             v[2] = ld_stream(s1 + lane);
             v[3] = ld_stream(s1 + lane + 32);
         }
         const RowDesc dr = rope_lane ? desc[rope_row] : d0;
         const bool do_rope = rope_lane && dr.src != nullptr;
         uint4 rx, ry;
-        const uint4* rs = dr.src + layer * dr.src_lstride + kLatentVecs;
         if (do_rope) {
+            const uint4* rs = dr.src + layer * dr.src_lstride + kLatentVecs;
             rx = ld_stream(rs + rope_q);
             if (kLayout == 0) ry = ld_stream(rs + rope_q + kRopeVecs / 2);
         }
@@ -300,23 +332,27 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const SpliceArgs
 // -------------------------------------------------------------------------
 // Move+rotate for any latent_dim (multiple of 8) and rope_dim (multiple of 16):
 // the same slot map, with plain strided loops over the vectors of the tile.
-template <bool kBf16>
-__global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const SpliceArgs a, long long units)
+template <bool kBf16, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const __grid_constant__ SpliceArgs a,
+                                                                    const __grid_constant__ PlanSrc plan)
 {
     __shared__ RowDesc desc[kTileRows];
-    const int L = a.g.num_layers;
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const long long L = a.g.num_layers;
     const int lv = a.g.latent_vecs, rvv = a.g.rope_vecs, half = a.g.rope_dim / 2;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
     const int rope_items = split ? rvv / 2 : rvv;
     long long u0, u1;
-    my_units(units, u0, u1);
+    my_units(a.total_tiles * L, u0, u1);
     long long cur_tile = -1;
     for (long long u = u0; u < u1; ++u) {
         const long long tile = u / L;
         const long long layer = u - tile * L;
         if (tile != cur_tile) {
             __syncthreads();
-            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, tile, threadIdx.x);
+            if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, pv, tile, threadIdx.x);
             __syncthreads();
             cur_tile = tile;
         }
@@ -337,8 +373,8 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const Splice
             const int np = split ? 8 : 4;
             if (d.trig >= 0) {
                 for (int w = 0; w < np; ++w) {
-                    cs[w] = a.trig[2 * ((long long)d.trig * half + j0 + w)];
-                    sn[w] = a.trig[2 * ((long long)d.trig * half + j0 + w) + 1];
+                    cs[w] = pv.trig[2 * ((long long)d.trig * half + j0 + w)];
+                    sn[w] = pv.trig[2 * ((long long)d.trig * half + j0 + w) + 1];
                 }
             }
             if (split) {
@@ -356,89 +392,43 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const Splice
 }
 
 // -------------------------------------------------------------------------
-// Plan kernel: cos/sin of Delta * theta_j for every rotated segment, and the
-// fresh page ids (the i-th page taken is stack[pop_top - 1 - i]).
-// The angle is formed and reduced in fp64: Delta * theta_0 reaches 1e5 rad, where
-// an fp32 angle would be off by ~1e-2 rad, more than a bf16 step.
-__global__ void plan_kernel(const SpliceArgs a)
-{
-    const int half = a.g.rope_dim / 2;
-    const long long n_trig = (long long)a.n_trig * half;
-    const long long n = n_trig > a.total_pop ? n_trig : a.total_pop;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-         i += (long long)gridDim.x * blockDim.x) {
-        if (i < n_trig) {
-            const long long t = i / half;
-            const int j = (int)(i - t * half);
-            const double theta_j = pow(a.g.theta, -2.0 * (double)j / (double)a.g.rope_dim);
-            const double phi = (double)a.trig_delta[t] * theta_j;
-            double s, c;
-            sincos(phi, &s, &c);
-            float cf, sf;
-            if (a.g.precision == LEYLINE_ROTATE_BF16_NAIVE) {
-                cf = __bfloat162float(__double2bfloat16(c));
-                sf = __bfloat162float(__double2bfloat16(s));
-            } else {
-                cf = (float)c;
-                sf = (float)s;
-            }
-            a.trig[2 * i] = cf;
-            a.trig[2 * i + 1] = sf;
-        }
-        if (i < a.total_pop) {
-            int page = a.free_stack[a.pop_top - 1 - i];
-            if (page < 0 || page >= a.g.num_pages) {
-                raise_status(a.status, ST_BAD_FRESH);
-                page = -1;
-            }
-            a.staged[i] = page;
-        }
-    }
-}
-
-__device__ __forceinline__ int find_req_by_commit(const SpliceArgs& a, long long i)
-{
-    int lo = 0, hi = a.n_reqs - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.reqs[mid].commit_begin <= i) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
 // Commit: block-table entries [b0, b0 + n_new) take the fresh pages, entries
 // [b0 + n_new, b0 + n_old) become -1, the old pages of [b0, b0 + n_old) go back
-// onto the free stack, and seq_lens_dev takes the new length.  One thread owns
-// one table entry, so reading the old id and writing the new one cannot race.
-__global__ void commit_kernel(const SpliceArgs a)
+// onto the free-page ring, and seq_lens_dev takes the new length.  One thread
+// owns one table entry, so reading the old id and writing the new one cannot
+// race; the pages taken ([pop_base, +total_pop) of the ring) and the slots
+// written ([push_base, +total_push)) never overlap.
+template <class PlanSrc>
+__global__ void commit_kernel(const __grid_constant__ SpliceArgs a, const __grid_constant__ PlanSrc plan)
 {
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_commit;
          i += (long long)gridDim.x * blockDim.x) {
-        const ReqPlan& rp = a.reqs[find_req_by_commit(a, i)];
+        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, i, false)];
         const long long k = i - rp.commit_begin;
         int32_t* row = a.table_w + (long long)rp.req * a.max_blocks + rp.b0;
         if (k == 0) a.seq_lens_dev[rp.req] = (int32_t)rp.new_len;
         int old = -1;
         if (k < rp.n_old) old = row[k];
-        if (k < rp.n_new) row[k] = a.staged[rp.pop_off + k];
+        if (k < rp.n_new) row[k] = a.free_q[ring(a.pop_base + rp.pop_off + k, a.q_cap)];
         else if (k < rp.n_old) row[k] = -1;
         if (k < rp.n_old) {
-            const long long slot = a.push_base + rp.push_off + k;
             if (old < 0 || old >= a.g.num_pages) {
                 raise_status(a.status, ST_BAD_OLD);
                 old = -1;
             }
-            if (slot < a.g.num_pages) a.free_stack[slot] = old;
-            else raise_status(a.status, ST_BAD_RANGE);
+            a.free_q[ring(a.push_base + rp.push_off + k, a.q_cap)] = old;
         }
     }
 }
 
-__global__ void init_stack_kernel(int32_t* stack, long long n)
+__global__ void init_queue_kernel(int32_t* q, long long num_pages)
 {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-        stack[i] = (int32_t)(n - 1 - i);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * num_pages;
+         i += (long long)gridDim.x * blockDim.x)
+        q[i] = i < num_pages ? (int32_t)i : -1;
 }
 
 // Gather logical rows [t0, t1) of one request and layer into a contiguous buffer.
@@ -470,49 +460,68 @@ int grid_for(long long items, int threads, int cap)
 
 bool mla_shape(const Geometry& g) { return g.latent_vecs == 64 && g.rope_vecs == 8; }
 
-}  // namespace
-
-int launch_init_stack(int32_t* stack, int64_t num_pages, void* stream)
+// Launch with programmatic stream serialization: the kernel may start before the
+// previous kernel in the stream ends; it calls griddepcontrol.wait before it
+// reads anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, cudaStream_t s, Args... args)
 {
-    init_stack_kernel<<<grid_for(num_pages, 256, 4096), 256, 0, (cudaStream_t)stream>>>(stack, num_pages);
-    return (int)cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-int launch_plan_kernel(const SpliceArgs& a, void* stream)
+template <class PlanSrc>
+cudaError_t launch_move(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s)
 {
-    const long long items = std::max<long long>((long long)a.n_trig * (a.g.rope_dim / 2), a.total_pop);
-    if (items == 0) return 0;
-    plan_kernel<<<grid_for(items, 256, 2048), 256, 0, (cudaStream_t)stream>>>(a);
-    return (int)cudaGetLastError();
-}
-
-int launch_move_rotate(const SpliceArgs& a, int grid, void* stream)
-{
-    const long long units = a.total_tiles * a.g.num_layers;
-    if (units == 0) return 0;
-    if ((long long)grid > units) grid = (int)units;
-    cudaStream_t s = (cudaStream_t)stream;
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     if (mla_shape(a.g)) {
-        if (a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT) {
-            if (bf16) move_rotate_mla<64, 8, 0, true><<<grid, kMoveThreads, 0, s>>>(a, units);
-            else move_rotate_mla<64, 8, 0, false><<<grid, kMoveThreads, 0, s>>>(a, units);
-        } else {
-            if (bf16) move_rotate_mla<64, 8, 1, true><<<grid, kMoveThreads, 0, s>>>(a, units);
-            else move_rotate_mla<64, 8, 1, false><<<grid, kMoveThreads, 0, s>>>(a, units);
-        }
-    } else {
-        if (bf16) move_rotate_generic<true><<<grid, kMoveThreads, 0, s>>>(a, units);
-        else move_rotate_generic<false><<<grid, kMoveThreads, 0, s>>>(a, units);
+        if (a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT)
+            return bf16 ? launch_dependent(move_rotate_mla<0, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                        : launch_dependent(move_rotate_mla<0, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+        return bf16 ? launch_dependent(move_rotate_mla<1, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                    : launch_dependent(move_rotate_mla<1, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
     }
+    return bf16 ? launch_dependent(move_rotate_generic<true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                : launch_dependent(move_rotate_generic<false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+}
+
+template <class PlanSrc>
+int launch_both(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s, cudaEvent_t t0, cudaEvent_t t1)
+{
+    const long long units = a.total_tiles * a.g.num_layers;
+    if (grid > units) grid = (int)std::max<long long>(units, 1);
+    cudaError_t e = cudaSuccess;
+    if (t0) e = cudaEventRecord(t0, s);
+    if (e == cudaSuccess && units > 0) e = launch_move(a, plan, grid, s);
+    if (e == cudaSuccess && t1) e = cudaEventRecord(t1, s);
+    if (e == cudaSuccess && a.total_commit > 0)
+        e = launch_dependent(commit_kernel<PlanSrc>, grid_for(a.total_commit, 256, 4096), 256, s, a, plan);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return (int)e;
+}
+
+}  // namespace
+
+int launch_init_queue(int32_t* q, int64_t num_pages, void* stream)
+{
+    init_queue_kernel<<<grid_for(2 * num_pages, 256, 4096), 256, 0, (cudaStream_t)stream>>>(q, num_pages);
     return (int)cudaGetLastError();
 }
 
-int launch_commit(const SpliceArgs& a, void* stream)
+int launch_splice(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stream, cudaEvent_t t0, cudaEvent_t t1)
 {
-    if (a.total_commit == 0) return 0;
-    commit_kernel<<<grid_for(a.total_commit, 256, 4096), 256, 0, (cudaStream_t)stream>>>(a);
-    return (int)cudaGetLastError();
+    cudaStream_t s = (cudaStream_t)stream;
+    if (pp) return launch_both(a, *pp, grid, s, t0, t1);
+    return launch_both(a, NoParamPlan{0}, grid, s, t0, t1);
 }
 
 int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
@@ -528,7 +537,7 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
 
 int move_rotate_blocks_per_sm(int* blocks)
 {
-    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, move_rotate_mla<64, 8, 0, false>,
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, move_rotate_mla<0, false, ParamPlan>,
                                                               kMoveThreads, 0);
 }
 

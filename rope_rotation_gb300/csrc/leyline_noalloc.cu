@@ -7,7 +7,7 @@
 // framework has already reserved nearly all device memory in its own caching
 // allocator (a cudaMalloc behind its back can fail or fragment the pool it
 // manages), or a process that forbids device allocations after start-up so
-// that its memory footprint stays fixed.  This entry point runs the same three
+// that its memory footprint stays fixed.  This entry point runs the same
 // kernels, but its scratch lives in a file-scope static device array of fixed
 // size, and the plan is staged through a static host array.
 //
@@ -19,9 +19,8 @@
 // the array: calls that overlap on the GPU (on different streams, or from
 // different pools, without ordering between them) race on it.  Calls on one pool
 // are ordered by the pool, as for leyline_splice.  Each call writes every byte
-// its kernels read (the uploaded plan, then the trig table and fresh page ids
-// written by the plan kernel), so nothing has to start at zero and what the
-// previous call left behind is never read.
+// its kernels read (the uploaded plan), so nothing has to start at zero and what
+// the previous call left behind is never read.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -81,25 +80,22 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
         if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
             return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
     Plan plan;
-    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, p->free_top, &plan);
+    const int64_t free_now = p->q_tail - p->q_head;
+    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
         return LEYLINE_OK;
     }
-    if (p->free_top - plan.total_pop + plan.total_push > p->g.num_pages)
+    if (free_now - plan.total_pop + plan.total_push > p->g.num_pages)
         return set_error(LEYLINE_ERR_INVALID_ARG,
                          "the rewritten requests hold more pages than the pool has free slots for: "
                          "their tables were not filled from this pool");
 
-    const int half = p->g.rope_dim / 2;
-    const size_t off_reqs = 0;
-    const size_t off_segs = align_up(off_reqs + sizeof(ReqPlan) * plan.reqs.size(), 16);
-    const size_t off_delta = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
-    const size_t upload = align_up(off_delta + sizeof(int64_t) * plan.trig_delta.size(), 16);
-    const size_t off_trig = upload;
-    const size_t off_staged = align_up(off_trig + sizeof(float) * 2 * half * plan.trig_delta.size(), 16);
-    const size_t total = off_staged + sizeof(int32_t) * (size_t)plan.total_pop;
+    // scratch layout: reqs | segs | trig (cos, sin per pair of every rotated segment)
+    const size_t off_segs = align_up(sizeof(ReqPlan) * plan.reqs.size(), 16);
+    const size_t off_trig = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
+    const size_t total = off_trig + sizeof(float) * plan.trig.size();
     if (total > kNoallocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
@@ -131,13 +127,12 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
         e = cudaStreamWaitEvent(stream, p->done, 0);
         if (e != cudaSuccess) return cuda_fail(e, "ordering after the previous splice");
     }
-    memcpy(g_host_plan + off_reqs, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
+    memcpy(g_host_plan, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
     memcpy(g_host_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
-    if (!plan.trig_delta.empty())
-        memcpy(g_host_plan + off_delta, plan.trig_delta.data(), sizeof(int64_t) * plan.trig_delta.size());
+    if (!plan.trig.empty()) memcpy(g_host_plan + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
     // From pageable memory: the copy is staged before the call returns, so the
     // static host buffer may be reused by the next call.
-    e = cudaMemcpyAsync(scratch, g_host_plan, upload, cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyAsync(scratch, g_host_plan, total, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "uploading the plan");
 
     SpliceArgs a{};
@@ -145,36 +140,31 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.table = bt->table;
     a.table_w = bt->table;
     a.seq_lens_dev = bt->seq_lens_dev;
-    a.free_stack = p->d_stack;
-    a.reqs = reinterpret_cast<const ReqPlan*>(scratch + off_reqs);
+    a.free_q = p->d_queue;
+    a.q_cap = p->q_cap;
+    a.pop_base = p->q_head;
+    a.push_base = p->q_tail;
+    a.reqs = reinterpret_cast<const ReqPlan*>(scratch);
     a.segs = reinterpret_cast<const Seg*>(scratch + off_segs);
-    a.trig_delta = reinterpret_cast<const int64_t*>(scratch + off_delta);
-    a.trig = reinterpret_cast<float*>(scratch + off_trig);
-    a.staged = reinterpret_cast<int32_t*>(scratch + off_staged);
+    a.trig = reinterpret_cast<const float*>(scratch + off_trig);
     a.status = p->d_status;
-    a.pop_top = p->free_top;
-    a.push_base = p->free_top - plan.total_pop;
     a.total_tiles = plan.total_tiles;
     a.total_commit = plan.total_commit;
-    a.total_pop = plan.total_pop;
     a.n_reqs = (int32_t)plan.reqs.size();
-    a.n_trig = (int32_t)plan.trig_delta.size();
+    a.n_trig = plan.n_trig;
     a.max_blocks = bt->max_blocks;
     a.g = p->g;
 
-    int err = launch_plan_kernel(a, stream);
-    if (err != 0) return cuda_fail((cudaError_t)err, "launching the plan kernel");
-    err = launch_move_rotate(a, p->sm_count * p->move_blocks_per_sm, stream);
-    if (err != 0) return cuda_fail((cudaError_t)err, "launching the move+rotate kernel");
-    err = launch_commit(a, stream);
-    if (err != 0) return cuda_fail((cudaError_t)err, "launching the commit kernel");
+    int err = launch_splice(a, nullptr, p->sm_count * p->move_blocks_per_sm, stream, nullptr, nullptr);
+    if (err != 0) return cuda_fail((cudaError_t)err, "launching the splice kernels");
     e = cudaEventRecord(p->done, stream);
     if (e != cudaSuccess) return cuda_fail(e, "recording completion event");
     p->has_work = true;
     p->last_stream = stream;
 
     for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
-    p->free_top = p->free_top - plan.total_pop + plan.total_push;
+    p->q_head += plan.total_pop;
+    p->q_tail += plan.total_push;
     p->last_stats = plan.stats;
     return LEYLINE_OK;
 }

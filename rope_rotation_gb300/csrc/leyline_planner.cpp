@@ -13,6 +13,7 @@
 // This equals applying the directives one at a time, right to left.
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 
@@ -24,6 +25,52 @@ namespace {
 thread_local std::string g_last_error;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Nearest bf16 value (ties to even) of a double, returned as the float it
+// denotes: the significand is cut to 8 bits straight from the double's bit
+// pattern, so the value is rounded once (not through float first).
+float bf16_nearest(double x)
+{
+    uint64_t b;
+    std::memcpy(&b, &x, sizeof b);
+    const bool neg = (b >> 63) != 0;
+    const int exp = (int)((b >> 52) & 0x7FF);
+    if (exp == 0x7FF) return (float)x;
+    if (exp == 0) return neg ? -0.0f : 0.0f;
+    const int E = exp - 1023;  // |x| in [2^E, 2^(E+1))
+    double r;
+    if (E >= -126) {
+        const uint64_t mant = (b & ((uint64_t(1) << 52) - 1)) | (uint64_t(1) << 52);
+        uint64_t q = mant >> 45;
+        const uint64_t rem = mant & ((uint64_t(1) << 45) - 1), half = uint64_t(1) << 44;
+        if (rem > half || (rem == half && (q & 1))) ++q;
+        r = std::ldexp((double)q, E - 7);
+    } else {  // bf16 subnormal range: steps of 2^-133
+        r = std::ldexp(std::nearbyint(std::ldexp(std::fabs(x), 133)), -133);
+    }
+    return neg ? -(float)r : (float)r;
+}
+
+// cos / sin of Delta * theta_j for every pair j of a rotated segment.  The angle is
+// formed in fp64 (Delta * theta_0 reaches 1e5 rad, where an fp32 angle would be off
+// by ~1e-2 rad, more than a bf16 step), the library's cos / sin reduce it exactly,
+// and the result is rounded once to the arithmetic of the rotation.
+void segment_trig(const Geometry& g, int64_t delta, float* out)
+{
+    const int half = g.rope_dim / 2;
+    for (int j = 0; j < half; ++j) {
+        const double theta_j = std::pow(g.theta, -2.0 * (double)j / (double)g.rope_dim);
+        const double phi = (double)delta * theta_j;
+        const double c = std::cos(phi), s = std::sin(phi);
+        if (g.precision == LEYLINE_ROTATE_BF16_NAIVE) {
+            out[2 * j] = bf16_nearest(c);
+            out[2 * j + 1] = bf16_nearest(s);
+        } else {
+            out[2 * j] = (float)c;
+            out[2 * j + 1] = (float)s;
+        }
+    }
+}
 }  // namespace
 
 int set_error(int code, const std::string& msg)
@@ -190,8 +237,9 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             if (run_end > d->s_end) {
                 Seg s{d->s_end + D, d->s_end, nullptr, D == 0 ? SEG_COPY : SEG_ROT, -1, 0, 0};
                 if (D != 0) {
-                    s.trig = (int32_t)plan->trig_delta.size();
-                    plan->trig_delta.push_back(D);
+                    s.trig = plan->n_trig++;
+                    plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
+                    segment_trig(g, D, plan->trig.data() + (size_t)s.trig * g.rope_dim);
                 }
                 plan->segs.push_back(s);
                 st.downstream_slots += run_end - d->s_end;
@@ -225,8 +273,22 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     st.pages_popped = pops;
     st.pages_pushed = pushes;
     st.requests_touched = (int32_t)plan->reqs.size();
-    st.kernels_launched = plan->reqs.empty() ? 0 : 3;
+    st.kernels_launched = plan->reqs.empty() ? 0 : 2;
     return LEYLINE_OK;
+}
+
+bool plan_fits_params(const Plan& plan)
+{
+    return plan.reqs.size() <= (size_t)kParamReqs && plan.segs.size() <= (size_t)kParamSegs &&
+           plan.trig.size() <= (size_t)kParamTrigFloats;
+}
+
+void pack_param_plan(const Plan& plan, ParamPlan* pp)
+{
+    std::memset(pp, 0, sizeof *pp);
+    std::copy(plan.reqs.begin(), plan.reqs.end(), pp->reqs);
+    std::copy(plan.segs.begin(), plan.segs.end(), pp->segs);
+    std::copy(plan.trig.begin(), plan.trig.end(), pp->trig);
 }
 
 }  // namespace leyline

@@ -107,12 +107,13 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
     cudaError_t e = cudaGetDevice(&p->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device);
     if (e == cudaSuccess) e = (cudaError_t)move_rotate_blocks_per_sm(&p->move_blocks_per_sm);
-    if (e == cudaSuccess) e = cudaMalloc(&p->d_stack, sizeof(int32_t) * (size_t)g.num_pages);
+    p->q_cap = 2 * g.num_pages;
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_queue, sizeof(int32_t) * (size_t)p->q_cap);
     if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->plan_uploaded, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = (cudaError_t)launch_init_stack(p->d_stack, g.num_pages, nullptr);
+    if (e == cudaSuccess) e = (cudaError_t)launch_init_queue(p->d_queue, g.num_pages, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         int r = cuda_error(e, "creating the pool");
@@ -120,7 +121,8 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         return r;
     }
     if (p->move_blocks_per_sm < 1) p->move_blocks_per_sm = 1;
-    p->free_top = g.num_pages;
+    p->q_head = 0;
+    p->q_tail = g.num_pages;  // all pages free, ids 0..num_pages-1 in order
     *out = p;
     return LEYLINE_OK;
 }
@@ -139,7 +141,7 @@ int leyline_pool_destroy(leyline_pool_t* p)
     if (p->d_plan) cudaFree(p->d_plan);
     if (p->h_plan) cudaFreeHost(p->h_plan);
     if (p->d_status) cudaFree(p->d_status);
-    if (p->d_stack) cudaFree(p->d_stack);
+    if (p->d_queue) cudaFree(p->d_queue);
     delete p;
     return LEYLINE_OK;
 }
@@ -147,24 +149,28 @@ int leyline_pool_destroy(leyline_pool_t* p)
 int64_t leyline_free_page_count(const leyline_pool_t* p)
 {
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
-    return p->free_top;
+    return p->q_tail - p->q_head;
 }
 
 int leyline_alloc_pages(leyline_pool_t* p, int32_t n, int32_t* ids)
 {
     clear_error();
     if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
-    if (n > p->free_top) return set_error(LEYLINE_ERR_NO_PAGES, "not enough free pages");
+    if (n > p->q_tail - p->q_head) return set_error(LEYLINE_ERR_NO_PAGES, "not enough free pages");
     if (n == 0) return LEYLINE_OK;
     DeviceGuard guard(p->device);
     int rc = wait_pool(p);
     if (rc != LEYLINE_OK) return rc;
-    std::vector<int32_t> top(n);
-    cudaError_t e = cudaMemcpy(top.data(), p->d_stack + (p->free_top - n), sizeof(int32_t) * (size_t)n,
-                               cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_error(e, "reading the free stack");
-    for (int32_t i = 0; i < n; ++i) ids[i] = top[n - 1 - i];
-    p->free_top -= n;
+    // the ring may wrap: at most two contiguous pieces
+    int64_t done = 0;
+    while (done < n) {
+        const int64_t at = (p->q_head + done) % p->q_cap;
+        const int64_t len = std::min<int64_t>(n - done, p->q_cap - at);
+        cudaError_t e = cudaMemcpy(ids + done, p->d_queue + at, sizeof(int32_t) * (size_t)len, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_error(e, "reading the free-page ring");
+        done += len;
+    }
+    p->q_head += n;
     return LEYLINE_OK;
 }
 
@@ -172,7 +178,7 @@ int leyline_free_pages(leyline_pool_t* p, int32_t n, const int32_t* ids)
 {
     clear_error();
     if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
-    if (p->free_top + n > p->g.num_pages)
+    if (p->q_tail - p->q_head + n > p->g.num_pages)
         return set_error(LEYLINE_ERR_INVALID_ARG, "more pages returned than the pool holds");
     for (int32_t i = 0; i < n; ++i)
         if (ids[i] < 0 || ids[i] >= p->g.num_pages) return set_error(LEYLINE_ERR_INVALID_ARG, "page id out of range");
@@ -180,12 +186,15 @@ int leyline_free_pages(leyline_pool_t* p, int32_t n, const int32_t* ids)
     DeviceGuard guard(p->device);
     int rc = wait_pool(p);
     if (rc != LEYLINE_OK) return rc;
-    std::vector<int32_t> v(ids, ids + n);
-    std::reverse(v.begin(), v.end());  // ids[0] is taken first by the next pop
-    cudaError_t e = cudaMemcpy(p->d_stack + p->free_top, v.data(), sizeof(int32_t) * (size_t)n,
-                               cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_error(e, "writing the free stack");
-    p->free_top += n;
+    int64_t done = 0;
+    while (done < n) {
+        const int64_t at = (p->q_tail + done) % p->q_cap;
+        const int64_t len = std::min<int64_t>(n - done, p->q_cap - at);
+        cudaError_t e = cudaMemcpy(p->d_queue + at, ids + done, sizeof(int32_t) * (size_t)len, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_error(e, "writing the free-page ring");
+        done += len;
+    }
+    p->q_tail += n;
     return LEYLINE_OK;
 }
 
@@ -220,13 +229,14 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
             return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
     Plan plan;
-    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, p->free_top, &plan);
+    const int64_t free_now = p->q_tail - p->q_head;
+    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
         return LEYLINE_OK;
     }
-    if (p->free_top - plan.total_pop + plan.total_push > p->g.num_pages)
+    if (free_now - plan.total_pop + plan.total_push > p->g.num_pages)
         return set_error(LEYLINE_ERR_INVALID_ARG,
                          "the rewritten requests hold more pages than the pool has free slots for: "
                          "their tables were not filled from this pool");
@@ -234,80 +244,75 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     DeviceGuard guard(p->device);
     if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
 
-    // plan buffer layout (16-byte aligned sections): uploaded part, then device-only part
-    const int half = p->g.rope_dim / 2;
-    const size_t off_reqs = 0;
-    const size_t off_segs = align_up(off_reqs + sizeof(ReqPlan) * plan.reqs.size(), 16);
-    const size_t off_delta = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
-    const size_t upload = align_up(off_delta + sizeof(int64_t) * plan.trig_delta.size(), 16);
-    const size_t off_trig = upload;
-    const size_t off_staged = align_up(off_trig + sizeof(float) * 2 * half * plan.trig_delta.size(), 16);
-    const size_t total = align_up(off_staged + sizeof(int32_t) * (size_t)plan.total_pop, 256);
-
-    cudaError_t e;
-    if (total > p->d_plan_cap) {
-        rc = wait_pool(p);
-        if (rc != LEYLINE_OK) return rc;
-        if (p->d_plan) cudaFree(p->d_plan);
-        p->d_plan = nullptr;
-        p->d_plan_cap = 0;
-        const size_t cap = std::max<size_t>(total * 2, 1 << 16);
-        e = cudaMalloc(&p->d_plan, cap);
-        if (e != cudaSuccess) return cuda_error(e, "allocating the plan buffer");
-        p->d_plan_cap = cap;
-    }
-    if (upload > p->h_plan_cap) {
-        if (p->h_plan) {
-            e = cudaEventSynchronize(p->plan_uploaded);
-            if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
-            cudaFreeHost(p->h_plan);
-            p->h_plan = nullptr;
-            p->h_plan_cap = 0;
-        }
-        const size_t cap = std::max<size_t>(upload * 2, 1 << 16);
-        e = cudaHostAlloc((void**)&p->h_plan, cap, cudaHostAllocDefault);
-        if (e != cudaSuccess) return cuda_error(e, "allocating the pinned plan buffer");
-        p->h_plan_cap = cap;
-    } else if (p->has_work) {
-        e = cudaEventSynchronize(p->plan_uploaded);  // the staging buffer may still be in flight
-        if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
-    }
-    memcpy(p->h_plan + off_reqs, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
-    memcpy(p->h_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
-    if (!plan.trig_delta.empty())
-        memcpy(p->h_plan + off_delta, plan.trig_delta.data(), sizeof(int64_t) * plan.trig_delta.size());
-
-    rc = order_after_previous(p, stream);
-    if (rc != LEYLINE_OK) return rc;
-    e = cudaMemcpyAsync(p->d_plan, p->h_plan, upload, cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
-    e = cudaEventRecord(p->plan_uploaded, stream);
-    if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
-
     SpliceArgs a{};
     a.kv = p->kv;
     a.table = bt->table;
     a.table_w = bt->table;
     a.seq_lens_dev = bt->seq_lens_dev;
-    a.free_stack = p->d_stack;
-    a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan + off_reqs);
-    a.segs = reinterpret_cast<const Seg*>(p->d_plan + off_segs);
-    a.trig_delta = reinterpret_cast<const int64_t*>(p->d_plan + off_delta);
-    a.trig = reinterpret_cast<float*>(p->d_plan + off_trig);
-    a.staged = reinterpret_cast<int32_t*>(p->d_plan + off_staged);
+    a.free_q = p->d_queue;
+    a.q_cap = p->q_cap;
+    a.pop_base = p->q_head;
+    a.push_base = p->q_tail;
     a.status = p->d_status;
-    a.pop_top = p->free_top;
-    a.push_base = p->free_top - plan.total_pop;
     a.total_tiles = plan.total_tiles;
     a.total_commit = plan.total_commit;
-    a.total_pop = plan.total_pop;
     a.n_reqs = (int32_t)plan.reqs.size();
-    a.n_trig = (int32_t)plan.trig_delta.size();
+    a.n_trig = plan.n_trig;
     a.max_blocks = bt->max_blocks;
     a.g = p->g;
 
-    int err = launch_plan_kernel(a, stream);
-    if (err != 0) return cuda_error((cudaError_t)err, "launching the plan kernel");
+    cudaError_t e;
+    rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    const bool in_params = plan_fits_params(plan);
+    ParamPlan pp;
+    if (in_params) {
+        pack_param_plan(plan, &pp);
+    } else {
+        // Plan too large for a kernel parameter: upload it (reqs | segs | trig).
+        const size_t off_segs = align_up(sizeof(ReqPlan) * plan.reqs.size(), 16);
+        const size_t off_trig = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
+        const size_t total = align_up(off_trig + sizeof(float) * plan.trig.size(), 256);
+        if (total > p->d_plan_cap) {
+            rc = wait_pool(p);
+            if (rc != LEYLINE_OK) return rc;
+            if (p->d_plan) cudaFree(p->d_plan);
+            p->d_plan = nullptr;
+            p->d_plan_cap = 0;
+            const size_t cap = std::max<size_t>(total * 2, 1 << 16);
+            e = cudaMalloc(&p->d_plan, cap);
+            if (e != cudaSuccess) return cuda_error(e, "allocating the plan buffer");
+            p->d_plan_cap = cap;
+        }
+        if (total > p->h_plan_cap) {
+            if (p->h_plan) {
+                e = cudaEventSynchronize(p->plan_uploaded);
+                if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
+                cudaFreeHost(p->h_plan);
+                p->h_plan = nullptr;
+                p->h_plan_cap = 0;
+            }
+            const size_t cap = std::max<size_t>(total * 2, 1 << 16);
+            e = cudaHostAlloc((void**)&p->h_plan, cap, cudaHostAllocDefault);
+            if (e != cudaSuccess) return cuda_error(e, "allocating the pinned plan buffer");
+            p->h_plan_cap = cap;
+        } else if (p->uploaded_once) {
+            e = cudaEventSynchronize(p->plan_uploaded);  // the staging buffer may still be in flight
+            if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
+        }
+        memcpy(p->h_plan, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
+        memcpy(p->h_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
+        if (!plan.trig.empty()) memcpy(p->h_plan + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
+        e = cudaMemcpyAsync(p->d_plan, p->h_plan, total, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
+        e = cudaEventRecord(p->plan_uploaded, stream);
+        if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
+        p->uploaded_once = true;
+        a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan);
+        a.segs = reinterpret_cast<const Seg*>(p->d_plan + off_segs);
+        a.trig = reinterpret_cast<const float*>(p->d_plan + off_trig);
+    }
+
     cudaEvent_t t0 = nullptr, t1 = nullptr;
     if (p->timing) {
         if (p->tev_used == p->tev.size()) {
@@ -319,19 +324,15 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         t0 = p->tev[p->tev_used].first;
         t1 = p->tev[p->tev_used].second;
         ++p->tev_used;
-        cudaEventRecord(t0, stream);
     }
-    const int grid = p->sm_count * p->move_blocks_per_sm;
-    err = launch_move_rotate(a, grid, stream);
-    if (err != 0) return cuda_error((cudaError_t)err, "launching the move+rotate kernel");
-    if (t1) cudaEventRecord(t1, stream);
-    err = launch_commit(a, stream);
-    if (err != 0) return cuda_error((cudaError_t)err, "launching the commit kernel");
+    int err = launch_splice(a, in_params ? &pp : nullptr, p->sm_count * p->move_blocks_per_sm, stream, t0, t1);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the splice kernels");
     rc = mark_done(p, stream);
     if (rc != LEYLINE_OK) return rc;
 
     for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
-    p->free_top = p->free_top - plan.total_pop + plan.total_push;
+    p->q_head += plan.total_pop;
+    p->q_tail += plan.total_push;
     p->last_stats = plan.stats;
     return LEYLINE_OK;
 }

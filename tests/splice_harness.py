@@ -222,3 +222,114 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
 
 def oracle_state(w: Workload) -> list[np.ndarray]:
     return [synth.cache_request(w.seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)]
+
+
+# ------------------------------------------------------------ full-size checks --
+
+def sample_positions(newlen: int, kind: np.ndarray, idx: np.ndarray, n: int, rng) -> np.ndarray:
+    """Every segment boundary (and its neighbours), both ends, and n random positions."""
+    if newlen == 0:
+        return np.zeros(0, dtype=np.int64)
+    jump = np.flatnonzero((np.diff(kind) != 0) | (np.diff(idx) != 1)) + 1
+    cand = np.concatenate([[0, newlen - 1], jump - 1, jump, jump + 1, rng.integers(0, newlen, size=n)])
+    return np.unique(np.clip(cand, 0, newlen - 1))
+
+
+def fetch_rows(cache, req: int, layers: np.ndarray, pos: np.ndarray) -> np.ndarray:
+    """GPU rows (uint16 [n][row]) of (layer, position) pairs, read through the block table."""
+    import torch
+    B = cache.block_size
+    row = cache.table[req].cpu().numpy().astype(np.int64)
+    page = torch.from_numpy(row[pos // B]).to(cache.device)
+    slot = torch.from_numpy(pos % B).to(cache.device)
+    lay = torch.from_numpy(layers.astype(np.int64)).to(cache.device)
+    got = cache.kv_view()[lay, page, slot]
+    return got.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_sampled_single_call(w: Workload, cache, step, before_lens, rng, n_samples: int = 1500) -> dict:
+    """One call from the generator's initial state: sampled rows against the oracle, element by element."""
+    lat = w.latent_dim
+    tot = {"rows": 0, "moved": 0, "floor_used": 0, "rel_l2_max": 0.0}
+    for r in range(w.num_reqs):
+        ds = [d for d in step if d.req == r]
+        if not ds:
+            continue
+        tup = [(d.s_start, d.s_end, d.n_repl) for d in ds]
+        newlen, kind, idx, which = oracle.splice_map(int(before_lens[r]), tup)
+        assert int(cache.seq_lens_host[r]) == newlen
+        pos = sample_positions(newlen, kind, idx, n_samples, rng)
+        if pos.size == 0:
+            continue
+        layers = rng.integers(0, w.num_layers, size=pos.size)
+        got = fetch_rows(cache, r, layers, pos)
+        want = np.empty_like(got)
+        moved = np.zeros(pos.size, dtype=bool)
+        reps = {k: synth.repl_rows(w.seed, r, ds[k].key, w.num_layers, ds[k].n_repl, w.row_elems)
+                for k in set(which[pos][kind[pos] == 1].tolist())}
+        for i, (p, layer) in enumerate(zip(pos, layers)):
+            if kind[p] == 1:
+                want[i] = reps[which[p]][layer, idx[p]]
+            else:
+                t = int(idx[p])
+                orig = synth.cache_rows(w.seed, r, int(layer), [t], w.row_elems)[0]
+                want[i, :lat] = orig[:lat]
+                want[i, lat:] = oracle.rerotate(orig[lat:], t, int(p), w.theta) if t != p else orig[lat:]
+                moved[i] = t != p
+        assert np.array_equal(got[:, :lat], want[:, :lat]), f"request {r}: latent bits differ"
+        assert np.array_equal(got[~moved], want[~moved]), f"request {r}: prefix / R rows differ"
+        c = compare_kpe(got[moved, lat:], want[moved, lat:], 0)
+        tot["rows"] += int(pos.size)
+        tot["moved"] += c["n"]
+        tot["floor_used"] += c["floor_used"]
+        tot["rel_l2_max"] = max(tot["rel_l2_max"], c["rel_l2"])
+    return tot
+
+
+def check_properties_all_rows(w: Workload, cache, step, before_lens) -> int:
+    """Every row of every touched request and layer, on the device: latents and unmoved rows
+    bit-exact against the generator's rows through the oracle's slot map, R rows bit-exact,
+    and each moved RoPE pair's norm preserved within bf16 rounding (2^-7 relative)."""
+    import torch
+    base = sfill._base_on_device(w.seed, w.row_elems, str(cache.device))
+    lat = w.latent_dim
+    h = w.rope_dim // 2
+    checked = 0
+    for r in range(w.num_reqs):
+        ds = [d for d in step if d.req == r]
+        if not ds:
+            continue
+        tup = [(d.s_start, d.s_end, d.n_repl) for d in ds]
+        newlen, kind, idx, which = oracle.splice_map(int(before_lens[r]), tup)
+        if newlen == 0:
+            continue
+        kept = np.flatnonzero(kind == 0)
+        moved_np = idx[kept] != kept
+        kept_t = torch.from_numpy(kept).to(cache.device)
+        moved_t = torch.from_numpy(moved_np).to(cache.device)
+        reps = [sfill.repl_tensor(w.seed, r, d.key, w.num_layers, d.n_repl, w.row_elems, str(cache.device))
+                if d.n_repl else None for d in ds]
+        buf = torch.empty((newlen, w.row_elems), dtype=torch.bfloat16, device=cache.device)
+        for layer in range(w.num_layers):
+            cache.gather(r, layer, 0, newlen, buf)
+            ids = torch.from_numpy(synth.row_ids(w.seed, synth.STREAM_CACHE, r, layer, idx[kept])).to(cache.device)
+            src = base.index_select(0, ids)
+            got = buf.index_select(0, kept_t)
+            gi, si = got.view(torch.int16), src.view(torch.int16)
+            assert torch.equal(gi[:, :lat], si[:, :lat]), f"request {r} layer {layer}: latent bits differ"
+            assert torch.equal(gi[~moved_t], si[~moved_t]), f"request {r} layer {layer}: unmoved rows differ"
+            a = got[moved_t, lat:].float()
+            b = src[moved_t, lat:].float()
+            na = torch.hypot(a[:, :h], a[:, h:])
+            nb = torch.hypot(b[:, :h], b[:, h:])
+            assert bool(torch.all((na - nb).abs() <= 2.0 ** -7 * nb + 1e-30)), \
+                f"request {r} layer {layer}: a rope pair's norm changed"
+            for k, d in enumerate(ds):
+                if not d.n_repl:
+                    continue
+                pk = np.flatnonzero((kind == 1) & (which == k))
+                rows = buf.index_select(0, torch.from_numpy(pk).to(cache.device))
+                assert torch.equal(rows.view(torch.int16), reps[k][layer].view(torch.int16)), \
+                    f"request {r} layer {layer}: replacement rows differ"
+            checked += newlen
+    return checked

@@ -68,20 +68,24 @@ def test_noalloc_matches_splice_on_two_calls():
 
 
 def test_noalloc_refuses_a_plan_larger_than_its_scratch():
-    """Block size 1 and a 1.1M-token request: rewriting it needs 1.1M fresh page ids,
-    more than the 4 MiB static scratch holds."""
+    """20,000 one-token deletions in one request: each shifts its downstream run by a
+    different Delta, so the plan carries 20,000 rotated segments with their cos/sin,
+    more than the 4 MiB static scratch holds.  The call is refused and changes nothing."""
     from rope_rotation_gb300 import leyline
     from rope_rotation_gb300.runtime import PagedCache
-    L = 1_100_000
-    cache = PagedCache(1, 1, 2 * L + 8, 1, L + 8)
+    L, B = 100_000, 16
+    nb = L // B
+    cache = PagedCache(1, B, 2 * nb + 8, 1, nb + 8)
     cache.add_request(0, L)
     torch.cuda.synchronize()
-    before = cache.table[0, :8].cpu().numpy().copy()
+    before = cache.table[0].cpu().numpy().copy()
     free = cache.free_pages()
+    dirs = [leyline.directive(0, 5 * k + 2, 5 * k + 3, None) for k in range(20_000)]
     with pytest.raises(leyline.LeylineError) as ei:
-        leyline.leyline_splice_noalloc(cache.pool, cache.tables, [leyline.directive(0, 0, 1, None)])
+        leyline.leyline_splice_noalloc(cache.pool, cache.tables, dirs)
     assert ei.value.code == leyline.LEYLINE_ERR_SCRATCH
     assert "scratch" in str(ei.value)
     assert int(cache.seq_lens_host[0]) == L and cache.free_pages() == free
-    assert np.array_equal(cache.table[0, :8].cpu().numpy(), before)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache.table[0].cpu().numpy(), before)
     cache.close()
