@@ -157,8 +157,11 @@ def run_ours(args, rank, world, local):
     w = workload(args.workload)
     K, W = args.steps, args.warmup
     C = w.num_reqs
-    legs = 1 if args.no_e2e else 2
-    groups = (W + K) * legs  # every step and warm-up splices its own copy of the workload's requests
+    # legs: value (plain steps), kernel (the same steps with CUDA events around the
+    # move+rotate kernel, for the roofline), e2e (host buffers); each step and warm-up
+    # of each leg splices its own copy of the workload's requests
+    legs = 2 if args.no_e2e else 3
+    groups = (W + K) * legs
     B = w.block_size
     max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
     pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
@@ -196,7 +199,6 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.2)
-    leyline.leyline_kernel_timing_enable(cache.pool, True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -207,6 +209,20 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
+    cache.check_status()
+
+    # kernel leg: the same steps on fresh requests, with events around move+rotate
+    base = W + K
+    for g in range(W):
+        cache.splice(dirs_for(base + g, repl_dev))
+    torch.cuda.synchronize()
+    leyline.leyline_kernel_timing_enable(cache.pool, True)
+    barrier()
+    torch.cuda.synchronize()
+    for k in range(K):
+        cache.splice(dirs_for(base + W + k, repl_dev))
+    torch.cuda.synchronize()
+    barrier()
     k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
     leyline.leyline_kernel_timing_enable(cache.pool, False)
     cache.check_status()
@@ -215,7 +231,7 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         # End to end through the public API: each step copies its replacement rows from
         # pinned host memory, splices, and reads back the request's new lengths and table row.
-        base = W + K
+        base = 2 * (W + K)
         rbuf = {k: torch.empty_like(v) for k, v in repl_dev.items()}
         out_tab = torch.empty((K, C, max_blocks), dtype=torch.int32).pin_memory()
         out_len = torch.empty((K, C), dtype=torch.int32).pin_memory()
@@ -282,11 +298,12 @@ def run_ours(args, rank, world, local):
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
+                   "move_kernel": os.environ.get("LEYLINE_MOVE_KERNEL", "bulk"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
-        "roofline": {"kernel": "move_rotate_mla", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "bulk"), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",

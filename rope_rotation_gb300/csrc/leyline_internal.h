@@ -45,13 +45,17 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
 constexpr int kParamReqs = 8;
 constexpr int kParamSegs = 24;
 constexpr int kParamTrigFloats = 640;  // 10 rotated segments of a 64-wide rope band
-struct ParamPlan {
+struct alignas(16) ParamPlan {
     ReqPlan reqs[kParamReqs];
     Seg segs[kParamSegs];
     float trig[kParamTrigFloats];
 };
 bool plan_fits_params(const Plan& plan);
 void pack_param_plan(const Plan& plan, ParamPlan* pp);
+
+// Which move+rotate kernel runs: 16-byte vector loads/stores through registers, or
+// bulk copies (TMA) staged through shared memory.
+enum MoveKernel : int32_t { MOVE_VECTOR = 0, MOVE_BULK = 1 };
 
 // Kernel arguments (passed by value).
 struct SpliceArgs {
@@ -72,7 +76,7 @@ struct SpliceArgs {
     int32_t n_reqs;
     int32_t n_trig;
     int32_t max_blocks;
-    int32_t pad;
+    int32_t move_kernel;      // MoveKernel
     Geometry g;
 };
 
@@ -85,8 +89,11 @@ int launch_splice(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stre
                   cudaEvent_t t1);
 int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
                   int64_t t1, void* out, int32_t* status, void* stream);
-// Resident CTAs per SM of the move+rotate kernel (occupancy query).
+// Resident CTAs per SM of the vector move+rotate kernel (occupancy query).
 int move_rotate_blocks_per_sm(int* blocks);
+// Allow the bulk kernel its shared memory for rows of row_bytes and report its
+// resident CTAs per SM (0 if the rows are too wide for it).
+int bulk_prepare(int32_t row_bytes, int* blocks);
 
 }  // namespace leyline
 
@@ -98,6 +105,8 @@ struct leyline_pool {
     int device = 0;
     int sm_count = 0;
     int move_blocks_per_sm = 1;
+    int bulk_blocks_per_sm = 0;
+    int32_t move_kernel = 0;  // MoveKernel used by this pool
     int32_t* d_queue = nullptr;  // free-page ring, 2 * num_pages entries
     int64_t q_cap = 0;
     int64_t q_head = 0;          // monotonic: next page to take is d_queue[q_head % q_cap]

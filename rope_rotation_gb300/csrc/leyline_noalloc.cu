@@ -155,7 +155,9 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.max_blocks = bt->max_blocks;
     a.g = p->g;
 
-    int err = launch_splice(a, nullptr, p->sm_count * p->move_blocks_per_sm, stream, nullptr, nullptr);
+    a.move_kernel = p->move_kernel;
+    const int grid = p->sm_count * (p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm : p->move_blocks_per_sm);
+    int err = launch_splice(a, nullptr, grid, stream, nullptr, nullptr);
     if (err != 0) return cuda_fail((cudaError_t)err, "launching the splice kernels");
     e = cudaEventRecord(p->done, stream);
     if (e != cudaSuccess) return cuda_fail(e, "recording completion event");

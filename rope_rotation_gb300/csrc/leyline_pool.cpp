@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -121,6 +122,21 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         return r;
     }
     if (p->move_blocks_per_sm < 1) p->move_blocks_per_sm = 1;
+    {
+        int err = bulk_prepare(g.row_vecs * 16, &p->bulk_blocks_per_sm);
+        if (err != 0) {
+            int r = cuda_error((cudaError_t)err, "preparing the bulk-copy kernel");
+            leyline_pool_destroy(p);
+            return r;
+        }
+        // LEYLINE_MOVE_KERNEL=vector|bulk selects the move+rotate kernel (for A/B
+        // measurements); by default the bulk-load kernel runs for the MLA row shape
+        // (latent 512 + rope 64), the generic vector kernel for other shapes.
+        const char* env = getenv("LEYLINE_MOVE_KERNEL");
+        const bool want_vector = env && strcmp(env, "vector") == 0;
+        const bool mla = g.latent_vecs == 64 && g.rope_vecs == 8;
+        p->move_kernel = (!want_vector && mla && p->bulk_blocks_per_sm > 0) ? MOVE_BULK : MOVE_VECTOR;
+    }
     p->q_head = 0;
     p->q_tail = g.num_pages;  // all pages free, ids 0..num_pages-1 in order
     *out = p;
@@ -325,7 +341,9 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         t1 = p->tev[p->tev_used].second;
         ++p->tev_used;
     }
-    int err = launch_splice(a, in_params ? &pp : nullptr, p->sm_count * p->move_blocks_per_sm, stream, t0, t1);
+    a.move_kernel = p->move_kernel;
+    const int grid = p->sm_count * (p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm : p->move_blocks_per_sm);
+    int err = launch_splice(a, in_params ? &pp : nullptr, grid, stream, t0, t1);
     if (err != 0) return cuda_error((cudaError_t)err, "launching the splice kernels");
     rc = mark_done(p, stream);
     if (rc != LEYLINE_OK) return rc;

@@ -44,8 +44,15 @@ EDGE = [
 ]
 
 
+@pytest.fixture(params=["bulk", "vector"])
+def move_kernel(request, monkeypatch):
+    """Both move+rotate kernels: bulk copies staged in shared memory, and vector loads."""
+    monkeypatch.setenv("LEYLINE_MOVE_KERNEL", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("B", [1, 2, 4, 16])
-def test_edge_grid(B):
+def test_edge_grid(B, move_kernel):
     for i, (L, dirs) in enumerate(EDGE):
         w = Workload(f"edge{i}-B{B}", 3, B, [L], [[Dir(0, s, e, n, k) for k, (s, e, n) in enumerate(dirs)]], seed=i)
         cache = H.make_cache(w)
@@ -55,7 +62,7 @@ def test_edge_grid(B):
 
 
 @pytest.mark.parametrize("B", [1, 16])
-def test_many_requests_one_call_and_chained_steps(B):
+def test_many_requests_one_call_and_chained_steps(B, move_kernel):
     lengths = [70, 16, 0, 129, 33]
     steps = [
         [Dir(0, 10, 40, 3, 0), Dir(1, 0, 16, 0, 1), Dir(3, 64, 64, 20, 2), Dir(3, 100, 120, 1, 3),
@@ -72,7 +79,7 @@ def test_many_requests_one_call_and_chained_steps(B):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-def test_interleaved_and_half_split_layouts(layout):
+def test_interleaved_and_half_split_layouts(layout, move_kernel):
     w = Workload(f"layout{layout}", 2, 16, [300, 211], [[Dir(0, 40, 200, 7, 0), Dir(1, 3, 50, 60, 1)]], seed=3)
     cache = H.make_cache(w, pair_layout=layout)
     H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0], layout=layout)
@@ -80,7 +87,7 @@ def test_interleaved_and_half_split_layouts(layout):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-def test_generic_shape_kernel(layout):
+def test_generic_shape_kernel(layout, move_kernel):
     """latent 64 + rope 16: not the MLA shape, so the generic move+rotate kernel runs."""
     w = Workload(f"generic{layout}", 3, 4, [90, 45], [[Dir(0, 20, 60, 5, 0), Dir(1, 44, 45, 3, 1)]], seed=4,
                  latent_dim=64, rope_dim=16)
@@ -90,7 +97,7 @@ def test_generic_shape_kernel(layout):
 
 
 @pytest.mark.parametrize("layout", [0, 1])
-def test_bf16_naive_arm_is_exact(layout):
+def test_bf16_naive_arm_is_exact(layout, move_kernel):
     w = Workload(f"bf16naive{layout}", 2, 16, [500], [[Dir(0, 100, 180, 12, 0)], [Dir(0, 0, 33, 1, 1)]], seed=5)
     cache = H.make_cache(w, pair_layout=layout, precision=1)
     state = H.oracle_state(w)
@@ -122,7 +129,7 @@ def test_contiguous_4k_workload():
     cache.close()
 
 
-def test_dsv2_lite_32k_workload_full():
+def test_dsv2_lite_32k_workload_full(move_kernel):
     """27 layers x 32768 tokens, block 16: every row checked against the oracle."""
     w = configs.dsv2_lite_32k()
     cache = H.make_cache(w)
