@@ -35,7 +35,10 @@ METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 
 FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic (read + write bytes) of the move+rotate kernel on this
 # workload, from an ncu capture, valid only for the kernel source it was taken on.
-NCU_TRAFFIC = {"kernel_sha256": None, "bytes_per_launch": None}
+# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.3 MB; the
+# rest of the 210.9 MB written was still in L2 when the single captured launch ended.)
+NCU_TRAFFIC = {"kernel_sha256": "8a35c2a6982d914856678e6215419240f7249e291b323b78a7a9994a1e5b5e89",
+               "bytes_per_launch": 210916608 + 161315840}
 
 
 def parse():
@@ -46,6 +49,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="cfg2")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--single-leg", action="store_true",
+                    help="time the move kernel inside the value leg and skip the other legs (large workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     return ap.parse_args()
@@ -56,6 +61,27 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank splices its own synthetic requests: the units are sharded, nothing is exchanged."""
+    return seed + 1000 * rank
+
+
+def reduce_max_over_ranks(values, world: int, device):
+    """Element-wise max of per-rank timings (the job ends when its slowest rank does)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_value(slots_per_rank_step: int, steps: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job throughput: slots spliced by all ranks / the slowest rank's time."""
+    return slots_per_rank_step * steps * world / (elapsed_ms_max / 1e3)
 
 
 def measured_peaks():
@@ -160,13 +186,15 @@ def run_ours(args, rank, world, local):
     # legs: value (plain steps), kernel (the same steps with CUDA events around the
     # move+rotate kernel, for the roofline), e2e (host buffers); each step and warm-up
     # of each leg splices its own copy of the workload's requests
-    legs = 2 if args.no_e2e else 3
+    if args.single_leg:
+        args.no_e2e = True
+    legs = 1 if args.single_leg else (2 if args.no_e2e else 3)
     groups = (W + K) * legs
     B = w.block_size
     max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
     pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
     cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta)
-    seed = w.seed + 1000 * rank
+    seed = rank_seed(w.seed, rank)
     for g in range(groups):
         for r, L in enumerate(w.lengths):
             cache.add_request(g * C + r, L)
@@ -200,6 +228,8 @@ def run_ours(args, rank, world, local):
     sampler.start()
     time.sleep(0.2)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.single_leg:
+        leyline.leyline_kernel_timing_enable(cache.pool, True)
     barrier()
     torch.cuda.synchronize()
     ev0.record(stream)
@@ -211,18 +241,19 @@ def run_ours(args, rank, world, local):
     elapsed_ms = ev0.elapsed_time(ev1)
     cache.check_status()
 
-    # kernel leg: the same steps on fresh requests, with events around move+rotate
-    base = W + K
-    for g in range(W):
-        cache.splice(dirs_for(base + g, repl_dev))
-    torch.cuda.synchronize()
-    leyline.leyline_kernel_timing_enable(cache.pool, True)
-    barrier()
-    torch.cuda.synchronize()
-    for k in range(K):
-        cache.splice(dirs_for(base + W + k, repl_dev))
-    torch.cuda.synchronize()
-    barrier()
+    if not args.single_leg:
+        # kernel leg: the same steps on fresh requests, with events around move+rotate
+        base = W + K
+        for g in range(W):
+            cache.splice(dirs_for(base + g, repl_dev))
+        torch.cuda.synchronize()
+        leyline.leyline_kernel_timing_enable(cache.pool, True)
+        barrier()
+        torch.cuda.synchronize()
+        for k in range(K):
+            cache.splice(dirs_for(base + W + k, repl_dev))
+        torch.cuda.synchronize()
+        barrier()
     k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
     leyline.leyline_kernel_timing_enable(cache.pool, False)
     cache.check_status()
@@ -264,15 +295,11 @@ def run_ours(args, rank, world, local):
     clocks = sampler.stop()
 
     # max over ranks
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms, e2e["ms"] if e2e else 0.0], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms_max = float(t[0]), float(t[1])
-        if e2e:
-            e2e["ms"] = e2e_ms_max
+    elapsed_ms, e2e_ms_max = reduce_max_over_ranks([elapsed_ms, e2e["ms"] if e2e else 0.0], world, dev)
+    if e2e:
+        e2e["ms"] = e2e_ms_max
     slots = st["downstream_slots"] * K * world
-    value = slots / (elapsed_ms / 1e3)
+    value = job_value(st["downstream_slots"], K, world, elapsed_ms)
     peak, peak_kind = measured_peaks()
     k2_avg_s = (k2_ms / max(k2_n, 1)) / 1e3
     achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
@@ -298,12 +325,12 @@ def run_ours(args, rank, world, local):
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
-                   "move_kernel": os.environ.get("LEYLINE_MOVE_KERNEL", "bulk"),
+                   "move_kernel": os.environ.get("LEYLINE_MOVE_KERNEL", "vector"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
-        "roofline": {"kernel": "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "bulk"), "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector"), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",

@@ -129,13 +129,13 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
             leyline_pool_destroy(p);
             return r;
         }
-        // LEYLINE_MOVE_KERNEL=vector|bulk selects the move+rotate kernel (for A/B
-        // measurements); by default the bulk-load kernel runs for the MLA row shape
-        // (latent 512 + rope 64), the generic vector kernel for other shapes.
+        // The register-staged vector kernel is the default (measured faster on
+        // GB300); LEYLINE_MOVE_KERNEL=bulk selects the bulk-load (TMA) kernel for
+        // the MLA row shape (latent 512 + rope 64), for A/B measurements.
         const char* env = getenv("LEYLINE_MOVE_KERNEL");
-        const bool want_vector = env && strcmp(env, "vector") == 0;
+        const bool want_bulk = env && strcmp(env, "bulk") == 0;
         const bool mla = g.latent_vecs == 64 && g.rope_vecs == 8;
-        p->move_kernel = (!want_vector && mla && p->bulk_blocks_per_sm > 0) ? MOVE_BULK : MOVE_VECTOR;
+        p->move_kernel = (want_bulk && mla && p->bulk_blocks_per_sm > 0) ? MOVE_BULK : MOVE_VECTOR;
     }
     p->q_head = 0;
     p->q_tail = g.num_pages;  // all pages free, ids 0..num_pages-1 in order
