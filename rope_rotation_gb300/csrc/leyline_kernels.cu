@@ -190,38 +190,35 @@ __device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long 
     const long long B = a.g.block_size;
     const long long rv = a.g.row_vecs;
     uint4* kv = static_cast<uint4*>(a.kv);
-    const uint4* src;
-    long long lstride;
-    int trig = -1;
-    if (s.kind == SEG_REPL) {
-        src = static_cast<const uint4*>(s.repl) + (s.src_start + off) * rv;
-        lstride = (long long)s.n_repl * rv;
-    } else {
-        const long long t = s.src_start + off;
-        const long long blk = t / B;
-        if (t < 0 || blk >= a.max_blocks) {
-            raise_status(a.status, ST_BAD_BLOCK);
-            return d;
-        }
-        const int page = a.table[(long long)rp.req * a.max_blocks + blk];
-        if (page < 0 || page >= a.g.num_pages) {
-            raise_status(a.status, ST_BAD_PAGE);
-            return d;
-        }
-        src = kv + ((long long)page * B + (t - blk * B)) * rv;
-        lstride = a.g.layer_vecs;
-        if (s.kind == SEG_ROT) trig = s.trig;
-    }
     const long long dblk = p / B;
+    const bool from_cache = s.kind != SEG_REPL;
+    const long long t = s.src_start + off;
+    const long long blk = t / B;
+    const bool blk_ok = !from_cache || (t >= 0 && blk < a.max_blocks);
+    // both global loads are issued before either result is checked
     const int fresh = a.free_q[ring(a.pop_base + rp.pop_off + (dblk - rp.b0), a.q_cap)];
+    const int page = (from_cache && blk_ok) ? a.table[(long long)rp.req * a.max_blocks + blk] : 0;
+    if (!blk_ok) {
+        raise_status(a.status, ST_BAD_BLOCK);
+        return d;
+    }
+    if (from_cache && (page < 0 || page >= a.g.num_pages)) {
+        raise_status(a.status, ST_BAD_PAGE);
+        return d;
+    }
     if (fresh < 0 || fresh >= a.g.num_pages) {
         raise_status(a.status, ST_BAD_FRESH);
         return d;
     }
-    d.src = src;
+    if (from_cache) {
+        d.src = kv + ((long long)page * B + (t - blk * B)) * rv;
+        d.src_lstride = a.g.layer_vecs;
+        d.trig = s.kind == SEG_ROT ? s.trig : -1;
+    } else {
+        d.src = static_cast<const uint4*>(s.repl) + (s.src_start + off) * rv;
+        d.src_lstride = (long long)s.n_repl * rv;
+    }
     d.dst = kv + ((long long)fresh * B + (p - dblk * B)) * rv;
-    d.src_lstride = lstride;
-    d.trig = trig;
     return d;
 }
 
@@ -242,7 +239,7 @@ __device__ __forceinline__ void my_units(long long units, long long& u0, long lo
 // covers 512 contiguous bytes), and 8 (half-split) or 16 (interleaved) lanes
 // move the rope band with the pair's cos/sin held in registers.
 template <int kLayout, bool kBf16, class PlanSrc>
-__global__ void __launch_bounds__(kMoveThreads) move_rotate_mla(const __grid_constant__ SpliceArgs a,
+__global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
     constexpr int kLatentVecs = 64, kRopeVecs = 8;
