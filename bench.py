@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="cfg2")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--reindex", action="store_true",
+                    help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
     ap.add_argument("--single-leg", action="store_true",
                     help="time the move kernel inside the value leg and skip the other legs (large workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -193,7 +195,8 @@ def run_ours(args, rank, world, local):
     B = w.block_size
     max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
     pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
-    cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta)
+    cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta,
+                       flags=leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
     seed = rank_seed(w.seed, rank)
     for g in range(groups):
         for r, L in enumerate(w.lengths):
@@ -325,12 +328,14 @@ def run_ours(args, rank, world, local):
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
-                   "move_kernel": os.environ.get("LEYLINE_MOVE_KERNEL", "vector"),
+                   "move_kernel": ("rotate_in_place" if args.reindex and B == 1
+                                   else os.environ.get("LEYLINE_MOVE_KERNEL", "vector")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
-        "roofline": {"kernel": "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector"), "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": ("rotate_in_place" if args.reindex and B == 1
+                                else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",

@@ -82,6 +82,16 @@ typedef enum { LEYLINE_PAIRS_HALF_SPLIT = 0, LEYLINE_PAIRS_INTERLEAVED = 1 } ley
  * as the comparison arm of drift studies. */
 typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_rotate_precision_t;
 
+/* Pool flags.
+ * LEYLINE_POOL_REINDEX: with block_size 1, a splice keeps every surviving
+ *   downstream token in its page: only its block-table entry moves, and its rope
+ *   band is turned in place (256 bytes per slot and layer instead of 2304; the
+ *   latent is not touched).  Rows of R go to fresh pages, the pages of dropped
+ *   tokens return to the free list.  The rotation happens in place before the
+ *   commit, so a call that fails after validation leaves the pool inconsistent
+ *   (as any LEYLINE_ERR_CUDA does).  Ignored for block_size > 1. */
+#define LEYLINE_POOL_REINDEX 1
+
 typedef struct {
     int32_t num_layers;       /* >= 1 */
     int32_t latent_dim;       /* multiple of 8 (512 for DeepSeek-V2/V3 MLA) */
@@ -91,6 +101,8 @@ typedef struct {
     double rope_theta;        /* RoPE base, > 0 (10000) */
     int32_t pair_layout;      /* leyline_pair_layout_t */
     int32_t rotate_precision; /* leyline_rotate_precision_t */
+    uint32_t flags;           /* LEYLINE_POOL_* bits */
+    int32_t reserved;         /* must be 0 */
 } leyline_pool_desc_t;
 
 /* Block tables of num_reqs requests.  Caller-owned; the library borrows them for
@@ -106,7 +118,13 @@ typedef struct {
     int32_t max_blocks;
 } leyline_block_table_t;
 
-typedef enum { LEYLINE_AMORTIZE = 0, LEYLINE_FORGET = 1 } leyline_mode_t;
+/* Directive modes.  AMORTIZE and FORGET are the two modes of section 2.1.
+ * EVICT is the compaction of the KV-streams page: the span is dropped (and R
+ * inserted) but downstream tokens keep the positions they were encoded at, so
+ * their rope bands are not turned.  In one call, a surviving run moves by the
+ * summed Delta of every directive to its left and is turned by the summed Delta
+ * of the AMORTIZE directives among them. */
+typedef enum { LEYLINE_AMORTIZE = 0, LEYLINE_FORGET = 1, LEYLINE_EVICT = 2 } leyline_mode_t;
 
 /* One directive D = (s_start, s_end, R, m) for request `req` (section 2.1).
  * [s_start, s_end) is half-open, in the request's coordinates before the call;
@@ -131,8 +149,10 @@ typedef struct {
     int64_t downstream_slots;  /* surviving tokens at or after each request's first s_end, summed */
     int64_t repl_slots;        /* rows of R written */
     int64_t head_slots;        /* unchanged prefix rows copied into the first rewritten block */
-    int64_t algorithmic_bytes; /* 2 * row_bytes * num_layers * (downstream_slots + repl_slots) */
-    int64_t moved_bytes;       /* 2 * row_bytes * num_layers * (downstream + repl + head slots) */
+    int64_t algorithmic_bytes; /* bytes that must move: 2 * row_bytes * num_layers * (downstream_slots +
+                                  repl_slots); re-indexed requests count 2 * rope_bytes per turned
+                                  downstream slot and nothing for unturned ones */
+    int64_t moved_bytes;       /* algorithmic bytes plus the head rows' 2 * row_bytes * num_layers */
     int64_t pages_popped;      /* fresh pages taken for the rewritten blocks */
     int64_t pages_pushed;      /* old pages returned to the free stack */
     int32_t requests_touched;

@@ -16,7 +16,8 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   rerotate         pinned: closure (equals one rotation by p - t), identity at t == p, brute force
   rotate_bf16only  pinned: quarter-turn case (exact), identity at Delta = 0, error bound
   splice_map       pinned: list-slicing brute force, sequential application, length identity
-  splice_request   pinned: brute force on tiny caches
+  splice_request   pinned: brute force on tiny caches; with EVICT modes: pure moves when every
+                   directive evicts, one composed call equals calls applied one after another
 """
 from __future__ import annotations
 
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
                                             ctypes.c_int, _u16p, ctypes.c_int64, ctypes.c_int32, _i64p, _i64p,
                                             _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int64]
             L.lo_splice_request.restype = ctypes.c_int64
+            L.lo_splice_request_modes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                                                  ctypes.c_int, _u16p, ctypes.c_int64, ctypes.c_int32, _i64p,
+                                                  _i64p, _i32p, _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int64]
+            L.lo_splice_request_modes.restype = ctypes.c_int64
             _lib = L
     return _lib
 
@@ -168,10 +173,12 @@ def splice_map(L: int, dirs, cap: int | None = None):
 
 
 def splice_request(cache: np.ndarray, dirs, repl: list[np.ndarray], latent_dim: int = 512,
-                   theta: float = 10000.0, layout: int = 0) -> np.ndarray:
+                   theta: float = 10000.0, layout: int = 0, modes=None) -> np.ndarray:
     """Splice one request's logical cache bf16 [layers][L][row] -> [layers][L'][row].
 
     dirs: (s_start, s_end, n_repl) per directive; repl[k]: bf16 [layers][n_repl][row].
+    modes: per directive, 0 = AMORTIZE (re-encode downstream tokens), 2 = EVICT (keep their
+    positions); None = all AMORTIZE.
     """
     c = np.ascontiguousarray(cache, dtype=np.uint16)
     layers, L, row = c.shape
@@ -188,8 +195,14 @@ def splice_request(cache: np.ndarray, dirs, repl: list[np.ndarray], latent_dim: 
             raise ValueError("replacement rows must be [layers][n_repl][row]")
     ptrs = (_u16p * max(n, 1))(*[_p(x, _u16p) for x in reps])
     out = np.zeros((layers, cap, row), dtype=np.uint16)
-    newlen = lib().lo_splice_request(layers, latent_dim, rope_dim, theta, layout, _p(c, _u16p), L, n,
-                                     _p(s, _i64p), _p(e, _i64p), _p(r, _i32p), ptrs, _p(out, _u16p), cap)
+    if modes is None:
+        newlen = lib().lo_splice_request(layers, latent_dim, rope_dim, theta, layout, _p(c, _u16p), L, n,
+                                         _p(s, _i64p), _p(e, _i64p), _p(r, _i32p), ptrs, _p(out, _u16p), cap)
+    else:
+        m = np.array(list(modes) or [0], dtype=np.int32)
+        newlen = lib().lo_splice_request_modes(layers, latent_dim, rope_dim, theta, layout, _p(c, _u16p), L, n,
+                                               _p(s, _i64p), _p(e, _i64p), _p(r, _i32p), _p(m, _i32p), ptrs,
+                                               _p(out, _u16p), cap)
     if newlen < 0:
         raise ValueError("invalid directives")
     return np.ascontiguousarray(out[:, :newlen])

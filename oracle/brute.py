@@ -75,13 +75,17 @@ def rerotate(kpe: list[int], t: int, p: int, theta: float, layout: int = 0) -> l
 
 
 def splice(rows: list[list[int]], dirs: list[tuple[int, int, list[list[int]]]],
-           latent_dim: int, theta: float, layout: int = 0) -> list[list[int]]:
+           latent_dim: int, theta: float, layout: int = 0, modes=None) -> list[list[int]]:
     """Splice one layer of one request.
 
     rows: bf16 rows (latent then k_pe) at positions 0..L-1.
     dirs: (s_start, s_end, R rows) with non-overlapping spans in the pre-call coordinates.
-    Returns the new rows: prefix and R copied, survivors re-encoded at their new positions.
+    modes: per directive, 0 = AMORTIZE (a survivor is re-encoded at its new position),
+    2 = EVICT (the KV-streams page's eviction: a survivor keeps its position).  With both,
+    a survivor is re-encoded at its new position minus the shift of the EVICT spans left of it.
+    Returns the new rows: prefix and R copied, survivors re-encoded.
     """
+    modes = list(modes) if modes is not None else [0] * len(dirs)
     items = [("old", t) for t in range(len(rows))]
     for k, (s, e, R) in sorted(enumerate(dirs), key=lambda kv: -kv[1][0]):
         items = items[:s] + [("repl", (k, i)) for i in range(len(R))] + items[e:]
@@ -92,5 +96,7 @@ def splice(rows: list[list[int]], dirs: list[tuple[int, int, list[list[int]]]],
             out.append(list(dirs[k][2][i]))
         else:
             row = rows[v]
-            out.append(list(row[:latent_dim]) + rerotate(row[latent_dim:], v, p, theta, layout))
+            # count the index shift that EVICT spans to the left contributed, and undo it
+            evict_shift = sum(len(R) - (e - s) for (s, e, R), m in zip(dirs, modes) if m == 2 and e <= v)
+            out.append(list(row[:latent_dim]) + rerotate(row[latent_dim:], v, p - evict_shift, theta, layout))
     return out

@@ -216,6 +216,22 @@ int64_t lo_splice_map(int64_t L, int32_t n, const int64_t* s_start, const int64_
     return len;
 }
 
+/* Rotation of a surviving token t: the summed Delta of the directives left of it
+ * (s_end <= t) whose mode turns positions.  Mode 0 (AMORTIZE, "Leyline: KV Cache
+ * Directives for Agentic Inference" section 2.1) re-indexes and re-encodes the
+ * downstream tokens; mode 2 (EVICT, the KV-streams page: evict without resetting
+ * positions) re-indexes them but keeps the positions they were encoded at.
+ * modes == NULL means every directive is AMORTIZE. */
+static int64_t lo_turn_of(int64_t t, int32_t n, const int64_t* s_start, const int64_t* s_end,
+                          const int32_t* n_repl, const int32_t* modes)
+{
+    int64_t a = 0;
+    for (int32_t k = 0; k < n; ++k)
+        if (s_end[k] <= t && (!modes || modes[k] == 0))
+            a += (int64_t)n_repl[k] - (s_end[k] - s_start[k]);
+    return a;
+}
+
 /* Splice the whole logical cache of one request.
  *   cache_in  : bf16 [num_layers][L][row], row = latent_dim + rope_dim, k_pe last
  *   repl[k]   : bf16 [num_layers][n_repl[k]][row], rows of R for directive k
@@ -223,10 +239,26 @@ int64_t lo_splice_map(int64_t L, int32_t n, const int64_t* s_start, const int64_
  * Latents, prefix rows and R rows are copied bit for bit; k_pe of a surviving
  * token moved from t to p is re-encoded from scratch (lo_rerotate).  Returns the
  * new length or -1 (as lo_splice_map). */
+int64_t lo_splice_request_modes(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
+                                const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
+                                const int64_t* s_end, const int32_t* n_repl, const int32_t* modes,
+                                const uint16_t* const* repl, uint16_t* cache_out, int64_t cap);
+
 int64_t lo_splice_request(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
                           const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
                           const int64_t* s_end, const int32_t* n_repl, const uint16_t* const* repl,
                           uint16_t* cache_out, int64_t cap)
+{
+    return lo_splice_request_modes(num_layers, latent_dim, rope_dim, theta, layout, cache_in, L, n, s_start, s_end,
+                                   n_repl, NULL, repl, cache_out, cap);
+}
+
+/* As lo_splice_request, with a mode per directive (see lo_turn_of): a surviving
+ * token t is re-encoded from position t to position t + turn(t). */
+int64_t lo_splice_request_modes(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
+                                const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
+                                const int64_t* s_end, const int32_t* n_repl, const int32_t* modes,
+                                const uint16_t* const* repl, uint16_t* cache_out, int64_t cap)
 {
     const int row = latent_dim + rope_dim;
     int32_t* kind = (int32_t*)malloc(sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1));
@@ -243,9 +275,10 @@ int64_t lo_splice_request(int num_layers, int latent_dim, int rope_dim, double t
                     memcpy(dst, src, sizeof(uint16_t) * (size_t)row);
                 } else {
                     int64_t t = idx[p];
+                    int64_t to = t + lo_turn_of(t, n, s_start, s_end, n_repl, modes);
                     const uint16_t* src = cache_in + ((int64_t)l * L + t) * row;
                     memcpy(dst, src, sizeof(uint16_t) * (size_t)latent_dim);
-                    lo_rerotate(src + latent_dim, 1, rope_dim, &t, &p, theta, layout, dst + latent_dim);
+                    lo_rerotate(src + latent_dim, 1, rope_dim, &t, &to, theta, layout, dst + latent_dim);
                 }
             }
         }

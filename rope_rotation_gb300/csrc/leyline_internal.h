@@ -27,6 +27,9 @@ struct Plan {
     std::vector<Seg> segs;
     std::vector<float> trig;  // per ROT segment: rope_dim / 2 pairs of (cos, sin) of Delta * theta_j
     int32_t n_trig = 0;       // ROT segments
+    bool reindex = false;     // the call re-indexes (block size 1, LEYLINE_POOL_REINDEX)
+    int64_t total_prep = 0;   // re-index: prep items (staged entries + dropped tokens)
+    int64_t total_stage = 0;  // re-index: staged table entries
     int64_t total_tiles = 0;  // move+rotate tiles over all requests
     int64_t total_commit = 0; // commit work items over all requests
     int64_t total_pop = 0;    // fresh pages
@@ -42,7 +45,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
 
 // A plan small enough to travel as a kernel parameter (__grid_constant__): no
 // host-to-device copy and no plan buffer on the path.
-constexpr int kParamReqs = 8;
+constexpr int kParamReqs = 8;  // 104 bytes each
 constexpr int kParamSegs = 24;
 constexpr int kParamTrigFloats = 640;  // 10 rotated segments of a 64-wide rope band
 struct alignas(16) ParamPlan {
@@ -70,13 +73,17 @@ struct SpliceArgs {
     const ReqPlan* reqs;      // plan in device memory (when it is not a kernel parameter)
     const Seg* segs;
     const float* trig;
+    int32_t* stage;           // re-index: staged table entries [total_stage]
     int32_t* status;          // device status word
+    int64_t total_prep;
     int64_t total_tiles;
     int64_t total_commit;
     int32_t n_reqs;
     int32_t n_trig;
     int32_t max_blocks;
     int32_t move_kernel;      // MoveKernel
+    int32_t reindex;          // 1: prep + in-place rotation + staged commit
+    int32_t pad2;
     Geometry g;
 };
 
@@ -91,6 +98,8 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
                   int64_t t1, void* out, int32_t* status, void* stream);
 // Resident CTAs per SM of the vector move+rotate kernel (occupancy query).
 int move_rotate_blocks_per_sm(int* blocks);
+// Resident CTAs per SM of the in-place rotation kernel of re-index mode.
+int rotate_in_place_blocks_per_sm(int* blocks);
 // Allow the bulk kernel its shared memory for rows of row_bytes and report its
 // resident CTAs per SM (0 if the rows are too wide for it).
 int bulk_prepare(int32_t row_bytes, int* blocks);
@@ -106,7 +115,10 @@ struct leyline_pool {
     int sm_count = 0;
     int move_blocks_per_sm = 1;
     int bulk_blocks_per_sm = 0;
+    int reindex_blocks_per_sm = 1;
     int32_t move_kernel = 0;  // MoveKernel used by this pool
+    int32_t* d_stage = nullptr;  // re-index: staged table entries
+    size_t d_stage_cap = 0;      // entries
     int32_t* d_queue = nullptr;  // free-page ring, 2 * num_pages entries
     int64_t q_cap = 0;
     int64_t q_head = 0;          // monotonic: next page to take is d_queue[q_head % q_cap]

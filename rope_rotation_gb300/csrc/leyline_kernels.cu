@@ -157,16 +157,31 @@ struct RowDesc {
     int pad;
 };
 
-__device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v, bool by_tile)
+enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2 };
+
+// Last request whose first tile / commit item / prep item is <= v.
+__device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v, int key_kind)
 {
     int lo = 0, hi = n - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        const long long key = by_tile ? reqs[mid].tile_begin : reqs[mid].commit_begin;
+        const long long key = key_kind == BY_TILE     ? reqs[mid].tile_begin
+                              : key_kind == BY_COMMIT ? reqs[mid].commit_begin
+                                                      : reqs[mid].prep_begin;
         if (key <= v) lo = mid;
         else hi = mid - 1;
     }
     return lo;
+}
+
+// Segment of destination row p among a request's row segments (linear: at most
+// 2 per directive plus one).
+__device__ __forceinline__ int find_seg(const Seg* sg, int count, long long p)
+{
+    int k = 0;
+    for (int q = 1; q < count; ++q)
+        if (sg[q].new_start <= p) k = q;
+    return k;
 }
 
 __device__ __forceinline__ long long ring(long long i, long long cap) { return i % cap; }
@@ -178,7 +193,7 @@ __device__ __forceinline__ long long ring(long long i, long long cap) { return i
 __device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long tile, int i)
 {
     RowDesc d{nullptr, nullptr, 0, -1, 0};
-    const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, true)];
+    const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
     const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + i;
     if (p >= rp.new_len) return d;
     const Seg* sg = pv.segs + rp.seg_begin;
@@ -673,7 +688,7 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
     long long k = 0;
     int old = -1, fresh = -1;
     if (i < a.total_commit) {
-        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, false)];
+        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
         k = i - rp->commit_begin;
         if (k < rp->n_old) old = a.table_w[(long long)rp->req * a.max_blocks + rp->b0 + k];
         if (k < rp->n_new) fresh = a.free_q[ring(a.pop_base + rp->pop_off + k, a.q_cap)];
@@ -694,10 +709,234 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
         }
         i += stride;
         if (i >= a.total_commit) break;
-        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, false)];
+        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
         k = i - rp->commit_begin;
         old = k < rp->n_old ? a.table_w[(long long)rp->req * a.max_blocks + rp->b0 + k] : -1;
         fresh = k < rp->n_new ? a.free_q[ring(a.pop_base + rp->pop_off + k, a.q_cap)] : -1;
+    }
+}
+
+// -------------------------------------------------------------------------
+// Re-index mode (block size 1, pool flag LEYLINE_POOL_REINDEX): a surviving
+// downstream token keeps its page.  Three kernels, each a programmatic dependent
+// of the one before:
+//   prep          stages the page of every rewritten table entry (the kept token's
+//                 old page, or a fresh page for a row of R) and returns the pages
+//                 of dropped tokens to the ring; it reads the old table and writes
+//                 only the staging array and the ring's push region;
+//   rotate        turns the rope band of every turned row in place (128 bytes read
+//                 and written per row and layer; the latent is not touched) and
+//                 copies rows of R into their fresh pages;
+//   commit        installs the staged entries, clears entries past the new end,
+//                 writes the new length.
+template <class PlanSrc>
+__global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_constant__ PlanSrc plan)
+{
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_prep; i += stride) {
+        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_PREP)];
+        const long long k = i - rp.prep_begin;
+        const long long rows = rp.new_len - rp.row0;
+        const int32_t* trow = a.table + (long long)rp.req * a.max_blocks;
+        if (k < rows) {
+            const long long p = rp.row0 + k;
+            const Seg* sg = pv.segs + rp.seg_begin;
+            const Seg s = sg[find_seg(sg, rp.seg_count, p)];
+            int page;
+            if (s.kind == SEG_REPL) {
+                page = a.free_q[ring(a.pop_base + rp.pop_off + s.aux + (p - s.new_start), a.q_cap)];
+                if (page < 0 || page >= a.g.num_pages) {
+                    raise_status(a.status, ST_BAD_FRESH);
+                    page = -1;
+                }
+            } else {
+                const long long t = s.src_start + (p - s.new_start);
+                page = (t >= 0 && t < a.max_blocks) ? trow[t] : -1;
+                if (page < 0 || page >= a.g.num_pages) {
+                    raise_status(a.status, ST_BAD_PAGE);
+                    page = -1;
+                }
+            }
+            a.stage[rp.stage_begin + k] = page;
+        } else {
+            const long long j = k - rows;  // j-th dropped token of the request
+            const Seg* dg = pv.segs + rp.drop_seg_begin;
+            int q = 0;
+            for (int x = 1; x < rp.drop_seg_count; ++x)
+                if (dg[x].aux <= j) q = x;
+            const long long t = dg[q].src_start + (j - dg[q].aux);
+            int page = (t >= 0 && t < a.max_blocks) ? trow[t] : -1;
+            if (page < 0 || page >= a.g.num_pages) {
+                raise_status(a.status, ST_BAD_OLD);
+                page = -1;
+            }
+            a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
+        }
+    }
+}
+
+// 16-byte load that may be followed by a store to the same address (no .nc path).
+__device__ __forceinline__ uint4 ld_rw(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Rotate kernel of re-index mode.  Work unit = (16-row tile, group of layers): the
+// 256 threads take the tile's rope-band work items (4 per row for half-split pairs,
+// 8 interleaved) for as many layers as fit, turning each band in place; rows of R
+// are copied whole into their fresh pages.  A band is 128 bytes every 1152, so this
+// kernel is bound by DRAM row activations rather than by streaming bandwidth.
+struct ReindexRow {
+    uint4* row;          // the row's page (layer 0); nullptr: nothing to do
+    const uint4* rsrc;   // row of R (layer 0), REPL only
+    long long rstride;   // vectors between layers of R
+    int kind;            // SegKind, -1 past the end
+    int trig;
+};
+
+constexpr int kMaxRopeDim = 256;
+
+template <int kLayout, bool kBf16, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_constant__ SpliceArgs a,
+                                                                const __grid_constant__ PlanSrc plan)
+{
+    __shared__ ReindexRow rr[kTileRows];
+    __shared__ __align__(16) float trig_s[kTileRows][kMaxRopeDim];  // (cos, sin) per pair of each row
+    __shared__ int has_repl;
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const long long L = a.g.num_layers;
+    const long long layer_vecs = a.g.layer_vecs;
+    const int rvv = a.g.rope_vecs, lv = a.g.latent_vecs, row_vecs = a.g.row_vecs;
+    const int rope_dim = a.g.rope_dim;
+    const int ipr = kLayout == 0 ? rvv / 2 : rvv;  // work items per row and layer
+    const int per_layer = kTileRows * ipr;
+    const int lpu = blockDim.x / per_layer > 0 ? (int)(blockDim.x / per_layer) : 1;  // layers per unit
+    const long long groups = (L + lpu - 1) / lpu;
+    long long u0, u1;
+    my_units(a.total_tiles * groups, u0, u1);
+    long long cur_tile = -1;
+    for (long long u = u0; u < u1; ++u) {
+        const long long tile = u / groups;
+        const long long layer0 = (u - tile * groups) * lpu;
+        if (tile != cur_tile) {
+            __syncthreads();
+            if (threadIdx.x == 0) has_repl = 0;
+            __syncthreads();
+            if (threadIdx.x < kTileRows) {
+                ReindexRow d{nullptr, nullptr, 0, -1, -1};
+                const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
+                const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + threadIdx.x;
+                if (p < rp.new_len) {
+                    const Seg* sg = pv.segs + rp.seg_begin;
+                    const Seg s = sg[find_seg(sg, rp.seg_count, p)];
+                    const int page = a.stage[rp.stage_begin + (p - rp.row0)];
+                    d.kind = s.kind;
+                    if (page >= 0 && page < a.g.num_pages) d.row = static_cast<uint4*>(a.kv) + (long long)page * row_vecs;
+                    if (s.kind == SEG_ROT) d.trig = s.trig;
+                    if (s.kind == SEG_REPL) {
+                        d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * row_vecs;
+                        d.rstride = (long long)s.n_repl * row_vecs;
+                        atomicOr(&has_repl, 1);
+                    }
+                }
+                rr[threadIdx.x] = d;
+            }
+            __syncthreads();
+            for (int e = threadIdx.x; e < kTileRows * rope_dim; e += blockDim.x) {
+                const int row = e / rope_dim, c = e - row * rope_dim;
+                const int t = rr[row].trig;
+                trig_s[row][c] = t >= 0 ? pv.trig[(long long)t * rope_dim + c] : 0.f;
+            }
+            __syncthreads();
+            cur_tile = tile;
+        }
+        // rope bands of turned rows, in place
+        for (int e = threadIdx.x; e < lpu * per_layer; e += blockDim.x) {
+            const int lo = e / per_layer, it = e - (e / per_layer) * per_layer;
+            const long long layer = layer0 + lo;
+            if (layer >= L) continue;
+            const int i = it / ipr, q = it - (it / ipr) * ipr;
+            const ReindexRow d = rr[i];
+            if (d.kind == SEG_ROT && d.row) {
+                uint4* r = d.row + layer * layer_vecs + lv;
+                float cs[8], sn[8];
+                const int np = kLayout == 0 ? 8 : 4;
+                const float* tp = &trig_s[i][2 * np * q];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) {
+                    if (w < np) {
+                        cs[w] = tp[2 * w];
+                        sn[w] = tp[2 * w + 1];
+                    }
+                }
+                if (kLayout == 0) {
+                    uint4 x = ld_rw(r + q), y = ld_rw(r + q + rvv / 2);
+                    rotate_half_split<kBf16>(x, y, cs, sn);
+                    st_stream(r + q, x);
+                    st_stream(r + q + rvv / 2, y);
+                } else {
+                    uint4 x = ld_rw(r + q);
+                    rotate_interleaved<kBf16>(x, cs, sn);
+                    st_stream(r + q, x);
+                }
+            }
+        }
+        // rows of R: whole rows into their fresh pages
+        if (has_repl) {
+            const int per_row = lpu * row_vecs;
+            for (int e = threadIdx.x; e < kTileRows * per_row; e += blockDim.x) {
+                const int i = e / per_row, rem = e - (e / per_row) * per_row;
+                const int lo2 = rem / row_vecs, c = rem - (rem / row_vecs) * row_vecs;
+                const long long lay = layer0 + lo2;
+                const ReindexRow d = rr[i];
+                if (d.kind != SEG_REPL || !d.row || lay >= L) continue;
+                st_stream(d.row + lay * layer_vecs + c, ld_stream(d.rsrc + lay * d.rstride + c));
+            }
+        }
+    }
+}
+
+// Commit of a re-indexed call: staged entries into [row0, new_len), -1 into
+// [new_len, old_len), the new length.  The staged values are final before the
+// rotate kernel starts and it never writes them, so they are loaded before
+// griddepcontrol.wait.
+template <class PlanSrc>
+__global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_constant__ SpliceArgs a,
+                                                                 const __grid_constant__ PlanSrc plan)
+{
+    const PlanView pv = plan_view(a, plan);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    int val = -1;
+    const ReqPlan* rp = nullptr;
+    long long k = 0;
+    if (i < a.total_commit) {
+        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
+        k = i - rp->commit_begin;
+        if (k < rp->new_len - rp->row0) val = a.stage[rp->stage_begin + k];
+    }
+    wait_for_previous_grid();
+    allow_next_grid();
+    while (i < a.total_commit) {
+        int32_t* trow = a.table_w + (long long)rp->req * a.max_blocks;
+        const long long rows = rp->new_len - rp->row0;
+        if (k == 0) a.seq_lens_dev[rp->req] = (int32_t)rp->new_len;
+        if (k < rows) trow[rp->row0 + k] = val;
+        else if (rp->new_len + (k - rows) < rp->old_len) trow[rp->new_len + (k - rows)] = -1;
+        i += stride;
+        if (i >= a.total_commit) break;
+        rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
+        k = i - rp->commit_begin;
+        val = k < rp->new_len - rp->row0 ? a.stage[rp->stage_begin + k] : -1;
     }
 }
 
@@ -803,8 +1042,38 @@ cudaError_t launch_move(const SpliceArgs& a, const PlanSrc& plan, int grid, cuda
 }
 
 template <class PlanSrc>
+int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s, cudaEvent_t t0, cudaEvent_t t1)
+{
+    cudaError_t e = cudaSuccess;
+    if (a.total_prep > 0)
+        e = launch_dependent(prep_reindex<PlanSrc>, grid_for(a.total_prep, 256, 8192), 256, s, a, plan);
+    const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
+    const int ipr = split ? a.g.rope_vecs / 2 : a.g.rope_vecs;
+    const int lpu = kMoveThreads / (kTileRows * ipr) > 0 ? kMoveThreads / (kTileRows * ipr) : 1;
+    const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
+    if (grid > units) grid = (int)std::max<long long>(units, 1);
+    if (e == cudaSuccess && t0) e = cudaEventRecord(t0, s);
+    if (e == cudaSuccess && units > 0) {
+        if (split)
+            e = bf16 ? launch_dependent(rotate_in_place<0, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                     : launch_dependent(rotate_in_place<0, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+        else
+            e = bf16 ? launch_dependent(rotate_in_place<1, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                     : launch_dependent(rotate_in_place<1, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+    }
+    if (e == cudaSuccess && t1) e = cudaEventRecord(t1, s);
+    if (e == cudaSuccess && a.total_commit > 0)
+        e = launch_dependent(commit_reindex<PlanSrc>, grid_for(a.total_commit, kCommitThreads, 8192), kCommitThreads, s,
+                             a, plan);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return (int)e;
+}
+
+template <class PlanSrc>
 int launch_both(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s, cudaEvent_t t0, cudaEvent_t t1)
 {
+    if (a.reindex) return launch_reindex(a, plan, grid, s, t0, t1);
     const long long units = a.total_tiles * a.g.num_layers;
     if (grid > units) grid = (int)std::max<long long>(units, 1);
     cudaError_t e = cudaSuccess;
@@ -848,6 +1117,12 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
         static_cast<const uint4*>(kv), table_row, g.block_size, g.row_vecs, (long long)layer * g.layer_vecs,
         g.num_pages, t0, n, static_cast<uint4*>(out), status);
     return (int)cudaGetLastError();
+}
+
+int rotate_in_place_blocks_per_sm(int* blocks)
+{
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, rotate_in_place<0, false, ParamPlan>,
+                                                              kMoveThreads, 0);
 }
 
 int move_rotate_blocks_per_sm(int* blocks)

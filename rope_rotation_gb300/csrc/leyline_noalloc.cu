@@ -19,8 +19,9 @@
 // the array: calls that overlap on the GPU (on different streams, or from
 // different pools, without ordering between them) race on it.  Calls on one pool
 // are ordered by the pool, as for leyline_splice.  Each call writes every byte
-// its kernels read (the uploaded plan), so nothing has to start at zero and what
-// the previous call left behind is never read.
+// its kernels read (the uploaded plan; in re-index mode also the staged table
+// entries, written by the prep kernel before anything reads them), so nothing has
+// to start at zero and what the previous call left behind is never read.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -93,9 +94,12 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
                          "their tables were not filled from this pool");
 
     // scratch layout: reqs | segs | trig (cos, sin per pair of every rotated segment)
+    //                 | staged table entries (re-index mode)
     const size_t off_segs = align_up(sizeof(ReqPlan) * plan.reqs.size(), 16);
     const size_t off_trig = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
-    const size_t total = off_trig + sizeof(float) * plan.trig.size();
+    const size_t upload = off_trig + sizeof(float) * plan.trig.size();
+    const size_t off_stage = align_up(upload, 16);
+    const size_t total = off_stage + sizeof(int32_t) * (size_t)plan.total_stage;
     if (total > kNoallocScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
@@ -132,7 +136,7 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     if (!plan.trig.empty()) memcpy(g_host_plan + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
     // From pageable memory: the copy is staged before the call returns, so the
     // static host buffer may be reused by the next call.
-    e = cudaMemcpyAsync(scratch, g_host_plan, total, cudaMemcpyHostToDevice, stream);
+    e = cudaMemcpyAsync(scratch, g_host_plan, upload, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return cuda_fail(e, "uploading the plan");
 
     SpliceArgs a{};
@@ -147,6 +151,11 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.reqs = reinterpret_cast<const ReqPlan*>(scratch);
     a.segs = reinterpret_cast<const Seg*>(scratch + off_segs);
     a.trig = reinterpret_cast<const float*>(scratch + off_trig);
+    if (plan.reindex) {
+        a.stage = reinterpret_cast<int32_t*>(scratch + off_stage);
+        a.total_prep = plan.total_prep;
+        a.reindex = 1;
+    }
     a.status = p->d_status;
     a.total_tiles = plan.total_tiles;
     a.total_commit = plan.total_commit;
@@ -156,7 +165,9 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.g = p->g;
 
     a.move_kernel = p->move_kernel;
-    const int grid = p->sm_count * (p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm : p->move_blocks_per_sm);
+    const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
+                                    : p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
+                                                                  : p->move_blocks_per_sm);
     int err = launch_splice(a, nullptr, grid, stream, nullptr, nullptr);
     if (err != 0) return cuda_fail((cudaError_t)err, "launching the splice kernels");
     e = cudaEventRecord(p->done, stream);

@@ -9,6 +9,12 @@
 //   ROT    a surviving run moved by Delta != 0; its rope band is turned by R(Delta)
 // The kernels look up the segment of a destination row, read the source row
 // through the old block table (or from R), and write it into a fresh page.
+// A re-indexed request (block size 1, pool flag LEYLINE_POOL_REINDEX) keeps its
+// surviving rows in their pages instead: a prep kernel stages the new table
+// entries (the old page of each kept row, a fresh page for each row of R) and
+// returns the pages of the dropped tokens (DROP segments) to the free ring; the
+// move kernel turns the rope bands of ROT rows in place and copies R rows; the
+// commit kernel installs the staged entries.
 #pragma once
 
 #include <cstdint>
@@ -17,7 +23,7 @@ namespace leyline {
 
 constexpr int kTileRows = 16;  // destination rows per move+rotate tile
 
-enum SegKind : int32_t { SEG_HEAD = 0, SEG_REPL = 1, SEG_COPY = 2, SEG_ROT = 3 };
+enum SegKind : int32_t { SEG_HEAD = 0, SEG_REPL = 1, SEG_COPY = 2, SEG_ROT = 3, SEG_DROP = 4 };
 
 struct Geometry {
     int32_t num_layers;
@@ -33,6 +39,8 @@ struct Geometry {
     double theta;
     int32_t pair_layout;
     int32_t precision;
+    uint32_t flags;       // LEYLINE_POOL_* bits
+    int32_t pad;
 };
 
 struct ReqPlan {
@@ -47,21 +55,27 @@ struct ReqPlan {
     int64_t commit_begin;  // first flat commit index of this request
     int32_t seg_begin;
     int32_t seg_count;
-    int32_t pop_off;       // into the staged fresh pages
-    int32_t push_off;      // into the push region of the free stack
+    int32_t pop_off;       // first fresh page of this request in the ring's pop region
+    int32_t push_off;      // first returned page of this request in the ring's push region
+    int64_t stage_begin;   // re-index: first staged table entry of this request
+    int64_t prep_begin;    // re-index: first flat prep item of this request
+    int64_t drop_count;    // re-index: tokens dropped (pages returned)
+    int32_t drop_seg_begin;
+    int32_t drop_seg_count;
 };
 
 struct Seg {
-    int64_t new_start;     // first destination row of the segment
-    int64_t src_start;     // source position (HEAD/COPY/ROT) or row index in R (REPL)
+    int64_t new_start;     // first destination row of the segment (not used by DROP)
+    int64_t src_start;     // source position (HEAD/COPY/ROT/DROP) or row index in R (REPL)
     const void* repl;      // R rows [num_layers][n_repl][row] (REPL only)
     int32_t kind;          // SegKind
     int32_t trig;          // trig table entry (ROT only), else -1
-    int32_t n_repl;        // rows of R per layer (REPL only)
-    int32_t pad;
+    int32_t n_repl;        // rows of R per layer (REPL); dropped tokens (DROP)
+    int32_t aux;           // re-index: R rows of the request before this segment (REPL),
+                           // dropped tokens of the request before this segment (DROP)
 };
 
-static_assert(sizeof(ReqPlan) == 72, "ReqPlan layout");
+static_assert(sizeof(ReqPlan) == 104, "ReqPlan layout");
 static_assert(sizeof(Seg) == 40, "Seg layout");
 
 }  // namespace leyline

@@ -99,6 +99,10 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pair_layout");
     if (d->rotate_precision != LEYLINE_ROTATE_FP32 && d->rotate_precision != LEYLINE_ROTATE_BF16_NAIVE)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown rotate_precision");
+    if ((d->flags & ~(uint32_t)LEYLINE_POOL_REINDEX) != 0 || d->reserved != 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags or nonzero reserved field");
+    if ((d->flags & LEYLINE_POOL_REINDEX) && d->rope_dim > 256)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "LEYLINE_POOL_REINDEX supports rope_dim <= 256");
     g->num_layers = d->num_layers;
     g->latent_dim = d->latent_dim;
     g->rope_dim = d->rope_dim;
@@ -112,6 +116,8 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
     g->theta = d->rope_theta;
     g->pair_layout = d->pair_layout;
     g->precision = d->rotate_precision;
+    g->flags = d->flags;
+    g->pad = 0;
     return LEYLINE_OK;
 }
 
@@ -137,7 +143,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             snprintf(msg, sizeof msg, "directive %d: FORGET is served by a re-prefill, not by the splice", k);
             return set_error(LEYLINE_ERR_UNSUPPORTED_MODE, msg);
         }
-        if (d.mode != LEYLINE_AMORTIZE) {
+        if (d.mode != LEYLINE_AMORTIZE && d.mode != LEYLINE_EVICT) {
             snprintf(msg, sizeof msg, "directive %d: unknown mode %d", k, d.mode);
             return set_error(LEYLINE_ERR_UNSUPPORTED_MODE, msg);
         }
@@ -180,7 +186,11 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     }
 
     // 3. plan each touched request
-    int64_t tiles = 0, commit = 0, pops = 0, pushes = 0;
+    const bool reindex = (g.flags & LEYLINE_POOL_REINDEX) && B == 1;
+    plan->reindex = reindex;
+    const int64_t row_bytes = (int64_t)g.row_elems * 2;
+    const int64_t rope_bytes = (int64_t)g.rope_dim * 2;
+    int64_t tiles = 0, commit = 0, pops = 0, pushes = 0, turned_rows = 0;
     leyline_stats_t& st = plan->stats;
     for (int32_t i = 0; i < n;) {
         const int32_t req = dirs[order[i]].req;
@@ -195,8 +205,16 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         if (eff.empty()) continue;
 
         const int64_t L = seq_lens_host[req];
-        int64_t delta_total = 0;
-        for (const auto* d : eff) delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
+        if (L > (int64_t)max_blocks * B) {
+            snprintf(msg, sizeof msg, "request %d: seq_len %lld exceeds the table capacity", req, (long long)L);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+        int64_t delta_total = 0, repl_total = 0, drop_total = 0;
+        for (const auto* d : eff) {
+            delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
+            repl_total += d->n_repl;
+            drop_total += d->s_end - d->s_start;
+        }
         const int64_t Lp = L + delta_total;
         if (Lp > (int64_t)max_blocks * B || Lp > INT32_MAX) {
             snprintf(msg, sizeof msg, "request %d: new length %lld exceeds the table capacity %lld", req,
@@ -209,37 +227,48 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         rp.row0 = (int64_t)rp.b0 * B;
         rp.old_len = L;
         rp.new_len = Lp;
-        rp.n_new = (int32_t)(ceil_div(Lp, B) - rp.b0);
-        rp.n_old = (int32_t)(ceil_div(L, B) - rp.b0);
+        if (reindex) {
+            rp.n_new = (int32_t)repl_total;  // fresh pages: one per row of R
+            rp.n_old = (int32_t)drop_total;  // returned pages: one per dropped token
+        } else {
+            rp.n_new = (int32_t)(ceil_div(Lp, B) - rp.b0);
+            rp.n_old = (int32_t)(ceil_div(L, B) - rp.b0);
+        }
         rp.seg_begin = (int32_t)plan->segs.size();
         rp.pop_off = (int32_t)pops;
         rp.push_off = (int32_t)pushes;
         rp.tile_begin = tiles;
         rp.commit_begin = commit;
 
-        // segments in new coordinates
+        // segments in new coordinates.  D: index shift left of the current position
+        // (every directive); A: rotation (AMORTIZE directives only, section 2.1; EVICT
+        // keeps positions).
         const int64_t s1 = eff.front()->s_start;
         if (rp.row0 < s1) {
             Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0};
             plan->segs.push_back(s);
             st.head_slots += s1 - rp.row0;
         }
-        int64_t D = 0;  // accumulated Delta left of the current position
+        int64_t D = 0, A = 0, repl_before = 0;
         for (size_t k = 0; k < eff.size(); ++k) {
             const leyline_directive_t* d = eff[k];
             if (d->n_repl > 0) {
-                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, 0};
+                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)repl_before};
                 plan->segs.push_back(s);
                 st.repl_slots += d->n_repl;
+                repl_before += d->n_repl;
             }
-            D += (int64_t)d->n_repl - (d->s_end - d->s_start);
+            const int64_t dk = (int64_t)d->n_repl - (d->s_end - d->s_start);
+            D += dk;
+            if (d->mode == LEYLINE_AMORTIZE) A += dk;
             const int64_t run_end = (k + 1 < eff.size()) ? eff[k + 1]->s_start : L;
             if (run_end > d->s_end) {
-                Seg s{d->s_end + D, d->s_end, nullptr, D == 0 ? SEG_COPY : SEG_ROT, -1, 0, 0};
-                if (D != 0) {
+                Seg s{d->s_end + D, d->s_end, nullptr, A == 0 ? SEG_COPY : SEG_ROT, -1, 0, 0};
+                if (A != 0) {
                     s.trig = plan->n_trig++;
                     plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
-                    segment_trig(g, D, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                    segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                    turned_rows += run_end - d->s_end;
                 }
                 plan->segs.push_back(s);
                 st.downstream_slots += run_end - d->s_end;
@@ -253,7 +282,27 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         }
         const int64_t rows = Lp - rp.row0;
         tiles += ceil_div(rows, kTileRows);
-        commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
+        if (reindex) {
+            rp.drop_seg_begin = (int32_t)plan->segs.size();
+            int64_t drops_before = 0;
+            for (const auto* d : eff) {
+                const int64_t len = d->s_end - d->s_start;
+                if (len == 0) continue;
+                Seg s{-1, d->s_start, nullptr, SEG_DROP, -1, (int32_t)len, (int32_t)drops_before};
+                plan->segs.push_back(s);
+                drops_before += len;
+            }
+            rp.drop_seg_count = (int32_t)plan->segs.size() - rp.drop_seg_begin;
+            rp.drop_count = drop_total;
+            rp.stage_begin = plan->total_stage;
+            rp.prep_begin = plan->total_prep;
+            plan->total_stage += rows;
+            plan->total_prep += rows + drop_total;
+            const int64_t tail = L > Lp ? L - Lp : 0;  // table entries past the new end
+            commit += std::max<int64_t>(1, rows + tail);
+        } else {
+            commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
+        }
         pops += rp.n_new;
         pushes += rp.n_old;
         plan->reqs.push_back(rp);
@@ -267,13 +316,17 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     plan->total_commit = commit;
     plan->total_pop = pops;
     plan->total_push = pushes;
-    const int64_t row_bytes = (int64_t)g.row_elems * 2;
-    st.algorithmic_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots);
-    st.moved_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots + st.head_slots);
+    if (reindex) {
+        st.algorithmic_bytes = 2 * g.num_layers * (rope_bytes * turned_rows + row_bytes * st.repl_slots);
+        st.moved_bytes = st.algorithmic_bytes;
+    } else {
+        st.algorithmic_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots);
+        st.moved_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots + st.head_slots);
+    }
     st.pages_popped = pops;
     st.pages_pushed = pushes;
     st.requests_touched = (int32_t)plan->reqs.size();
-    st.kernels_launched = plan->reqs.empty() ? 0 : 2;
+    st.kernels_launched = plan->reqs.empty() ? 0 : (reindex ? 3 : 2);
     return LEYLINE_OK;
 }
 

@@ -122,6 +122,9 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         return r;
     }
     if (p->move_blocks_per_sm < 1) p->move_blocks_per_sm = 1;
+    if ((cudaError_t)rotate_in_place_blocks_per_sm(&p->reindex_blocks_per_sm) != cudaSuccess ||
+        p->reindex_blocks_per_sm < 1)
+        p->reindex_blocks_per_sm = 1;
     {
         int err = bulk_prepare(g.row_vecs * 16, &p->bulk_blocks_per_sm);
         if (err != 0) {
@@ -158,6 +161,7 @@ int leyline_pool_destroy(leyline_pool_t* p)
     if (p->h_plan) cudaFreeHost(p->h_plan);
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_queue) cudaFree(p->d_queue);
+    if (p->d_stage) cudaFree(p->d_stage);
     delete p;
     return LEYLINE_OK;
 }
@@ -278,6 +282,22 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     a.g = p->g;
 
     cudaError_t e;
+    if (plan.reindex) {
+        if ((size_t)plan.total_stage > p->d_stage_cap) {
+            rc = wait_pool(p);
+            if (rc != LEYLINE_OK) return rc;
+            if (p->d_stage) cudaFree(p->d_stage);
+            p->d_stage = nullptr;
+            p->d_stage_cap = 0;
+            const size_t cap = std::max<size_t>((size_t)plan.total_stage * 2, 1 << 14);
+            e = cudaMalloc(&p->d_stage, sizeof(int32_t) * cap);
+            if (e != cudaSuccess) return cuda_error(e, "allocating the staging buffer");
+            p->d_stage_cap = cap;
+        }
+        a.stage = p->d_stage;
+        a.total_prep = plan.total_prep;
+        a.reindex = 1;
+    }
     rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
     const bool in_params = plan_fits_params(plan);
@@ -342,7 +362,9 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         ++p->tev_used;
     }
     a.move_kernel = p->move_kernel;
-    const int grid = p->sm_count * (p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm : p->move_blocks_per_sm);
+    const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
+                                    : p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
+                                                                  : p->move_blocks_per_sm);
     int err = launch_splice(a, in_params ? &pp : nullptr, grid, stream, t0, t1);
     if (err != 0) return cuda_error((cudaError_t)err, "launching the splice kernels");
     rc = mark_done(p, stream);

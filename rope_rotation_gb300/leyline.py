@@ -35,6 +35,8 @@ LEYLINE_ROTATE_FP32 = 0
 LEYLINE_ROTATE_BF16_NAIVE = 1
 LEYLINE_AMORTIZE = 0
 LEYLINE_FORGET = 1
+LEYLINE_EVICT = 2
+LEYLINE_POOL_REINDEX = 1
 
 
 class LeylineError(RuntimeError):
@@ -46,7 +48,8 @@ class LeylineError(RuntimeError):
 class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("latent_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_pages", ctypes.c_int64), ("rope_theta", ctypes.c_double),
-                ("pair_layout", ctypes.c_int32), ("rotate_precision", ctypes.c_int32)]
+                ("pair_layout", ctypes.c_int32), ("rotate_precision", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_int32)]
 
 
 class BlockTable(ctypes.Structure):
@@ -143,9 +146,9 @@ def _tensor_ptr(t) -> int:
 
 def pool_desc(num_layers: int, block_size: int, num_pages: int, latent_dim: int = 512, rope_dim: int = 64,
               rope_theta: float = 10000.0, pair_layout: int = LEYLINE_PAIRS_HALF_SPLIT,
-              rotate_precision: int = LEYLINE_ROTATE_FP32) -> PoolDesc:
+              rotate_precision: int = LEYLINE_ROTATE_FP32, flags: int = 0) -> PoolDesc:
     return PoolDesc(num_layers, latent_dim, rope_dim, block_size, num_pages, rope_theta, pair_layout,
-                    rotate_precision)
+                    rotate_precision, flags, 0)
 
 
 def leyline_pool_create(desc: PoolDesc, kv) -> ctypes.c_void_p:

@@ -25,6 +25,7 @@ class Dir:
     s_end: int
     n_repl: int
     key: int
+    mode: int = 0  # 0 AMORTIZE (re-encode survivors), 2 EVICT (keep their positions)
 
 
 @dataclass

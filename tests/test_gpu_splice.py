@@ -139,3 +139,83 @@ def test_dsv2_lite_32k_workload_full(move_kernel):
     assert st["algorithmic_bytes"] == 2304 * 27 * (6768 + 12)
     print("cfg2 rope parity:", {k: v for k, v in c.items() if k != "stats"})
     cache.close()
+
+
+# ------------------------------------------------------------------------------
+# EVICT (KV-streams page: evict without resetting positions): survivors move but keep
+# the positions they were encoded at; mixed with AMORTIZE, a survivor is turned by the
+# AMORTIZE shifts left of it only.
+MODES = [
+    (60, [(5, 20, 3, 2)]),                                  # evict only: pure move
+    (60, [(5, 20, 3, 2), (30, 40, 0, 0)]),                  # evict then amortize
+    (60, [(5, 20, 3, 0), (30, 40, 0, 2), (50, 52, 9, 0)]),  # amortize, evict, amortize
+    (48, [(0, 48, 5, 2)]),
+]
+
+
+@pytest.mark.parametrize("B", [1, 16])
+def test_evict_and_mixed_modes(B, move_kernel):
+    for i, (L, dirs) in enumerate(MODES):
+        w = Workload(f"modes{i}-B{B}", 3, B, [L],
+                     [[Dir(0, s, e, n, k, mode=m) for k, (s, e, n, m) in enumerate(dirs)]], seed=20 + i)
+        cache = H.make_cache(w)
+        H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0])
+        cache.close()
+
+
+# ------------------------------------------------------------------------------
+# Re-index mode (block size 1, LEYLINE_POOL_REINDEX): survivors keep their pages, only
+# the table entries move and rope bands turn in place.
+REINDEX = 1
+
+
+def test_reindex_edge_grid():
+    for i, (L, dirs) in enumerate(EDGE + [(60, [(5, 20, 3), (30, 40, 0)])]):
+        w = Workload(f"reindex{i}", 3, 1, [L], [[Dir(0, s, e, n, k) for k, (s, e, n) in enumerate(dirs)]], seed=30 + i)
+        cache = H.make_cache(w, flags=REINDEX)
+        c = H.splice_step_and_check(w, cache, H.oracle_state(w), w.steps[0])
+        st = c["stats"]
+        assert st["kernels_launched"] == 3
+        assert st["pages_popped"] == sum(n for (_, _, n) in dirs if not (n == 0))
+        cache.close()
+
+
+def test_reindex_many_requests_chained_and_modes():
+    lengths = [70, 16, 0, 129, 33]
+    steps = [
+        [Dir(0, 10, 40, 3, 0), Dir(1, 0, 16, 0, 1), Dir(3, 64, 64, 20, 2), Dir(3, 100, 120, 1, 3),
+         Dir(4, 32, 33, 1, 4), Dir(2, 0, 0, 5, 5)],
+        [Dir(0, 0, 1, 0, 6, mode=2), Dir(3, 1, 2, 2, 7), Dir(4, 0, 0, 0, 8)],
+        [Dir(2, 5, 5, 17, 9), Dir(0, 30, 42, 7, 10), Dir(3, 40, 41, 0, 11, mode=2)],
+    ]
+    w = Workload("reindex-multi", 2, 1, lengths, steps, seed=12)
+    cache = H.make_cache(w, slack_pages=8, flags=REINDEX)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step)
+    cache.close()
+
+
+@pytest.mark.parametrize("layout,precision,latent,rope", [(0, 0, 512, 64), (1, 0, 512, 64), (0, 1, 512, 64),
+                                                          (1, 0, 64, 16), (0, 0, 64, 128)])
+def test_reindex_layouts_precisions_shapes(layout, precision, latent, rope):
+    w = Workload(f"reindex-l{layout}-p{precision}-{latent}-{rope}", 2, 1, [300, 211],
+                 [[Dir(0, 40, 200, 7, 0), Dir(1, 3, 50, 60, 1)], [Dir(0, 0, 5, 1, 2)]], seed=13,
+                 latent_dim=latent, rope_dim=rope)
+    cache = H.make_cache(w, pair_layout=layout, precision=precision, flags=REINDEX)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step, layout=layout, precision=precision)
+    cache.close()
+
+
+def test_reindex_chain_matches_oracle_chain_call_by_call():
+    """16 chained splices on 6 layers x 32768 tokens: every call checked against the oracle
+    applied to its own previous state."""
+    w = configs.chain_64(seed=3, num_layers=6, length=32768, n_steps=16)
+    cache = H.make_cache(w, flags=REINDEX)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        c = H.splice_step_and_check(w, cache, state, step, guard=False)
+        assert c["stats"]["algorithmic_bytes"] == 2 * 6 * (128 * c["stats"]["downstream_slots"] + 1152 * 12)
+    cache.close()

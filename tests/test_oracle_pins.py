@@ -340,3 +340,66 @@ def test_splice_request_keeps_latents_prefix_and_repl_bits():
     na = np.hypot(a[..., :32], a[..., 32:])
     nb = np.hypot(b[..., :32], b[..., 32:])
     assert np.all(np.abs(na - nb) <= 2.0 ** -7 * nb + 1e-30)
+
+
+# ---------------------------------------------------------------- modes ----
+# EVICT (KV-streams page: evict without resetting positions) re-indexes survivors but
+# keeps their positions; AMORTIZE ("Leyline: KV Cache Directives for Agentic Inference",
+# section 2.1) re-encodes them at the new position.
+
+def test_modes_match_brute_force():
+    r = _rng(16)
+    row, lat = 16, 8
+    for _ in range(30):
+        L = int(r.integers(5, 40))
+        dirs = _random_dirs(r, L, int(r.integers(1, 4)))
+        if dirs is None:
+            continue
+        modes = [int(m) for m in r.choice([0, 2], size=len(dirs))]
+        cache = _tiny_cache(r, 1, L, row)
+        repl = [_tiny_cache(r, 1, n, row) for (_, _, n) in dirs]
+        got = oracle.splice_request(cache, dirs, repl, lat, THETA, 0, modes)
+        rows = [[int(x) for x in cache[0, t]] for t in range(L)]
+        bd = [(s, e, [[int(x) for x in repl[k][0, i]] for i in range(n)]) for k, (s, e, n) in enumerate(dirs)]
+        want = np.array(brute.splice(rows, bd, lat, THETA, 0, modes), dtype=np.uint16).reshape(-1, row)
+        assert np.array_equal(got[0], want)
+
+
+def test_evict_only_is_a_pure_move():
+    r = _rng(17)
+    cache = _tiny_cache(r, 2, 60, 72)
+    dirs = [(5, 20, 3), (30, 31, 0), (40, 40, 2)]
+    repl = [_tiny_cache(r, 2, n, 72) for (_, _, n) in dirs]
+    out = oracle.splice_request(cache, dirs, repl, 8, THETA, 0, [2, 2, 2])
+    _, kind, idx, _ = oracle.splice_map(60, dirs)
+    kept = kind == 0
+    assert np.array_equal(out[:, kept], cache[:, idx[kept]])
+    # with AMORTIZE the same survivors are re-encoded
+    out_a = oracle.splice_request(cache, dirs, repl, 8, THETA, 0, [0, 0, 0])
+    assert not np.array_equal(out_a[:, kept, 8:], cache[:, idx[kept], 8:])
+
+
+def test_one_call_equals_calls_one_after_another():
+    r = _rng(18)
+    for trial in range(20):
+        L = 50
+        dirs = _random_dirs(r, L, 3)
+        if dirs is None:
+            continue
+        modes = [int(m) for m in r.choice([0, 2], size=3)]
+        cache = _tiny_cache(r, 1, L, 24)
+        repl = [_tiny_cache(r, 1, n, 24) for (_, _, n) in dirs]
+        one = oracle.splice_request(cache, dirs, repl, 8, THETA, 0, modes)
+        seq, shift = cache, 0
+        for k in sorted(range(3), key=lambda i: dirs[i][0]):
+            s, e, n = dirs[k]
+            seq = oracle.splice_request(seq, [(s + shift, e + shift, n)], [repl[k]], 8, THETA, 0, [modes[k]])
+            shift += n - (e - s)
+        # one call rounds a survivor once; one call per directive rounds it up to three
+        # times.  Each rounding moves a pair by at most sqrt(2) * 2^-8 of its norm.
+        assert one.shape == seq.shape
+        assert np.array_equal(one[..., :8], seq[..., :8])
+        a, b = oracle.bf16_value(one[..., 8:]), oracle.bf16_value(seq[..., 8:])
+        pn = np.hypot(a[..., :8], a[..., 8:])
+        pn = np.concatenate([pn, pn], axis=-1)
+        assert np.all(np.abs(a - b) <= 4 * np.sqrt(2) * 2.0 ** -8 * pn + 1e-30)

@@ -89,3 +89,34 @@ def test_noalloc_refuses_a_plan_larger_than_its_scratch():
     torch.cuda.synchronize()
     assert np.array_equal(cache.table[0].cpu().numpy(), before)
     cache.close()
+
+
+def test_noalloc_matches_splice_in_reindex_mode():
+    """The same two-call comparison on a block-size-1 pool in re-index mode, where the
+    static scratch also holds the staged table entries."""
+    from rope_rotation_gb300 import leyline
+    steps = [[Dir(0, 40, 130, 9, 0), Dir(1, 5, 700, 3, 1), Dir(2, 76, 77, 1, 3)],
+             [Dir(0, 0, 3, 0, 4), Dir(1, 100, 101, 30, 5, mode=2)]]
+    w = Workload("noalloc-reindex", 3, 1, [300, 1000, 77], steps, seed=22)
+    ref = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_REINDEX)
+    new = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_REINDEX)
+    for step in w.steps:
+        dirs_ref, keep_ref = H.gpu_directives(w, step)
+        dirs_new, keep_new = H.gpu_directives(w, step)
+        leyline.leyline_splice(ref.pool, ref.tables, dirs_ref)
+        leyline.leyline_splice_noalloc(new.pool, new.tables, dirs_new)
+        torch.cuda.synchronize()
+        ref.check_status()
+        new.check_status()
+        assert np.array_equal(ref.seq_lens_host, new.seq_lens_host)
+        assert ref.last_stats() == new.last_stats()
+        for r in range(w.num_reqs):
+            n = int(ref.seq_lens_host[r])
+            a = H.logical_rows(ref, r, n)
+            b = H.logical_rows(new, r, n)
+            assert np.array_equal(a[:, :, :w.latent_dim], b[:, :, :w.latent_dim])
+            H.compare_kpe(b[:, :, w.latent_dim:].reshape(-1, w.rope_dim),
+                          a[:, :, w.latent_dim:].reshape(-1, w.rope_dim), 0)
+        del keep_ref, keep_new
+    ref.close()
+    new.close()
