@@ -27,8 +27,9 @@
  * Storage model.  A pool holds num_pages pages per layer.  One page stores
  * block_size consecutive token slots of one request.  A slot row is
  * latent_dim + rope_dim bf16 values: the compressed latent first (moved bit for
- * bit, never recomputed), the RoPE band k_pe last.  The pool memory is laid out
- *     kv[layer][page][slot][latent_dim + rope_dim]      (bf16, row-major)
+ * bit, never recomputed), the RoPE band k_pe last (rope_heads bands for GQA/MHA
+ * rows).  The pool memory is laid out
+ *     kv[layer][page][slot][latent_dim + rope_heads * rope_dim]      (bf16, row-major)
  * and one block table, shared by all layers, maps block b of request r to a page:
  *     table[r * max_blocks + b] = page id, for b < ceil(seq_len[r] / block_size).
  *
@@ -102,7 +103,11 @@ typedef struct {
     int32_t pair_layout;      /* leyline_pair_layout_t */
     int32_t rotate_precision; /* leyline_rotate_precision_t */
     uint32_t flags;           /* LEYLINE_POOL_* bits */
-    int32_t reserved;         /* must be 0 */
+    int32_t rope_heads;       /* RoPE bands per row, each rope_dim wide (0 or 1: one band, the MLA
+                                 row).  > 1 for GQA/MHA caches (section 5: the directive
+                                 abstraction extends to GQA/MHA): the row is then [V | keys of
+                                 rope_heads heads], the keys fully RoPE'd, each head's band turned
+                                 with the same theta_j */
 } leyline_pool_desc_t;
 
 /* Block tables of num_reqs requests.  Caller-owned; the library borrows them for
@@ -129,7 +134,7 @@ typedef enum { LEYLINE_AMORTIZE = 0, LEYLINE_FORGET = 1, LEYLINE_EVICT = 2 } ley
 /* One directive D = (s_start, s_end, R, m) for request `req` (section 2.1).
  * [s_start, s_end) is half-open, in the request's coordinates before the call;
  * several directives of one request must not overlap and must have distinct
- * s_start.  repl_rows: device bf16 [num_layers][n_repl][latent_dim + rope_dim],
+ * s_start.  repl_rows: device bf16 [num_layers][n_repl][row] (row as in the pool),
  * the rows of R already encoded at their final positions s_start + D_before + i
  * (D_before = the summed Delta of the request's directives left of this one),
  * as prefill writes them (section 2.3); they are copied bit for bit and must stay
@@ -162,7 +167,8 @@ typedef struct {
 /* -------------------------------------------------------------- pool ---- */
 
 /* Create a pool over caller-owned device memory kv_dev (bf16
- * [num_layers][num_pages][block_size][latent_dim + rope_dim], 16-byte aligned).
+ * [num_layers][num_pages][block_size][row], row = latent_dim + rope_heads * rope_dim,
+ * 16-byte aligned).
  * All pages start free.  The library allocates the free-page stack and a small
  * plan buffer on the current device.  Synchronous.
  * Errors: INVALID_ARG (bad descriptor, null/misaligned kv_dev), CUDA. */
@@ -239,7 +245,7 @@ int leyline_last_stats(const leyline_pool_t* pool, leyline_stats_t* out);
 /* -------------------------------------------------------------- gather ---- */
 
 /* Copy the logical rows [t0, t1) of request `req`, layer `layer` into out_dev
- * (device bf16 [t1 - t0][latent_dim + rope_dim], 16-byte aligned), reading
+ * (device bf16 [t1 - t0][row], 16-byte aligned), reading
  * through the block table.  Asynchronous on `stream`.
  * Errors: INVALID_ARG (range outside [0, seq_lens_host[req]], bad layer/req). */
 int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, int32_t layer,

@@ -86,6 +86,11 @@ def lib() -> ctypes.CDLL:
                                                   ctypes.c_int, _u16p, ctypes.c_int64, ctypes.c_int32, _i64p,
                                                   _i64p, _i32p, _i32p, ctypes.POINTER(_u16p), _u16p, ctypes.c_int64]
             L.lo_splice_request_modes.restype = ctypes.c_int64
+            L.lo_splice_request_heads.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_double, ctypes.c_int, _u16p, ctypes.c_int64,
+                                                  ctypes.c_int32, _i64p, _i64p, _i32p, _i32p, ctypes.POINTER(_u16p),
+                                                  _u16p, ctypes.c_int64]
+            L.lo_splice_request_heads.restype = ctypes.c_int64
             _lib = L
     return _lib
 
@@ -173,16 +178,17 @@ def splice_map(L: int, dirs, cap: int | None = None):
 
 
 def splice_request(cache: np.ndarray, dirs, repl: list[np.ndarray], latent_dim: int = 512,
-                   theta: float = 10000.0, layout: int = 0, modes=None) -> np.ndarray:
+                   theta: float = 10000.0, layout: int = 0, modes=None, rope_heads: int = 1) -> np.ndarray:
     """Splice one request's logical cache bf16 [layers][L][row] -> [layers][L'][row].
 
     dirs: (s_start, s_end, n_repl) per directive; repl[k]: bf16 [layers][n_repl][row].
     modes: per directive, 0 = AMORTIZE (re-encode downstream tokens), 2 = EVICT (keep their
     positions); None = all AMORTIZE.
+    rope_heads: the row ends in that many RoPE bands of equal width (GQA/MHA keys); 1 for MLA.
     """
     c = np.ascontiguousarray(cache, dtype=np.uint16)
     layers, L, row = c.shape
-    rope_dim = row - latent_dim
+    rope_dim = (row - latent_dim) // rope_heads
     dirs = list(dirs)
     n = len(dirs)
     s = np.array([d[0] for d in dirs] or [0], dtype=np.int64)
@@ -195,7 +201,14 @@ def splice_request(cache: np.ndarray, dirs, repl: list[np.ndarray], latent_dim: 
             raise ValueError("replacement rows must be [layers][n_repl][row]")
     ptrs = (_u16p * max(n, 1))(*[_p(x, _u16p) for x in reps])
     out = np.zeros((layers, cap, row), dtype=np.uint16)
-    if modes is None:
+    if rope_heads != 1:
+        m = np.array(list(modes) if modes is not None else [0] * max(n, 1), dtype=np.int32)
+        if m.size == 0:
+            m = np.zeros(1, dtype=np.int32)
+        newlen = lib().lo_splice_request_heads(layers, latent_dim, rope_dim, rope_heads, theta, layout,
+                                               _p(c, _u16p), L, n, _p(s, _i64p), _p(e, _i64p), _p(r, _i32p),
+                                               _p(m, _i32p), ptrs, _p(out, _u16p), cap)
+    elif modes is None:
         newlen = lib().lo_splice_request(layers, latent_dim, rope_dim, theta, layout, _p(c, _u16p), L, n,
                                          _p(s, _i64p), _p(e, _i64p), _p(r, _i32p), ptrs, _p(out, _u16p), cap)
     else:

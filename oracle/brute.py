@@ -75,7 +75,7 @@ def rerotate(kpe: list[int], t: int, p: int, theta: float, layout: int = 0) -> l
 
 
 def splice(rows: list[list[int]], dirs: list[tuple[int, int, list[list[int]]]],
-           latent_dim: int, theta: float, layout: int = 0, modes=None) -> list[list[int]]:
+           latent_dim: int, theta: float, layout: int = 0, modes=None, rope_heads: int = 1) -> list[list[int]]:
     """Splice one layer of one request.
 
     rows: bf16 rows (latent then k_pe) at positions 0..L-1.
@@ -83,6 +83,7 @@ def splice(rows: list[list[int]], dirs: list[tuple[int, int, list[list[int]]]],
     modes: per directive, 0 = AMORTIZE (a survivor is re-encoded at its new position),
     2 = EVICT (the KV-streams page's eviction: a survivor keeps its position).  With both,
     a survivor is re-encoded at its new position minus the shift of the EVICT spans left of it.
+    rope_heads: the row ends in that many RoPE bands of equal width, each re-encoded alone.
     Returns the new rows: prefix and R copied, survivors re-encoded.
     """
     modes = list(modes) if modes is not None else [0] * len(dirs)
@@ -98,5 +99,10 @@ def splice(rows: list[list[int]], dirs: list[tuple[int, int, list[list[int]]]],
             row = rows[v]
             # count the index shift that EVICT spans to the left contributed, and undo it
             evict_shift = sum(len(R) - (e - s) for (s, e, R), m in zip(dirs, modes) if m == 2 and e <= v)
-            out.append(list(row[:latent_dim]) + rerotate(row[latent_dim:], v, p - evict_shift, theta, layout))
+            band = (len(row) - latent_dim) // rope_heads
+            new_row = list(row[:latent_dim])
+            for h in range(rope_heads):
+                lo = latent_dim + h * band
+                new_row += rerotate(row[lo:lo + band], v, p - evict_shift, theta, layout)
+            out.append(new_row)
     return out

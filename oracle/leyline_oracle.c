@@ -239,10 +239,20 @@ static int64_t lo_turn_of(int64_t t, int32_t n, const int64_t* s_start, const in
  * Latents, prefix rows and R rows are copied bit for bit; k_pe of a surviving
  * token moved from t to p is re-encoded from scratch (lo_rerotate).  Returns the
  * new length or -1 (as lo_splice_map). */
+int64_t lo_splice_request_heads(int num_layers, int latent_dim, int rope_dim, int rope_heads, double theta,
+                                int layout, const uint16_t* cache_in, int64_t L, int32_t n,
+                                const int64_t* s_start, const int64_t* s_end, const int32_t* n_repl,
+                                const int32_t* modes, const uint16_t* const* repl, uint16_t* cache_out,
+                                int64_t cap);
+
 int64_t lo_splice_request_modes(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
                                 const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
                                 const int64_t* s_end, const int32_t* n_repl, const int32_t* modes,
-                                const uint16_t* const* repl, uint16_t* cache_out, int64_t cap);
+                                const uint16_t* const* repl, uint16_t* cache_out, int64_t cap)
+{
+    return lo_splice_request_heads(num_layers, latent_dim, rope_dim, 1, theta, layout, cache_in, L, n, s_start,
+                                   s_end, n_repl, modes, repl, cache_out, cap);
+}
 
 int64_t lo_splice_request(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
                           const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
@@ -254,13 +264,17 @@ int64_t lo_splice_request(int num_layers, int latent_dim, int rope_dim, double t
 }
 
 /* As lo_splice_request, with a mode per directive (see lo_turn_of): a surviving
- * token t is re-encoded from position t to position t + turn(t). */
-int64_t lo_splice_request_modes(int num_layers, int latent_dim, int rope_dim, double theta, int layout,
-                                const uint16_t* cache_in, int64_t L, int32_t n, const int64_t* s_start,
-                                const int64_t* s_end, const int32_t* n_repl, const int32_t* modes,
-                                const uint16_t* const* repl, uint16_t* cache_out, int64_t cap)
+ * token t is re-encoded from position t to position t + turn(t).  The row ends
+ * in rope_heads RoPE bands of width rope_dim (the keys of rope_heads attention
+ * heads, the GQA/MHA extension named in section 5 of the Leyline page); each band
+ * is re-encoded on its own.  rope_heads = 1 is the MLA row (latent, then k_pe). */
+int64_t lo_splice_request_heads(int num_layers, int latent_dim, int rope_dim, int rope_heads, double theta,
+                                int layout, const uint16_t* cache_in, int64_t L, int32_t n,
+                                const int64_t* s_start, const int64_t* s_end, const int32_t* n_repl,
+                                const int32_t* modes, const uint16_t* const* repl, uint16_t* cache_out,
+                                int64_t cap)
 {
-    const int row = latent_dim + rope_dim;
+    const int row = latent_dim + rope_heads * rope_dim;
     int32_t* kind = (int32_t*)malloc(sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1));
     int64_t* idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cap > 0 ? cap : 1));
     int32_t* which = (int32_t*)malloc(sizeof(int32_t) * (size_t)(cap > 0 ? cap : 1));
@@ -278,7 +292,9 @@ int64_t lo_splice_request_modes(int num_layers, int latent_dim, int rope_dim, do
                     int64_t to = t + lo_turn_of(t, n, s_start, s_end, n_repl, modes);
                     const uint16_t* src = cache_in + ((int64_t)l * L + t) * row;
                     memcpy(dst, src, sizeof(uint16_t) * (size_t)latent_dim);
-                    lo_rerotate(src + latent_dim, 1, rope_dim, &t, &to, theta, layout, dst + latent_dim);
+                    for (int h = 0; h < rope_heads; ++h)
+                        lo_rerotate(src + latent_dim + h * rope_dim, 1, rope_dim, &t, &to, theta, layout,
+                                    dst + latent_dim + h * rope_dim);
                 }
             }
         }

@@ -353,9 +353,10 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const __grid
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const long long L = a.g.num_layers;
-    const int lv = a.g.latent_vecs, rvv = a.g.rope_vecs, half = a.g.rope_dim / 2;
+    const int lv = a.g.latent_vecs, hv = a.g.head_vecs, half = a.g.rope_dim / 2;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
-    const int rope_items = split ? rvv / 2 : rvv;
+    const int head_items = split ? hv / 2 : hv;  // work items per RoPE band
+    const int rope_items = a.g.rope_heads * head_items;
     long long u0, u1;
     my_units(a.total_tiles * L, u0, u1);
     long long cur_tile = -1;
@@ -377,9 +378,10 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const __grid
         for (int it = threadIdx.x; it < kTileRows * rope_items; it += blockDim.x) {
             const RowDesc d = desc[it / rope_items];
             if (!d.src) continue;
-            const int q = it % rope_items;
-            const uint4* rs = d.src + layer * d.src_lstride + lv;
-            uint4* rd = d.dst + layer * a.g.layer_vecs + lv;
+            const int hq = it % rope_items;
+            const int head = hq / head_items, q = hq - head * head_items;
+            const uint4* rs = d.src + layer * d.src_lstride + lv + head * hv;
+            uint4* rd = d.dst + layer * a.g.layer_vecs + lv + head * hv;
             float cs[8], sn[8];
             const int j0 = split ? 8 * q : 4 * q;
             const int np = split ? 8 : 4;
@@ -390,10 +392,10 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const __grid
                 }
             }
             if (split) {
-                uint4 x = ld_stream(rs + q), y = ld_stream(rs + q + rvv / 2);
+                uint4 x = ld_stream(rs + q), y = ld_stream(rs + q + hv / 2);
                 if (d.trig >= 0) rotate_half_split<kBf16>(x, y, cs, sn);
                 st_stream(rd + q, x);
-                st_stream(rd + q + rvv / 2, y);
+                st_stream(rd + q + hv / 2, y);
             } else {
                 uint4 x = ld_stream(rs + q);
                 if (d.trig >= 0) rotate_interleaved<kBf16>(x, cs, sn);
@@ -815,9 +817,10 @@ __global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_con
     const PlanView pv = plan_view(a, plan);
     const long long L = a.g.num_layers;
     const long long layer_vecs = a.g.layer_vecs;
-    const int rvv = a.g.rope_vecs, lv = a.g.latent_vecs, row_vecs = a.g.row_vecs;
+    const int hv = a.g.head_vecs, lv = a.g.latent_vecs, row_vecs = a.g.row_vecs;
     const int rope_dim = a.g.rope_dim;
-    const int ipr = kLayout == 0 ? rvv / 2 : rvv;  // work items per row and layer
+    const int head_items = kLayout == 0 ? hv / 2 : hv;  // work items per RoPE band
+    const int ipr = a.g.rope_heads * head_items;        // work items per row and layer
     const int per_layer = kTileRows * ipr;
     const int lpu = blockDim.x / per_layer > 0 ? (int)(blockDim.x / per_layer) : 1;  // layers per unit
     const long long groups = (L + lpu - 1) / lpu;
@@ -864,10 +867,11 @@ __global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_con
             const int lo = e / per_layer, it = e - (e / per_layer) * per_layer;
             const long long layer = layer0 + lo;
             if (layer >= L) continue;
-            const int i = it / ipr, q = it - (it / ipr) * ipr;
+            const int i = it / ipr, hq = it - (it / ipr) * ipr;
+            const int head = hq / head_items, q = hq - head * head_items;
             const ReindexRow d = rr[i];
             if (d.kind == SEG_ROT && d.row) {
-                uint4* r = d.row + layer * layer_vecs + lv;
+                uint4* r = d.row + layer * layer_vecs + lv + head * hv;
                 float cs[8], sn[8];
                 const int np = kLayout == 0 ? 8 : 4;
                 const float* tp = &trig_s[i][2 * np * q];
@@ -879,10 +883,10 @@ __global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_con
                     }
                 }
                 if (kLayout == 0) {
-                    uint4 x = ld_rw(r + q), y = ld_rw(r + q + rvv / 2);
+                    uint4 x = ld_rw(r + q), y = ld_rw(r + q + hv / 2);
                     rotate_half_split<kBf16>(x, y, cs, sn);
                     st_stream(r + q, x);
-                    st_stream(r + q + rvv / 2, y);
+                    st_stream(r + q + hv / 2, y);
                 } else {
                     uint4 x = ld_rw(r + q);
                     rotate_interleaved<kBf16>(x, cs, sn);
@@ -974,7 +978,7 @@ int grid_for(long long items, int threads, int cap)
     return (int)g;
 }
 
-bool mla_shape(const Geometry& g) { return g.latent_vecs == 64 && g.rope_vecs == 8; }
+bool mla_shape(const Geometry& g) { return g.latent_vecs == 64 && g.rope_vecs == 8 && g.rope_heads == 1; }
 
 // Launch with programmatic stream serialization: the kernel may start before the
 // previous kernel in the stream ends; it calls griddepcontrol.wait before it
@@ -1049,7 +1053,7 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
         e = launch_dependent(prep_reindex<PlanSrc>, grid_for(a.total_prep, 256, 8192), 256, s, a, plan);
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
-    const int ipr = split ? a.g.rope_vecs / 2 : a.g.rope_vecs;
+    const int ipr = a.g.rope_heads * (split ? a.g.head_vecs / 2 : a.g.head_vecs);
     const int lpu = kMoveThreads / (kTileRows * ipr) > 0 ? kMoveThreads / (kTileRows * ipr) : 1;
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);

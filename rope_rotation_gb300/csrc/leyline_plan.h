@@ -30,10 +30,12 @@ struct Geometry {
     int32_t latent_dim;
     int32_t rope_dim;
     int32_t block_size;
-    int32_t row_elems;    // latent_dim + rope_dim
+    int32_t row_elems;    // latent_dim + rope_heads * rope_dim
     int32_t row_vecs;     // row_elems / 8 (16-byte vectors)
     int32_t latent_vecs;  // latent_dim / 8
-    int32_t rope_vecs;    // rope_dim / 8
+    int32_t rope_vecs;    // rope_heads * rope_dim / 8 (all RoPE bands of a row)
+    int32_t rope_heads;   // RoPE bands per row (1: MLA)
+    int32_t head_vecs;    // rope_dim / 8 (one band)
     int64_t num_pages;
     int64_t layer_vecs;   // num_pages * block_size * row_vecs
     double theta;

@@ -99,18 +99,23 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pair_layout");
     if (d->rotate_precision != LEYLINE_ROTATE_FP32 && d->rotate_precision != LEYLINE_ROTATE_BF16_NAIVE)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown rotate_precision");
-    if ((d->flags & ~(uint32_t)LEYLINE_POOL_REINDEX) != 0 || d->reserved != 0)
-        return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags or nonzero reserved field");
+    if ((d->flags & ~(uint32_t)LEYLINE_POOL_REINDEX) != 0)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags");
+    if (d->rope_heads < 0 || d->rope_heads > 1024)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "rope_heads must be in [0, 1024]");
     if ((d->flags & LEYLINE_POOL_REINDEX) && d->rope_dim > 256)
         return set_error(LEYLINE_ERR_INVALID_ARG, "LEYLINE_POOL_REINDEX supports rope_dim <= 256");
     g->num_layers = d->num_layers;
     g->latent_dim = d->latent_dim;
     g->rope_dim = d->rope_dim;
     g->block_size = d->block_size;
-    g->row_elems = d->latent_dim + d->rope_dim;
+    const int heads = d->rope_heads > 1 ? d->rope_heads : 1;
+    g->rope_heads = heads;
+    g->row_elems = d->latent_dim + heads * d->rope_dim;
     g->row_vecs = g->row_elems / 8;
     g->latent_vecs = d->latent_dim / 8;
-    g->rope_vecs = d->rope_dim / 8;
+    g->head_vecs = d->rope_dim / 8;
+    g->rope_vecs = heads * g->head_vecs;
     g->num_pages = d->num_pages;
     g->layer_vecs = d->num_pages * (int64_t)d->block_size * g->row_vecs;
     g->theta = d->rope_theta;
@@ -189,7 +194,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     const bool reindex = (g.flags & LEYLINE_POOL_REINDEX) && B == 1;
     plan->reindex = reindex;
     const int64_t row_bytes = (int64_t)g.row_elems * 2;
-    const int64_t rope_bytes = (int64_t)g.rope_dim * 2;
+    const int64_t rope_bytes = (int64_t)g.rope_vecs * 16;  // every RoPE band of a row
     int64_t tiles = 0, commit = 0, pops = 0, pushes = 0, turned_rows = 0;
     leyline_stats_t& st = plan->stats;
     for (int32_t i = 0; i < n;) {

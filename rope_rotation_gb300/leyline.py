@@ -49,7 +49,11 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("num_layers", ctypes.c_int32), ("latent_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("num_pages", ctypes.c_int64), ("rope_theta", ctypes.c_double),
                 ("pair_layout", ctypes.c_int32), ("rotate_precision", ctypes.c_int32), ("flags", ctypes.c_uint32),
-                ("reserved", ctypes.c_int32)]
+                ("rope_heads", ctypes.c_int32)]
+
+    @property
+    def row_elems(self) -> int:
+        return self.latent_dim + max(self.rope_heads, 1) * self.rope_dim
 
 
 class BlockTable(ctypes.Structure):
@@ -146,14 +150,14 @@ def _tensor_ptr(t) -> int:
 
 def pool_desc(num_layers: int, block_size: int, num_pages: int, latent_dim: int = 512, rope_dim: int = 64,
               rope_theta: float = 10000.0, pair_layout: int = LEYLINE_PAIRS_HALF_SPLIT,
-              rotate_precision: int = LEYLINE_ROTATE_FP32, flags: int = 0) -> PoolDesc:
+              rotate_precision: int = LEYLINE_ROTATE_FP32, flags: int = 0, rope_heads: int = 1) -> PoolDesc:
     return PoolDesc(num_layers, latent_dim, rope_dim, block_size, num_pages, rope_theta, pair_layout,
-                    rotate_precision, flags, 0)
+                    rotate_precision, flags, rope_heads)
 
 
 def leyline_pool_create(desc: PoolDesc, kv) -> ctypes.c_void_p:
-    """kv: torch bf16 CUDA tensor with num_layers*num_pages*block_size*(latent+rope) elements."""
-    need = desc.num_layers * desc.num_pages * desc.block_size * (desc.latent_dim + desc.rope_dim)
+    """kv: torch bf16 CUDA tensor with num_layers*num_pages*block_size*row elements."""
+    need = desc.num_layers * desc.num_pages * desc.block_size * desc.row_elems
     if kv.numel() != need or kv.element_size() != 2 or not kv.is_cuda or not kv.is_contiguous():
         raise LeylineError(LEYLINE_ERR_INVALID_ARG, "kv must be a contiguous 2-byte CUDA tensor of the pool's size")
     h = ctypes.c_void_p()

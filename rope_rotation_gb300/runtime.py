@@ -18,7 +18,8 @@ class PagedCache:
     def __init__(self, num_layers: int, block_size: int, num_pages: int, max_reqs: int, max_blocks: int,
                  latent_dim: int = 512, rope_dim: int = 64, rope_theta: float = 10000.0,
                  pair_layout: int = leyline.LEYLINE_PAIRS_HALF_SPLIT,
-                 rotate_precision: int = leyline.LEYLINE_ROTATE_FP32, flags: int = 0, device: str = "cuda"):
+                 rotate_precision: int = leyline.LEYLINE_ROTATE_FP32, flags: int = 0, rope_heads: int = 1,
+                 device: str = "cuda"):
         import torch
         self.torch = torch
         self.num_layers = num_layers
@@ -26,12 +27,13 @@ class PagedCache:
         self.num_pages = num_pages
         self.latent_dim = latent_dim
         self.rope_dim = rope_dim
-        self.row = latent_dim + rope_dim
+        self.rope_heads = max(rope_heads, 1)
+        self.row = latent_dim + self.rope_heads * rope_dim
         self.device = torch.device(device)
         self.kv = torch.empty(num_layers * num_pages * block_size * self.row, dtype=torch.bfloat16,
                               device=self.device)
         self.desc = leyline.pool_desc(num_layers, block_size, num_pages, latent_dim, rope_dim, rope_theta,
-                                      pair_layout, rotate_precision, flags)
+                                      pair_layout, rotate_precision, flags, rope_heads)
         self.pool = leyline.leyline_pool_create(self.desc, self.kv)
         self.table = torch.full((max_reqs, max_blocks), -1, dtype=torch.int32, device=self.device)
         self.seq_lens_dev = torch.zeros(max_reqs, dtype=torch.int32, device=self.device)

@@ -40,6 +40,7 @@ class Workload:
     latent_dim: int = 512
     rope_dim: int = 64
     theta: float = 10000.0
+    rope_heads: int = 1  # RoPE bands per row (GQA/MHA keys); 1 for MLA
     notes: dict = field(default_factory=dict)
 
     @property
@@ -48,7 +49,7 @@ class Workload:
 
     @property
     def row_elems(self) -> int:
-        return self.latent_dim + self.rope_dim
+        return self.latent_dim + self.rope_heads * self.rope_dim
 
 
 def contiguous_4k(seed: int = 0) -> Workload:

@@ -105,7 +105,7 @@ def make_cache(w: Workload, pair_layout: int = 0, precision: int = 0, slack_page
     if max_blocks is None:
         max_blocks = -(-mx // B) + 1
     cache = PagedCache(w.num_layers, B, pages_for(w, slack_pages), w.num_reqs, max_blocks, w.latent_dim,
-                       w.rope_dim, w.theta, pair_layout, precision, flags)
+                       w.rope_dim, w.theta, pair_layout, precision, flags, w.rope_heads)
     for r, L in enumerate(w.lengths):
         cache.add_request(r, L)
         sfill.fill_request(cache, w.seed, r, L)
@@ -201,9 +201,11 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
         lat = w.latent_dim
         dm = [(d.s_start, d.s_end, d.n_repl, d.mode) for d in ds]
         turn = np.array([turn_of(int(idx[p]), dm) if kind[p] == 0 else 0 for p in range(newlen)], dtype=np.int64)
+        H_ = w.rope_heads
         if precision == 0:
             want = oracle.splice_request(state[r], tup, reps, lat, w.theta, layout,
-                                         None if all(m == 0 for m in modes) else modes)
+                                         None if (all(m == 0 for m in modes) and H_ == 1) else modes,
+                                         rope_heads=H_)
         else:
             want = np.empty_like(got)
             for p in range(newlen):
@@ -212,7 +214,9 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
                 else:
                     t = int(idx[p])
                     want[:, p, :lat] = state[r][:, t, :lat]
-                    want[:, p, lat:] = oracle.rotate_bf16only(state[r][:, t, lat:], int(turn[p]), w.theta, layout)
+                    bands = state[r][:, t, lat:].reshape(w.num_layers, H_, w.rope_dim)
+                    want[:, p, lat:] = oracle.rotate_bf16only(bands, int(turn[p]), w.theta,
+                                                              layout).reshape(w.num_layers, -1)
         assert np.array_equal(got[:, :, :lat], want[:, :, :lat]), f"request {r}: latent bits differ"
         prev = getattr(state, "turns", None)
         old_turns = prev[r] if prev is not None else np.zeros(int(before_lens[r]), dtype=np.int64)
@@ -220,7 +224,7 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
         turns = np.where(kind == 0, carried + (turn != 0), 0)
         moved = turns > 0  # rows whose rope band has been turned at least once
         assert np.array_equal(got[:, ~moved], want[:, ~moved]), f"request {r}: prefix / R rows differ"
-        tl = np.broadcast_to(turns[moved], (w.num_layers, int(moved.sum()))).reshape(-1)
+        tl = np.repeat(np.broadcast_to(turns[moved], (w.num_layers, int(moved.sum()))).reshape(-1), w.rope_heads)
         c = compare_kpe(got[:, moved, lat:].reshape(-1, w.rope_dim), want[:, moved, lat:].reshape(-1, w.rope_dim),
                         layout, exact=(precision != 0), turns=tl)
         if prev is not None:

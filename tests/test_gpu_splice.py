@@ -219,3 +219,20 @@ def test_reindex_chain_matches_oracle_chain_call_by_call():
         c = H.splice_step_and_check(w, cache, state, step, guard=False)
         assert c["stats"]["algorithmic_bytes"] == 2 * 6 * (128 * c["stats"]["downstream_slots"] + 1152 * 12)
     cache.close()
+
+
+# ------------------------------------------------------------------------------
+# GQA/MHA rows (section 5 of the Leyline page: the directive abstraction extends to
+# GQA/MHA): [V | keys of 4 heads x 128], every key band turned with the same theta_j.
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("B,flags", [(16, 0), (1, 0), (1, 1)])
+def test_gqa_rows(layout, B, flags):
+    steps = [[Dir(0, 20, 90, 6, 0), Dir(1, 3, 3, 9, 1, mode=2), Dir(1, 40, 41, 0, 2)],
+             [Dir(0, 0, 10, 2, 3), Dir(1, 60, 70, 1, 4)]]
+    w = Workload(f"gqa-l{layout}-B{B}-f{flags}", 2, B, [200, 123], steps, seed=40,
+                 latent_dim=512, rope_dim=128, rope_heads=4)
+    cache = H.make_cache(w, pair_layout=layout, flags=flags)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step, layout=layout)
+    cache.close()

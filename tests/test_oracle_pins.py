@@ -403,3 +403,33 @@ def test_one_call_equals_calls_one_after_another():
         pn = np.hypot(a[..., :8], a[..., 8:])
         pn = np.concatenate([pn, pn], axis=-1)
         assert np.all(np.abs(a - b) <= 4 * np.sqrt(2) * 2.0 ** -8 * pn + 1e-30)
+
+
+# ---------------------------------------------------------------- heads ----
+# GQA/MHA rows ("Leyline: KV Cache Directives for Agentic Inference", section 5: the
+# directive abstraction extends to GQA/MHA): the row ends in several RoPE bands, the
+# keys of several heads, each re-encoded alone with the same theta_j.
+
+def test_heads_match_brute_force_and_single_band_per_head():
+    r = _rng(19)
+    lat, d, H = 8, 16, 3
+    row = lat + H * d
+    for _ in range(10):
+        L = int(r.integers(5, 30))
+        dirs = _random_dirs(r, L, int(r.integers(1, 3)))
+        if dirs is None:
+            continue
+        modes = [int(m) for m in r.choice([0, 2], size=len(dirs))]
+        cache = _tiny_cache(r, 1, L, row)
+        repl = [_tiny_cache(r, 1, n, row) for (_, _, n) in dirs]
+        got = oracle.splice_request(cache, dirs, repl, lat, THETA, 0, modes, rope_heads=H)
+        rows = [[int(x) for x in cache[0, t]] for t in range(L)]
+        bd = [(s, e, [[int(x) for x in repl[k][0, i]] for i in range(n)]) for k, (s, e, n) in enumerate(dirs)]
+        want = np.array(brute.splice(rows, bd, lat, THETA, 0, modes, rope_heads=H), dtype=np.uint16).reshape(-1, row)
+        assert np.array_equal(got[0], want)
+        # head h alone, as a single-band row (its band after the copied part), gives the same bits
+        for h in range(H):
+            sub = np.concatenate([cache[..., :lat], cache[..., lat + h * d: lat + (h + 1) * d]], axis=-1)
+            sub_repl = [np.concatenate([x[..., :lat], x[..., lat + h * d: lat + (h + 1) * d]], axis=-1) for x in repl]
+            one = oracle.splice_request(sub, dirs, sub_repl, lat, THETA, 0, modes)
+            assert np.array_equal(one[..., lat:], got[..., lat + h * d: lat + (h + 1) * d])
