@@ -35,8 +35,8 @@
  *
  * How a splice is carried out.  Every block from floor(s_min / block_size) on
  * (s_min = the smallest s_start of the request's directives) is rewritten into
- * fresh pages taken from the pool's free-page stack; the request's old pages from
- * that block on go back onto the stack when the rewrite is committed.  Source
+ * fresh pages taken from the pool's free-page list; the request's old pages from
+ * that block on go back onto the list when the rewrite is committed.  Source
  * rows are never written, so the call has no read/write hazard whatever the sign
  * of Delta, and a call that fails validation changes nothing.  The prefix rows
  * of the first rewritten block are copied unchanged.
@@ -159,7 +159,7 @@ typedef struct {
                                   downstream slot and nothing for unturned ones */
     int64_t moved_bytes;       /* algorithmic bytes plus the head rows' 2 * row_bytes * num_layers */
     int64_t pages_popped;      /* fresh pages taken for the rewritten blocks */
-    int64_t pages_pushed;      /* old pages returned to the free stack */
+    int64_t pages_pushed;      /* old pages returned to the free-page list */
     int32_t requests_touched;
     int32_t kernels_launched;  /* kernels this call enqueued */
 } leyline_stats_t;
@@ -169,20 +169,21 @@ typedef struct {
 /* Create a pool over caller-owned device memory kv_dev (bf16
  * [num_layers][num_pages][block_size][row], row = latent_dim + rope_heads * rope_dim,
  * 16-byte aligned).
- * All pages start free.  The library allocates the free-page stack and a small
- * plan buffer on the current device.  Synchronous.
+ * All pages start free.  The library allocates the free-page list (a ring of
+ * 2 * num_pages ids) and small plan and staging buffers on the current device.
+ * Synchronous.
  * Errors: INVALID_ARG (bad descriptor, null/misaligned kv_dev), CUDA. */
 int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_pool_t** out);
 
 /* Wait for the pool's enqueued work and free what the library allocated (never kv_dev). */
 int leyline_pool_destroy(leyline_pool_t* pool);
 
-/* Take n pages off the free stack, for the caller's initial fill or prefill.
+/* Take n pages off the free-page list, for the caller's initial fill or prefill.
  * Synchronous (waits for the pool's enqueued work).  page_ids_host receives n ids
  * (the k-th id taken first).  Errors: INVALID_ARG, NO_PAGES, CUDA. */
 int leyline_alloc_pages(leyline_pool_t* pool, int32_t n, int32_t* page_ids_host);
 
-/* Return n pages (ids from page_ids_host) to the free stack.  Synchronous.
+/* Return n pages (ids from page_ids_host) to the free-page list.  Synchronous.
  * Errors: INVALID_ARG (id out of range, more pages than the pool holds), CUDA. */
 int leyline_free_pages(leyline_pool_t* pool, int32_t n, const int32_t* page_ids_host);
 

@@ -1,17 +1,21 @@
-// leyline_pool.cpp -- pool, free-page stack, splice / gather entry points (C ABI).
+// leyline_pool.cpp -- pool, free-page list, splice / gather entry points (C ABI).
 //
 // The pool borrows the caller's KV memory and block tables.  It owns the
-// free-page stack (device int32 [num_pages], top counted on the host), a device
-// plan buffer and a pinned host staging buffer for the plan, a status word and
-// a few events.  A splice call:
+// free-page list (a device ring of 2 * num_pages page ids; head and tail are
+// counted on the host), device plan and staging buffers, a pinned host buffer
+// for plans too large to travel as a kernel parameter, a status word and a few
+// events.  A splice call:
 //   1. validates and plans on the host (leyline_planner.cpp) -- on error nothing
 //      is enqueued and nothing changes;
-//   2. uploads the plan (a few KB) with one async host-to-device copy;
-//   3. enqueues the plan, move+rotate and commit kernels on the caller's stream;
+//   2. passes the plan to the kernels as a __grid_constant__ parameter when it
+//      is small, else uploads it with one async host-to-device copy;
+//   3. enqueues the move+rotate and commit kernels (re-index mode: prep, rotate,
+//      commit) on the caller's stream, each a programmatic dependent of the last;
 //   4. updates the host mirrors (lengths, free-page count) at enqueue time.
-// Source pages are only read and fresh pages only written, so a splice whose
-// spans shift downstream rows left (Delta < 0) or right (Delta > 0) has no
-// read/write overlap; the old pages are recycled by the commit kernel.
+// In the default mode source pages are only read and fresh pages only written,
+// so a splice whose spans shift downstream rows left (Delta < 0) or right
+// (Delta > 0) has no read/write overlap; the old pages are recycled by the
+// commit kernel.
 #include <cuda_runtime.h>
 
 #include <algorithm>
