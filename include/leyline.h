@@ -92,6 +92,16 @@ typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_
  *   commit, so a call that fails after validation leaves the pool inconsistent
  *   (as any LEYLINE_ERR_CUDA does).  Ignored for block_size > 1. */
 #define LEYLINE_POOL_REINDEX 1
+/* LEYLINE_POOL_LAZY: a splice does not turn rope bands.  The pool keeps, per slot,
+ * an int32 count of positions that the stored band still has to turn (the
+ * "pending" turn); a splice moves a survivor's count with it and adds the turn
+ * the eager splice would have applied, and rows of R start at 0.  Readers apply
+ * R(pending) once: leyline_gather does, leyline_materialize applies it in place
+ * and clears it, and attention kernels can read the counts through
+ * leyline_pending_ptr.  A band is then rounded to bf16 once per read instead of
+ * once per splice (section 4.3: the drift of repeated bf16 rotation), and with
+ * LEYLINE_POOL_REINDEX a splice moves no cache bytes for survivors at all. */
+#define LEYLINE_POOL_LAZY 2
 
 typedef struct {
     int32_t num_layers;       /* >= 1 */
@@ -247,10 +257,25 @@ int leyline_last_stats(const leyline_pool_t* pool, leyline_stats_t* out);
 
 /* Copy the logical rows [t0, t1) of request `req`, layer `layer` into out_dev
  * (device bf16 [t1 - t0][row], 16-byte aligned), reading
- * through the block table.  Asynchronous on `stream`.
+ * through the block table.  In a LEYLINE_POOL_LAZY pool each row's rope bands
+ * are turned by the row's pending count on the way out.  Asynchronous on `stream`.
  * Errors: INVALID_ARG (range outside [0, seq_lens_host[req]], bad layer/req). */
 int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, int32_t layer,
                    int64_t t0, int64_t t1, void* out_dev, void* stream);
+
+/* ---------------------------------------------------------- lazy mode ---- */
+
+/* LEYLINE_POOL_LAZY pools: turn the stored rope bands of rows [0, seq_len) of
+ * request `req` (all layers) by their pending counts, in fp32, storing bf16, and
+ * set the counts to 0.  Asynchronous on `stream`.  Errors: INVALID_ARG (not a lazy
+ * pool, bad request). */
+int leyline_materialize(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, void* stream);
+
+/* LEYLINE_POOL_LAZY pools: device pointer to the pending counts, int32
+ * [num_pages][block_size] (the count of the slot at position t of a request is
+ * at page * block_size + t % block_size, page = table[t / block_size]).  Owned by
+ * the pool; NULL for other pools. */
+int32_t* leyline_pending_ptr(leyline_pool_t* pool);
 
 /* ----------------------------------------------------------- checking ---- */
 

@@ -74,6 +74,7 @@ struct SpliceArgs {
     const Seg* segs;
     const float* trig;
     int32_t* stage;           // re-index: staged table entries [total_stage]
+    int32_t* pending;         // lazy pools: pending turns [num_pages * block_size], else nullptr
     int32_t* status;          // device status word
     int64_t total_prep;
     int64_t total_tiles;
@@ -96,6 +97,16 @@ int launch_splice(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stre
                   cudaEvent_t t1);
 int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
                   int64_t t1, void* out, int32_t* status, void* stream);
+// Lazy pools: gather turning each row's rope bands by its pending count; theta_j is
+// the device table of theta^(-2j/rope_dim) (fp64, rope_dim / 2 entries).
+int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
+                       int64_t t1, void* out, const int32_t* pending, const double* theta_j, int32_t* status,
+                       void* stream);
+// Lazy pools: turn rows [0, len) of one request by their pending counts, in place, and clear the counts.
+int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
+                       const double* theta_j, int32_t* status, void* stream);
+// Lazy pools: set the pending counts of n pages (device ids) to 0.
+int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream);
 // Resident CTAs per SM of the vector move+rotate kernel (occupancy query).
 int move_rotate_blocks_per_sm(int* blocks);
 // Resident CTAs per SM of the in-place rotation kernel of re-index mode.
@@ -118,6 +129,8 @@ struct leyline_pool {
     int reindex_blocks_per_sm = 1;
     int32_t move_kernel = 0;  // MoveKernel used by this pool
     int32_t* d_stage = nullptr;  // re-index: staged table entries
+    int32_t* d_pending = nullptr;  // lazy: pending turns per slot
+    double* d_theta_j = nullptr;   // lazy: theta_j table for readers
     size_t d_stage_cap = 0;      // entries
     int32_t* d_queue = nullptr;  // free-page ring, 2 * num_pages entries
     int64_t q_cap = 0;

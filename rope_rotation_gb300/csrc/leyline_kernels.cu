@@ -234,6 +234,10 @@ __device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long 
         d.src_lstride = (long long)s.n_repl * rv;
     }
     d.dst = kv + ((long long)fresh * B + (p - dblk * B)) * rv;
+    if (a.pending) {  // lazy pool: the destination slot carries the source's pending turn plus this one
+        const long long dslot = (long long)fresh * B + (p - dblk * B);
+        a.pending[dslot] = from_cache ? a.pending[(long long)page * B + (t - blk * B)] + s.turn : 0;
+    }
     return d;
 }
 
@@ -708,6 +712,8 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
                 old = -1;
             }
             a.free_q[ring(a.push_base + rp->push_off + k, a.q_cap)] = old;
+            if (a.pending && old >= 0)  // a free page carries no pending turn
+                for (int j = 0; j < a.g.block_size; ++j) a.pending[(long long)old * a.g.block_size + j] = 0;
         }
         i += stride;
         if (i >= a.total_commit) break;
@@ -754,6 +760,7 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
                     raise_status(a.status, ST_BAD_FRESH);
                     page = -1;
                 }
+                if (a.pending && page >= 0) a.pending[page] = 0;  // R is encoded at its final position
             } else {
                 const long long t = s.src_start + (p - s.new_start);
                 page = (t >= 0 && t < a.max_blocks) ? trow[t] : -1;
@@ -761,6 +768,7 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
                     raise_status(a.status, ST_BAD_PAGE);
                     page = -1;
                 }
+                if (a.pending && page >= 0 && s.turn != 0) a.pending[page] += s.turn;  // one row per page
             }
             a.stage[rp.stage_begin + k] = page;
         } else {
@@ -776,6 +784,7 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
                 page = -1;
             }
             a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
+            if (a.pending && page >= 0) a.pending[page] = 0;  // a free page carries no pending turn
         }
     }
 }
@@ -970,6 +979,143 @@ __global__ void gather_kernel(const uint4* kv, const int32_t* table_row, long lo
     }
 }
 
+// -------------------------------------------------------------------------
+// Lazy pools.  cos / sin of pending * theta_j: the angle is formed in fp64 and the
+// fp64 sincos reduces it, then it is rounded once to the rotation's arithmetic,
+// exactly as the host does for an eager splice.
+__device__ __forceinline__ void pending_trig(int pend, double theta_j, bool bf16, float& c, float& s)
+{
+    double sd, cd;
+    sincos((double)pend * theta_j, &sd, &cd);
+    if (bf16) {
+        c = __bfloat162float(__double2bfloat16(cd));
+        s = __bfloat162float(__double2bfloat16(sd));
+    } else {
+        c = (float)cd;
+        s = (float)sd;
+    }
+}
+
+// cos / sin of the pairs of item q of a band: 8 pairs j = 8q.. (half-split) or 4
+// pairs j = 4q.. (interleaved).
+template <int kLayout>
+__device__ __forceinline__ void item_trig(int pend, int q, const double* theta_j, bool bf16, float* c, float* s)
+{
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) pending_trig(pend, theta_j[kPairs * q + w], bf16, c[w], s[w]);
+}
+
+// Item q of the band at `band` (x at q, y at q + head_vecs / 2 for half-split),
+// turned by (c, s) and written to `dst`.
+template <int kLayout>
+__device__ __forceinline__ void turn_item(const uint4* band, uint4* dst, int q, int hv, bool bf16, const float* c,
+                                          const float* s)
+{
+    if (kLayout == 0) {
+        uint4 x = band[q], y = band[q + hv / 2];
+        if (bf16) rotate_half_split<true>(x, y, c, s);
+        else rotate_half_split<false>(x, y, c, s);
+        dst[q] = x;
+        dst[q + hv / 2] = y;
+    } else {
+        uint4 x = band[q];
+        if (bf16) rotate_interleaved<true>(x, c, s);
+        else rotate_interleaved<false>(x, c, s);
+        dst[q] = x;
+    }
+}
+
+// Gather from a lazy pool: one warp per row.  The latent is copied; item q of each
+// rope band is turned by the slot's pending count on the way out.
+template <int kLayout>
+__global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, const Geometry g, long long layer,
+                                   long long t0, long long n, uint4* out, const int32_t* pending,
+                                   const double* theta_j, int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    const int hv = g.head_vecs;
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long r = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; r < n; r += warps) {
+        const long long t = t0 + r;
+        const long long B = g.block_size;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= g.num_pages) {
+            if (lane == 0) raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        const long long slot = (long long)page * B + t % B;
+        const uint4* row = kv + layer * g.layer_vecs + slot * g.row_vecs;
+        uint4* o = out + r * g.row_vecs;
+        for (int c = lane; c < g.latent_vecs; c += 32) o[c] = row[c];
+        const int pend = pending[slot];
+        for (int it = lane; it < g.rope_heads * head_items; it += 32) {
+            const int head = it / head_items, q = it - head * head_items;
+            const uint4* band = row + g.latent_vecs + head * hv;
+            uint4* dst = o + g.latent_vecs + head * hv;
+            if (pend == 0) {
+                dst[q] = band[q];
+                if (kLayout == 0) dst[q + hv / 2] = band[q + hv / 2];
+                continue;
+            }
+            float c[8], s[8];
+            item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
+            turn_item<kLayout>(band, dst, q, hv, bf16, c, s);
+        }
+    }
+}
+
+// Materialize a lazy request: one warp per row.  Lanes take the row's (layer,
+// band item) pairs in turn, so the pair group q of a lane, and the cos / sin held
+// for it, change only when the items per layer do not divide 32.  The count is
+// read before and cleared after every layer of the row is turned in place.
+template <int kLayout>
+__global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Geometry g, long long len,
+                                   int32_t* pending, const double* theta_j, int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    const int hv = g.head_vecs;
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const int items = g.rope_heads * head_items;  // per layer
+    const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long t = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; t < len; t += warps) {
+        const long long B = g.block_size;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= g.num_pages) {
+            if (lane == 0) raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        const long long slot = (long long)page * B + t % B;
+        const int pend = pending[slot];
+        if (pend == 0) continue;
+        float c[8], s[8];
+        int have_q = -1;
+        for (long long idx = lane; idx < (long long)g.num_layers * items; idx += 32) {
+            const long long layer = idx / items;
+            const int it = (int)(idx - layer * items);
+            const int head = it / head_items, q = it - head * head_items;
+            if (q != have_q) {
+                item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
+                have_q = q;
+            }
+            uint4* band = kv + layer * g.layer_vecs + slot * g.row_vecs + g.latent_vecs + head * hv;
+            turn_item<kLayout>(band, band, q, hv, bf16, c, s);
+        }
+        __syncwarp();
+        if (lane == 0) pending[slot] = 0;
+    }
+}
+
+__global__ void clear_pending_kernel(int32_t* pending, const int32_t* page_ids, long long n, int block_size)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n * block_size;
+         i += (long long)gridDim.x * blockDim.x)
+        pending[(long long)page_ids[i / block_size] * block_size + i % block_size] = 0;
+}
+
 int grid_for(long long items, int threads, int cap)
 {
     long long g = (items + threads - 1) / threads;
@@ -1127,6 +1273,37 @@ int rotate_in_place_blocks_per_sm(int* blocks)
 {
     return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, rotate_in_place<0, false, ParamPlan>,
                                                               kMoveThreads, 0);
+}
+
+int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
+                       int64_t t1, void* out, const int32_t* pending, const double* theta_j, int32_t* status,
+                       void* stream)
+{
+    const long long n = t1 - t0;
+    if (n <= 0) return 0;
+    auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? gather_lazy_kernel<0> : gather_lazy_kernel<1>;
+    k<<<grid_for(n * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(kv), table_row, g,
+                                                                      layer, t0, n, static_cast<uint4*>(out),
+                                                                      pending, theta_j, status);
+    return (int)cudaGetLastError();
+}
+
+int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
+                       const double* theta_j, int32_t* status, void* stream)
+{
+    if (len <= 0) return 0;
+    auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
+    k<<<grid_for(len * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
+                                                                        pending, theta_j, status);
+    return (int)cudaGetLastError();
+}
+
+int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream)
+{
+    if (n <= 0) return 0;
+    clear_pending_kernel<<<grid_for(n * block_size, 256, 4096), 256, 0, (cudaStream_t)stream>>>(pending, page_ids, n,
+                                                                                             block_size);
+    return (int)cudaGetLastError();
 }
 
 int move_rotate_blocks_per_sm(int* blocks)

@@ -162,6 +162,7 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.n_reqs = (int32_t)plan.reqs.size();
     a.n_trig = plan.n_trig;
     a.max_blocks = bt->max_blocks;
+    a.pending = p->d_pending;
     a.g = p->g;
 
     a.move_kernel = p->move_kernel;

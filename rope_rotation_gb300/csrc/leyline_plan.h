@@ -7,6 +7,8 @@
 //   REPL   rows of a directive's R, copied bit for bit
 //   COPY   a surviving run whose accumulated Delta is 0, moved unchanged
 //   ROT    a surviving run moved by Delta != 0; its rope band is turned by R(Delta)
+//          (in a lazy pool such a run is a COPY segment whose turn is added to the
+//          rows' pending counts instead)
 // The kernels look up the segment of a destination row, read the source row
 // through the old block table (or from R), and write it into a fresh page.
 // A re-indexed request (block size 1, pool flag LEYLINE_POOL_REINDEX) keeps its
@@ -75,9 +77,11 @@ struct Seg {
     int32_t n_repl;        // rows of R per layer (REPL); dropped tokens (DROP)
     int32_t aux;           // re-index: R rows of the request before this segment (REPL),
                            // dropped tokens of the request before this segment (DROP)
+    int32_t turn;          // positions the segment's rows turn (ROT; in lazy pools also COPY)
+    int32_t pad;
 };
 
 static_assert(sizeof(ReqPlan) == 104, "ReqPlan layout");
-static_assert(sizeof(Seg) == 40, "Seg layout");
+static_assert(sizeof(Seg) == 48, "Seg layout");
 
 }  // namespace leyline

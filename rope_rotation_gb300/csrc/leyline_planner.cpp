@@ -99,7 +99,7 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pair_layout");
     if (d->rotate_precision != LEYLINE_ROTATE_FP32 && d->rotate_precision != LEYLINE_ROTATE_BF16_NAIVE)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown rotate_precision");
-    if ((d->flags & ~(uint32_t)LEYLINE_POOL_REINDEX) != 0)
+    if ((d->flags & ~(uint32_t)(LEYLINE_POOL_REINDEX | LEYLINE_POOL_LAZY)) != 0)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags");
     if (d->rope_heads < 0 || d->rope_heads > 1024)
         return set_error(LEYLINE_ERR_INVALID_ARG, "rope_heads must be in [0, 1024]");
@@ -192,6 +192,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
 
     // 3. plan each touched request
     const bool reindex = (g.flags & LEYLINE_POOL_REINDEX) && B == 1;
+    const bool lazy = (g.flags & LEYLINE_POOL_LAZY) != 0;
     plan->reindex = reindex;
     const int64_t row_bytes = (int64_t)g.row_elems * 2;
     const int64_t rope_bytes = (int64_t)g.rope_vecs * 16;  // every RoPE band of a row
@@ -250,7 +251,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         // keeps positions).
         const int64_t s1 = eff.front()->s_start;
         if (rp.row0 < s1) {
-            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0};
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
             plan->segs.push_back(s);
             st.head_slots += s1 - rp.row0;
         }
@@ -258,7 +259,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         for (size_t k = 0; k < eff.size(); ++k) {
             const leyline_directive_t* d = eff[k];
             if (d->n_repl > 0) {
-                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)repl_before};
+                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)repl_before, 0, 0};
                 plan->segs.push_back(s);
                 st.repl_slots += d->n_repl;
                 repl_before += d->n_repl;
@@ -268,11 +269,14 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             if (d->mode == LEYLINE_AMORTIZE) A += dk;
             const int64_t run_end = (k + 1 < eff.size()) ? eff[k + 1]->s_start : L;
             if (run_end > d->s_end) {
-                Seg s{d->s_end + D, d->s_end, nullptr, A == 0 ? SEG_COPY : SEG_ROT, -1, 0, 0};
+                Seg s{d->s_end + D, d->s_end, nullptr, (A == 0 || lazy) ? SEG_COPY : SEG_ROT, -1, 0, 0, (int32_t)A,
+                      0};
                 if (A != 0) {
-                    s.trig = plan->n_trig++;
-                    plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
-                    segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                    if (!lazy) {
+                        s.trig = plan->n_trig++;
+                        plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
+                        segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                    }
                     turned_rows += run_end - d->s_end;
                 }
                 plan->segs.push_back(s);
@@ -281,7 +285,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         }
         rp.seg_count = (int32_t)plan->segs.size() - rp.seg_begin;
         if (rp.seg_count == 0) {  // nothing left to write (pure truncation at a block boundary)
-            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0};
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
             plan->segs.push_back(s);
             rp.seg_count = 1;
         }
@@ -293,7 +297,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             for (const auto* d : eff) {
                 const int64_t len = d->s_end - d->s_start;
                 if (len == 0) continue;
-                Seg s{-1, d->s_start, nullptr, SEG_DROP, -1, (int32_t)len, (int32_t)drops_before};
+                Seg s{-1, d->s_start, nullptr, SEG_DROP, -1, (int32_t)len, (int32_t)drops_before, 0, 0};
                 plan->segs.push_back(s);
                 drops_before += len;
             }
@@ -321,7 +325,10 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     plan->total_commit = commit;
     plan->total_pop = pops;
     plan->total_push = pushes;
-    if (reindex) {
+    if (reindex && lazy) {  // survivors keep page and bits: only their pending counts change
+        st.algorithmic_bytes = 2 * row_bytes * g.num_layers * st.repl_slots + 8 * turned_rows;
+        st.moved_bytes = st.algorithmic_bytes;
+    } else if (reindex) {
         st.algorithmic_bytes = 2 * g.num_layers * (rope_bytes * turned_rows + row_bytes * st.repl_slots);
         st.moved_bytes = st.algorithmic_bytes;
     } else {

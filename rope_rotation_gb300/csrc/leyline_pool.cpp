@@ -21,6 +21,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <string>
@@ -118,6 +119,17 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->plan_uploaded, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+    if (e == cudaSuccess && (g.flags & LEYLINE_POOL_LAZY)) {
+        // every slot starts with nothing pending; readers take theta_j from a device table
+        const size_t slots = (size_t)g.num_pages * (size_t)g.block_size;
+        e = cudaMalloc(&p->d_pending, sizeof(int32_t) * slots);
+        if (e == cudaSuccess) e = cudaMemset(p->d_pending, 0, sizeof(int32_t) * slots);
+        std::vector<double> th(g.rope_dim / 2);
+        for (int j = 0; j < g.rope_dim / 2; ++j) th[j] = std::pow(g.theta, -2.0 * j / g.rope_dim);
+        if (e == cudaSuccess) e = cudaMalloc(&p->d_theta_j, sizeof(double) * th.size());
+        if (e == cudaSuccess)
+            e = cudaMemcpy(p->d_theta_j, th.data(), sizeof(double) * th.size(), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = (cudaError_t)launch_init_queue(p->d_queue, g.num_pages, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
@@ -166,6 +178,8 @@ int leyline_pool_destroy(leyline_pool_t* p)
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_queue) cudaFree(p->d_queue);
     if (p->d_stage) cudaFree(p->d_stage);
+    if (p->d_pending) cudaFree(p->d_pending);
+    if (p->d_theta_j) cudaFree(p->d_theta_j);
     delete p;
     return LEYLINE_OK;
 }
@@ -216,6 +230,11 @@ int leyline_free_pages(leyline_pool_t* p, int32_t n, const int32_t* ids)
         const int64_t len = std::min<int64_t>(n - done, p->q_cap - at);
         cudaError_t e = cudaMemcpy(p->d_queue + at, ids + done, sizeof(int32_t) * (size_t)len, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return cuda_error(e, "writing the free-page ring");
+        if (p->d_pending) {  // a free page carries no pending turn: clear the returned pages' counts
+            e = (cudaError_t)launch_clear_pending(p->d_pending, p->d_queue + at, len, p->g.block_size, nullptr);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+            if (e != cudaSuccess) return cuda_error(e, "clearing pending turns of returned pages");
+        }
         done += len;
     }
     p->q_tail += n;
@@ -283,6 +302,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     a.n_reqs = (int32_t)plan.reqs.size();
     a.n_trig = plan.n_trig;
     a.max_blocks = bt->max_blocks;
+    a.pending = p->d_pending;
     a.g = p->g;
 
     cudaError_t e;
@@ -404,10 +424,42 @@ int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t r
     DeviceGuard guard(p->device);
     int rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
-    int err = launch_gather(p->kv, bt->table + (int64_t)req * bt->max_blocks, p->g, layer, t0, t1, out, p->d_status,
-                            stream);
+    const int32_t* row = bt->table + (int64_t)req * bt->max_blocks;
+    int err = p->d_pending ? launch_gather_lazy(p->kv, row, p->g, layer, t0, t1, out, p->d_pending, p->d_theta_j,
+                                                p->d_status, stream)
+                           : launch_gather(p->kv, row, p->g, layer, t0, t1, out, p->d_status, stream);
     if (err != 0) return cuda_error((cudaError_t)err, "launching the gather kernel");
     return mark_done(p, stream);
+}
+
+int leyline_materialize(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t req, void* stream_v)
+{
+    clear_error();
+    if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    if (!p->d_pending) return set_error(LEYLINE_ERR_INVALID_ARG, "the pool was not created with LEYLINE_POOL_LAZY");
+    if (req < 0 || req >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
+    const int64_t len = bt->seq_lens_host[req];
+    if (len < 0 || len > (int64_t)bt->max_blocks * p->g.block_size)
+        return set_error(LEYLINE_ERR_INVALID_ARG, "seq_len outside the block table");
+    if (len == 0) return LEYLINE_OK;
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    DeviceGuard guard(p->device);
+    int rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    int err = launch_materialize(p->kv, bt->table + (int64_t)req * bt->max_blocks, p->g, len, p->d_pending,
+                                 p->d_theta_j, p->d_status, stream);
+    if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
+    return mark_done(p, stream);
+}
+
+int32_t* leyline_pending_ptr(leyline_pool_t* p)
+{
+    clear_error();
+    if (!p) {
+        set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+        return nullptr;
+    }
+    return p->d_pending;
 }
 
 int leyline_sync_status(leyline_pool_t* p)

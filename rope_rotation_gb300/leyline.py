@@ -37,6 +37,7 @@ LEYLINE_AMORTIZE = 0
 LEYLINE_FORGET = 1
 LEYLINE_EVICT = 2
 LEYLINE_POOL_REINDEX = 1
+LEYLINE_POOL_LAZY = 2
 
 
 class LeylineError(RuntimeError):
@@ -95,6 +96,8 @@ _SIGNATURES = {
     "leyline_last_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
     "leyline_gather": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int64, ctypes.c_int64, _vp, _vp]),
+    "leyline_materialize": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, _vp]),
+    "leyline_pending_ptr": (ctypes.c_void_p, [_vp]),
     "leyline_sync_status": (ctypes.c_int, [_vp]),
     "leyline_kernel_timing_enable": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "leyline_kernel_timing_read": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double),
@@ -249,6 +252,15 @@ def leyline_gather(pool, tables: Tables, req: int, layer: int, t0: int, t1: int,
     """out: bf16 CUDA tensor [t1 - t0][row]."""
     _check(load().leyline_gather(pool, ctypes.byref(tables.bt), req, layer, t0, t1, _tensor_ptr(out),
                                  _stream_ptr(stream)))
+
+
+def leyline_materialize(pool, tables: Tables, req: int, stream=None) -> None:
+    _check(load().leyline_materialize(pool, ctypes.byref(tables.bt), req, _stream_ptr(stream)))
+
+
+def leyline_pending_ptr(pool) -> int:
+    """Device address of the pending counts (0 when the pool is not lazy)."""
+    return load().leyline_pending_ptr(pool) or 0
 
 
 def leyline_sync_status(pool) -> None:

@@ -14,6 +14,14 @@ import numpy as np
 from . import leyline
 
 
+class _DeviceArray:
+    """int32 device memory owned by the pool, exposed through __cuda_array_interface__."""
+
+    def __init__(self, addr: int, n: int, device: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (addr, False), "version": 3}
+        self.device = device
+
+
 class PagedCache:
     def __init__(self, num_layers: int, block_size: int, num_pages: int, max_reqs: int, max_blocks: int,
                  latent_dim: int = 512, rope_dim: int = 64, rope_theta: float = 10000.0,
@@ -73,6 +81,18 @@ class PagedCache:
             out = self.torch.empty((t1 - t0, self.row), dtype=self.torch.bfloat16, device=self.device)
         leyline.leyline_gather(self.pool, self.tables, req, layer, t0, t1, out, stream)
         return out
+
+    def materialize(self, req: int, stream=None) -> None:
+        leyline.leyline_materialize(self.pool, self.tables, req, stream)
+
+    def pending(self):
+        """Pending counts [num_pages][block_size] of a lazy pool, as a torch view (None otherwise)."""
+        addr = leyline.leyline_pending_ptr(self.pool)
+        if not addr:
+            return None
+        n = self.num_pages * self.block_size
+        holder = _DeviceArray(addr, n, self.device.index or 0)
+        return self.torch.as_tensor(holder, device=self.device).view(self.num_pages, self.block_size)
 
     def free_pages(self) -> int:
         return leyline.leyline_free_page_count(self.pool)

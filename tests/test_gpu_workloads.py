@@ -167,3 +167,67 @@ def test_chain_64_drift():
     with open(os.path.join(OUT, "chain_drift.json"), "w") as f:
         json.dump(report, f, indent=1)
     print("chain drift:", report)
+
+
+def test_chain_64_lazy_drift():
+    """The same 64-splice chain on a lazy pool (block 1, re-index): splices move bits and
+    count turns, and each read turns the row once, so a read equals the from-scratch
+    encoding at the final position within one rounding, however many splices moved it."""
+    w = configs.chain_64()
+    lat = w.latent_dim
+    maps, L = [], w.lengths[0]
+    for step in w.steps:
+        d = step[0]
+        L, kind, idx, _ = oracle.splice_map(L, [(d.s_start, d.s_end, d.n_repl)])
+        maps.append((kind, idx))
+    final_len = L
+    rng = np.random.default_rng(65)
+    pos = np.unique(np.concatenate([rng.integers(0, final_len, size=1200), [0, final_len - 1]]))
+    layers = rng.integers(0, w.num_layers, size=pos.size)
+    cache = H.make_cache(w, flags=2 | 1)
+    keep = []
+    for step in w.steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        cache.splice(dirs)
+    torch.cuda.synchronize()
+    cache.check_status()
+    assert int(cache.seq_lens_host[0]) == final_len
+    buf = torch.empty((1, cache.row), dtype=torch.bfloat16, device=cache.device)
+    got = np.empty((pos.size, cache.row), dtype=np.uint16)
+    for i, (p, layer) in enumerate(zip(pos, layers)):
+        cache.gather(0, int(layer), int(p), int(p) + 1, buf)
+        got[i] = buf.view(torch.int16).cpu().numpy().view(np.uint16)[0]
+    stats = cache.last_stats()
+    _release(cache)
+    del keep
+    truth, moved = [], []
+    for i, p in enumerate(pos):
+        origin, path = _trace_back(maps, int(p))
+        layer = int(layers[i])
+        if origin[0] == "old":
+            row = synth.cache_rows(w.seed, 0, layer, [origin[1]])[0]
+            start = origin[1]
+        else:
+            _, k, ri = origin
+            d = w.steps[k][0]
+            row = synth.repl_rows(w.seed, 0, d.key, w.num_layers, d.n_repl)[layer, ri]
+            start = path[0]
+        assert np.array_equal(got[i, :lat], row[:lat]), "latent bits differ after the chain"
+        truth.append(oracle.rerotate(row[lat:], start, path[-1], w.theta))
+        moved.append(start != path[-1])
+    truth = np.array(truth)
+    moved = np.array(moved)
+    assert np.array_equal(got[~moved, lat:], truth[~moved])
+    c = H.compare_kpe(got[moved, lat:], truth[moved], 0)
+    g = oracle.bf16_value(got[:, lat:])
+    t = oracle.bf16_value(truth)
+    report = {"final_len": final_len, "rows": int(pos.size), "moved_rows": int(moved.sum()),
+              "lazy_drift_rel_l2": float(np.linalg.norm(g - t) / np.linalg.norm(t)),
+              "lazy_elements_off_by_floor_clause": c["floor_used"], "lazy_max_bf16_steps": c["max_steps"],
+              "last_splice_algorithmic_bytes": int(stats["algorithmic_bytes"])}
+    os.makedirs(OUT, exist_ok=True)
+    with open(os.path.join(OUT, "chain_drift_lazy.json"), "w") as f:
+        json.dump(report, f, indent=1)
+    print("lazy chain drift:", report)
+    assert report["lazy_drift_rel_l2"] < 1e-3

@@ -120,3 +120,33 @@ def test_noalloc_matches_splice_in_reindex_mode():
         del keep_ref, keep_new
     ref.close()
     new.close()
+
+
+def test_noalloc_matches_splice_on_lazy_pools():
+    """Lazy pools: both entry points move the same bits and leave the same pending counts."""
+    from rope_rotation_gb300 import leyline
+    steps = [[Dir(0, 40, 130, 9, 0), Dir(1, 5, 700, 3, 1)],
+             [Dir(0, 0, 3, 0, 4), Dir(1, 100, 101, 30, 5, mode=2)]]
+    w = Workload("noalloc-lazy", 2, 16, [300, 1000], steps, seed=23)
+    ref = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_LAZY)
+    new = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_LAZY)
+    for step in w.steps:
+        dirs_ref, keep_ref = H.gpu_directives(w, step)
+        dirs_new, keep_new = H.gpu_directives(w, step)
+        leyline.leyline_splice(ref.pool, ref.tables, dirs_ref)
+        leyline.leyline_splice_noalloc(new.pool, new.tables, dirs_new)
+        torch.cuda.synchronize()
+        ref.check_status()
+        new.check_status()
+        assert np.array_equal(ref.seq_lens_host, new.seq_lens_host)
+        assert ref.last_stats() == new.last_stats()
+        for r in range(w.num_reqs):
+            n = int(ref.seq_lens_host[r])
+            assert np.array_equal(H.logical_rows(ref, r, n), H.logical_rows(new, r, n))
+            nb = -(-n // w.block_size)
+            pr = ref.pending()[ref.table[r, :nb].long()].reshape(-1)[:n]
+            pn = new.pending()[new.table[r, :nb].long()].reshape(-1)[:n]
+            assert torch.equal(pr, pn)
+        del keep_ref, keep_new
+    ref.close()
+    new.close()
