@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--reindex", action="store_true",
                     help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
+    ap.add_argument("--lazy", action="store_true",
+                    help="lazy pools: splices count pending turns instead of rotating (LEYLINE_POOL_LAZY)")
     ap.add_argument("--single-leg", action="store_true",
                     help="time the move kernel inside the value leg and skip the other legs (large workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -196,7 +198,8 @@ def run_ours(args, rank, world, local):
     max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
     pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
     cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta,
-                       flags=leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
+                       flags=(leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
+                       | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0))
     seed = rank_seed(w.seed, rank)
     for g in range(groups):
         for r, L in enumerate(w.lengths):
@@ -328,6 +331,8 @@ def run_ours(args, rank, world, local):
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
+                   "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
+                   + (", re-index" if args.reindex and B == 1 else ""),
                    "move_kernel": ("rotate_in_place" if args.reindex and B == 1
                                    else os.environ.get("LEYLINE_MOVE_KERNEL", "vector")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -90,7 +90,9 @@ typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_
  *   latent is not touched).  Rows of R go to fresh pages, the pages of dropped
  *   tokens return to the free list.  The rotation happens in place before the
  *   commit, so a call that fails after validation leaves the pool inconsistent
- *   (as any LEYLINE_ERR_CUDA does).  Ignored for block_size > 1. */
+ *   (as any LEYLINE_ERR_CUDA does).  Ignored for block_size > 1.  Requires
+ *   rope_dim <= 256 and rope_heads * rope_dim <= 512 (else pool creation fails
+ *   with LEYLINE_ERR_INVALID_ARG). */
 #define LEYLINE_POOL_REINDEX 1
 /* LEYLINE_POOL_LAZY: a splice does not turn rope bands.  The pool keeps, per slot,
  * an int32 count of positions that the stored band still has to turn (the

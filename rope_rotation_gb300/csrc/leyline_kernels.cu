@@ -799,28 +799,40 @@ __device__ __forceinline__ uint4 ld_rw(const uint4* p)
     return v;
 }
 
-// Rotate kernel of re-index mode.  Work unit = (16-row tile, group of layers): the
-// 256 threads take the tile's rope-band work items (4 per row for half-split pairs,
-// 8 interleaved) for as many layers as fit, turning each band in place; rows of R
-// are copied whole into their fresh pages.  A band is 128 bytes every 1152, so this
-// kernel is bound by DRAM row activations rather than by streaming bandwidth.
+// Rotate kernel of re-index mode.  Its tiles cover only the rows that need work:
+// each turned (ROT) or R (REPL) segment is cut into 16-row tiles of its own (the
+// planner numbers them in Seg::tile_off), so survivors that keep their encoding
+// -- every survivor of a lazy pool -- cost nothing here.  Work unit = (tile, group
+// of layers).  The threads' work items (4 per band and layer for half-split pairs,
+// 8 interleaved; at most kMaxItems per thread) are decoded once at kernel start,
+// and the unit loop advances tile and layer group by counters, so a unit costs
+// only its loads, its arithmetic and its stores.  A band is 128 bytes every 1152.
 struct ReindexRow {
     uint4* row;          // the row's page (layer 0); nullptr: nothing to do
     const uint4* rsrc;   // row of R (layer 0), REPL only
-    long long rstride;   // vectors between layers of R
-    int kind;            // SegKind, -1 past the end
-    int trig;
 };
 
 constexpr int kMaxRopeDim = 256;
+constexpr int kMaxItems = 4;  // work items per thread: rope_heads * rope_dim <= 512
 
-template <int kLayout, bool kBf16, class PlanSrc>
-__global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_constant__ SpliceArgs a,
+// Layers per work unit of the re-index rotate kernel: as many as give each of the
+// CTA's threads kItems work items (at least one layer).
+__host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, int items)
+{
+    const int l = items * kMoveThreads / per_layer;
+    return l > 0 ? l : 1;
+}
+
+// kItems: work items per thread.  1 for the MLA row (16 rows x 4 or 8 items per
+// layer: a unit covers 4 or 2 layers), with 8 CTAs per SM; kMaxItems for wider rows.
+template <int kLayout, bool kBf16, int kItems, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_place(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
     __shared__ ReindexRow rr[kTileRows];
-    __shared__ __align__(16) float trig_s[kTileRows][kMaxRopeDim];  // (cos, sin) per pair of each row
-    __shared__ int has_repl;
+    __shared__ __align__(16) float trig_s[kMaxRopeDim];  // (cos, sin) per pair of the tile's segment
+    __shared__ int tile_kind;                             // SEG_ROT or SEG_REPL
+    __shared__ long long tile_rstride;                    // vectors between layers of R (REPL)
     wait_for_previous_grid();
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
@@ -828,92 +840,108 @@ __global__ void __launch_bounds__(kMoveThreads) rotate_in_place(const __grid_con
     const long long layer_vecs = a.g.layer_vecs;
     const int hv = a.g.head_vecs, lv = a.g.latent_vecs, row_vecs = a.g.row_vecs;
     const int rope_dim = a.g.rope_dim;
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;        // pairs per work item
     const int head_items = kLayout == 0 ? hv / 2 : hv;  // work items per RoPE band
     const int ipr = a.g.rope_heads * head_items;        // work items per row and layer
     const int per_layer = kTileRows * ipr;
-    const int lpu = blockDim.x / per_layer > 0 ? (int)(blockDim.x / per_layer) : 1;  // layers per unit
+    const int lpu = reindex_layers_per_unit(per_layer, kItems);
     const long long groups = (L + lpu - 1) / lpu;
+    // this thread's items: row i, layer offset lo, vector offset in the rope region, pair group q
+    int it_row[kItems], it_lo[kItems], it_off[kItems], it_q[kItems];
+    int n_items = 0;
+#pragma unroll
+    for (int k = 0; k < kItems; ++k) {
+        const int e = threadIdx.x + k * kMoveThreads;
+        it_row[k] = it_lo[k] = it_off[k] = it_q[k] = 0;
+        if (e < lpu * per_layer) {
+            const int lo = e / per_layer, it = e - lo * per_layer;
+            const int i = it / ipr, hq = it - i * ipr;
+            const int head = hq / head_items, q = hq - head * head_items;
+            it_row[k] = i;
+            it_lo[k] = lo;
+            it_off[k] = lv + head * hv + q;
+            it_q[k] = q;
+            n_items = k + 1;
+        }
+    }
     long long u0, u1;
     my_units(a.total_tiles * groups, u0, u1);
+    long long tile = u0 / groups, grp = u0 - (u0 / groups) * groups;
     long long cur_tile = -1;
     for (long long u = u0; u < u1; ++u) {
-        const long long tile = u / groups;
-        const long long layer0 = (u - tile * groups) * lpu;
         if (tile != cur_tile) {
             __syncthreads();
-            if (threadIdx.x == 0) has_repl = 0;
-            __syncthreads();
             if (threadIdx.x < kTileRows) {
-                ReindexRow d{nullptr, nullptr, 0, -1, -1};
+                ReindexRow d{nullptr, nullptr};
                 const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
-                const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + threadIdx.x;
-                if (p < rp.new_len) {
-                    const Seg* sg = pv.segs + rp.seg_begin;
-                    const Seg s = sg[find_seg(sg, rp.seg_count, p)];
+                const long long lt = tile - rp.tile_begin;
+                const Seg* sg = pv.segs + rp.seg_begin;
+                int k = 0;
+                for (int q = 0; q < rp.seg_count; ++q)
+                    if (sg[q].tile_off >= 0 && sg[q].tile_off <= lt) k = q;
+                const Seg s = sg[k];
+                const long long end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
+                const long long p = s.new_start + (lt - s.tile_off) * kTileRows + threadIdx.x;
+                if (p < end) {
                     const int page = a.stage[rp.stage_begin + (p - rp.row0)];
-                    d.kind = s.kind;
-                    if (page >= 0 && page < a.g.num_pages) d.row = static_cast<uint4*>(a.kv) + (long long)page * row_vecs;
-                    if (s.kind == SEG_ROT) d.trig = s.trig;
-                    if (s.kind == SEG_REPL) {
+                    if (page >= 0 && page < a.g.num_pages)
+                        d.row = static_cast<uint4*>(a.kv) + (long long)page * row_vecs;
+                    if (s.kind == SEG_REPL)
                         d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * row_vecs;
-                        d.rstride = (long long)s.n_repl * row_vecs;
-                        atomicOr(&has_repl, 1);
-                    }
                 }
                 rr[threadIdx.x] = d;
-            }
-            __syncthreads();
-            for (int e = threadIdx.x; e < kTileRows * rope_dim; e += blockDim.x) {
-                const int row = e / rope_dim, c = e - row * rope_dim;
-                const int t = rr[row].trig;
-                trig_s[row][c] = t >= 0 ? pv.trig[(long long)t * rope_dim + c] : 0.f;
+                if (threadIdx.x == 0) {
+                    tile_kind = s.kind;
+                    tile_rstride = (long long)s.n_repl * row_vecs;
+                }
+                if (s.kind == SEG_ROT)  // the segment's cos/sin, rope_dim floats
+                    for (int c = threadIdx.x; c < rope_dim; c += kTileRows)
+                        trig_s[c] = pv.trig[(long long)s.trig * rope_dim + c];
             }
             __syncthreads();
             cur_tile = tile;
         }
-        // rope bands of turned rows, in place
-        for (int e = threadIdx.x; e < lpu * per_layer; e += blockDim.x) {
-            const int lo = e / per_layer, it = e - (e / per_layer) * per_layer;
-            const long long layer = layer0 + lo;
-            if (layer >= L) continue;
-            const int i = it / ipr, hq = it - (it / ipr) * ipr;
-            const int head = hq / head_items, q = hq - head * head_items;
-            const ReindexRow d = rr[i];
-            if (d.kind == SEG_ROT && d.row) {
-                uint4* r = d.row + layer * layer_vecs + lv + head * hv;
-                float cs[8], sn[8];
-                const int np = kLayout == 0 ? 8 : 4;
-                const float* tp = &trig_s[i][2 * np * q];
+        const long long layer0 = grp * lpu;
+        if (tile_kind == SEG_ROT) {  // rope bands, in place
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    if (w < np) {
-                        cs[w] = tp[2 * w];
-                        sn[w] = tp[2 * w + 1];
-                    }
+            for (int k = 0; k < kItems; ++k) {
+                if (k >= n_items) break;
+                const long long layer = layer0 + it_lo[k];
+                uint4* row = rr[it_row[k]].row;
+                if (layer >= L || !row) continue;
+                uint4* r = row + layer * layer_vecs + it_off[k];
+                float cs[8], sn[8];
+                const float* tp = &trig_s[2 * kPairs * it_q[k]];
+#pragma unroll
+                for (int w = 0; w < kPairs; ++w) {
+                    cs[w] = tp[2 * w];
+                    sn[w] = tp[2 * w + 1];
                 }
                 if (kLayout == 0) {
-                    uint4 x = ld_rw(r + q), y = ld_rw(r + q + hv / 2);
+                    uint4 x = ld_rw(r), y = ld_rw(r + hv / 2);
                     rotate_half_split<kBf16>(x, y, cs, sn);
-                    st_stream(r + q, x);
-                    st_stream(r + q + hv / 2, y);
+                    st_stream(r, x);
+                    st_stream(r + hv / 2, y);
                 } else {
-                    uint4 x = ld_rw(r + q);
+                    uint4 x = ld_rw(r);
                     rotate_interleaved<kBf16>(x, cs, sn);
-                    st_stream(r + q, x);
+                    st_stream(r, x);
                 }
             }
-        }
-        // rows of R: whole rows into their fresh pages
-        if (has_repl) {
+        } else {  // rows of R: whole rows into their fresh pages
             const int per_row = lpu * row_vecs;
             for (int e = threadIdx.x; e < kTileRows * per_row; e += blockDim.x) {
                 const int i = e / per_row, rem = e - (e / per_row) * per_row;
                 const int lo2 = rem / row_vecs, c = rem - (rem / row_vecs) * row_vecs;
                 const long long lay = layer0 + lo2;
                 const ReindexRow d = rr[i];
-                if (d.kind != SEG_REPL || !d.row || lay >= L) continue;
-                st_stream(d.row + lay * layer_vecs + c, ld_stream(d.rsrc + lay * d.rstride + c));
+                if (!d.row || !d.rsrc || lay >= L) continue;
+                st_stream(d.row + lay * layer_vecs + c, ld_stream(d.rsrc + lay * tile_rstride + c));
             }
+        }
+        if (++grp == groups) {
+            grp = 0;
+            ++tile;
         }
     }
 }
@@ -1200,17 +1228,27 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
     const int ipr = a.g.rope_heads * (split ? a.g.head_vecs / 2 : a.g.head_vecs);
-    const int lpu = kMoveThreads / (kTileRows * ipr) > 0 ? kMoveThreads / (kTileRows * ipr) : 1;
+    const int per_layer = kTileRows * ipr;
+    const bool mla = per_layer <= kMoveThreads;  // one item per thread; else kMaxItems
+    const int lpu = reindex_layers_per_unit(per_layer, mla ? 1 : kMaxItems);
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);
     if (e == cudaSuccess && t0) e = cudaEventRecord(t0, s);
     if (e == cudaSuccess && units > 0) {
         if (split)
-            e = bf16 ? launch_dependent(rotate_in_place<0, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
-                     : launch_dependent(rotate_in_place<0, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+            e = bf16 ? (mla ? launch_dependent(rotate_in_place<0, true, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                            : launch_dependent(rotate_in_place<0, true, kMaxItems, PlanSrc>, grid, kMoveThreads, s, a,
+                                               plan))
+                     : (mla ? launch_dependent(rotate_in_place<0, false, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                            : launch_dependent(rotate_in_place<0, false, kMaxItems, PlanSrc>, grid, kMoveThreads, s,
+                                               a, plan));
         else
-            e = bf16 ? launch_dependent(rotate_in_place<1, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
-                     : launch_dependent(rotate_in_place<1, false, PlanSrc>, grid, kMoveThreads, s, a, plan);
+            e = bf16 ? (mla ? launch_dependent(rotate_in_place<1, true, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                            : launch_dependent(rotate_in_place<1, true, kMaxItems, PlanSrc>, grid, kMoveThreads, s, a,
+                                               plan))
+                     : (mla ? launch_dependent(rotate_in_place<1, false, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                            : launch_dependent(rotate_in_place<1, false, kMaxItems, PlanSrc>, grid, kMoveThreads, s,
+                                               a, plan));
     }
     if (e == cudaSuccess && t1) e = cudaEventRecord(t1, s);
     if (e == cudaSuccess && a.total_commit > 0)
@@ -1271,7 +1309,7 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
 
 int rotate_in_place_blocks_per_sm(int* blocks)
 {
-    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, rotate_in_place<0, false, ParamPlan>,
+    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, rotate_in_place<0, false, 1, ParamPlan>,
                                                               kMoveThreads, 0);
 }
 

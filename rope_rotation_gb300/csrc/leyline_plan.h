@@ -78,7 +78,8 @@ struct Seg {
     int32_t aux;           // re-index: R rows of the request before this segment (REPL),
                            // dropped tokens of the request before this segment (DROP)
     int32_t turn;          // positions the segment's rows turn (ROT; in lazy pools also COPY)
-    int32_t pad;
+    int32_t tile_off;      // re-index: first rotate-kernel tile of this ROT/REPL segment within
+                           // its request, -1 for segments the rotate kernel skips
 };
 
 static_assert(sizeof(ReqPlan) == 104, "ReqPlan layout");

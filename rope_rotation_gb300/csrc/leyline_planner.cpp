@@ -103,8 +103,9 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags");
     if (d->rope_heads < 0 || d->rope_heads > 1024)
         return set_error(LEYLINE_ERR_INVALID_ARG, "rope_heads must be in [0, 1024]");
-    if ((d->flags & LEYLINE_POOL_REINDEX) && d->rope_dim > 256)
-        return set_error(LEYLINE_ERR_INVALID_ARG, "LEYLINE_POOL_REINDEX supports rope_dim <= 256");
+    if ((d->flags & LEYLINE_POOL_REINDEX) && (d->rope_dim > 256 || (int64_t)d->rope_dim * std::max(d->rope_heads, 1) > 512))
+        return set_error(LEYLINE_ERR_INVALID_ARG,
+                         "LEYLINE_POOL_REINDEX supports rope_dim <= 256 and rope_heads * rope_dim <= 512");
     g->num_layers = d->num_layers;
     g->latent_dim = d->latent_dim;
     g->rope_dim = d->rope_dim;
@@ -290,7 +291,23 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             rp.seg_count = 1;
         }
         const int64_t rows = Lp - rp.row0;
-        tiles += ceil_div(rows, kTileRows);
+        if (reindex) {
+            // the rotate kernel's tiles cover ROT and REPL segments only, each cut on its own
+            int64_t wt = 0;
+            const int32_t last = rp.seg_begin + rp.seg_count;
+            for (int32_t k = rp.seg_begin; k < last; ++k) {
+                Seg& s = plan->segs[k];
+                const int64_t end = k + 1 < last ? plan->segs[k + 1].new_start : Lp;
+                s.tile_off = -1;
+                if ((s.kind == SEG_ROT || s.kind == SEG_REPL) && end > s.new_start) {
+                    s.tile_off = (int32_t)wt;
+                    wt += ceil_div(end - s.new_start, kTileRows);
+                }
+            }
+            tiles += wt;
+        } else {
+            tiles += ceil_div(rows, kTileRows);
+        }
         if (reindex) {
             rp.drop_seg_begin = (int32_t)plan->segs.size();
             int64_t drops_before = 0;
