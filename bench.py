@@ -53,6 +53,8 @@ def parse():
                     help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
     ap.add_argument("--lazy", action="store_true",
                     help="lazy pools: splices count pending turns instead of rotating (LEYLINE_POOL_LAZY)")
+    ap.add_argument("--e2e-copy", action="store_true",
+                    help="e2e leg: copy rows of R to device buffers first, instead of passing pinned host rows")
     ap.add_argument("--single-leg", action="store_true",
                     help="time the move kernel inside the value leg and skip the other legs (large workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -272,10 +274,14 @@ def run_ours(args, rank, world, local):
         rbuf = {k: torch.empty_like(v) for k, v in repl_dev.items()}
         out_tab = torch.empty((K, C, max_blocks), dtype=torch.int32).pin_memory()
         out_len = torch.empty((K, C), dtype=torch.int32).pin_memory()
+        # rows of R: by default the splice is given the pinned host rows and its move kernel
+        # reads them in place over the host link; --e2e-copy stages them on the device first
+        src = rbuf if args.e2e_copy else repl_host
         for g in range(W):  # warm the copy path
-            for k2, v in repl_host.items():
-                rbuf[k2].copy_(v, non_blocking=True)
-            cache.splice(dirs_for(base + g, rbuf))
+            if args.e2e_copy:
+                for k2, v in repl_host.items():
+                    rbuf[k2].copy_(v, non_blocking=True)
+            cache.splice(dirs_for(base + g, src))
         torch.cuda.synchronize()
         h2d = sum(v.numel() * v.element_size() for v in repl_host.values())
         d2h = C * max_blocks * 4 + C * 4
@@ -285,9 +291,10 @@ def run_ours(args, rank, world, local):
         e0.record(stream)
         for k in range(K):
             g = base + W + k
-            for k2, v in repl_host.items():
-                rbuf[k2].copy_(v, non_blocking=True)
-            cache.splice(dirs_for(g, rbuf))
+            if args.e2e_copy:
+                for k2, v in repl_host.items():
+                    rbuf[k2].copy_(v, non_blocking=True)
+            cache.splice(dirs_for(g, src))
             out_tab[k].copy_(cache.table[g * C:(g + 1) * C], non_blocking=True)
             out_len[k].copy_(cache.seq_lens_dev[g * C:(g + 1) * C], non_blocking=True)
         e1.record(stream)
@@ -297,7 +304,9 @@ def run_ours(args, rank, world, local):
         cache.check_status()
         exp_len = cache.seq_lens_host[(base + W) * C:(base + W + K) * C].reshape(K, C)
         assert np.array_equal(out_len.numpy(), exp_len), "e2e read-back lengths differ"
-        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h}
+        e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+               "inputs": "rows of R copied to device buffers, then spliced" if args.e2e_copy
+               else "rows of R read in place from pinned host memory by the move kernel"}
     clocks = sampler.stop()
 
     # max over ranks
@@ -349,7 +358,8 @@ def run_ours(args, rank, world, local):
     }
     if e2e:
         line["e2e"] = {"value": slots / (e2e["ms"] / 1e3), "unit": "slots/s", "h2d_bytes_per_step": e2e["h2d"],
-                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"] / K}
+                       "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"] / K,
+                       "inputs": e2e["inputs"]}
     cache.close()
     return line, w
 

@@ -107,6 +107,17 @@ int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, in
                        const double* theta_j, int32_t* status, void* stream);
 // Lazy pools: set the pending counts of n pages (device ids) to 0.
 int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream);
+// Device access to a caller buffer.  Memory of `device` and managed memory are
+// used as they are; pinned host memory (cudaHostAlloc, cudaHostRegister) is used
+// through its device alias, so kernels read or write it in place over the host
+// link (NVLink-C2C on Grace hosts).  Pageable host memory and memory of another
+// device are refused (LEYLINE_ERR_INVALID_ARG, message naming `what`).
+int resolve_access(const void* ptr, int device, const char* what, void** alias, bool* is_host);
+// resolve_access for every directive's rows of R.  *out points at the directives
+// to plan from: `dirs` itself, or a copy in *work with aliases substituted.
+// *host_rows is set when any rows of R live in host memory.
+int resolve_repl_rows(const leyline_directive_t* dirs, int32_t n, int device, std::vector<leyline_directive_t>* work,
+                      const leyline_directive_t** out, bool* host_rows);
 // Resident CTAs per SM of the vector move+rotate kernel (occupancy query).
 int move_rotate_blocks_per_sm(int* blocks);
 // Resident CTAs per SM of the in-place rotation kernel of re-index mode.

@@ -80,9 +80,14 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     for (int32_t r = 0; r < bt->num_reqs; ++r)
         if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
             return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
+    std::vector<leyline_directive_t> resolved;  // filled only when a host alias differs from its pointer
+    const leyline_directive_t* use = dirs;
+    bool host_rows = false;
+    int rc = resolve_repl_rows(dirs, n, p->device, &resolved, &use, &host_rows);
+    if (rc != LEYLINE_OK) return rc;
     Plan plan;
     const int64_t free_now = p->q_tail - p->q_head;
-    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, free_now, &plan);
+    rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
@@ -165,10 +170,10 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     a.pending = p->d_pending;
     a.g = p->g;
 
-    a.move_kernel = p->move_kernel;
+    a.move_kernel = host_rows ? MOVE_VECTOR : p->move_kernel;  // rows of R in host memory: plain loads
     const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
-                                    : p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
-                                                                  : p->move_blocks_per_sm);
+                                    : a.move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
+                                                                 : p->move_blocks_per_sm);
     int err = launch_splice(a, nullptr, grid, stream, nullptr, nullptr);
     if (err != 0) return cuda_fail((cudaError_t)err, "launching the splice kernels");
     e = cudaEventRecord(p->done, stream);

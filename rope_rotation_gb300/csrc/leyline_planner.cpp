@@ -168,7 +168,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             return set_error(LEYLINE_ERR_INVALID_DIRECTIVE, msg);
         }
         if (d.n_repl > 0 && (!d.repl_rows || (reinterpret_cast<uintptr_t>(d.repl_rows) & 15) != 0)) {
-            snprintf(msg, sizeof msg, "directive %d: repl_rows must be a 16-byte aligned device pointer", k);
+            snprintf(msg, sizeof msg, "directive %d: repl_rows must be a non-null 16-byte aligned pointer", k);
             return set_error(LEYLINE_ERR_INVALID_ARG, msg);
         }
     }

@@ -89,6 +89,69 @@ int mark_done(leyline_pool_t* p, cudaStream_t stream)
 
 }  // namespace
 
+namespace leyline {
+
+int resolve_access(const void* ptr, int device, const char* what, void** alias, bool* is_host)
+{
+    char msg[256];
+    *alias = const_cast<void*>(ptr);
+    *is_host = false;
+    DeviceGuard guard(device);
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        snprintf(msg, sizeof msg, "%s: not a CUDA-visible pointer (%s)", what, cudaGetErrorString(e));
+        return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+    }
+    switch (at.type) {
+    case cudaMemoryTypeDevice:
+        if (at.device != device) {
+            snprintf(msg, sizeof msg, "%s: memory of device %d, the pool is on device %d", what, at.device, device);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+        return LEYLINE_OK;
+    case cudaMemoryTypeManaged:
+        return LEYLINE_OK;
+    case cudaMemoryTypeHost:
+        if (!at.devicePointer) {
+            snprintf(msg, sizeof msg, "%s: pinned host memory without a device mapping", what);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+        *alias = at.devicePointer;
+        *is_host = true;
+        return LEYLINE_OK;
+    default:
+        snprintf(msg, sizeof msg, "%s: pageable host memory; use device memory or pinned host memory", what);
+        return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+    }
+}
+
+int resolve_repl_rows(const leyline_directive_t* dirs, int32_t n, int device, std::vector<leyline_directive_t>* work,
+                      const leyline_directive_t** out, bool* host_rows)
+{
+    *out = dirs;
+    *host_rows = false;
+    for (int32_t k = 0; k < n; ++k) {
+        if (dirs[k].n_repl <= 0 || !dirs[k].repl_rows) continue;  // the planner reports a missing pointer
+        char what[64];
+        snprintf(what, sizeof what, "directive %d: repl_rows", k);
+        void* alias;
+        bool host;
+        int rc = resolve_access(dirs[k].repl_rows, device, what, &alias, &host);
+        if (rc != LEYLINE_OK) return rc;
+        *host_rows = *host_rows || host;
+        if (alias != dirs[k].repl_rows) {
+            if (work->empty()) work->assign(dirs, dirs + n);
+            (*work)[k].repl_rows = alias;
+            *out = work->data();
+        }
+    }
+    return LEYLINE_OK;
+}
+
+}  // namespace leyline
+
 extern "C" {
 
 const char* leyline_last_error(void) { return last_error_cstr(); }
@@ -271,9 +334,14 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     for (int32_t r = 0; r < bt->num_reqs; ++r)
         if (bt->seq_lens_host[r] < 0 || bt->seq_lens_host[r] > (int64_t)bt->max_blocks * p->g.block_size)
             return set_error(LEYLINE_ERR_INVALID_ARG, "seq_lens_host entry outside [0, max_blocks * block_size]");
+    std::vector<leyline_directive_t> resolved;
+    const leyline_directive_t* use = dirs;
+    bool host_rows = false;
+    int rc = resolve_repl_rows(dirs, n, p->device, &resolved, &use, &host_rows);
+    if (rc != LEYLINE_OK) return rc;
     Plan plan;
     const int64_t free_now = p->q_tail - p->q_head;
-    int rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, dirs, n, free_now, &plan);
+    rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
@@ -385,10 +453,10 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         t1 = p->tev[p->tev_used].second;
         ++p->tev_used;
     }
-    a.move_kernel = p->move_kernel;
+    a.move_kernel = host_rows ? MOVE_VECTOR : p->move_kernel;  // rows of R in host memory: plain loads
     const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
-                                    : p->move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
-                                                                  : p->move_blocks_per_sm);
+                                    : a.move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
+                                                                 : p->move_blocks_per_sm);
     int err = launch_splice(a, in_params ? &pp : nullptr, grid, stream, t0, t1);
     if (err != 0) return cuda_error((cudaError_t)err, "launching the splice kernels");
     rc = mark_done(p, stream);
@@ -418,8 +486,11 @@ int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t r
     if (t0 < 0 || t0 > t1 || t1 > bt->seq_lens_host[req] || t1 > (int64_t)bt->max_blocks * p->g.block_size)
         return set_error(LEYLINE_ERR_INVALID_ARG, "rows outside [0, seq_len]");
     if (t1 > t0 && (!out || (reinterpret_cast<uintptr_t>(out) & 15) != 0))
-        return set_error(LEYLINE_ERR_INVALID_ARG, "out must be a 16-byte aligned device pointer");
+        return set_error(LEYLINE_ERR_INVALID_ARG, "out must be a 16-byte aligned pointer");
     if (t1 == t0) return LEYLINE_OK;
+    bool out_host = false;
+    int rc0 = resolve_access(out, p->device, "gather output", &out, &out_host);
+    if (rc0 != LEYLINE_OK) return rc0;
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
     int rc = order_after_previous(p, stream);

@@ -205,7 +205,8 @@ class Tables:
 
 def directive(req: int, s_start: int, s_end: int, repl=None, n_repl: Optional[int] = None,
               mode: int = LEYLINE_AMORTIZE) -> Directive:
-    """repl: bf16 CUDA tensor [num_layers][n_repl][row] or None."""
+    """repl: bf16 tensor [num_layers][n_repl][row], contiguous, on the pool's GPU or in pinned host
+    memory (read in place by the kernel), or None."""
     if n_repl is None:
         n_repl = 0 if repl is None else int(repl.shape[1])
     return Directive(req, mode, s_start, s_end, n_repl, 0, None if repl is None else _tensor_ptr(repl))
