@@ -725,12 +725,12 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
 }
 
 // -------------------------------------------------------------------------
-// Re-index mode (block size 1, pool flag LEYLINE_POOL_REINDEX): a surviving
-// downstream token keeps its page.  Three kernels, each a programmatic dependent
-// of the one before:
-//   prep          stages the page of every rewritten table entry (the kept token's
-//                 old page, or a fresh page for a row of R) and returns the pages
-//                 of dropped tokens to the ring; it reads the old table and writes
+// Re-index mode (pool flag LEYLINE_POOL_REINDEX; block size 1, or a call whose
+// directives all lie on block boundaries): a surviving downstream block keeps its
+// page.  Three kernels, each a programmatic dependent of the one before:
+//   prep          stages the page of every rewritten table entry (the kept block's
+//                 old page, or a fresh page for a block of R) and returns the pages
+//                 of dropped blocks to the ring; it reads the old table and writes
 //                 only the staging array and the ring's push region;
 //   rotate        turns the rope band of every turned row in place (128 bytes read
 //                 and written per row and layer; the latent is not touched) and
@@ -744,47 +744,52 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const long long stride = (long long)gridDim.x * blockDim.x;
+    const long long B = a.g.block_size;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_prep; i += stride) {
         const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_PREP)];
         const long long k = i - rp.prep_begin;
-        const long long rows = rp.new_len - rp.row0;
+        const long long blocks = (rp.new_len + B - 1) / B - rp.b0;  // new blocks from b0 on
         const int32_t* trow = a.table + (long long)rp.req * a.max_blocks;
-        if (k < rows) {
-            const long long p = rp.row0 + k;
+        if (k < blocks) {
+            const long long p = (rp.b0 + k) * B;  // first row of the block (every segment starts on one)
+            const long long valid = rp.new_len - p < B ? rp.new_len - p : B;
             const Seg* sg = pv.segs + rp.seg_begin;
             const Seg s = sg[find_seg(sg, rp.seg_count, p)];
             int page;
             if (s.kind == SEG_REPL) {
-                page = a.free_q[ring(a.pop_base + rp.pop_off + s.aux + (p - s.new_start), a.q_cap)];
+                page = a.free_q[ring(a.pop_base + rp.pop_off + s.aux + (p - s.new_start) / B, a.q_cap)];
                 if (page < 0 || page >= a.g.num_pages) {
                     raise_status(a.status, ST_BAD_FRESH);
                     page = -1;
                 }
-                if (a.pending && page >= 0) a.pending[page] = 0;  // R is encoded at its final position
+                if (a.pending && page >= 0)  // R is encoded at its final position
+                    for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] = 0;
             } else {
-                const long long t = s.src_start + (p - s.new_start);
-                page = (t >= 0 && t < a.max_blocks) ? trow[t] : -1;
+                const long long ob = (s.src_start + (p - s.new_start)) / B;  // the old block kept
+                page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
                 if (page < 0 || page >= a.g.num_pages) {
                     raise_status(a.status, ST_BAD_PAGE);
                     page = -1;
                 }
-                if (a.pending && page >= 0 && s.turn != 0) a.pending[page] += s.turn;  // one row per page
+                if (a.pending && page >= 0 && s.turn != 0)  // the valid slots turn; the others stay 0
+                    for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] += s.turn;
             }
             a.stage[rp.stage_begin + k] = page;
         } else {
-            const long long j = k - rows;  // j-th dropped token of the request
+            const long long j = k - blocks;  // j-th dropped block of the request
             const Seg* dg = pv.segs + rp.drop_seg_begin;
             int q = 0;
             for (int x = 1; x < rp.drop_seg_count; ++x)
                 if (dg[x].aux <= j) q = x;
-            const long long t = dg[q].src_start + (j - dg[q].aux);
-            int page = (t >= 0 && t < a.max_blocks) ? trow[t] : -1;
+            const long long ob = dg[q].src_start + (j - dg[q].aux);
+            int page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
             if (page < 0 || page >= a.g.num_pages) {
                 raise_status(a.status, ST_BAD_OLD);
                 page = -1;
             }
             a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
-            if (a.pending && page >= 0) a.pending[page] = 0;  // a free page carries no pending turn
+            if (a.pending && page >= 0)  // a free page carries no pending turn
+                for (long long sl = 0; sl < B; ++sl) a.pending[(long long)page * B + sl] = 0;
         }
     }
 }
@@ -883,9 +888,10 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 const long long end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
                 const long long p = s.new_start + (lt - s.tile_off) * kTileRows + threadIdx.x;
                 if (p < end) {
-                    const int page = a.stage[rp.stage_begin + (p - rp.row0)];
+                    const long long B = a.g.block_size;
+                    const int page = a.stage[rp.stage_begin + (p / B - rp.b0)];
                     if (page >= 0 && page < a.g.num_pages)
-                        d.row = static_cast<uint4*>(a.kv) + (long long)page * row_vecs;
+                        d.row = static_cast<uint4*>(a.kv) + ((long long)page * B + p % B) * row_vecs;
                     if (s.kind == SEG_REPL)
                         d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * row_vecs;
                 }
@@ -946,8 +952,8 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
     }
 }
 
-// Commit of a re-indexed call: staged entries into [row0, new_len), -1 into
-// [new_len, old_len), the new length.  The staged values are final before the
+// Commit of a re-indexed call: staged entries into the new blocks [b0, new end),
+// -1 into the blocks past the new end, the new length.  The staged values are final before the
 // rotate kernel starts and it never writes them, so they are loaded before
 // griddepcontrol.wait.
 template <class PlanSrc>
@@ -960,24 +966,26 @@ __global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_co
     int val = -1;
     const ReqPlan* rp = nullptr;
     long long k = 0;
+    const long long B = a.g.block_size;
     if (i < a.total_commit) {
         rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
         k = i - rp->commit_begin;
-        if (k < rp->new_len - rp->row0) val = a.stage[rp->stage_begin + k];
+        if (k < (rp->new_len + B - 1) / B - rp->b0) val = a.stage[rp->stage_begin + k];
     }
     wait_for_previous_grid();
     allow_next_grid();
     while (i < a.total_commit) {
         int32_t* trow = a.table_w + (long long)rp->req * a.max_blocks;
-        const long long rows = rp->new_len - rp->row0;
+        const long long nb_new = (rp->new_len + B - 1) / B, nb_old = (rp->old_len + B - 1) / B;
+        const long long blocks = nb_new - rp->b0;
         if (k == 0) a.seq_lens_dev[rp->req] = (int32_t)rp->new_len;
-        if (k < rows) trow[rp->row0 + k] = val;
-        else if (rp->new_len + (k - rows) < rp->old_len) trow[rp->new_len + (k - rows)] = -1;
+        if (k < blocks) trow[rp->b0 + k] = val;
+        else if (nb_new + (k - blocks) < nb_old) trow[nb_new + (k - blocks)] = -1;
         i += stride;
         if (i >= a.total_commit) break;
         rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
         k = i - rp->commit_begin;
-        val = k < rp->new_len - rp->row0 ? a.stage[rp->stage_begin + k] : -1;
+        val = k < (rp->new_len + B - 1) / B - rp->b0 ? a.stage[rp->stage_begin + k] : -1;
     }
 }
 

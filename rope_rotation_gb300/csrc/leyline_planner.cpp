@@ -192,7 +192,17 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     }
 
     // 3. plan each touched request
-    const bool reindex = (g.flags & LEYLINE_POOL_REINDEX) && B == 1;
+    // re-index: block size 1, or every directive of the call on block boundaries (the
+    // splice then drops, inserts and shifts whole pages)
+    bool reindex = (g.flags & LEYLINE_POOL_REINDEX) != 0;
+    if (reindex && B > 1) {
+        for (int32_t k = 0; k < n && reindex; ++k) {
+            const leyline_directive_t& d = dirs[k];
+            if (d.s_start == d.s_end && d.n_repl == 0) continue;
+            const bool to_end = d.s_end == seq_lens_host[d.req];
+            reindex = d.s_start % B == 0 && (d.s_end % B == 0 || to_end) && (d.n_repl % B == 0 || to_end);
+        }
+    }
     const bool lazy = (g.flags & LEYLINE_POOL_LAZY) != 0;
     plan->reindex = reindex;
     const int64_t row_bytes = (int64_t)g.row_elems * 2;
@@ -216,11 +226,9 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             snprintf(msg, sizeof msg, "request %d: seq_len %lld exceeds the table capacity", req, (long long)L);
             return set_error(LEYLINE_ERR_INVALID_ARG, msg);
         }
-        int64_t delta_total = 0, repl_total = 0, drop_total = 0;
+        int64_t delta_total = 0;
         for (const auto* d : eff) {
             delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
-            repl_total += d->n_repl;
-            drop_total += d->s_end - d->s_start;
         }
         const int64_t Lp = L + delta_total;
         if (Lp > (int64_t)max_blocks * B || Lp > INT32_MAX) {
@@ -234,9 +242,14 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         rp.row0 = (int64_t)rp.b0 * B;
         rp.old_len = L;
         rp.new_len = Lp;
+        int64_t repl_blocks = 0, drop_blocks = 0;
+        for (const auto* d : eff) {
+            repl_blocks += ceil_div(d->n_repl, B);
+            if (d->s_end > d->s_start) drop_blocks += ceil_div(d->s_end, B) - d->s_start / B;
+        }
         if (reindex) {
-            rp.n_new = (int32_t)repl_total;  // fresh pages: one per row of R
-            rp.n_old = (int32_t)drop_total;  // returned pages: one per dropped token
+            rp.n_new = (int32_t)repl_blocks;  // fresh pages: the blocks of R
+            rp.n_old = (int32_t)drop_blocks;  // returned pages: the dropped blocks
         } else {
             rp.n_new = (int32_t)(ceil_div(Lp, B) - rp.b0);
             rp.n_old = (int32_t)(ceil_div(L, B) - rp.b0);
@@ -256,14 +269,15 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             plan->segs.push_back(s);
             st.head_slots += s1 - rp.row0;
         }
-        int64_t D = 0, A = 0, repl_before = 0;
+        int64_t D = 0, A = 0, pops_before = 0;
         for (size_t k = 0; k < eff.size(); ++k) {
             const leyline_directive_t* d = eff[k];
             if (d->n_repl > 0) {
-                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)repl_before, 0, 0};
+                // aux: fresh pages of the request's earlier R segments (re-index mode)
+                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)pops_before, 0, 0};
                 plan->segs.push_back(s);
                 st.repl_slots += d->n_repl;
-                repl_before += d->n_repl;
+                pops_before += ceil_div(d->n_repl, B);
             }
             const int64_t dk = (int64_t)d->n_repl - (d->s_end - d->s_start);
             D += dk;
@@ -309,23 +323,26 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
             tiles += ceil_div(rows, kTileRows);
         }
         if (reindex) {
+            // in block units: DROP segments name the first dropped block and the dropped
+            // blocks before them; the stage holds one page per new block from b0 on
             rp.drop_seg_begin = (int32_t)plan->segs.size();
             int64_t drops_before = 0;
             for (const auto* d : eff) {
-                const int64_t len = d->s_end - d->s_start;
-                if (len == 0) continue;
-                Seg s{-1, d->s_start, nullptr, SEG_DROP, -1, (int32_t)len, (int32_t)drops_before, 0, 0};
+                if (d->s_end == d->s_start) continue;
+                const int64_t nb = ceil_div(d->s_end, B) - d->s_start / B;
+                Seg s{-1, d->s_start / B, nullptr, SEG_DROP, -1, (int32_t)nb, (int32_t)drops_before, 0, 0};
                 plan->segs.push_back(s);
-                drops_before += len;
+                drops_before += nb;
             }
             rp.drop_seg_count = (int32_t)plan->segs.size() - rp.drop_seg_begin;
-            rp.drop_count = drop_total;
+            rp.drop_count = drop_blocks;
             rp.stage_begin = plan->total_stage;
             rp.prep_begin = plan->total_prep;
-            plan->total_stage += rows;
-            plan->total_prep += rows + drop_total;
-            const int64_t tail = L > Lp ? L - Lp : 0;  // table entries past the new end
-            commit += std::max<int64_t>(1, rows + tail);
+            const int64_t new_blocks = ceil_div(Lp, B) - rp.b0;
+            plan->total_stage += new_blocks;
+            plan->total_prep += new_blocks + drop_blocks;
+            const int64_t tail = std::max<int64_t>(0, ceil_div(L, B) - ceil_div(Lp, B));  // entries past the new end
+            commit += std::max<int64_t>(1, new_blocks + tail);
         } else {
             commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
         }

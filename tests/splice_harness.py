@@ -234,7 +234,7 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
         counters["rel_l2_max"] = max(counters["rel_l2_max"], c["rel_l2"])
         state[r] = want
     check_tables(cache, before_table, after_table, before_lens, cache.seq_lens_host, touched,
-                 reindex=bool(cache.desc.flags & 1) and cache.block_size == 1)
+                 reindex=stats["kernels_launched"] == 3)  # re-indexed calls keep pages
     assert cache.free_pages() == free_before - stats["pages_popped"] + stats["pages_pushed"]
     if guard:
         new_pages = set()
@@ -264,6 +264,36 @@ class State(list):
 
 def oracle_state(w: Workload) -> State:
     return State([synth.cache_request(w.seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)])
+
+
+def aligned_steps(seed, B, lengths, n_steps, evict_every=0) -> list[list[Dir]]:
+    """Chained calls whose directives all lie on block boundaries (s_start a multiple of B;
+    s_end and |R| multiples of B unless s_end is the request's end), one per request."""
+    rng = np.random.default_rng(seed)
+    lens = list(lengths)
+    steps, key = [], 0
+    for k in range(n_steps):
+        step = []
+        for r, L in enumerate(lens):
+            nb = -(-L // B)
+            b0 = int(rng.integers(0, nb + 1))
+            if rng.random() < 0.25 and L % B:  # to the end, with a partial last block
+                s, e, n = b0 * B if b0 * B <= L else (nb - 1) * B, L, int(rng.integers(0, 2 * B + 3))
+            else:
+                b1 = int(rng.integers(b0, min(nb, b0 + 6) + 1))
+                s, e = b0 * B, min(b1 * B, L)
+                if e % B and e != L:
+                    e = (e // B) * B
+                s = min(s, e)
+                n = B * int(rng.integers(0, 3)) if e != L else int(rng.integers(0, 2 * B + 3))
+                if s % B:  # past a partial last block: nothing to do here
+                    s, e, n = 0, 0, 0
+            mode = 2 if (evict_every and k % evict_every == evict_every - 1) else 0
+            step.append(Dir(r, s, e, n, key, mode))
+            key += 1
+            lens[r] = L - (e - s) + n
+        steps.append(step)
+    return steps
 
 
 # ------------------------------------------------------------ full-size checks --

@@ -160,3 +160,28 @@ def test_noop_directives_touch_nothing(L):
     st, newlens = _plan(L, [64, 10], [_d(L, 0, 5, 5, 0), _d(L, 1, 10, 10, 0)])
     assert list(newlens) == [64, 10]
     assert st.requests_touched == 0 and st.kernels_launched == 0 and st.pages_popped == 0
+
+
+def test_reindex_pages_only_on_block_boundaries(L):
+    """Re-index pools with 16-slot pages re-index a call only when every directive lies on
+    block boundaries (s_start a multiple of 16; s_end and |R| multiples of 16 unless
+    s_end = seq_len); pages are then counted in blocks."""
+    desc = L.pool_desc(4, 16, 1 << 20, flags=L.LEYLINE_POOL_REINDEX)
+    lens = [16 * 10 + 3, 64]
+    cases = [
+        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 16, 0)], 3, 1, 3),
+        ([_d(L, 0, 48, 163, 5)], 3, 1, 8),                       # to the end, partial blocks
+        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 17, 0)], 2, None, None),  # s_end off the grid
+        ([_d(L, 0, 32, 64, 3)], 2, None, None),                  # |R| off the grid
+        ([_d(L, 0, 40, 64, 16)], 2, None, None),                 # s_start off the grid
+        ([_d(L, 0, 160, 160, 16)], 3, 1, 0),                     # the partial last block moves whole
+        ([_d(L, 0, 163, 163, 16)], 2, None, None),               # insertion inside it
+    ]
+    for dirs, kernels, pops, pushes in cases:
+        st, new = _plan(L, lens, dirs, desc=desc)
+        assert st.kernels_launched == kernels, [(d.s_start, d.s_end, d.n_repl) for d in dirs]
+        if pops is not None:
+            assert (st.pages_popped, st.pages_pushed) == (pops, pushes)
+    # block size 1: every call re-indexes, one page per row
+    st, _ = _plan(L, [100], [_d(L, 0, 3, 50, 7)], B=1, desc=L.pool_desc(4, 1, 1 << 20, flags=L.LEYLINE_POOL_REINDEX))
+    assert (st.kernels_launched, st.pages_popped, st.pages_pushed) == (3, 7, 47)

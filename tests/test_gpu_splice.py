@@ -222,6 +222,36 @@ def test_reindex_chain_matches_oracle_chain_call_by_call():
 
 
 # ------------------------------------------------------------------------------
+# Re-index mode with pages of several slots: calls whose directives all lie on block
+# boundaries drop, insert and shift whole pages; other calls rewrite.
+@pytest.mark.parametrize("B,layout", [(16, 0), (4, 1), (2, 0)])
+def test_block_reindex_aligned_chain(B, layout):
+    lengths = [16 * 37 + 5, 16 * 20, 7]
+    steps = H.aligned_steps(50 + B, B, lengths, 8, evict_every=3)
+    w = Workload(f"block-reindex-B{B}", 3, B, lengths, steps, seed=50 + B)
+    cache = H.make_cache(w, pair_layout=layout, slack_pages=64, flags=REINDEX)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        c = H.splice_step_and_check(w, cache, state, step, layout=layout)
+        if any(not (d.s_start == d.s_end and d.n_repl == 0) for d in step):
+            assert c["stats"]["kernels_launched"] == 3, "an aligned call was not re-indexed"
+    cache.close()
+
+
+def test_block_reindex_misaligned_call_rewrites():
+    """On a block-16 re-index pool, a call with one directive off the block grid rewrites
+    (two kernels), and an aligned call after it re-indexes (three)."""
+    steps = [[Dir(0, 32, 64, 16, 0), Dir(1, 20, 40, 3, 1)],
+             [Dir(0, 16, 48, 0, 2), Dir(1, 0, 16, 32, 3)]]
+    w = Workload("block-reindex-mixed", 2, 16, [300, 170], steps, seed=60)
+    cache = H.make_cache(w, slack_pages=32, flags=REINDEX)
+    state = H.oracle_state(w)
+    assert H.splice_step_and_check(w, cache, state, steps[0])["stats"]["kernels_launched"] == 2
+    assert H.splice_step_and_check(w, cache, state, steps[1])["stats"]["kernels_launched"] == 3
+    cache.close()
+
+
+# ------------------------------------------------------------------------------
 # GQA/MHA rows (section 5 of the Leyline page: the directive abstraction extends to
 # GQA/MHA): [V | keys of 4 heads x 128], every key band turned with the same theta_j.
 @pytest.mark.parametrize("layout", [0, 1])
