@@ -314,6 +314,7 @@ def run_ours(args, rank, world, local):
     if e2e:
         e2e["ms"] = e2e_ms_max
     slots = st["downstream_slots"] * K * world
+    reindexed = st["kernels_launched"] == 3  # prep, in-place rotation, commit
     value = job_value(st["downstream_slots"], K, world, elapsed_ms)
     peak, peak_kind = measured_peaks()
     k2_avg_s = (k2_ms / max(k2_n, 1)) / 1e3
@@ -341,14 +342,14 @@ def run_ours(args, rank, world, local):
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
                    "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
-                   + (", re-index" if args.reindex and B == 1 else ""),
-                   "move_kernel": ("rotate_in_place" if args.reindex and B == 1
+                   + (", re-index" if reindexed else ""),
+                   "move_kernel": ("rotate_in_place" if reindexed
                                    else os.environ.get("LEYLINE_MOVE_KERNEL", "vector")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
-        "roofline": {"kernel": ("rotate_in_place" if args.reindex and B == 1
+        "roofline": {"kernel": ("rotate_in_place" if reindexed
                                 else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")), "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"

@@ -113,6 +113,18 @@ def sweep(C: int, block_size: int, seed: int = 0, num_layers: int = 61) -> Workl
     return Workload(f"sweep-C{C}-61L-B{block_size}", num_layers, block_size, lengths, [dirs], seed=seed)
 
 
+def sweep_aligned(C: int, block_size: int, seed: int = 0, num_layers: int = 61) -> Workload:
+    """The sweep with every directive moved onto the block grid: s_start and s_end rounded
+    down to multiples of the block size, |R| rounded up to one (page-granular compaction)."""
+    w = sweep(C, block_size, seed, num_layers)
+    B = block_size
+    dirs = []
+    for d in w.steps[0]:
+        s, e = (d.s_start // B) * B, (d.s_end // B) * B
+        dirs.append(Dir(d.req, s, max(s, e), -(-d.n_repl // B) * B, d.key))
+    return Workload(f"sweep-aligned-C{C}-61L-B{B}", num_layers, B, w.lengths, [dirs], seed=seed)
+
+
 def by_name(name: str, seed: int = 0) -> Workload:
     table = {
         "cfg1": contiguous_4k,
@@ -125,4 +137,7 @@ def by_name(name: str, seed: int = 0) -> Workload:
     if name.startswith("cfg5-"):  # cfg5-C16-B16
         _, c, b = name.split("-")
         return sweep(int(c[1:]), int(b[1:]), seed)
+    if name.startswith("cfg5a-"):  # cfg5a-C16-B16: the same sweep on the block grid
+        _, c, b = name.split("-")
+        return sweep_aligned(int(c[1:]), int(b[1:]), seed)
     raise KeyError(name)
