@@ -33,12 +33,12 @@ if ROOT not in sys.path:
 
 METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-# Per-launch DRAM traffic (read + write bytes) of the move+rotate kernel on this
-# workload, from an ncu capture, valid only for the kernel source it was taken on.
-# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.3 MB; the
-# rest of the 210.9 MB written was still in L2 when the single captured launch ended.)
-NCU_TRAFFIC = {"kernel_sha256": "8a35c2a6982d914856678e6215419240f7249e291b323b78a7a9994a1e5b5e89",
-               "bytes_per_launch": 210916608 + 161315840}
+# Per-launch DRAM traffic (read + write bytes) of a kernel on a workload, from an ncu
+# capture, valid only for the kernel source it was taken on
+# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.7 MB; the
+# rest of the 210.9 MB written was still in L2 when the single captured launch ended).
+NCU_TRAFFIC = {"kernel_sha256": "8128ab09092ad662257830985b15771327c728b7215ab5c440e72ec13fa625ea",
+               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210942720 + 160714752}}
 
 
 def parse():
@@ -57,6 +57,8 @@ def parse():
                     help="e2e leg: copy rows of R to device buffers first, instead of passing pinned host rows")
     ap.add_argument("--single-leg", action="store_true",
                     help="time the move kernel inside the value leg and skip the other legs (large workloads)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
     return ap.parse_args()
@@ -153,11 +155,14 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload --
 
-def workload(name: str):
+def workload(name: str, layers: int = 0):
     from synth import configs
     w = configs.by_name(name)
     if len(w.steps) != 1:
         raise SystemExit(f"workload {name} is a multi-step chain; bench runs single-call workloads")
+    if layers > 0:
+        w.num_layers = layers
+        w.name = f"{w.name}-as-{layers}L"
     return w
 
 
@@ -186,7 +191,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    w = workload(args.workload)
+    w = workload(args.workload, args.layers)
     K, W = args.steps, args.warmup
     C = w.num_reqs
     # legs: value (plain steps), kernel (the same steps with CUDA events around the
@@ -319,9 +324,10 @@ def run_ours(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     k2_avg_s = (k2_ms / max(k2_n, 1)) / 1e3
     achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
+    kernel_name = "rotate_in_place" if reindexed else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha():
-        traffic = NCU_TRAFFIC["bytes_per_launch"]
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and not args.lazy:
+        traffic = NCU_TRAFFIC["launches"].get((w.name, kernel_name))
     line = {
         "metric": METRIC,
         "value": value,
@@ -349,8 +355,7 @@ def run_ours(args, rank, world, local):
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
-        "roofline": {"kernel": ("rotate_in_place" if reindexed
-                                else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")), "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
@@ -395,7 +400,7 @@ def run_reference(args, rank, world):
     """The reference arm: the fp64 CPU oracle timed as it stands on the same workload."""
     if rank != 0:
         return None
-    w = workload(args.workload)
+    w = workload(args.workload, args.layers)
     import oracle
     import synth
     st = per_request_counts(w)
