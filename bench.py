@@ -53,6 +53,8 @@ def parse():
                     help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
     ap.add_argument("--lazy", action="store_true",
                     help="lazy pools: splices count pending turns instead of rotating (LEYLINE_POOL_LAZY)")
+    ap.add_argument("--split", action="store_true",
+                    help="latents and rope bands in two arrays (LEYLINE_POOL_SPLIT_ROPE)")
     ap.add_argument("--e2e-copy", action="store_true",
                     help="e2e leg: copy rows of R to device buffers first, instead of passing pinned host rows")
     ap.add_argument("--single-leg", action="store_true",
@@ -206,7 +208,8 @@ def run_ours(args, rank, world, local):
     pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
     cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta,
                        flags=(leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
-                       | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0))
+                       | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)
+                       | (leyline.LEYLINE_POOL_SPLIT_ROPE if args.split else 0))
     seed = rank_seed(w.seed, rank)
     for g in range(groups):
         for r, L in enumerate(w.lengths):
@@ -326,7 +329,7 @@ def run_ours(args, rank, world, local):
     achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
     kernel_name = "rotate_in_place" if reindexed else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and not args.lazy:
+    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and not args.lazy and not args.split:
         traffic = NCU_TRAFFIC["launches"].get((w.name, kernel_name))
     line = {
         "metric": METRIC,
@@ -348,7 +351,7 @@ def run_ours(args, rank, world, local):
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
                    "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
-                   + (", re-index" if reindexed else ""),
+                   + (", re-index" if reindexed else "") + (", split rope" if args.split else ""),
                    "move_kernel": ("rotate_in_place" if reindexed
                                    else os.environ.get("LEYLINE_MOVE_KERNEL", "vector")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -107,6 +107,15 @@ typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_
  * once per splice (section 4.3: the drift of repeated bf16 rotation), and with
  * LEYLINE_POOL_REINDEX a splice moves no cache bytes for survivors at all. */
 #define LEYLINE_POOL_LAZY 2
+/* LEYLINE_POOL_SPLIT_ROPE: the pool buffer holds the latents and the rope bands in
+ * two arrays instead of whole rows: bf16 latent[num_layers][num_pages][block_size]
+ * [latent_dim], then bf16 rope[num_layers][num_pages][block_size][rope_heads *
+ * rope_dim] (the layout of paged MLA attention kernels that take a latent cache and a
+ * rope cache).  The buffer size is the same.  Rows of R, gather outputs and every
+ * other interface keep whole rows [latent | rope bands].  A splice that turns bands
+ * in place (LEYLINE_POOL_REINDEX, leyline_materialize) then streams contiguous bands
+ * instead of 128 bytes out of every row. */
+#define LEYLINE_POOL_SPLIT_ROPE 4
 
 typedef struct {
     int32_t num_layers;       /* >= 1 */
@@ -183,7 +192,7 @@ typedef struct {
 
 /* Create a pool over caller-owned device memory kv_dev (bf16
  * [num_layers][num_pages][block_size][row], row = latent_dim + rope_heads * rope_dim,
- * 16-byte aligned).
+ * 16-byte aligned; with LEYLINE_POOL_SPLIT_ROPE the latent array then the rope array).
  * All pages start free.  The library allocates the free-page list (a ring of
  * 2 * num_pages ids) and small plan and staging buffers on the current device.
  * Synchronous.

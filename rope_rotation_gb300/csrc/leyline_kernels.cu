@@ -150,12 +150,26 @@ __device__ __forceinline__ PlanView plan_view(const SpliceArgs& a, const NoParam
 
 // Where one destination row of a tile comes from and goes to (layer 0).
 struct RowDesc {
-    const uint4* src;       // nullptr: row is not written
-    uint4* dst;
-    long long src_lstride;  // 16-byte vectors between consecutive layers of the source
-    int trig;               // trig entry, -1: no rotation
+    const uint4* src;        // latent of the source row (layer 0); nullptr: row is not written
+    uint4* dst;              // latent of the destination row (layer 0)
+    long long src_lstride;   // 16-byte vectors between consecutive layers of the source latent
+    const uint4* src_band;   // rope bands of the source row (layer 0)
+    uint4* dst_band;         // rope bands of the destination row (layer 0)
+    long long band_lstride;  // 16-byte vectors between consecutive layers of the source bands
+    int trig;                // trig entry, -1: no rotation
     int pad;
 };
+
+// Offsets (16-byte vectors from the pool base) of the latent and of the rope bands of
+// the row of (layer, slot).
+__device__ __forceinline__ long long lat_off(const Geometry& g, long long layer, long long slot)
+{
+    return layer * g.lat_layer_vecs + slot * g.lat_row_vecs;
+}
+__device__ __forceinline__ long long band_off(const Geometry& g, long long layer, long long slot)
+{
+    return g.rope_base_vecs + layer * g.rope_layer_vecs + slot * g.rope_row_vecs;
+}
 
 enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2 };
 
@@ -192,7 +206,7 @@ __device__ __forceinline__ long long ring(long long i, long long cap) { return i
 // in the status word and the row is skipped.
 __device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long tile, int i)
 {
-    RowDesc d{nullptr, nullptr, 0, -1, 0};
+    RowDesc d{nullptr, nullptr, 0, nullptr, nullptr, 0, -1, 0};
     const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
     const long long p = rp.row0 + (tile - rp.tile_begin) * kTileRows + i;
     if (p >= rp.new_len) return d;
@@ -226,18 +240,22 @@ __device__ RowDesc make_desc(const SpliceArgs& a, const PlanView& pv, long long 
         return d;
     }
     if (from_cache) {
-        d.src = kv + ((long long)page * B + (t - blk * B)) * rv;
-        d.src_lstride = a.g.layer_vecs;
+        const long long sslot = (long long)page * B + (t - blk * B);
+        d.src = kv + lat_off(a.g, 0, sslot);
+        d.src_band = kv + band_off(a.g, 0, sslot);
+        d.src_lstride = a.g.lat_layer_vecs;
+        d.band_lstride = a.g.rope_layer_vecs;
         d.trig = s.kind == SEG_ROT ? s.trig : -1;
-    } else {
+    } else {  // rows of R are whole rows [latent | bands]
         d.src = static_cast<const uint4*>(s.repl) + (s.src_start + off) * rv;
-        d.src_lstride = (long long)s.n_repl * rv;
+        d.src_band = d.src + a.g.latent_vecs;
+        d.src_lstride = d.band_lstride = (long long)s.n_repl * rv;
     }
-    d.dst = kv + ((long long)fresh * B + (p - dblk * B)) * rv;
-    if (a.pending) {  // lazy pool: the destination slot carries the source's pending turn plus this one
-        const long long dslot = (long long)fresh * B + (p - dblk * B);
+    const long long dslot = (long long)fresh * B + (p - dblk * B);
+    d.dst = kv + lat_off(a.g, 0, dslot);
+    d.dst_band = kv + band_off(a.g, 0, dslot);
+    if (a.pending)  // lazy pool: the destination slot carries the source's pending turn plus this one
         a.pending[dslot] = from_cache ? a.pending[(long long)page * B + (t - blk * B)] + s.turn : 0;
-    }
     return d;
 }
 
@@ -261,14 +279,14 @@ template <int kLayout, bool kBf16, class PlanSrc>
 __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
-    constexpr int kLatentVecs = 64, kRopeVecs = 8;
+    constexpr int kRopeVecs = 8;
     __shared__ RowDesc desc[kTileRows];
     wait_for_previous_grid();
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long L = a.g.num_layers;
-    const long long layer_vecs = a.g.layer_vecs;
+    const long long lat_layer = a.g.lat_layer_vecs, rope_layer = a.g.rope_layer_vecs;
     const int half = 4 * kRopeVecs;  // pairs per row
     constexpr int kRopeLanesPerRow = kLayout == 0 ? kRopeVecs / 2 : kRopeVecs;  // 4 or 8
     const bool rope_lane = lane < kRowsPerWarp * kRopeLanesPerRow;
@@ -317,22 +335,22 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
         const bool do_rope = rope_lane && dr.src != nullptr;
         uint4 rx, ry;
         if (do_rope) {
-            const uint4* rs = dr.src + layer * dr.src_lstride + kLatentVecs;
+            const uint4* rs = dr.src_band + layer * dr.band_lstride;
             rx = ld_stream(rs + rope_q);
             if (kLayout == 0) ry = ld_stream(rs + rope_q + kRopeVecs / 2);
         }
         if (d0.src) {
-            uint4* t0 = d0.dst + layer * layer_vecs;
+            uint4* t0 = d0.dst + layer * lat_layer;
             st_stream(t0 + lane, v[0]);
             st_stream(t0 + lane + 32, v[1]);
         }
         if (d1.src) {
-            uint4* t1 = d1.dst + layer * layer_vecs;
+            uint4* t1 = d1.dst + layer * lat_layer;
             st_stream(t1 + lane, v[2]);
             st_stream(t1 + lane + 32, v[3]);
         }
         if (do_rope) {
-            uint4* rd = dr.dst + layer * layer_vecs + kLatentVecs;
+            uint4* rd = dr.dst_band + layer * rope_layer;
             if (kLayout == 0) {
                 if (trig >= 0) rotate_half_split<kBf16>(rx, ry, cs, sn);
                 st_stream(rd + rope_q, rx);
@@ -377,15 +395,15 @@ __global__ void __launch_bounds__(kMoveThreads) move_rotate_generic(const __grid
             const RowDesc d = desc[it / lv];
             if (!d.src) continue;
             const int c = it % lv;
-            st_stream(d.dst + layer * a.g.layer_vecs + c, ld_stream(d.src + layer * d.src_lstride + c));
+            st_stream(d.dst + layer * a.g.lat_layer_vecs + c, ld_stream(d.src + layer * d.src_lstride + c));
         }
         for (int it = threadIdx.x; it < kTileRows * rope_items; it += blockDim.x) {
             const RowDesc d = desc[it / rope_items];
             if (!d.src) continue;
             const int hq = it % rope_items;
             const int head = hq / head_items, q = hq - head * head_items;
-            const uint4* rs = d.src + layer * d.src_lstride + lv + head * hv;
-            uint4* rd = d.dst + layer * a.g.layer_vecs + lv + head * hv;
+            const uint4* rs = d.src_band + layer * d.band_lstride + head * hv;
+            uint4* rd = d.dst_band + layer * a.g.rope_layer_vecs + head * hv;
             float cs[8], sn[8];
             const int j0 = split ? 8 * q : 4 * q;
             const int np = split ? 8 : 4;
@@ -813,7 +831,8 @@ __device__ __forceinline__ uint4 ld_rw(const uint4* p)
 // and the unit loop advances tile and layer group by counters, so a unit costs
 // only its loads, its arithmetic and its stores.  A band is 128 bytes every 1152.
 struct ReindexRow {
-    uint4* row;          // the row's page (layer 0); nullptr: nothing to do
+    uint4* band;         // the row's rope bands (layer 0); nullptr: nothing to do
+    long long slot;      // the row's pool slot (page * block_size + offset)
     const uint4* rsrc;   // row of R (layer 0), REPL only
 };
 
@@ -826,6 +845,24 @@ __host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, i
 {
     const int l = items * kMoveThreads / per_layer;
     return l > 0 ? l : 1;
+}
+
+// Rows of R of a re-index tile (layers [layer0, layer0 + lpu)): whole rows of R,
+// split into the latent and the bands of their fresh slots.
+__device__ __forceinline__ void copy_repl_rows(uint4* kv, const Geometry& g, const ReindexRow* rr,
+                                               long long layer0, int lpu, long long rstride)
+{
+    const int row_vecs = g.row_vecs, lv = g.latent_vecs;
+    const int per_row = lpu * row_vecs;
+    for (int e = threadIdx.x; e < kTileRows * per_row; e += blockDim.x) {
+        const int i = e / per_row, rem = e - (e / per_row) * per_row;
+        const int lo2 = rem / row_vecs, c = rem - (rem / row_vecs) * row_vecs;
+        const long long lay = layer0 + lo2;
+        const ReindexRow d = rr[i];
+        if (!d.band || !d.rsrc || lay >= g.num_layers) continue;
+        uint4* to = kv + (c < lv ? lat_off(g, lay, d.slot) + c : band_off(g, lay, d.slot) + (c - lv));
+        st_stream(to, ld_stream(d.rsrc + lay * rstride + c));
+    }
 }
 
 // kItems: work items per thread.  1 for the MLA row (16 rows x 4 or 8 items per
@@ -842,8 +879,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const long long L = a.g.num_layers;
-    const long long layer_vecs = a.g.layer_vecs;
-    const int hv = a.g.head_vecs, lv = a.g.latent_vecs, row_vecs = a.g.row_vecs;
+    const int hv = a.g.head_vecs;
     const int rope_dim = a.g.rope_dim;
     constexpr int kPairs = kLayout == 0 ? 8 : 4;        // pairs per work item
     const int head_items = kLayout == 0 ? hv / 2 : hv;  // work items per RoPE band
@@ -864,7 +900,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
             const int head = hq / head_items, q = hq - head * head_items;
             it_row[k] = i;
             it_lo[k] = lo;
-            it_off[k] = lv + head * hv + q;
+            it_off[k] = head * hv + q;
             it_q[k] = q;
             n_items = k + 1;
         }
@@ -877,7 +913,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
         if (tile != cur_tile) {
             __syncthreads();
             if (threadIdx.x < kTileRows) {
-                ReindexRow d{nullptr, nullptr};
+                ReindexRow d{nullptr, 0, nullptr};
                 const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
                 const long long lt = tile - rp.tile_begin;
                 const Seg* sg = pv.segs + rp.seg_begin;
@@ -887,18 +923,20 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 const Seg s = sg[k];
                 const long long end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
                 const long long p = s.new_start + (lt - s.tile_off) * kTileRows + threadIdx.x;
-                if (p < end) {
-                    const long long B = a.g.block_size;
-                    const int page = a.stage[rp.stage_begin + (p / B - rp.b0)];
-                    if (page >= 0 && page < a.g.num_pages)
-                        d.row = static_cast<uint4*>(a.kv) + ((long long)page * B + p % B) * row_vecs;
+                if (p < end) {  // rows and block sizes fit 32 bits (the planner checks lengths)
+                    const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
+                    const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
+                    if (page >= 0 && page < a.g.num_pages) {
+                        d.slot = (long long)page * B + ((unsigned)p - pb * B);
+                        d.band = static_cast<uint4*>(a.kv) + band_off(a.g, 0, d.slot);
+                    }
                     if (s.kind == SEG_REPL)
-                        d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * row_vecs;
+                        d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * a.g.row_vecs;
                 }
                 rr[threadIdx.x] = d;
                 if (threadIdx.x == 0) {
                     tile_kind = s.kind;
-                    tile_rstride = (long long)s.n_repl * row_vecs;
+                    tile_rstride = (long long)s.n_repl * a.g.row_vecs;
                 }
                 if (s.kind == SEG_ROT)  // the segment's cos/sin, rope_dim floats
                     for (int c = threadIdx.x; c < rope_dim; c += kTileRows)
@@ -913,9 +951,9 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
             for (int k = 0; k < kItems; ++k) {
                 if (k >= n_items) break;
                 const long long layer = layer0 + it_lo[k];
-                uint4* row = rr[it_row[k]].row;
-                if (layer >= L || !row) continue;
-                uint4* r = row + layer * layer_vecs + it_off[k];
+                uint4* band = rr[it_row[k]].band;
+                if (layer >= L || !band) continue;
+                uint4* r = band + layer * a.g.rope_layer_vecs + it_off[k];
                 float cs[8], sn[8];
                 const float* tp = &trig_s[2 * kPairs * it_q[k]];
 #pragma unroll
@@ -935,15 +973,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 }
             }
         } else {  // rows of R: whole rows into their fresh pages
-            const int per_row = lpu * row_vecs;
-            for (int e = threadIdx.x; e < kTileRows * per_row; e += blockDim.x) {
-                const int i = e / per_row, rem = e - (e / per_row) * per_row;
-                const int lo2 = rem / row_vecs, c = rem - (rem / row_vecs) * row_vecs;
-                const long long lay = layer0 + lo2;
-                const ReindexRow d = rr[i];
-                if (!d.row || !d.rsrc || lay >= L) continue;
-                st_stream(d.row + lay * layer_vecs + c, ld_stream(d.rsrc + lay * tile_rstride + c));
-            }
+            copy_repl_rows(static_cast<uint4*>(a.kv), a.g, rr, layer0, lpu, tile_rstride);
         }
         if (++grp == groups) {
             grp = 0;
@@ -997,21 +1027,22 @@ __global__ void init_queue_kernel(int32_t* q, long long num_pages)
 }
 
 // Gather logical rows [t0, t1) of one request and layer into a contiguous buffer.
-__global__ void gather_kernel(const uint4* kv, const int32_t* table_row, long long B, long long row_vecs,
-                              long long layer_off, long long num_pages, long long t0, long long n, uint4* out,
-                              int32_t* status)
+__global__ void gather_kernel(const uint4* kv, const int32_t* table_row, const Geometry g, long long layer,
+                              long long t0, long long n, uint4* out, int32_t* status)
 {
+    const long long row_vecs = g.row_vecs, lv = g.latent_vecs, B = g.block_size;
     const long long total = n * row_vecs;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const long long r = i / row_vecs, c = i - r * row_vecs;
         const long long t = t0 + r;
         const int page = table_row[t / B];
-        if (page < 0 || page >= num_pages) {
+        if (page < 0 || page >= g.num_pages) {
             raise_status(status, ST_BAD_PAGE);
             continue;
         }
-        out[i] = kv[layer_off + ((long long)page * B + t % B) * row_vecs + c];
+        const long long slot = (long long)page * B + t % B;
+        out[i] = c < lv ? kv[lat_off(g, layer, slot) + c] : kv[band_off(g, layer, slot) + (c - lv)];
     }
 }
 
@@ -1083,13 +1114,14 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
             continue;
         }
         const long long slot = (long long)page * B + t % B;
-        const uint4* row = kv + layer * g.layer_vecs + slot * g.row_vecs;
+        const uint4* lat = kv + lat_off(g, layer, slot);
+        const uint4* bands = kv + band_off(g, layer, slot);
         uint4* o = out + r * g.row_vecs;
-        for (int c = lane; c < g.latent_vecs; c += 32) o[c] = row[c];
+        for (int c = lane; c < g.latent_vecs; c += 32) o[c] = lat[c];
         const int pend = pending[slot];
         for (int it = lane; it < g.rope_heads * head_items; it += 32) {
             const int head = it / head_items, q = it - head * head_items;
-            const uint4* band = row + g.latent_vecs + head * hv;
+            const uint4* band = bands + head * hv;
             uint4* dst = o + g.latent_vecs + head * hv;
             if (pend == 0) {
                 dst[q] = band[q];
@@ -1137,7 +1169,7 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Ge
                 item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
                 have_q = q;
             }
-            uint4* band = kv + layer * g.layer_vecs + slot * g.row_vecs + g.latent_vecs + head * hv;
+            uint4* band = kv + band_off(g, layer, slot) + head * hv;
             turn_item<kLayout>(band, band, q, hv, bf16, c, s);
         }
         __syncwarp();
@@ -1214,7 +1246,9 @@ cudaError_t launch_bulk(const SpliceArgs& a, const PlanSrc& plan, int grid, cuda
 template <class PlanSrc>
 cudaError_t launch_move(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s)
 {
-    if (a.move_kernel == MOVE_BULK && mla_shape(a.g)) return launch_bulk(a, plan, grid, s);
+    // the bulk kernel copies whole rows: pools of whole rows only
+    if (a.move_kernel == MOVE_BULK && mla_shape(a.g) && !(a.g.flags & LEYLINE_POOL_SPLIT_ROPE))
+        return launch_bulk(a, plan, grid, s);
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     if (mla_shape(a.g)) {
         if (a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT)
@@ -1310,8 +1344,7 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
     const long long n = t1 - t0;
     if (n <= 0) return 0;
     gather_kernel<<<grid_for(n * g.row_vecs, 256, 8192), 256, 0, (cudaStream_t)stream>>>(
-        static_cast<const uint4*>(kv), table_row, g.block_size, g.row_vecs, (long long)layer * g.layer_vecs,
-        g.num_pages, t0, n, static_cast<uint4*>(out), status);
+        static_cast<const uint4*>(kv), table_row, g, layer, t0, n, static_cast<uint4*>(out), status);
     return (int)cudaGetLastError();
 }
 

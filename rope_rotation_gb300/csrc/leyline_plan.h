@@ -40,6 +40,16 @@ struct Geometry {
     int32_t head_vecs;    // rope_dim / 8 (one band)
     int64_t num_pages;
     int64_t layer_vecs;   // num_pages * block_size * row_vecs
+    // Where the parts of the row of (layer, slot) live, in 16-byte vectors from the
+    // pool base: the latent at lat_layer_vecs * layer + lat_row_vecs * slot, the rope
+    // bands at rope_base_vecs + rope_layer_vecs * layer + rope_row_vecs * slot.  One
+    // array of whole rows: the bands follow the latent in the row.  Split rope
+    // (LEYLINE_POOL_SPLIT_ROPE): an array of latents followed by an array of bands.
+    int64_t lat_layer_vecs;
+    int64_t rope_layer_vecs;
+    int64_t rope_base_vecs;
+    int32_t lat_row_vecs;
+    int32_t rope_row_vecs;
     double theta;
     int32_t pair_layout;
     int32_t precision;

@@ -99,7 +99,7 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pair_layout");
     if (d->rotate_precision != LEYLINE_ROTATE_FP32 && d->rotate_precision != LEYLINE_ROTATE_BF16_NAIVE)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown rotate_precision");
-    if ((d->flags & ~(uint32_t)(LEYLINE_POOL_REINDEX | LEYLINE_POOL_LAZY)) != 0)
+    if ((d->flags & ~(uint32_t)(LEYLINE_POOL_REINDEX | LEYLINE_POOL_LAZY | LEYLINE_POOL_SPLIT_ROPE)) != 0)
         return set_error(LEYLINE_ERR_INVALID_ARG, "unknown pool flags");
     if (d->rope_heads < 0 || d->rope_heads > 1024)
         return set_error(LEYLINE_ERR_INVALID_ARG, "rope_heads must be in [0, 1024]");
@@ -119,6 +119,18 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
     g->rope_vecs = heads * g->head_vecs;
     g->num_pages = d->num_pages;
     g->layer_vecs = d->num_pages * (int64_t)d->block_size * g->row_vecs;
+    const int64_t slots = d->num_pages * (int64_t)d->block_size;
+    if (d->flags & LEYLINE_POOL_SPLIT_ROPE) {
+        g->lat_row_vecs = g->latent_vecs;
+        g->rope_row_vecs = g->rope_vecs;
+        g->lat_layer_vecs = slots * g->latent_vecs;
+        g->rope_layer_vecs = slots * g->rope_vecs;
+        g->rope_base_vecs = (int64_t)d->num_layers * g->lat_layer_vecs;
+    } else {
+        g->lat_row_vecs = g->rope_row_vecs = g->row_vecs;
+        g->lat_layer_vecs = g->rope_layer_vecs = g->layer_vecs;
+        g->rope_base_vecs = g->latent_vecs;
+    }
     g->theta = d->rope_theta;
     g->pair_layout = d->pair_layout;
     g->precision = d->rotate_precision;

@@ -216,7 +216,7 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         // the MLA row shape (latent 512 + rope 64), for A/B measurements.
         const char* env = getenv("LEYLINE_MOVE_KERNEL");
         const bool want_bulk = env && strcmp(env, "bulk") == 0;
-        const bool mla = g.latent_vecs == 64 && g.rope_vecs == 8;
+        const bool mla = g.latent_vecs == 64 && g.rope_vecs == 8 && !(g.flags & LEYLINE_POOL_SPLIT_ROPE);
         p->move_kernel = (want_bulk && mla && p->bulk_blocks_per_sm > 0) ? MOVE_BULK : MOVE_VECTOR;
     }
     p->q_head = 0;

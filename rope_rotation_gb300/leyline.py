@@ -38,6 +38,7 @@ LEYLINE_FORGET = 1
 LEYLINE_EVICT = 2
 LEYLINE_POOL_REINDEX = 1
 LEYLINE_POOL_LAZY = 2
+LEYLINE_POOL_SPLIT_ROPE = 4
 
 
 class LeylineError(RuntimeError):

@@ -1,9 +1,11 @@
 """A paged MLA KV cache in torch device memory, driven through libleyline.so.
 
 Plumbing for callers: it allocates the pool tensor (layout
-``kv[layer][page][slot][latent + rope]``, bf16), the block table and the length
-arrays, takes pages for new requests, and forwards splices and gathers to the
-C ABI.  It computes nothing itself.
+``kv[layer][page][slot][latent + rope]``, bf16; with LEYLINE_POOL_SPLIT_ROPE the
+latents ``[layer][page][slot][latent]`` followed by the rope bands
+``[layer][page][slot][rope]``), the block table and the length arrays, takes pages
+for new requests, and forwards splices and gathers to the C ABI.  It computes
+nothing itself.
 """
 from __future__ import annotations
 
@@ -52,9 +54,51 @@ class PagedCache:
     def seq_lens_host(self) -> np.ndarray:
         return self.tables.seq_lens_host
 
+    @property
+    def split(self) -> bool:
+        return bool(self.desc.flags & leyline.LEYLINE_POOL_SPLIT_ROPE)
+
     def kv_view(self):
-        """[layers][pages][block_size][row] view of the pool."""
+        """[layers][pages][block_size][row] view of a pool of whole rows."""
+        if self.split:
+            raise ValueError("a split-rope pool has no array of whole rows: use latent_view / rope_view")
         return self.kv.view(self.num_layers, self.num_pages, self.block_size, self.row)
+
+    def latent_view(self):
+        """[layers][pages][block_size][latent] view of the latents."""
+        if not self.split:
+            return self.kv_view()[..., :self.latent_dim]
+        n = self.num_layers * self.num_pages * self.block_size * self.latent_dim
+        return self.kv[:n].view(self.num_layers, self.num_pages, self.block_size, self.latent_dim)
+
+    def rope_view(self):
+        """[layers][pages][block_size][rope_heads * rope_dim] view of the rope bands."""
+        if not self.split:
+            return self.kv_view()[..., self.latent_dim:]
+        n = self.num_layers * self.num_pages * self.block_size * self.latent_dim
+        return self.kv[n:].view(self.num_layers, self.num_pages, self.block_size, self.row - self.latent_dim)
+
+    def page_views(self):
+        """The pool's arrays as [layers][pages][...] views, for comparing pages."""
+        if not self.split:
+            return [self.kv.view(self.num_layers, self.num_pages, -1)]
+        return [self.latent_view().reshape(self.num_layers, self.num_pages, -1),
+                self.rope_view().reshape(self.num_layers, self.num_pages, -1)]
+
+    def read_rows(self, layers, pages, slots):
+        """Stored whole rows [n][row] of (layer, page, slot) index tensors."""
+        return self.torch.cat((self.latent_view()[layers, pages, slots], self.rope_view()[layers, pages, slots]), -1)
+
+    def write_layer_rows(self, layer: int, flat_slots, rows) -> None:
+        """Store whole rows [n][row] at flat slots (page * block_size + offset) of one layer."""
+        if not self.split:
+            flat = self.kv_view()[layer].reshape(self.num_pages * self.block_size, self.row)
+            flat.index_copy_(0, flat_slots, rows)
+            return
+        lat = self.latent_view()[layer].reshape(self.num_pages * self.block_size, self.latent_dim)
+        rope = self.rope_view()[layer].reshape(self.num_pages * self.block_size, self.row - self.latent_dim)
+        lat.index_copy_(0, flat_slots, rows[:, :self.latent_dim].contiguous())
+        rope.index_copy_(0, flat_slots, rows[:, self.latent_dim:].contiguous())
 
     def add_request(self, req: int, length: int) -> np.ndarray:
         """Take pages for a new request of `length` tokens and install its table row; returns the page ids."""

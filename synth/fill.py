@@ -26,11 +26,10 @@ def fill_request(cache, seed: int, req: int, length: int) -> None:
     import torch
     base = _base_on_device(seed, cache.row, str(cache.device))
     slots = torch.from_numpy(cache.slot_index(req, np.arange(length))).to(cache.device)
-    flat = cache.kv_view().view(cache.num_layers, cache.num_pages * cache.block_size, cache.row)
     toks = np.arange(length)
     for layer in range(cache.num_layers):
         ids = torch.from_numpy(row_ids(seed, STREAM_CACHE, req, layer, toks)).to(cache.device)
-        flat[layer].index_copy_(0, slots, base.index_select(0, ids))
+        cache.write_layer_rows(layer, slots, base.index_select(0, ids))
 
 
 def repl_tensor(seed: int, req: int, key: int, num_layers: int, n_repl: int, row_elems: int, device: str):

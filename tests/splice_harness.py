@@ -174,7 +174,7 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
     B = w.block_size
     before_table = cache.table.cpu().numpy().copy()
     before_lens = cache.seq_lens_host.copy()
-    snap = cache.kv.clone() if guard else None
+    snap = [v.clone() for v in cache.page_views()] if guard else None
     free_before = cache.free_pages()
     dirs, repl_t = gpu_directives(w, step)
     cache.splice(dirs)
@@ -243,11 +243,10 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
             new_pages |= set(after_table[r][touched[r]:nb].tolist())
         keep = np.ones(cache.num_pages, dtype=bool)
         keep[list(new_pages)] = False
-        kv_b = snap.view(cache.num_layers, cache.num_pages, -1)
-        kv_a = cache.kv.view(cache.num_layers, cache.num_pages, -1)
         keep_t = torch.from_numpy(keep).to(cache.device)
-        assert torch.equal(kv_a[:, keep_t].view(torch.int16), kv_b[:, keep_t].view(torch.int16)), \
-            "a page outside the rewritten blocks changed"
+        for kv_b, kv_a in zip(snap, cache.page_views()):
+            assert torch.equal(kv_a[:, keep_t].view(torch.int16), kv_b[:, keep_t].view(torch.int16)), \
+                "a page outside the rewritten blocks changed"
     del repl_t
     counters["stats"] = stats
     return counters
@@ -315,7 +314,7 @@ def fetch_rows(cache, req: int, layers: np.ndarray, pos: np.ndarray) -> np.ndarr
     page = torch.from_numpy(row[pos // B]).to(cache.device)
     slot = torch.from_numpy(pos % B).to(cache.device)
     lay = torch.from_numpy(layers.astype(np.int64)).to(cache.device)
-    got = cache.kv_view()[lay, page, slot]
+    got = cache.read_rows(lay, page, slot)
     return got.view(torch.int16).cpu().numpy().view(np.uint16)
 
 

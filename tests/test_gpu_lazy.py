@@ -36,7 +36,8 @@ def _raw_rows(cache, req: int, length: int) -> np.ndarray:
     B = cache.block_size
     nb = -(-length // B)
     pages = cache.table[req, :nb].long()
-    rows = cache.kv_view()[:, pages].reshape(cache.num_layers, nb * B, cache.row)[:, :length]
+    rows = torch.cat((cache.latent_view()[:, pages], cache.rope_view()[:, pages]), -1)
+    rows = rows.reshape(cache.num_layers, nb * B, cache.row)[:, :length]
     return rows.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
