@@ -186,6 +186,8 @@ typedef struct {
     int64_t pages_pushed;      /* old pages returned to the free-page list */
     int32_t requests_touched;
     int32_t kernels_launched;  /* kernels this call enqueued */
+    int32_t reindexed;         /* 1: the call kept survivors in their pages (LEYLINE_POOL_REINDEX) */
+    int32_t reserved;
 } leyline_stats_t;
 
 /* -------------------------------------------------------------- pool ---- */

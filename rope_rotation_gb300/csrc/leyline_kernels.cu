@@ -171,9 +171,9 @@ __device__ __forceinline__ long long band_off(const Geometry& g, long long layer
     return g.rope_base_vecs + layer * g.rope_layer_vecs + slot * g.rope_row_vecs;
 }
 
-enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2 };
+enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2, BY_REPL = 3 };
 
-// Last request whose first tile / commit item / prep item is <= v.
+// Last request whose first tile / commit item / prep item / row of R is <= v.
 __device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v, int key_kind)
 {
     int lo = 0, hi = n - 1;
@@ -181,7 +181,8 @@ __device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v,
         const int mid = (lo + hi + 1) >> 1;
         const long long key = key_kind == BY_TILE     ? reqs[mid].tile_begin
                               : key_kind == BY_COMMIT ? reqs[mid].commit_begin
-                                                      : reqs[mid].prep_begin;
+                              : key_kind == BY_PREP   ? reqs[mid].prep_begin
+                                                      : reqs[mid].repl_begin;
         if (key <= v) lo = mid;
         else hi = mid - 1;
     }
@@ -822,22 +823,21 @@ __device__ __forceinline__ uint4 ld_rw(const uint4* p)
     return v;
 }
 
-// Rotate kernel of re-index mode.  Its tiles cover only the rows that need work:
-// each turned (ROT) or R (REPL) segment is cut into 16-row tiles of its own (the
-// planner numbers them in Seg::tile_off), so survivors that keep their encoding
-// -- every survivor of a lazy pool -- cost nothing here.  Work unit = (tile, group
-// of layers).  The threads' work items (4 per band and layer for half-split pairs,
-// 8 interleaved; at most kMaxItems per thread) are decoded once at kernel start,
-// and the unit loop advances tile and layer group by counters, so a unit costs
-// only its loads, its arithmetic and its stores.  A band is 128 bytes every 1152.
-struct ReindexRow {
-    uint4* band;         // the row's rope bands (layer 0); nullptr: nothing to do
-    long long slot;      // the row's pool slot (page * block_size + offset)
-    const uint4* rsrc;   // row of R (layer 0), REPL only
-};
-
+// Re-index mode moves rows of R and turns bands in two kernels.
+//   copy_repl_reindex: the call's rows of R form one list; items of (row, 8 layers)
+//   are spread over every warp of the grid, a lane moving every 32nd vector of the
+//   row with four loads in flight.  A row of R moves 9 times the bytes of a turned
+//   band, so rows of R are not tied to one CTA's share of the tiles.
+//   rotate_in_place: each turned (ROT) segment is cut into 16-row tiles of its own
+//   (the planner numbers them in Seg::tile_off); survivors that keep their encoding
+//   -- every survivor of a lazy pool -- cost nothing.  Work unit = (tile, group of
+//   layers).  The threads' work items (4 per band and layer for half-split pairs, 8
+//   interleaved; at most kMaxItems per thread) are decoded once at kernel start, and
+//   the unit loop advances tile and layer group by counters, so a unit costs only
+//   its loads, its arithmetic and its stores.
 constexpr int kMaxRopeDim = 256;
-constexpr int kMaxItems = 4;  // work items per thread: rope_heads * rope_dim <= 512
+constexpr int kMaxItems = 4;    // work items per thread: rope_heads * rope_dim <= 512
+constexpr int kReplLayers = 8;  // layers per item of the rows-of-R phase
 
 // Layers per work unit of the re-index rotate kernel: as many as give each of the
 // CTA's threads kItems work items (at least one layer).
@@ -847,21 +847,63 @@ __host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, i
     return l > 0 ? l : 1;
 }
 
-// Rows of R of a re-index tile (layers [layer0, layer0 + lpu)): whole rows of R,
-// split into the latent and the bands of their fresh slots.
-__device__ __forceinline__ void copy_repl_rows(uint4* kv, const Geometry& g, const ReindexRow* rr,
-                                               long long layer0, int lpu, long long rstride)
+// Rows of R of a re-indexed call into their fresh pages (the pages prep staged).
+template <class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads) copy_repl_reindex(const __grid_constant__ SpliceArgs a,
+                                                                  const __grid_constant__ PlanSrc plan)
 {
-    const int row_vecs = g.row_vecs, lv = g.latent_vecs;
-    const int per_row = lpu * row_vecs;
-    for (int e = threadIdx.x; e < kTileRows * per_row; e += blockDim.x) {
-        const int i = e / per_row, rem = e - (e / per_row) * per_row;
-        const int lo2 = rem / row_vecs, c = rem - (rem / row_vecs) * row_vecs;
-        const long long lay = layer0 + lo2;
-        const ReindexRow d = rr[i];
-        if (!d.band || !d.rsrc || lay >= g.num_layers) continue;
-        uint4* to = kv + (c < lv ? lat_off(g, lay, d.slot) + c : band_off(g, lay, d.slot) + (c - lv));
-        st_stream(to, ld_stream(d.rsrc + lay * rstride + c));
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const int lane = threadIdx.x & 31;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long L = a.g.num_layers;
+    const int chunks = (int)((L + kReplLayers - 1) / kReplLayers);
+    const int row_vecs = a.g.row_vecs, lv = a.g.latent_vecs;
+    uint4* kv = static_cast<uint4*>(a.kv);
+    for (long long w = gw; w < a.total_repl * chunks; w += nw) {
+        const long long rrow = w / chunks;
+        const long long l0 = (w - rrow * chunks) * kReplLayers;
+        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, rrow, BY_REPL)];
+        long long j = rrow - rp.repl_begin;  // row within the request's rows of R
+        const Seg* sg = pv.segs + rp.seg_begin;
+        int k = -1;
+        for (int q = 0; q < rp.seg_count && k < 0; ++q) {
+            if (sg[q].kind != SEG_REPL) continue;
+            if (j < sg[q].n_repl) k = q;
+            else j -= sg[q].n_repl;
+        }
+        if (k < 0) {
+            if (lane == 0) raise_status(a.status, ST_BAD_FRESH);
+            continue;
+        }
+        const Seg s = sg[k];
+        const long long p = s.new_start + j;  // rows fit 32 bits (the planner checks lengths)
+        const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
+        const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
+        if (page < 0 || page >= a.g.num_pages) continue;  // prep has recorded a bad fresh page
+        const long long slot = (long long)page * B + ((unsigned)p - pb * B);
+        const long long rstride = (long long)s.n_repl * row_vecs;
+        const uint4* src = static_cast<const uint4*>(s.repl) + j * row_vecs;
+        const long long l1 = l0 + kReplLayers < L ? l0 + kReplLayers : L;
+        for (long long layer = l0; layer < l1; ++layer) {
+            for (int c0 = 0; c0 < row_vecs; c0 += 4 * 32) {
+                uint4 v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + 32 * q + lane;
+                    if (c < row_vecs) v[q] = ld_stream(src + layer * rstride + c);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int c = c0 + 32 * q + lane;
+                    if (c < row_vecs)
+                        st_stream(kv + (c < lv ? lat_off(a.g, layer, slot) + c : band_off(a.g, layer, slot) + (c - lv)),
+                                  v[q]);
+                }
+            }
+        }
     }
 }
 
@@ -871,10 +913,8 @@ template <int kLayout, bool kBf16, int kItems, class PlanSrc>
 __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_place(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
-    __shared__ ReindexRow rr[kTileRows];
+    __shared__ uint4* band_s[kTileRows];                  // the tile's rows' bands (layer 0); nullptr: none
     __shared__ __align__(16) float trig_s[kMaxRopeDim];  // (cos, sin) per pair of the tile's segment
-    __shared__ int tile_kind;                             // SEG_ROT or SEG_REPL
-    __shared__ long long tile_rstride;                    // vectors between layers of R (REPL)
     wait_for_previous_grid();
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
@@ -887,7 +927,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
     const int per_layer = kTileRows * ipr;
     const int lpu = reindex_layers_per_unit(per_layer, kItems);
     const long long groups = (L + lpu - 1) / lpu;
-    // this thread's items: row i, layer offset lo, vector offset in the rope region, pair group q
+    // this thread's items: row i, layer offset lo, vector offset in the bands, pair group q
     int it_row[kItems], it_lo[kItems], it_off[kItems], it_q[kItems];
     int n_items = 0;
 #pragma unroll
@@ -913,7 +953,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
         if (tile != cur_tile) {
             __syncthreads();
             if (threadIdx.x < kTileRows) {
-                ReindexRow d{nullptr, 0, nullptr};
+                uint4* band = nullptr;
                 const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
                 const long long lt = tile - rp.tile_begin;
                 const Seg* sg = pv.segs + rp.seg_begin;
@@ -926,54 +966,41 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 if (p < end) {  // rows and block sizes fit 32 bits (the planner checks lengths)
                     const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
                     const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
-                    if (page >= 0 && page < a.g.num_pages) {
-                        d.slot = (long long)page * B + ((unsigned)p - pb * B);
-                        d.band = static_cast<uint4*>(a.kv) + band_off(a.g, 0, d.slot);
-                    }
-                    if (s.kind == SEG_REPL)
-                        d.rsrc = static_cast<const uint4*>(s.repl) + (s.src_start + (p - s.new_start)) * a.g.row_vecs;
+                    if (page >= 0 && page < a.g.num_pages)
+                        band = static_cast<uint4*>(a.kv) + band_off(a.g, 0, (long long)page * B + ((unsigned)p - pb * B));
                 }
-                rr[threadIdx.x] = d;
-                if (threadIdx.x == 0) {
-                    tile_kind = s.kind;
-                    tile_rstride = (long long)s.n_repl * a.g.row_vecs;
-                }
-                if (s.kind == SEG_ROT)  // the segment's cos/sin, rope_dim floats
-                    for (int c = threadIdx.x; c < rope_dim; c += kTileRows)
-                        trig_s[c] = pv.trig[(long long)s.trig * rope_dim + c];
+                band_s[threadIdx.x] = band;
+                for (int c = threadIdx.x; c < rope_dim; c += kTileRows)  // the segment's cos/sin
+                    trig_s[c] = pv.trig[(long long)s.trig * rope_dim + c];
             }
             __syncthreads();
             cur_tile = tile;
         }
         const long long layer0 = grp * lpu;
-        if (tile_kind == SEG_ROT) {  // rope bands, in place
 #pragma unroll
-            for (int k = 0; k < kItems; ++k) {
-                if (k >= n_items) break;
-                const long long layer = layer0 + it_lo[k];
-                uint4* band = rr[it_row[k]].band;
-                if (layer >= L || !band) continue;
-                uint4* r = band + layer * a.g.rope_layer_vecs + it_off[k];
-                float cs[8], sn[8];
-                const float* tp = &trig_s[2 * kPairs * it_q[k]];
+        for (int k = 0; k < kItems; ++k) {
+            if (k >= n_items) break;
+            const long long layer = layer0 + it_lo[k];
+            uint4* band = band_s[it_row[k]];
+            if (layer >= L || !band) continue;
+            uint4* r = band + layer * a.g.rope_layer_vecs + it_off[k];
+            float cs[8], sn[8];
+            const float* tp = &trig_s[2 * kPairs * it_q[k]];
 #pragma unroll
-                for (int w = 0; w < kPairs; ++w) {
-                    cs[w] = tp[2 * w];
-                    sn[w] = tp[2 * w + 1];
-                }
-                if (kLayout == 0) {
-                    uint4 x = ld_rw(r), y = ld_rw(r + hv / 2);
-                    rotate_half_split<kBf16>(x, y, cs, sn);
-                    st_stream(r, x);
-                    st_stream(r + hv / 2, y);
-                } else {
-                    uint4 x = ld_rw(r);
-                    rotate_interleaved<kBf16>(x, cs, sn);
-                    st_stream(r, x);
-                }
+            for (int w = 0; w < kPairs; ++w) {
+                cs[w] = tp[2 * w];
+                sn[w] = tp[2 * w + 1];
             }
-        } else {  // rows of R: whole rows into their fresh pages
-            copy_repl_rows(static_cast<uint4*>(a.kv), a.g, rr, layer0, lpu, tile_rstride);
+            if (kLayout == 0) {
+                uint4 x = ld_rw(r), y = ld_rw(r + hv / 2);
+                rotate_half_split<kBf16>(x, y, cs, sn);
+                st_stream(r, x);
+                st_stream(r + hv / 2, y);
+            } else {
+                uint4 x = ld_rw(r);
+                rotate_interleaved<kBf16>(x, cs, sn);
+                st_stream(r, x);
+            }
         }
         if (++grp == groups) {
             grp = 0;
@@ -1276,6 +1303,11 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);
     if (e == cudaSuccess && t0) e = cudaEventRecord(t0, s);
+    if (e == cudaSuccess && a.total_repl > 0) {  // rows of R: items of (row, kReplLayers layers), a warp each
+        const long long items = a.total_repl * ((a.g.num_layers + kReplLayers - 1) / kReplLayers);
+        e = launch_dependent(copy_repl_reindex<PlanSrc>, grid_for(items * 32, kMoveThreads, 8192), kMoveThreads, s,
+                             a, plan);
+    }
     if (e == cudaSuccess && units > 0) {
         if (split)
             e = bf16 ? (mla ? launch_dependent(rotate_in_place<0, true, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)

@@ -73,9 +73,10 @@ struct ReqPlan {
     int32_t push_off;      // first returned page of this request in the ring's push region
     int64_t stage_begin;   // re-index: first staged table entry of this request
     int64_t prep_begin;    // re-index: first flat prep item of this request
-    int64_t drop_count;    // re-index: tokens dropped (pages returned)
+    int64_t drop_count;    // re-index: blocks dropped (pages returned)
     int32_t drop_seg_begin;
     int32_t drop_seg_count;
+    int64_t repl_begin;    // re-index: first row of R of this request in the call's list of rows of R
 };
 
 struct Seg {
@@ -88,11 +89,11 @@ struct Seg {
     int32_t aux;           // re-index: R rows of the request before this segment (REPL),
                            // dropped tokens of the request before this segment (DROP)
     int32_t turn;          // positions the segment's rows turn (ROT; in lazy pools also COPY)
-    int32_t tile_off;      // re-index: first rotate-kernel tile of this ROT/REPL segment within
-                           // its request, -1 for segments the rotate kernel skips
+    int32_t tile_off;      // re-index: first rotate-kernel tile of this ROT segment within its
+                           // request, -1 for other segments
 };
 
-static_assert(sizeof(ReqPlan) == 104, "ReqPlan layout");
+static_assert(sizeof(ReqPlan) == 112, "ReqPlan layout");
 static_assert(sizeof(Seg) == 48, "Seg layout");
 
 }  // namespace leyline

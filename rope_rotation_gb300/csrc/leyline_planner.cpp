@@ -318,14 +318,18 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         }
         const int64_t rows = Lp - rp.row0;
         if (reindex) {
-            // the rotate kernel's tiles cover ROT and REPL segments only, each cut on its own
+            // the rotate kernel's tiles cover ROT segments only, each cut on its own; rows of
+            // R form one list for the whole call
+            rp.repl_begin = plan->total_repl;
+            for (int32_t k = rp.seg_begin; k < rp.seg_begin + rp.seg_count; ++k)
+                if (plan->segs[k].kind == SEG_REPL) plan->total_repl += plan->segs[k].n_repl;
             int64_t wt = 0;
             const int32_t last = rp.seg_begin + rp.seg_count;
             for (int32_t k = rp.seg_begin; k < last; ++k) {
                 Seg& s = plan->segs[k];
                 const int64_t end = k + 1 < last ? plan->segs[k + 1].new_start : Lp;
                 s.tile_off = -1;
-                if ((s.kind == SEG_ROT || s.kind == SEG_REPL) && end > s.new_start) {
+                if (s.kind == SEG_ROT && end > s.new_start) {
                     s.tile_off = (int32_t)wt;
                     wt += ceil_div(end - s.new_start, kTileRows);
                 }
@@ -384,7 +388,11 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     st.pages_popped = pops;
     st.pages_pushed = pushes;
     st.requests_touched = (int32_t)plan->reqs.size();
-    st.kernels_launched = plan->reqs.empty() ? 0 : (reindex ? 3 : 2);
+    // re-index: prep, the rows of R (if any), the in-place rotation (if any turned rows), commit
+    st.kernels_launched = plan->reqs.empty() ? 0
+                          : reindex          ? 2 + (plan->total_repl > 0) + (plan->total_tiles > 0)
+                                             : 2;
+    st.reindexed = (!plan->reqs.empty() && reindex) ? 1 : 0;
     return LEYLINE_OK;
 }
 

@@ -74,7 +74,8 @@ class Stats(ctypes.Structure):
                 ("head_slots", ctypes.c_int64), ("algorithmic_bytes", ctypes.c_int64),
                 ("moved_bytes", ctypes.c_int64), ("pages_popped", ctypes.c_int64),
                 ("pages_pushed", ctypes.c_int64), ("requests_touched", ctypes.c_int32),
-                ("kernels_launched", ctypes.c_int32)]
+                ("kernels_launched", ctypes.c_int32), ("reindexed", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -234,7 +234,7 @@ def splice_step_and_check(w: Workload, cache, state: list[np.ndarray], step: lis
         counters["rel_l2_max"] = max(counters["rel_l2_max"], c["rel_l2"])
         state[r] = want
     check_tables(cache, before_table, after_table, before_lens, cache.seq_lens_host, touched,
-                 reindex=stats["kernels_launched"] == 3)  # re-indexed calls keep pages
+                 reindex=stats["reindexed"] == 1)  # re-indexed calls keep pages
     assert cache.free_pages() == free_before - stats["pages_popped"] + stats["pages_pushed"]
     if guard:
         new_pages = set()
