@@ -746,14 +746,14 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
 // -------------------------------------------------------------------------
 // Re-index mode (pool flag LEYLINE_POOL_REINDEX; block size 1, or a call whose
 // directives all lie on block boundaries): a surviving downstream block keeps its
-// page.  Three kernels, each a programmatic dependent of the one before:
+// page.  Up to four kernels, each a programmatic dependent of the one before:
 //   prep          stages the page of every rewritten table entry (the kept block's
 //                 old page, or a fresh page for a block of R) and returns the pages
 //                 of dropped blocks to the ring; it reads the old table and writes
 //                 only the staging array and the ring's push region;
-//   rotate        turns the rope band of every turned row in place (128 bytes read
-//                 and written per row and layer; the latent is not touched) and
-//                 copies rows of R into their fresh pages;
+//   rows of R     copies the call's rows of R into their fresh pages (if any);
+//   rotate        turns the rope bands of every turned row in place (128 bytes read
+//                 and written per band and layer; the latent is not touched; if any);
 //   commit        installs the staged entries, clears entries past the new end,
 //                 writes the new length.
 template <class PlanSrc>
