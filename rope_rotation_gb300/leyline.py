@@ -151,6 +151,19 @@ def _tensor_ptr(t) -> int:
     return int(t.data_ptr())
 
 
+def _rows_ptr(t, what: str, rows: Optional[int] = None) -> int:
+    """Address of a contiguous bf16 tensor of whole rows; refuses other dtypes and strided views
+    (the library reads raw bytes, so those would be read as something else)."""
+    import torch
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{what}: dtype {t.dtype}, expected torch.bfloat16")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if rows is not None and t.numel() < rows:
+        raise ValueError(f"{what}: {t.numel()} elements, need {rows}")
+    return int(t.data_ptr())
+
+
 # ------------------------------------------------------------------ pool ----
 
 def pool_desc(num_layers: int, block_size: int, num_pages: int, latent_dim: int = 512, rope_dim: int = 64,
@@ -211,7 +224,14 @@ def directive(req: int, s_start: int, s_end: int, repl=None, n_repl: Optional[in
     memory (read in place by the kernel), or None."""
     if n_repl is None:
         n_repl = 0 if repl is None else int(repl.shape[1])
-    return Directive(req, mode, s_start, s_end, n_repl, 0, None if repl is None else _tensor_ptr(repl))
+    if repl is None:
+        return Directive(req, mode, s_start, s_end, n_repl, 0, None)
+    if repl.dim() != 3 or int(repl.shape[1]) < n_repl:
+        raise ValueError(f"repl: shape {tuple(repl.shape)}, expected [num_layers][>= {n_repl}][row]")
+    if int(repl.shape[1]) != n_repl:
+        raise ValueError(f"repl: {int(repl.shape[1])} rows per layer but n_repl = {n_repl}; the layer stride "
+                         "of R is n_repl rows, so pass R with exactly n_repl rows per layer")
+    return Directive(req, mode, s_start, s_end, n_repl, 0, _rows_ptr(repl, "repl"))
 
 
 def _dir_array(dirs: Sequence[Directive]):
@@ -252,9 +272,9 @@ def leyline_last_stats(pool) -> Stats:
 
 
 def leyline_gather(pool, tables: Tables, req: int, layer: int, t0: int, t1: int, out, stream=None) -> None:
-    """out: bf16 CUDA tensor [t1 - t0][row]."""
-    _check(load().leyline_gather(pool, ctypes.byref(tables.bt), req, layer, t0, t1, _tensor_ptr(out),
-                                 _stream_ptr(stream)))
+    """out: contiguous bf16 tensor of at least (t1 - t0) rows, on the pool's GPU or in pinned host memory."""
+    ptr = _rows_ptr(out, "out") if t1 > t0 else _tensor_ptr(out)
+    _check(load().leyline_gather(pool, ctypes.byref(tables.bt), req, layer, t0, t1, ptr, _stream_ptr(stream)))
 
 
 def leyline_materialize(pool, tables: Tables, req: int, stream=None) -> None:

@@ -185,3 +185,17 @@ def test_reindex_pages_only_on_block_boundaries(L):
     # block size 1: every call re-indexes, one page per row
     st, _ = _plan(L, [100], [_d(L, 0, 3, 50, 7)], B=1, desc=L.pool_desc(4, 1, 1 << 20, flags=L.LEYLINE_POOL_REINDEX))
     assert (st.reindexed, st.kernels_launched, st.pages_popped, st.pages_pushed) == (1, 4, 7, 47)
+
+
+def test_binding_refuses_tensors_it_cannot_pass_as_rows(L):
+    """The library reads raw bf16 rows: the binding refuses other dtypes, strided views and
+    an R whose row count differs from n_repl (its layer stride is n_repl rows)."""
+    import torch
+    good = torch.zeros((2, 3, 576), dtype=torch.bfloat16)
+    assert L.directive(0, 1, 2, good).n_repl == 3
+    for bad, kw in [(torch.zeros((2, 3, 576), dtype=torch.float32), {}),
+                    (torch.zeros((2, 576, 3), dtype=torch.bfloat16).transpose(1, 2), {}),
+                    (good, {"n_repl": 2}),
+                    (torch.zeros((3, 576), dtype=torch.bfloat16), {})]:
+        with pytest.raises(ValueError):
+            L.directive(0, 1, 2, bad, **kw)
