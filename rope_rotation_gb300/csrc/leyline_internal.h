@@ -31,6 +31,7 @@ struct Plan {
     int64_t total_prep = 0;   // re-index: prep items (staged entries + dropped tokens)
     int64_t total_stage = 0;  // re-index: staged table entries
     int64_t total_repl = 0;   // re-index: rows of R of the call
+    int64_t total_fresh = 0;  // re-index: survivor and prefix rows written into fresh pages
     int64_t total_tiles = 0;  // move+rotate tiles over all requests
     int64_t total_commit = 0; // commit work items over all requests
     int64_t total_pop = 0;    // fresh pages
@@ -79,6 +80,7 @@ struct SpliceArgs {
     int32_t* status;          // device status word
     int64_t total_prep;
     int64_t total_repl;       // re-index: rows of R of the call
+    int64_t total_fresh;      // re-index: survivor and prefix rows written into fresh pages
     int64_t total_tiles;
     int64_t total_commit;
     int32_t n_reqs;

@@ -171,9 +171,9 @@ __device__ __forceinline__ long long band_off(const Geometry& g, long long layer
     return g.rope_base_vecs + layer * g.rope_layer_vecs + slot * g.rope_row_vecs;
 }
 
-enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2, BY_REPL = 3 };
+enum ReqKey : int { BY_TILE = 0, BY_COMMIT = 1, BY_PREP = 2, BY_FRESH = 3, BY_REPL = 4 };
 
-// Last request whose first tile / commit item / prep item / row of R is <= v.
+// Last request whose first tile / commit item / prep item / fresh row / row of R is <= v.
 __device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v, int key_kind)
 {
     int lo = 0, hi = n - 1;
@@ -182,6 +182,7 @@ __device__ __forceinline__ int find_req(const ReqPlan* reqs, int n, long long v,
         const long long key = key_kind == BY_TILE     ? reqs[mid].tile_begin
                               : key_kind == BY_COMMIT ? reqs[mid].commit_begin
                               : key_kind == BY_PREP   ? reqs[mid].prep_begin
+                              : key_kind == BY_FRESH  ? reqs[mid].fresh_begin
                                                       : reqs[mid].repl_begin;
         if (key <= v) lo = mid;
         else hi = mid - 1;
@@ -770,21 +771,14 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
         const long long blocks = (rp.new_len + B - 1) / B - rp.b0;  // new blocks from b0 on
         const int32_t* trow = a.table + (long long)rp.req * a.max_blocks;
         if (k < blocks) {
-            const long long p = (rp.b0 + k) * B;  // first row of the block (every segment starts on one)
+            const long long jb = rp.b0 + k;  // new block
+            const long long p = jb * B;      // its first row
             const long long valid = rp.new_len - p < B ? rp.new_len - p : B;
             const Seg* sg = pv.segs + rp.seg_begin;
             const Seg s = sg[find_seg(sg, rp.seg_count, p)];
             int page;
-            if (s.kind == SEG_REPL) {
-                page = a.free_q[ring(a.pop_base + rp.pop_off + s.aux + (p - s.new_start) / B, a.q_cap)];
-                if (page < 0 || page >= a.g.num_pages) {
-                    raise_status(a.status, ST_BAD_FRESH);
-                    page = -1;
-                }
-                if (a.pending && page >= 0)  // R is encoded at its final position
-                    for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] = 0;
-            } else {
-                const long long ob = (s.src_start + (p - s.new_start)) / B;  // the old block kept
+            if (jb >= s.kb0 && jb < s.kb1) {  // kept: the old block holding exactly these rows
+                const long long ob = (s.src_start + (p - s.new_start)) / B;
                 page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
                 if (page < 0 || page >= a.g.num_pages) {
                     raise_status(a.status, ST_BAD_PAGE);
@@ -792,10 +786,17 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
                 }
                 if (a.pending && page >= 0 && s.turn != 0)  // the valid slots turn; the others stay 0
                     for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] += s.turn;
+            } else {  // fresh: the new block's position among the request's fresh blocks
+                const long long kept_before = s.kept_before + (jb < s.kb0 ? 0 : (long long)s.kb1 - s.kb0);
+                page = a.free_q[ring(a.pop_base + rp.pop_off + (k - kept_before), a.q_cap)];
+                if (page < 0 || page >= a.g.num_pages) {
+                    raise_status(a.status, ST_BAD_FRESH);
+                    page = -1;
+                }
             }
             a.stage[rp.stage_begin + k] = page;
         } else {
-            const long long j = k - blocks;  // j-th dropped block of the request
+            const long long j = k - blocks;  // j-th returned old block of the request
             const Seg* dg = pv.segs + rp.drop_seg_begin;
             int q = 0;
             for (int x = 1; x < rp.drop_seg_count; ++x)
@@ -807,7 +808,9 @@ __global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_
                 page = -1;
             }
             a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
-            if (a.pending && page >= 0)  // a free page carries no pending turn
+            // a free page carries no pending turn; when the fresh-rows kernel still reads
+            // survivors from the request's returned pages, the commit clears them instead
+            if (a.pending && page >= 0 && rp.fresh_seg_count == 0)
                 for (long long sl = 0; sl < B; ++sl) a.pending[(long long)page * B + sl] = 0;
         }
     }
@@ -823,21 +826,24 @@ __device__ __forceinline__ uint4 ld_rw(const uint4* p)
     return v;
 }
 
-// Re-index mode moves rows of R and turns bands in two kernels.
+// Re-index mode writes fresh rows and turns kept bands.
 //   copy_repl_reindex: the call's rows of R form one list; items of (row, 8 layers)
 //   are spread over every warp of the grid, a lane moving every 32nd vector of the
 //   row with four loads in flight.  A row of R moves 9 times the bytes of a turned
 //   band, so rows of R are not tied to one CTA's share of the tiles.
-//   rotate_in_place: each turned (ROT) segment is cut into 16-row tiles of its own
-//   (the planner numbers them in Seg::tile_off); survivors that keep their encoding
-//   -- every survivor of a lazy pool -- cost nothing.  Work unit = (tile, group of
-//   layers).  The threads' work items (4 per band and layer for half-split pairs, 8
-//   interleaved; at most kMaxItems per thread) are decoded once at kernel start, and
-//   the unit loop advances tile and layer group by counters, so a unit costs only
-//   its loads, its arithmetic and its stores.
+//   copy_fresh_reindex: the other rows of blocks that get fresh pages (survivors and
+//   prefix rows of boundary blocks), likewise spread over warps, read through the old
+//   table and turned by their segment's cos/sin.
+//   rotate_in_place: the kept rows of each turned (ROT) segment are cut into 16-row
+//   tiles of their own (the planner numbers them in Seg::tile_off); survivors that
+//   keep their encoding -- every survivor of a lazy pool -- cost nothing.  Work unit
+//   = (tile, group of layers).  The threads' work items (4 per band and layer for
+//   half-split pairs, 8 interleaved; at most kMaxItems per thread) are decoded once
+//   at kernel start, and the unit loop advances tile and layer group by counters, so
+//   a unit costs only its loads, its arithmetic and its stores.
 constexpr int kMaxRopeDim = 256;
 constexpr int kMaxItems = 4;    // work items per thread: rope_heads * rope_dim <= 512
-constexpr int kReplLayers = 8;  // layers per item of the rows-of-R phase
+constexpr int kFreshLayers = 8;  // layers per item of the fresh-rows kernel
 
 // Layers per work unit of the re-index rotate kernel: as many as give each of the
 // CTA's threads kItems work items (at least one layer).
@@ -859,12 +865,12 @@ __global__ void __launch_bounds__(kMoveThreads) copy_repl_reindex(const __grid_c
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     const long long L = a.g.num_layers;
-    const int chunks = (int)((L + kReplLayers - 1) / kReplLayers);
+    const int chunks = (int)((L + kFreshLayers - 1) / kFreshLayers);
     const int row_vecs = a.g.row_vecs, lv = a.g.latent_vecs;
     uint4* kv = static_cast<uint4*>(a.kv);
     for (long long w = gw; w < a.total_repl * chunks; w += nw) {
         const long long rrow = w / chunks;
-        const long long l0 = (w - rrow * chunks) * kReplLayers;
+        const long long l0 = (w - rrow * chunks) * kFreshLayers;
         const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, rrow, BY_REPL)];
         long long j = rrow - rp.repl_begin;  // row within the request's rows of R
         const Seg* sg = pv.segs + rp.seg_begin;
@@ -884,9 +890,10 @@ __global__ void __launch_bounds__(kMoveThreads) copy_repl_reindex(const __grid_c
         const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
         if (page < 0 || page >= a.g.num_pages) continue;  // prep has recorded a bad fresh page
         const long long slot = (long long)page * B + ((unsigned)p - pb * B);
+        if (a.pending && l0 == 0 && lane == 0) a.pending[slot] = 0;  // R is encoded at its final position
         const long long rstride = (long long)s.n_repl * row_vecs;
         const uint4* src = static_cast<const uint4*>(s.repl) + j * row_vecs;
-        const long long l1 = l0 + kReplLayers < L ? l0 + kReplLayers : L;
+        const long long l1 = l0 + kFreshLayers < L ? l0 + kFreshLayers : L;
         for (long long layer = l0; layer < l1; ++layer) {
             for (int c0 = 0; c0 < row_vecs; c0 += 4 * 32) {
                 uint4 v[4];
@@ -903,6 +910,151 @@ __global__ void __launch_bounds__(kMoveThreads) copy_repl_reindex(const __grid_c
                                   v[q]);
                 }
             }
+        }
+    }
+}
+
+
+// The part of a fresh row beyond the first 64 latent vectors and the first 32 band
+// items (wider rows than MLA), out of line so the common path keeps its registers.
+template <int kLayout, bool kBf16>
+__device__ __forceinline__ void copy_fresh_rest(const Geometry& g, const uint4* sl, uint4* dl, const uint4* sb,
+                                             uint4* db, const float* trig_table, int trig, int lane)
+{
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;
+    const int lv = g.latent_vecs, hv = g.head_vecs, half = g.rope_dim / 2;
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const int band_items = g.rope_heads * head_items;
+    for (int c = 64 + lane; c < lv; c += 32) st_stream(dl + c, ld_stream(sl + c));
+    for (int it = 32 + lane; it < band_items; it += 32) {
+        const int head = it / head_items, qi = it - head * head_items;
+        float cs[8], sn[8];
+        const float* tp = trig_table ? trig_table + 2 * ((long long)trig * half + kPairs * qi) : nullptr;
+        if (tp) {
+#pragma unroll
+            for (int u = 0; u < kPairs; ++u) {
+                cs[u] = tp[2 * u];
+                sn[u] = tp[2 * u + 1];
+            }
+        }
+        if (kLayout == 0) {
+            uint4 x = ld_stream(sb + head * hv + qi), y = ld_stream(sb + head * hv + qi + hv / 2);
+            if (tp) rotate_half_split<kBf16>(x, y, cs, sn);
+            st_stream(db + head * hv + qi, x);
+            st_stream(db + head * hv + qi + hv / 2, y);
+        } else {
+            uint4 x = ld_stream(sb + head * hv + qi);
+            if (tp) rotate_interleaved<kBf16>(x, cs, sn);
+            st_stream(db + head * hv + qi, x);
+        }
+    }
+}
+
+// Fresh rows of a re-indexed call other than rows of R: the survivors and prefix rows
+// of blocks that do not keep their pages, written into the fresh page prep staged for
+// their block.  A survivor is read through the old table and
+// turned by its segment's cos/sin; in a lazy pool its pending count moves with it.
+template <int kLayout, bool kBf16, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads, 3) copy_fresh_reindex(const __grid_constant__ SpliceArgs a,
+                                                                   const __grid_constant__ PlanSrc plan)
+{
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const int lane = threadIdx.x & 31;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long L = a.g.num_layers;
+    const int chunks = (int)((L + kFreshLayers - 1) / kFreshLayers);
+    const int row_vecs = a.g.row_vecs, lv = a.g.latent_vecs, hv = a.g.head_vecs, half = a.g.rope_dim / 2;
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;  // pairs per work item
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const int band_items = a.g.rope_heads * head_items;
+    const unsigned B = (unsigned)a.g.block_size;
+    uint4* kv = static_cast<uint4*>(a.kv);
+    for (long long w = gw; w < a.total_fresh * chunks; w += nw) {
+        const long long frow = w / chunks;
+        const long long l0 = (w - frow * chunks) * kFreshLayers;
+        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, frow, BY_FRESH)];
+        const long long f = frow - rp.fresh_begin;  // fresh row within the request
+        const Seg* fg = pv.segs + rp.fresh_seg_begin;
+        int q = 0;
+        for (int x = 1; x < rp.fresh_seg_count; ++x)
+            if (fg[x].aux <= f) q = x;
+        const long long p = fg[q].new_start + (f - fg[q].aux);  // its new row (rows fit 32 bits)
+        const Seg* sg = pv.segs + rp.seg_begin;
+        const Seg s = sg[find_seg(sg, rp.seg_count, p)];
+        const unsigned pb = (unsigned)p / B;
+        const int dpage = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
+        if (dpage < 0 || dpage >= a.g.num_pages) continue;  // prep has recorded a bad fresh page
+        const long long dslot = (long long)dpage * B + ((unsigned)p - pb * B);
+        const uint4 *src_lat, *src_band;
+        long long lat_stride, band_stride, sslot = -1;
+        if (s.kind == SEG_REPL) {
+            src_lat = static_cast<const uint4*>(s.repl) + (p - s.new_start) * row_vecs;
+            src_band = src_lat + lv;
+            lat_stride = band_stride = (long long)s.n_repl * row_vecs;
+        } else {
+            const long long t = s.src_start + (p - s.new_start);  // old row
+            const unsigned tb = (unsigned)t / B;
+            const int spage = (t >= 0 && (long long)tb < a.max_blocks) ? a.table[(long long)rp.req * a.max_blocks + tb]
+                                                                      : -1;
+            if (spage < 0 || spage >= a.g.num_pages) {
+                if (lane == 0) raise_status(a.status, ST_BAD_PAGE);
+                continue;
+            }
+            sslot = (long long)spage * B + ((unsigned)t - tb * B);
+            src_lat = kv + lat_off(a.g, 0, sslot);
+            src_band = kv + band_off(a.g, 0, sslot);
+            lat_stride = a.g.lat_layer_vecs;
+            band_stride = a.g.rope_layer_vecs;
+        }
+        if (a.pending && l0 == 0 && lane == 0)  // once per row: R at its final position, survivors carried
+            a.pending[dslot] = sslot < 0 ? 0 : a.pending[sslot] + s.turn;
+        const int trig = s.kind == SEG_ROT ? s.trig : -1;
+        const long long l1 = l0 + kFreshLayers < L ? l0 + kFreshLayers : L;
+        const bool band_lane = lane < band_items;  // this lane's first band item: it = lane
+        const int head0 = band_lane ? lane / head_items : 0, q0 = lane - head0 * head_items;
+        const float* tp0 = trig >= 0 ? pv.trig + 2 * ((long long)trig * half + kPairs * q0) : nullptr;
+#pragma unroll 1
+        for (long long layer = l0; layer < l1; ++layer) {
+            // one round per layer: the first 64 latent vectors (the MLA latent) and the first
+            // band item of every lane are loaded before anything is stored
+            const uint4* sl = src_lat + layer * lat_stride;
+            uint4* dl = kv + lat_off(a.g, layer, dslot);
+            const uint4* sb = src_band + layer * band_stride + head0 * hv + q0;
+            uint4* db = kv + band_off(a.g, layer, dslot) + head0 * hv + q0;
+            uint4 v0, v1, x, y;
+            if (lane < lv) v0 = ld_stream(sl + lane);
+            if (32 + lane < lv) v1 = ld_stream(sl + 32 + lane);
+            if (band_lane) {
+                x = ld_stream(sb);
+                if (kLayout == 0) y = ld_stream(sb + hv / 2);
+            }
+            if (lane < lv) st_stream(dl + lane, v0);
+            if (32 + lane < lv) st_stream(dl + 32 + lane, v1);
+            if (band_lane) {
+                float cs[8], sn[8];
+                if (tp0) {
+#pragma unroll
+                    for (int u = 0; u < kPairs; ++u) {
+                        cs[u] = tp0[2 * u];
+                        sn[u] = tp0[2 * u + 1];
+                    }
+                }
+                if (kLayout == 0) {
+                    if (tp0) rotate_half_split<kBf16>(x, y, cs, sn);
+                    st_stream(db, x);
+                    st_stream(db + hv / 2, y);
+                } else {
+                    if (tp0) rotate_interleaved<kBf16>(x, cs, sn);
+                    st_stream(db, x);
+                }
+            }
+            if (lv > 64 || band_items > 32)  // wider latents, more than 32 band items: out of line
+                copy_fresh_rest<kLayout, kBf16>(a.g, sl, dl, src_band + layer * band_stride,
+                                                kv + band_off(a.g, layer, dslot), trig >= 0 ? pv.trig : nullptr,
+                                                trig, lane);
         }
     }
 }
@@ -961,9 +1113,11 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 for (int q = 0; q < rp.seg_count; ++q)
                     if (sg[q].tile_off >= 0 && sg[q].tile_off <= lt) k = q;
                 const Seg s = sg[k];
-                const long long end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
-                const long long p = s.new_start + (lt - s.tile_off) * kTileRows + threadIdx.x;
-                if (p < end) {  // rows and block sizes fit 32 bits (the planner checks lengths)
+                const long long B0 = a.g.block_size;
+                const long long seg_end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
+                const long long kept_end = (long long)s.kb1 * B0 < seg_end ? (long long)s.kb1 * B0 : seg_end;
+                const long long p = (long long)s.kb0 * B0 + (lt - s.tile_off) * kTileRows + threadIdx.x;
+                if (p < kept_end) {  // rows and block sizes fit 32 bits (the planner checks lengths)
                     const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
                     const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
                     if (page >= 0 && page < a.g.num_pages)
@@ -1010,7 +1164,8 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
 }
 
 // Commit of a re-indexed call: staged entries into the new blocks [b0, new end),
-// -1 into the blocks past the new end, the new length.  The staged values are final before the
+// -1 into the blocks past the new end, the new length, and (lazy pools) pending
+// counts of 0 on the returned pages.  The staged values are final before the
 // rotate kernel starts and it never writes them, so they are loaded before
 // griddepcontrol.wait.
 template <class PlanSrc>
@@ -1035,9 +1190,18 @@ __global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_co
         int32_t* trow = a.table_w + (long long)rp->req * a.max_blocks;
         const long long nb_new = (rp->new_len + B - 1) / B, nb_old = (rp->old_len + B - 1) / B;
         const long long blocks = nb_new - rp->b0;
+        const long long tail = nb_old > nb_new ? nb_old - nb_new : 0;
         if (k == 0) a.seq_lens_dev[rp->req] = (int32_t)rp->new_len;
-        if (k < blocks) trow[rp->b0 + k] = val;
-        else if (nb_new + (k - blocks) < nb_old) trow[nb_new + (k - blocks)] = -1;
+        if (k < blocks) {
+            trow[rp->b0 + k] = val;
+        } else if (k < blocks + tail) {
+            trow[nb_new + (k - blocks)] = -1;
+        } else if (a.pending && rp->fresh_seg_count > 0 && k < blocks + tail + rp->drop_count) {
+            // a returned page carries no pending turn (its rows have been read by now)
+            const int page = a.free_q[ring(a.push_base + rp->push_off + (k - blocks - tail), a.q_cap)];
+            if (page >= 0 && page < a.g.num_pages)
+                for (long long sl = 0; sl < B; ++sl) a.pending[(long long)page * B + sl] = 0;
+        }
         i += stride;
         if (i >= a.total_commit) break;
         rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
@@ -1303,10 +1467,17 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);
     if (e == cudaSuccess && t0) e = cudaEventRecord(t0, s);
-    if (e == cudaSuccess && a.total_repl > 0) {  // rows of R: items of (row, kReplLayers layers), a warp each
-        const long long items = a.total_repl * ((a.g.num_layers + kReplLayers - 1) / kReplLayers);
+    if (e == cudaSuccess && a.total_repl > 0) {  // rows of R: items of (row, kFreshLayers layers), a warp each
+        const long long items = a.total_repl * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
         e = launch_dependent(copy_repl_reindex<PlanSrc>, grid_for(items * 32, kMoveThreads, 8192), kMoveThreads, s,
                              a, plan);
+    }
+    if (e == cudaSuccess && a.total_fresh > 0) {  // other fresh rows: items of (row, kFreshLayers layers)
+        const long long items = a.total_fresh * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
+        const int fgrid = grid_for(items * 32, kMoveThreads, 8192);
+        auto k = split ? (bf16 ? copy_fresh_reindex<0, true, PlanSrc> : copy_fresh_reindex<0, false, PlanSrc>)
+                       : (bf16 ? copy_fresh_reindex<1, true, PlanSrc> : copy_fresh_reindex<1, false, PlanSrc>);
+        e = launch_dependent(k, fgrid, kMoveThreads, s, a, plan);
     }
     if (e == cudaSuccess && units > 0) {
         if (split)

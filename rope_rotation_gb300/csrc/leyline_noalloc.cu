@@ -160,6 +160,7 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
         a.stage = reinterpret_cast<int32_t*>(scratch + off_stage);
         a.total_prep = plan.total_prep;
         a.total_repl = plan.total_repl;
+        a.total_fresh = plan.total_fresh;
         a.reindex = 1;
     }
     a.status = p->d_status;

@@ -25,7 +25,10 @@ namespace leyline {
 
 constexpr int kTileRows = 16;  // destination rows per move+rotate tile
 
-enum SegKind : int32_t { SEG_HEAD = 0, SEG_REPL = 1, SEG_COPY = 2, SEG_ROT = 3, SEG_DROP = 4 };
+// Row segments (HEAD, REPL, COPY, ROT) cover a request's new rows [row0, new_len) in
+// order.  Re-index mode adds two lists after them: DROP runs of old blocks returned to
+// the free list, and FRESH runs of new rows written into fresh pages.
+enum SegKind : int32_t { SEG_HEAD = 0, SEG_REPL = 1, SEG_COPY = 2, SEG_ROT = 3, SEG_DROP = 4, SEG_FRESH = 5 };
 
 struct Geometry {
     int32_t num_layers;
@@ -73,10 +76,13 @@ struct ReqPlan {
     int32_t push_off;      // first returned page of this request in the ring's push region
     int64_t stage_begin;   // re-index: first staged table entry of this request
     int64_t prep_begin;    // re-index: first flat prep item of this request
-    int64_t drop_count;    // re-index: blocks dropped (pages returned)
-    int32_t drop_seg_begin;
+    int64_t drop_count;    // re-index: old blocks returned to the free list
+    int32_t drop_seg_begin;  // re-index: DROP runs (old blocks returned)
     int32_t drop_seg_count;
-    int64_t repl_begin;    // re-index: first row of R of this request in the call's list of rows of R
+    int64_t repl_begin;    // re-index: first of this request's rows of R in the call's list of them
+    int64_t fresh_begin;   // re-index: first of this request's other fresh rows in the call's list
+    int32_t fresh_seg_begin;  // re-index: FRESH runs (survivor and prefix rows written into fresh pages)
+    int32_t fresh_seg_count;
 };
 
 struct Seg {
@@ -89,11 +95,15 @@ struct Seg {
     int32_t aux;           // re-index: R rows of the request before this segment (REPL),
                            // dropped tokens of the request before this segment (DROP)
     int32_t turn;          // positions the segment's rows turn (ROT; in lazy pools also COPY)
-    int32_t tile_off;      // re-index: first rotate-kernel tile of this ROT segment within its
-                           // request, -1 for other segments
+    int32_t tile_off;      // re-index: first rotate-kernel tile of this ROT segment's kept rows
+                           // within its request, -1 for other segments
+    int32_t kb0, kb1;      // re-index, COPY/ROT: new blocks [kb0, kb1) keep their old pages
+                           // (block kb0 - shift / B ...), all rows of the segment; else kb0 = kb1
+    int32_t kept_before;   // re-index: kept blocks of the request's earlier segments
+    int32_t pad2;
 };
 
-static_assert(sizeof(ReqPlan) == 112, "ReqPlan layout");
-static_assert(sizeof(Seg) == 48, "Seg layout");
+static_assert(sizeof(ReqPlan) == 128, "ReqPlan layout");
+static_assert(sizeof(Seg) == 64, "Seg layout");
 
 }  // namespace leyline

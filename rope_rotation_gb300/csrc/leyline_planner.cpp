@@ -139,6 +139,219 @@ int make_geometry(const leyline_pool_desc_t* d, Geometry* g)
     return LEYLINE_OK;
 }
 
+namespace {
+
+struct PlanCounts {
+    int64_t kept_rows = 0;          // re-index: rows whose blocks keep their pages
+    int64_t kept_turned_rows = 0;   // of which turned in place
+    int64_t fresh_rows = 0;         // survivor and prefix rows written into fresh pages
+    int64_t fresh_head_rows = 0;    // of which unchanged prefix rows of a boundary block
+    int64_t fresh_repl_rows = 0;    // rows of R (written into fresh pages too)
+};
+
+// Segments, pages and work counts of every touched request, as a rewrite (reindex =
+// false) or re-indexed (true).  Directives are validated and ordered by request and
+// s_start (order).
+int plan_requests(const Geometry& g, const int64_t* seq_lens_host, int32_t max_blocks,
+                  const leyline_directive_t* dirs, int32_t n, const std::vector<int32_t>& order, bool reindex,
+                  bool lazy, Plan* plan, PlanCounts* counts, char* msg, size_t msg_size)
+{
+    const int64_t B = g.block_size;
+    plan->reindex = reindex;
+    int64_t tiles = 0, commit = 0, pops = 0, pushes = 0;
+    leyline_stats_t& st = plan->stats;
+    for (int32_t i = 0; i < n;) {
+        const int32_t req = dirs[order[i]].req;
+        int32_t j = i;
+        std::vector<const leyline_directive_t*> eff;
+        for (; j < n && dirs[order[j]].req == req; ++j) {
+            const leyline_directive_t* d = &dirs[order[j]];
+            if (d->s_start == d->s_end && d->n_repl == 0) continue;  // no-op
+            eff.push_back(d);
+        }
+        i = j;
+        if (eff.empty()) continue;
+
+        const int64_t L = seq_lens_host[req];
+        if (L > (int64_t)max_blocks * B) {
+            snprintf(msg, msg_size, "request %d: seq_len %lld exceeds the table capacity", req, (long long)L);
+            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+        }
+        int64_t delta_total = 0;
+        for (const auto* d : eff) delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
+        const int64_t Lp = L + delta_total;
+        if (Lp > (int64_t)max_blocks * B || Lp > INT32_MAX) {
+            snprintf(msg, msg_size, "request %d: new length %lld exceeds the table capacity %lld", req,
+                     (long long)Lp, (long long)max_blocks * B);
+            return set_error(LEYLINE_ERR_CAPACITY, msg);
+        }
+        ReqPlan rp{};
+        rp.req = req;
+        rp.b0 = (int32_t)(eff.front()->s_start / B);
+        rp.row0 = (int64_t)rp.b0 * B;
+        rp.old_len = L;
+        rp.new_len = Lp;
+        rp.seg_begin = (int32_t)plan->segs.size();
+        rp.pop_off = (int32_t)pops;
+        rp.push_off = (int32_t)pushes;
+        rp.tile_begin = tiles;
+        rp.commit_begin = commit;
+
+        // row segments in new coordinates.  D: index shift left of the current position
+        // (every directive); A: rotation (AMORTIZE directives only, section 2.1; EVICT
+        // keeps positions).
+        const int64_t s1 = eff.front()->s_start;
+        if (rp.row0 < s1) {
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
+            plan->segs.push_back(s);
+            st.head_slots += s1 - rp.row0;
+        }
+        int64_t D = 0, A = 0;
+        for (size_t k = 0; k < eff.size(); ++k) {
+            const leyline_directive_t* d = eff[k];
+            if (d->n_repl > 0) {
+                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, 0, 0, 0};
+                plan->segs.push_back(s);
+                st.repl_slots += d->n_repl;
+            }
+            const int64_t dk = (int64_t)d->n_repl - (d->s_end - d->s_start);
+            D += dk;
+            if (d->mode == LEYLINE_AMORTIZE) A += dk;
+            const int64_t run_end = (k + 1 < eff.size()) ? eff[k + 1]->s_start : L;
+            if (run_end > d->s_end) {
+                Seg s{d->s_end + D, d->s_end, nullptr, (A == 0 || lazy) ? SEG_COPY : SEG_ROT, -1, 0, 0, (int32_t)A,
+                      0};
+                if (A != 0 && !lazy) {
+                    s.trig = plan->n_trig++;
+                    plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
+                    segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                }
+                plan->segs.push_back(s);
+                st.downstream_slots += run_end - d->s_end;
+            }
+        }
+        rp.seg_count = (int32_t)plan->segs.size() - rp.seg_begin;
+        if (rp.seg_count == 0) {  // nothing left to write (pure truncation at a block boundary)
+            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
+            plan->segs.push_back(s);
+            rp.seg_count = 1;
+        }
+        const int64_t nb_new = ceil_div(Lp, B), nb_old = ceil_div(L, B);
+        if (!reindex) {
+            rp.n_new = (int32_t)(nb_new - rp.b0);
+            rp.n_old = (int32_t)(nb_old - rp.b0);
+            tiles += ceil_div(Lp - rp.row0, kTileRows);
+            commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
+        } else {
+            // Kept blocks: new block j keeps its old page when every row of it comes from one
+            // COPY/ROT segment whose shift is a multiple of B (then old block j - shift / B
+            // holds exactly those rows).  Every other new block gets a fresh page, written
+            // row by row; every old block not kept returns to the free list.
+            const int32_t last = rp.seg_begin + rp.seg_count;
+            int64_t kept = 0, wt = 0;
+            for (int32_t k = rp.seg_begin; k < last; ++k) {
+                Seg& s = plan->segs[k];
+                const int64_t end = k + 1 < last ? plan->segs[k + 1].new_start : Lp;
+                s.kept_before = (int32_t)kept;
+                s.kb0 = s.kb1 = 0;
+                s.tile_off = -1;
+                const int64_t shift = s.new_start - s.src_start;
+                if ((s.kind == SEG_COPY || s.kind == SEG_ROT) && end > s.new_start && shift % B == 0) {
+                    const int64_t k0 = ceil_div(s.new_start, B);
+                    const int64_t k1 = end == Lp ? nb_new : end / B;  // a last partial block moves whole
+                    if (k1 > k0) {
+                        s.kb0 = (int32_t)k0;
+                        s.kb1 = (int32_t)k1;
+                        kept += k1 - k0;
+                        const int64_t kr = std::min(k1 * B, end) - k0 * B;  // kept rows
+                        counts->kept_rows += kr;
+                        if (s.kind == SEG_ROT) {
+                            s.tile_off = (int32_t)wt;
+                            wt += ceil_div(kr, kTileRows);
+                            counts->kept_turned_rows += kr;
+                        } else if (lazy && s.turn != 0) {
+                            counts->kept_turned_rows += kr;
+                        }
+                    }
+                }
+            }
+            tiles += wt;
+            rp.n_new = (int32_t)(nb_new - rp.b0 - kept);  // fresh pages
+            rp.n_old = (int32_t)(nb_old - rp.b0 - kept);  // pages returned
+            // Rows of the fresh blocks: rows of R (one list per call), and FRESH runs of the
+            // other rows (survivors and prefix rows of segments outside their kept blocks)
+            rp.repl_begin = plan->total_repl;
+            rp.fresh_seg_begin = (int32_t)plan->segs.size();
+            rp.fresh_begin = plan->total_fresh;
+            int64_t fresh = 0;
+            auto fresh_run = [&](int64_t r0, int64_t r1) {
+                if (r1 <= r0) return;
+                Seg f{r0, 0, nullptr, SEG_FRESH, -1, (int32_t)(r1 - r0), (int32_t)fresh, 0, 0};
+                plan->segs.push_back(f);
+                fresh += r1 - r0;
+            };
+            for (int32_t k = rp.seg_begin; k < last; ++k) {
+                const Seg s = plan->segs[k];
+                const int64_t end = k + 1 < last ? plan->segs[k + 1].new_start : Lp;
+                if (s.kind == SEG_REPL) {
+                    plan->total_repl += s.n_repl;
+                    counts->fresh_repl_rows += s.n_repl;
+                } else if (s.kb1 > s.kb0) {
+                    fresh_run(s.new_start, (int64_t)s.kb0 * B);
+                    fresh_run(std::min((int64_t)s.kb1 * B, end), end);
+                } else {
+                    fresh_run(s.new_start, end);
+                }
+            }
+            rp.fresh_seg_count = (int32_t)plan->segs.size() - rp.fresh_seg_begin;
+            plan->total_fresh += fresh;
+            counts->fresh_rows += fresh;
+            // rows of the first block before the first directive are unchanged prefix rows
+            counts->fresh_head_rows += s1 - rp.row0;
+            // DROP runs: old blocks [b0, nb_old) minus the kept ones, in order
+            rp.drop_seg_begin = (int32_t)plan->segs.size();
+            int64_t ob = rp.b0, pushed = 0;
+            auto drop_run = [&](int64_t o0, int64_t o1) {
+                if (o1 <= o0) return;
+                Seg d{-1, o0, nullptr, SEG_DROP, -1, (int32_t)(o1 - o0), (int32_t)pushed, 0, 0};
+                plan->segs.push_back(d);
+                pushed += o1 - o0;
+            };
+            for (int32_t k = rp.seg_begin; k < last; ++k) {
+                const Seg s = plan->segs[k];
+                if (s.kb1 > s.kb0) {
+                    const int64_t sb = (s.new_start - s.src_start) / B;  // block shift
+                    drop_run(ob, s.kb0 - sb);
+                    ob = s.kb1 - sb;
+                }
+            }
+            drop_run(ob, nb_old);
+            rp.drop_seg_count = (int32_t)plan->segs.size() - rp.drop_seg_begin;
+            rp.drop_count = pushed;
+            rp.stage_begin = plan->total_stage;
+            rp.prep_begin = plan->total_prep;
+            const int64_t new_blocks = nb_new - rp.b0;
+            plan->total_stage += new_blocks;
+            plan->total_prep += new_blocks + pushed;
+            const int64_t tail = std::max<int64_t>(0, nb_old - nb_new);  // entries past the new end
+            // lazy pools clear the counts of returned pages: at prep, or at commit when the
+            // fresh-rows kernel still reads survivors from them (the request has FRESH runs)
+            const int64_t clears = (lazy && rp.fresh_seg_count > 0) ? pushed : 0;
+            commit += std::max<int64_t>(1, new_blocks + tail + clears);
+        }
+        pops += rp.n_new;
+        pushes += rp.n_old;
+        plan->reqs.push_back(rp);
+    }
+    plan->total_tiles = tiles;
+    plan->total_commit = commit;
+    plan->total_pop = pops;
+    plan->total_push = pushes;
+    return LEYLINE_OK;
+}
+
+}  // namespace
+
 int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs, int32_t max_blocks,
                const leyline_directive_t* dirs, int32_t n, int64_t free_pages, Plan* plan)
 {
@@ -203,195 +416,53 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         }
     }
 
-    // 3. plan each touched request
-    // re-index: block size 1, or every directive of the call on block boundaries (the
-    // splice then drops, inserts and shifts whole pages)
-    bool reindex = (g.flags & LEYLINE_POOL_REINDEX) != 0;
-    if (reindex && B > 1) {
-        for (int32_t k = 0; k < n && reindex; ++k) {
-            const leyline_directive_t& d = dirs[k];
-            if (d.s_start == d.s_end && d.n_repl == 0) continue;
-            const bool to_end = d.s_end == seq_lens_host[d.req];
-            reindex = d.s_start % B == 0 && (d.s_end % B == 0 || to_end) && (d.n_repl % B == 0 || to_end);
-        }
-    }
+    // 3. plan each touched request.  Re-index pools keep the pages of surviving blocks
+    // whose rows all shift by a multiple of the block size and write the other blocks'
+    // rows into fresh pages.  With pages of several slots, a call whose fresh pages take
+    // more survivor and prefix rows than the kept pages hold is planned as a rewrite: the
+    // rewrite kernel moves whole rows faster than the fresh-rows kernel.  (Rows of R are
+    // written by their own kernel in either plan.)
     const bool lazy = (g.flags & LEYLINE_POOL_LAZY) != 0;
-    plan->reindex = reindex;
-    const int64_t row_bytes = (int64_t)g.row_elems * 2;
-    const int64_t rope_bytes = (int64_t)g.rope_vecs * 16;  // every RoPE band of a row
-    int64_t tiles = 0, commit = 0, pops = 0, pushes = 0, turned_rows = 0;
-    leyline_stats_t& st = plan->stats;
-    for (int32_t i = 0; i < n;) {
-        const int32_t req = dirs[order[i]].req;
-        int32_t j = i;
-        std::vector<const leyline_directive_t*> eff;
-        for (; j < n && dirs[order[j]].req == req; ++j) {
-            const leyline_directive_t* d = &dirs[order[j]];
-            if (d->s_start == d->s_end && d->n_repl == 0) continue;  // no-op
-            eff.push_back(d);
-        }
-        i = j;
-        if (eff.empty()) continue;
-
-        const int64_t L = seq_lens_host[req];
-        if (L > (int64_t)max_blocks * B) {
-            snprintf(msg, sizeof msg, "request %d: seq_len %lld exceeds the table capacity", req, (long long)L);
-            return set_error(LEYLINE_ERR_INVALID_ARG, msg);
-        }
-        int64_t delta_total = 0;
-        for (const auto* d : eff) {
-            delta_total += (int64_t)d->n_repl - (d->s_end - d->s_start);
-        }
-        const int64_t Lp = L + delta_total;
-        if (Lp > (int64_t)max_blocks * B || Lp > INT32_MAX) {
-            snprintf(msg, sizeof msg, "request %d: new length %lld exceeds the table capacity %lld", req,
-                     (long long)Lp, (long long)max_blocks * B);
-            return set_error(LEYLINE_ERR_CAPACITY, msg);
-        }
-        ReqPlan rp{};
-        rp.req = req;
-        rp.b0 = (int32_t)(eff.front()->s_start / B);
-        rp.row0 = (int64_t)rp.b0 * B;
-        rp.old_len = L;
-        rp.new_len = Lp;
-        int64_t repl_blocks = 0, drop_blocks = 0;
-        for (const auto* d : eff) {
-            repl_blocks += ceil_div(d->n_repl, B);
-            if (d->s_end > d->s_start) drop_blocks += ceil_div(d->s_end, B) - d->s_start / B;
-        }
-        if (reindex) {
-            rp.n_new = (int32_t)repl_blocks;  // fresh pages: the blocks of R
-            rp.n_old = (int32_t)drop_blocks;  // returned pages: the dropped blocks
-        } else {
-            rp.n_new = (int32_t)(ceil_div(Lp, B) - rp.b0);
-            rp.n_old = (int32_t)(ceil_div(L, B) - rp.b0);
-        }
-        rp.seg_begin = (int32_t)plan->segs.size();
-        rp.pop_off = (int32_t)pops;
-        rp.push_off = (int32_t)pushes;
-        rp.tile_begin = tiles;
-        rp.commit_begin = commit;
-
-        // segments in new coordinates.  D: index shift left of the current position
-        // (every directive); A: rotation (AMORTIZE directives only, section 2.1; EVICT
-        // keeps positions).
-        const int64_t s1 = eff.front()->s_start;
-        if (rp.row0 < s1) {
-            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
-            plan->segs.push_back(s);
-            st.head_slots += s1 - rp.row0;
-        }
-        int64_t D = 0, A = 0, pops_before = 0;
-        for (size_t k = 0; k < eff.size(); ++k) {
-            const leyline_directive_t* d = eff[k];
-            if (d->n_repl > 0) {
-                // aux: fresh pages of the request's earlier R segments (re-index mode)
-                Seg s{d->s_start + D, 0, d->repl_rows, SEG_REPL, -1, d->n_repl, (int32_t)pops_before, 0, 0};
-                plan->segs.push_back(s);
-                st.repl_slots += d->n_repl;
-                pops_before += ceil_div(d->n_repl, B);
-            }
-            const int64_t dk = (int64_t)d->n_repl - (d->s_end - d->s_start);
-            D += dk;
-            if (d->mode == LEYLINE_AMORTIZE) A += dk;
-            const int64_t run_end = (k + 1 < eff.size()) ? eff[k + 1]->s_start : L;
-            if (run_end > d->s_end) {
-                Seg s{d->s_end + D, d->s_end, nullptr, (A == 0 || lazy) ? SEG_COPY : SEG_ROT, -1, 0, 0, (int32_t)A,
-                      0};
-                if (A != 0) {
-                    if (!lazy) {
-                        s.trig = plan->n_trig++;
-                        plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
-                        segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
-                    }
-                    turned_rows += run_end - d->s_end;
-                }
-                plan->segs.push_back(s);
-                st.downstream_slots += run_end - d->s_end;
-            }
-        }
-        rp.seg_count = (int32_t)plan->segs.size() - rp.seg_begin;
-        if (rp.seg_count == 0) {  // nothing left to write (pure truncation at a block boundary)
-            Seg s{rp.row0, rp.row0, nullptr, SEG_HEAD, -1, 0, 0, 0, 0};
-            plan->segs.push_back(s);
-            rp.seg_count = 1;
-        }
-        const int64_t rows = Lp - rp.row0;
-        if (reindex) {
-            // the rotate kernel's tiles cover ROT segments only, each cut on its own; rows of
-            // R form one list for the whole call
-            rp.repl_begin = plan->total_repl;
-            for (int32_t k = rp.seg_begin; k < rp.seg_begin + rp.seg_count; ++k)
-                if (plan->segs[k].kind == SEG_REPL) plan->total_repl += plan->segs[k].n_repl;
-            int64_t wt = 0;
-            const int32_t last = rp.seg_begin + rp.seg_count;
-            for (int32_t k = rp.seg_begin; k < last; ++k) {
-                Seg& s = plan->segs[k];
-                const int64_t end = k + 1 < last ? plan->segs[k + 1].new_start : Lp;
-                s.tile_off = -1;
-                if (s.kind == SEG_ROT && end > s.new_start) {
-                    s.tile_off = (int32_t)wt;
-                    wt += ceil_div(end - s.new_start, kTileRows);
-                }
-            }
-            tiles += wt;
-        } else {
-            tiles += ceil_div(rows, kTileRows);
-        }
-        if (reindex) {
-            // in block units: DROP segments name the first dropped block and the dropped
-            // blocks before them; the stage holds one page per new block from b0 on
-            rp.drop_seg_begin = (int32_t)plan->segs.size();
-            int64_t drops_before = 0;
-            for (const auto* d : eff) {
-                if (d->s_end == d->s_start) continue;
-                const int64_t nb = ceil_div(d->s_end, B) - d->s_start / B;
-                Seg s{-1, d->s_start / B, nullptr, SEG_DROP, -1, (int32_t)nb, (int32_t)drops_before, 0, 0};
-                plan->segs.push_back(s);
-                drops_before += nb;
-            }
-            rp.drop_seg_count = (int32_t)plan->segs.size() - rp.drop_seg_begin;
-            rp.drop_count = drop_blocks;
-            rp.stage_begin = plan->total_stage;
-            rp.prep_begin = plan->total_prep;
-            const int64_t new_blocks = ceil_div(Lp, B) - rp.b0;
-            plan->total_stage += new_blocks;
-            plan->total_prep += new_blocks + drop_blocks;
-            const int64_t tail = std::max<int64_t>(0, ceil_div(L, B) - ceil_div(Lp, B));  // entries past the new end
-            commit += std::max<int64_t>(1, new_blocks + tail);
-        } else {
-            commit += std::max<int64_t>(1, std::max(rp.n_new, rp.n_old));
-        }
-        pops += rp.n_new;
-        pushes += rp.n_old;
-        plan->reqs.push_back(rp);
+    PlanCounts counts;
+    int rc = plan_requests(g, seq_lens_host, max_blocks, dirs, n, order, (g.flags & LEYLINE_POOL_REINDEX) != 0, lazy,
+                           plan, &counts, msg, sizeof msg);
+    if (rc != LEYLINE_OK) return rc;
+    if (plan->reindex && B > 1 && counts.kept_rows < counts.fresh_rows) {
+        *plan = Plan{};
+        counts = PlanCounts{};
+        rc = plan_requests(g, seq_lens_host, max_blocks, dirs, n, order, false, lazy, plan, &counts, msg, sizeof msg);
+        if (rc != LEYLINE_OK) return rc;
     }
+    const bool reindex = plan->reindex;
 
-    if (free_pages >= 0 && pops > free_pages) {
-        snprintf(msg, sizeof msg, "splice needs %lld fresh pages, %lld free", (long long)pops, (long long)free_pages);
+    if (free_pages >= 0 && plan->total_pop > free_pages) {
+        snprintf(msg, sizeof msg, "splice needs %lld fresh pages, %lld free", (long long)plan->total_pop,
+                 (long long)free_pages);
         return set_error(LEYLINE_ERR_NO_PAGES, msg);
     }
-    plan->total_tiles = tiles;
-    plan->total_commit = commit;
-    plan->total_pop = pops;
-    plan->total_push = pushes;
-    if (reindex && lazy) {  // survivors keep page and bits: only their pending counts change
-        st.algorithmic_bytes = 2 * row_bytes * g.num_layers * st.repl_slots + 8 * turned_rows;
-        st.moved_bytes = st.algorithmic_bytes;
-    } else if (reindex) {
-        st.algorithmic_bytes = 2 * g.num_layers * (rope_bytes * turned_rows + row_bytes * st.repl_slots);
-        st.moved_bytes = st.algorithmic_bytes;
+    const int64_t row_bytes = (int64_t)g.row_elems * 2;
+    const int64_t rope_bytes = (int64_t)g.rope_vecs * 16;  // every RoPE band of a row
+    leyline_stats_t& st = plan->stats;
+    const int64_t L2 = 2 * (int64_t)g.num_layers;
+    if (reindex) {
+        // kept rows: turned bands in place (lazy: the 4-byte count read and written);
+        // fresh rows: whole rows of R and of boundary survivors, head rows as overhead
+        const int64_t fresh_alg = plan->total_repl + plan->total_fresh - counts.fresh_head_rows;
+        st.algorithmic_bytes = lazy ? L2 * row_bytes * fresh_alg + 8 * (counts.kept_turned_rows + fresh_alg)
+                                    : L2 * (rope_bytes * counts.kept_turned_rows + row_bytes * fresh_alg);
+        st.moved_bytes = st.algorithmic_bytes + L2 * row_bytes * counts.fresh_head_rows;
     } else {
-        st.algorithmic_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots);
-        st.moved_bytes = 2 * row_bytes * g.num_layers * (st.downstream_slots + st.repl_slots + st.head_slots);
+        st.algorithmic_bytes = L2 * row_bytes * (st.downstream_slots + st.repl_slots);
+        st.moved_bytes = L2 * row_bytes * (st.downstream_slots + st.repl_slots + st.head_slots);
     }
-    st.pages_popped = pops;
-    st.pages_pushed = pushes;
+    st.pages_popped = plan->total_pop;
+    st.pages_pushed = plan->total_push;
     st.requests_touched = (int32_t)plan->reqs.size();
-    // re-index: prep, the rows of R (if any), the in-place rotation (if any turned rows), commit
-    st.kernels_launched = plan->reqs.empty() ? 0
-                          : reindex          ? 2 + (plan->total_repl > 0) + (plan->total_tiles > 0)
-                                             : 2;
+    // re-index: prep, rows of R, other fresh rows, the in-place rotation (each if any), commit
+    st.kernels_launched =
+        plan->reqs.empty() ? 0
+        : reindex          ? 2 + (plan->total_repl > 0) + (plan->total_fresh > 0) + (plan->total_tiles > 0)
+                           : 2;
     st.reindexed = (!plan->reqs.empty() && reindex) ? 1 : 0;
     return LEYLINE_OK;
 }

@@ -389,6 +389,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         a.stage = p->d_stage;
         a.total_prep = plan.total_prep;
         a.total_repl = plan.total_repl;
+        a.total_fresh = plan.total_fresh;
         a.reindex = 1;
     }
     rc = order_after_previous(p, stream);

@@ -162,27 +162,36 @@ def test_noop_directives_touch_nothing(L):
     assert st.requests_touched == 0 and st.kernels_launched == 0 and st.pages_popped == 0
 
 
-def test_reindex_pages_only_on_block_boundaries(L):
-    """Re-index pools with 16-slot pages re-index a call only when every directive lies on
-    block boundaries (s_start a multiple of 16; s_end and |R| multiples of 16 unless
-    s_end = seq_len); pages are then counted in blocks."""
+def test_reindex_keeps_pages_of_runs_shifted_by_whole_blocks(L):
+    """Re-index pools with 16-slot pages keep the page of every new block whose rows all come
+    from one surviving run shifted by a multiple of 16 (that old block holds exactly those
+    rows); every other new block gets a fresh page and every old block not kept is returned.
+    A call whose fresh pages would take more survivor and prefix rows than the kept pages
+    hold is rewritten instead (same page counts when nothing is kept).  Counts worked out by
+    hand for a 163-token and a 64-token request."""
     desc = L.pool_desc(4, 16, 1 << 20, flags=L.LEYLINE_POOL_REINDEX)
     lens = [16 * 10 + 3, 64]
-    cases = [
-        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 16, 0)], 3, 1, 3),
-        ([_d(L, 0, 48, 163, 5)], 3, 1, 8),                       # to the end, partial blocks
-        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 17, 0)], 2, None, None),  # s_end off the grid
-        ([_d(L, 0, 32, 64, 3)], 2, None, None),                  # |R| off the grid
-        ([_d(L, 0, 40, 64, 16)], 2, None, None),                 # s_start off the grid
-        ([_d(L, 0, 160, 160, 16)], 3, 1, 0),                     # the partial last block moves whole
-        ([_d(L, 0, 163, 163, 16)], 2, None, None),               # insertion inside it
+    cases = [  # directives, re-indexed, pages popped, pages pushed
+        # Delta -16: blocks 3..9 kept (old 4..10), R in fresh block 2; request 1 keeps 0..2
+        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 16, 0)], 1, 1, 3),
+        ([_d(L, 0, 48, 163, 5)], 1, 1, 8),                        # to the end: block 3 fresh
+        # request 1: Delta -17 keeps nothing, its 47 survivors go to 3 fresh pages; request 0
+        # keeps 99 rows, so the call is re-indexed
+        ([_d(L, 0, 32, 64, 16), _d(L, 1, 0, 17, 0)], 1, 4, 6),
+        ([_d(L, 0, 32, 64, 3)], 0, 7, 9),                         # Delta -29: nothing kept, rewritten
+        ([_d(L, 0, 40, 64, 16)], 0, 8, 9),                        # Delta -8: nothing kept, rewritten
+        ([_d(L, 0, 160, 160, 16)], 1, 1, 0),                      # the partial last block moves whole
+        ([_d(L, 0, 163, 163, 16)], 0, 2, 1),                      # appended inside it: rewritten
+        # Delta = 18 - 34 = -16 with s_start off the grid: blocks 1 and 2 get fresh pages (head
+        # rows 16..19, rows of R, survivors 38..47), blocks 3..9 keep old blocks 4..10, old
+        # blocks 1..3 are returned
+        ([_d(L, 0, 20, 54, 18)], 1, 2, 3),
     ]
-    for dirs, kernels, pops, pushes in cases:
+    for dirs, reindexed, pops, pushes in cases:
         st, new = _plan(L, lens, dirs, desc=desc)
-        assert st.reindexed == (kernels == 3), [(d.s_start, d.s_end, d.n_repl) for d in dirs]
-        if pops is not None:
-            assert (st.pages_popped, st.pages_pushed) == (pops, pushes)
-    # block size 1: every call re-indexes, one page per row
+        got = (st.reindexed, st.pages_popped, st.pages_pushed)
+        assert got == (reindexed, pops, pushes), [(d.s_start, d.s_end, d.n_repl) for d in dirs]
+    # block size 1: every row of R gets a fresh page, every dropped token returns one
     st, _ = _plan(L, [100], [_d(L, 0, 3, 50, 7)], B=1, desc=L.pool_desc(4, 1, 1 << 20, flags=L.LEYLINE_POOL_REINDEX))
     assert (st.reindexed, st.kernels_launched, st.pages_popped, st.pages_pushed) == (1, 4, 7, 47)
 

@@ -88,6 +88,52 @@ def test_fuzz_block_grid(seed):
     cache.close()
 
 
+def _shift_aligned_steps(rng, lengths, n_steps, B):
+    """Random spans, with |R| chosen half the time so that Delta is a multiple of B (the
+    survivors' whole blocks then keep their pages)."""
+    lens = list(lengths)
+    steps, key = [], 0
+    for _ in range(n_steps):
+        step = []
+        for r, L in enumerate(lens):
+            s = int(rng.integers(0, L + 1))
+            e = int(rng.integers(s, min(L, s + 5 * B) + 1))
+            n = int(rng.integers(0, 3 * B))
+            if rng.random() < 0.5:
+                n = (e - s) % B + B * int(rng.integers(0, 3))
+            mode = 2 if rng.random() < 0.2 else 0
+            step.append(Dir(r, s, e, n, key, mode))
+            key += 1
+            lens[r] = L - (e - s) + n
+        steps.append(step)
+    return steps
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_reindex_shift_aligned(seed):
+    """Re-index pools with pages of several slots and spans off the grid: kept pages for runs
+    shifted by whole blocks, fresh pages for the boundary blocks, in eager, lazy and split pools."""
+    rng = np.random.default_rng(5000 + seed)
+    n_req = int(rng.integers(1, 4))
+    B = int(rng.choice([2, 4, 8, 16]))
+    lengths = [int(rng.integers(0, 40 * B)) for _ in range(n_req)]
+    layers = int(rng.integers(1, 4))
+    steps = _shift_aligned_steps(rng, lengths, 3, B)
+    flags = REINDEX | (SPLIT if seed % 3 == 0 else 0)
+    w = Workload(f"fuzz-shift-{seed}", layers, B, lengths, steps, seed=seed)
+    cache = H.make_cache(w, slack_pages=64, flags=flags | (LAZY if seed % 2 else 0))
+    if seed % 2:
+        import test_gpu_lazy as TL
+        st = TL.LazyState(w)
+        for step in steps:
+            TL._step(w, cache, st, step)
+    else:
+        state = H.oracle_state(w)
+        for step in steps:
+            H.splice_step_and_check(w, cache, state, step)
+    cache.close()
+
+
 @pytest.mark.parametrize("seed", range(6))
 def test_fuzz_lazy(seed):
     import test_gpu_lazy as TL

@@ -238,15 +238,24 @@ def test_block_reindex_aligned_chain(B, layout):
     cache.close()
 
 
-def test_block_reindex_misaligned_call_rewrites():
-    """On a block-16 re-index pool, a call with one directive off the block grid rewrites
-    (two kernels), and an aligned call after it re-indexes (three)."""
-    steps = [[Dir(0, 32, 64, 16, 0), Dir(1, 20, 40, 3, 1)],
+def test_block_reindex_keeps_pages_of_runs_shifted_by_whole_blocks():
+    """Block 16, directives off the block grid.  Delta = -16 keeps the pages of the survivors'
+    whole blocks (the table's entries move by one block); Delta = -3 keeps nothing.  Both are
+    checked against the oracle."""
+    steps = [[Dir(0, 20, 54, 18, 0), Dir(1, 20, 40, 3, 1)],
              [Dir(0, 16, 48, 0, 2), Dir(1, 0, 16, 32, 3)]]
     w = Workload("block-reindex-mixed", 2, 16, [300, 170], steps, seed=60)
     cache = H.make_cache(w, slack_pages=32, flags=REINDEX)
     state = H.oracle_state(w)
-    assert H.splice_step_and_check(w, cache, state, steps[0])["stats"]["reindexed"] == 0
+    before = cache.table.cpu().numpy().copy()
+    c = H.splice_step_and_check(w, cache, state, steps[0])
+    assert c["stats"]["reindexed"] == 1
+    after = cache.table.cpu().numpy()
+    # request 0: rows from 54 on move to 38 on; new blocks 3.. hold old blocks 4.. (19 blocks
+    # before, 18 after: 300 - 16 = 284 rows)
+    assert np.array_equal(after[0, 3:18], before[0, 4:19])
+    # request 1: Delta = -17, no block keeps its page from b0 = 1 on
+    assert not (set(after[1, 1:10].tolist()) & set(before[1, 1:11].tolist()))
     assert H.splice_step_and_check(w, cache, state, steps[1])["stats"]["reindexed"] == 1
     cache.close()
 
