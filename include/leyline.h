@@ -84,16 +84,16 @@ typedef enum { LEYLINE_PAIRS_HALF_SPLIT = 0, LEYLINE_PAIRS_INTERLEAVED = 1 } ley
 typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_rotate_precision_t;
 
 /* Pool flags.
- * LEYLINE_POOL_REINDEX: a splice keeps every surviving downstream block in its
- *   page: only its block-table entry moves, and its rope bands are turned in place
- *   (256 bytes per slot and layer instead of 2304; the latent is not touched).
- *   Rows of R go to fresh pages, the pages of dropped blocks return to the free
- *   list.  With block_size 1 this applies to every call.  With block_size > 1 it
- *   applies to calls whose directives all lie on block boundaries: s_start a
- *   multiple of block_size, s_end and n_repl multiples of block_size unless
- *   s_end = seq_len; other calls rewrite as without the flag.  The rotation
- *   happens in place before the commit, so a call that fails after validation
- *   leaves the pool inconsistent (as any LEYLINE_ERR_CUDA does).  Requires
+ * LEYLINE_POOL_REINDEX: a splice keeps a surviving block in its page when all the
+ *   block's rows come from one run of survivors shifted by a multiple of block_size
+ *   (every survivor at block_size 1): only its block-table entry moves, and its rope
+ *   bands are turned in place (256 bytes per slot and layer instead of 2304; the
+ *   latent is not touched).  The other new blocks (rows of R, and survivors or prefix
+ *   rows at run boundaries) get fresh pages, and old blocks not kept return to the
+ *   free list.  A call whose fresh pages would take more survivor and prefix rows
+ *   than its kept pages hold rewrites as without the flag (statistics: reindexed).
+ *   The rotation happens in place before the commit, so a call that fails after
+ *   validation leaves the pool inconsistent (as any LEYLINE_ERR_CUDA does).  Requires
  *   rope_dim <= 256 and rope_heads * rope_dim <= 512 (else pool creation fails
  *   with LEYLINE_ERR_INVALID_ARG). */
 #define LEYLINE_POOL_REINDEX 1
