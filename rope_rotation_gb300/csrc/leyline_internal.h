@@ -154,10 +154,14 @@ struct leyline_pool {
     int32_t* d_status = nullptr;
     char* d_plan = nullptr;
     size_t d_plan_cap = 0;
-    char* h_plan = nullptr;  // pinned
-    size_t h_plan_cap = 0;
-    cudaEvent_t plan_uploaded = nullptr;  // staging buffer reusable once this completes
-    bool uploaded_once = false;
+    // pinned staging of uploaded plans: a ring of slots, so the host can plan several calls
+    // ahead of the GPU; a slot is reused once its upload event has completed
+    static constexpr int kPlanSlots = 8;
+    char* h_plan[kPlanSlots] = {};
+    size_t h_plan_cap[kPlanSlots] = {};
+    cudaEvent_t plan_uploaded[kPlanSlots] = {};
+    bool slot_used[kPlanSlots] = {};
+    int next_slot = 0;
     cudaEvent_t done = nullptr;           // last enqueued work of the pool
     bool has_work = false;
     cudaStream_t last_stream = nullptr;

@@ -37,6 +37,8 @@ using namespace leyline;
 
 namespace {
 
+constexpr size_t kPlanSlotBytes = 64 << 10;  // pinned plan staging per slot (grown on demand)
+
 struct DeviceGuard {
     int prev = -1;
     bool ok = false;
@@ -180,7 +182,12 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
     if (e == cudaSuccess) e = cudaMalloc(&p->d_queue, sizeof(int32_t) * (size_t)p->q_cap);
     if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->plan_uploaded, cudaEventDisableTiming);
+    // the staging slots are allocated now: cudaHostAlloc during a call would wait for the GPU
+    for (int i = 0; i < leyline_pool::kPlanSlots && e == cudaSuccess; ++i) {
+        e = cudaEventCreateWithFlags(&p->plan_uploaded[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaHostAlloc((void**)&p->h_plan[i], kPlanSlotBytes, cudaHostAllocDefault);
+        if (e == cudaSuccess) p->h_plan_cap[i] = kPlanSlotBytes;
+    }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
     if (e == cudaSuccess && (g.flags & LEYLINE_POOL_LAZY)) {
         // every slot starts with nothing pending; readers take theta_j from a device table
@@ -234,10 +241,12 @@ int leyline_pool_destroy(leyline_pool_t* p)
         cudaEventDestroy(ev.first);
         cudaEventDestroy(ev.second);
     }
-    if (p->plan_uploaded) cudaEventDestroy(p->plan_uploaded);
+    for (int i = 0; i < leyline_pool::kPlanSlots; ++i) {
+        if (p->plan_uploaded[i]) cudaEventDestroy(p->plan_uploaded[i]);
+        if (p->h_plan[i]) cudaFreeHost(p->h_plan[i]);
+    }
     if (p->done) cudaEventDestroy(p->done);
     if (p->d_plan) cudaFree(p->d_plan);
-    if (p->h_plan) cudaFreeHost(p->h_plan);
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_queue) cudaFree(p->d_queue);
     if (p->d_stage) cudaFree(p->d_stage);
@@ -414,30 +423,31 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
             if (e != cudaSuccess) return cuda_error(e, "allocating the plan buffer");
             p->d_plan_cap = cap;
         }
-        if (total > p->h_plan_cap) {
-            if (p->h_plan) {
-                e = cudaEventSynchronize(p->plan_uploaded);
-                if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
-                cudaFreeHost(p->h_plan);
-                p->h_plan = nullptr;
-                p->h_plan_cap = 0;
-            }
-            const size_t cap = std::max<size_t>(total * 2, 1 << 16);
-            e = cudaHostAlloc((void**)&p->h_plan, cap, cudaHostAllocDefault);
-            if (e != cudaSuccess) return cuda_error(e, "allocating the pinned plan buffer");
-            p->h_plan_cap = cap;
-        } else if (p->uploaded_once) {
-            e = cudaEventSynchronize(p->plan_uploaded);  // the staging buffer may still be in flight
-            if (e != cudaSuccess) return cuda_error(e, "waiting for the previous plan upload");
+        const int slot = p->next_slot;
+        p->next_slot = (slot + 1) % leyline_pool::kPlanSlots;
+        if (p->slot_used[slot]) {  // the slot's last upload may still be in flight
+            e = cudaEventSynchronize(p->plan_uploaded[slot]);
+            if (e != cudaSuccess) return cuda_error(e, "waiting for an earlier plan upload");
         }
-        memcpy(p->h_plan, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
-        memcpy(p->h_plan + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
-        if (!plan.trig.empty()) memcpy(p->h_plan + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
-        e = cudaMemcpyAsync(p->d_plan, p->h_plan, total, cudaMemcpyHostToDevice, stream);
+        if (total > p->h_plan_cap[slot]) {
+            if (p->h_plan[slot]) cudaFreeHost(p->h_plan[slot]);
+            p->h_plan[slot] = nullptr;
+            p->h_plan_cap[slot] = 0;
+            const size_t cap = std::max<size_t>(total * 2, 1 << 16);
+            e = cudaHostAlloc((void**)&p->h_plan[slot], cap, cudaHostAllocDefault);
+            if (e != cudaSuccess) return cuda_error(e, "allocating the pinned plan buffer");
+            p->h_plan_cap[slot] = cap;
+        }
+        char* h = p->h_plan[slot];
+        memcpy(h, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
+        memcpy(h + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
+        if (!plan.trig.empty()) memcpy(h + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
+        // the device buffer is reused: this copy is stream-ordered after the previous call's kernels
+        e = cudaMemcpyAsync(p->d_plan, h, total, cudaMemcpyHostToDevice, stream);
         if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
-        e = cudaEventRecord(p->plan_uploaded, stream);
+        e = cudaEventRecord(p->plan_uploaded[slot], stream);
         if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
-        p->uploaded_once = true;
+        p->slot_used[slot] = true;
         a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan);
         a.segs = reinterpret_cast<const Seg*>(p->d_plan + off_segs);
         a.trig = reinterpret_cast<const float*>(p->d_plan + off_trig);
