@@ -125,6 +125,19 @@ def sweep_aligned(C: int, block_size: int, seed: int = 0, num_layers: int = 61) 
     return Workload(f"sweep-aligned-C{C}-61L-B{B}", num_layers, B, w.lengths, [dirs], seed=seed)
 
 
+def sweep_shift_aligned(C: int, block_size: int, seed: int = 0, num_layers: int = 61) -> Workload:
+    """The sweep with spans as drawn and |R| raised to the next value that makes Delta a
+    multiple of the block size: survivors shift by whole blocks, boundary blocks do not."""
+    w = sweep(C, block_size, seed, num_layers)
+    B = block_size
+    dirs = []
+    for d in w.steps[0]:
+        span = d.s_end - d.s_start
+        n = d.n_repl + (span - d.n_repl) % B  # n - span is a multiple of B
+        dirs.append(Dir(d.req, d.s_start, d.s_end, n, d.key))
+    return Workload(f"sweep-shift-aligned-C{C}-61L-B{B}", num_layers, B, w.lengths, [dirs], seed=seed)
+
+
 def by_name(name: str, seed: int = 0) -> Workload:
     table = {
         "cfg1": contiguous_4k,
@@ -140,4 +153,7 @@ def by_name(name: str, seed: int = 0) -> Workload:
     if name.startswith("cfg5a-"):  # cfg5a-C16-B16: the same sweep on the block grid
         _, c, b = name.split("-")
         return sweep_aligned(int(c[1:]), int(b[1:]), seed)
+    if name.startswith("cfg5s-"):  # cfg5s-C16-B16: the same sweep with Delta a multiple of B
+        _, c, b = name.split("-")
+        return sweep_shift_aligned(int(c[1:]), int(b[1:]), seed)
     raise KeyError(name)
