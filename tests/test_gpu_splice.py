@@ -275,3 +275,60 @@ def test_gqa_rows(layout, B, flags):
     for step in w.steps:
         H.splice_step_and_check(w, cache, state, step, layout=layout)
     cache.close()
+
+
+# ------------------------------------------------------------------------------
+# Many calls in flight: plans too large for a kernel parameter are staged through a
+# ring of pinned slots, so the host enqueues call after call without waiting; the
+# final caches must equal the oracle's chain.
+@pytest.mark.parametrize("flags", [0, REINDEX])
+def test_many_calls_in_flight_with_uploaded_plans(flags):
+    import torch
+    from rope_rotation_gb300 import leyline
+    rng = np.random.default_rng(77)
+    n_req, B = 10, 1 if flags else 16
+    lengths = [int(rng.integers(200, 600)) for _ in range(n_req)]
+    lens = list(lengths)
+    steps, key = [], 0
+    for _ in range(20):  # 20 calls, 10 requests x 2 directives each: 30+ segments per plan
+        step = []
+        for r in range(n_req):
+            L = lens[r]
+            a, b = sorted(int(x) for x in rng.integers(0, L // 2, size=2))
+            c, d = sorted(int(x) for x in rng.integers(L // 2 + 1, L, size=2))
+            for s, e in ((a, b), (c, d)):
+                n = int(rng.integers(0, 6))
+                step.append(Dir(r, s, e, n, key))
+                key += 1
+                L += n - (e - s)
+            lens[r] = L
+        steps.append(step)
+    w = Workload(f"in-flight-f{flags}", 2, B, lengths, steps, seed=78)
+    cache = H.make_cache(w, slack_pages=64, flags=flags)
+    keep = []
+    for step in steps:  # no synchronisation between calls
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        cache.splice(dirs)
+    torch.cuda.synchronize()
+    cache.check_status()
+    state = H.oracle_state(w)
+    import oracle
+    import synth
+    for step in steps:
+        for r in range(w.num_reqs):
+            ds = [d for d in step if d.req == r]
+            reps = [synth.repl_rows(w.seed, r, d.key, w.num_layers, d.n_repl, w.row_elems) for d in ds]
+            state[r] = oracle.splice_request(state[r], [(d.s_start, d.s_end, d.n_repl) for d in ds], reps,
+                                             w.latent_dim, w.theta, 0)
+    for r in range(w.num_reqs):
+        n = int(cache.seq_lens_host[r])
+        assert n == state[r].shape[1]
+        got = H.logical_rows(cache, r, n)
+        lat = w.latent_dim
+        assert np.array_equal(got[:, :, :lat], state[r][:, :, :lat])
+        # each row may have been turned by up to 20 calls: the chain allowance covers it
+        H.compare_kpe(got[:, :, lat:].reshape(-1, w.rope_dim), state[r][:, :, lat:].reshape(-1, w.rope_dim), 0,
+                      turns=np.full(got.shape[0] * got.shape[1], 20))
+    del keep
+    cache.close()

@@ -150,3 +150,30 @@ def test_noalloc_matches_splice_on_lazy_pools():
         del keep_ref, keep_new
     ref.close()
     new.close()
+
+
+def test_noalloc_matches_splice_when_runs_shift_by_whole_blocks():
+    """Re-index pool, block 16, spans off the grid with Delta a multiple of 16: kept pages,
+    fresh boundary blocks and rows of R, through both entry points."""
+    from rope_rotation_gb300 import leyline
+    steps = [[Dir(0, 20, 54, 18, 0), Dir(1, 5, 40, 3, 1)],
+             [Dir(0, 3, 19, 0, 2), Dir(1, 70, 71, 17, 3)]]
+    w = Workload("noalloc-shift", 2, 16, [300, 170], steps, seed=24)
+    ref = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_REINDEX)
+    new = H.make_cache(w, slack_pages=16, flags=leyline.LEYLINE_POOL_REINDEX)
+    for step in w.steps:
+        dirs_ref, keep_ref = H.gpu_directives(w, step)
+        dirs_new, keep_new = H.gpu_directives(w, step)
+        leyline.leyline_splice(ref.pool, ref.tables, dirs_ref)
+        leyline.leyline_splice_noalloc(new.pool, new.tables, dirs_new)
+        torch.cuda.synchronize()
+        ref.check_status()
+        new.check_status()
+        assert ref.last_stats() == new.last_stats()
+        assert ref.last_stats()["reindexed"] == 1
+        for r in range(w.num_reqs):
+            n = int(ref.seq_lens_host[r])
+            assert np.array_equal(H.logical_rows(ref, r, n), H.logical_rows(new, r, n))
+        del keep_ref, keep_new
+    ref.close()
+    new.close()
