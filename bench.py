@@ -184,6 +184,23 @@ def per_request_counts(w):
     return st
 
 
+def host_plan_us(w, flags: int, reps: int = 50) -> float:
+    """Median time of the host planner alone (leyline_splice_plan, C, no device) for one call."""
+    from rope_rotation_gb300 import leyline
+    desc = leyline.pool_desc(w.num_layers, w.block_size, 1, w.latent_dim, w.rope_dim, w.theta, flags=flags)
+    fake = 1 << 40  # a 16-byte aligned stand-in for the rows of R: the dry run never reads them
+    dirs = [leyline.Directive(d.req, d.mode, d.s_start, d.s_end, d.n_repl, 0, fake if d.n_repl else None)
+            for d in w.steps[0]]
+    nb = max(-(-(L + 64 * 3) // w.block_size) for L in w.lengths)
+    lens = np.array(w.lengths, dtype=np.int64)
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        leyline.leyline_splice_plan(desc, lens, nb, dirs)
+        times.append((time.perf_counter() - t) * 1e6)
+    return float(statistics.median(times))
+
+
 # ---------------------------------------------------------------- our arm ---
 
 def run_ours(args, rank, world, local):
@@ -362,6 +379,9 @@ def run_ours(args, rank, world, local):
                                    else os.environ.get("LEYLINE_MOVE_KERNEL", "vector")),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
+        "slot_layers_per_s": value * w.num_layers,
+        "host_plan_us": host_plan_us(w, (leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
+                                     | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)),
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,
