@@ -51,17 +51,17 @@ float bf16_nearest(double x)
     return neg ? -(float)r : (float)r;
 }
 
-// cos / sin of Delta * theta_j for every pair j of a rotated segment.  The angle is
+// cos / sin of Delta * theta_j for every pair j of a rotated segment (theta_j given).  The angle is
 // formed in fp64 (Delta * theta_0 reaches 1e5 rad, where an fp32 angle would be off
 // by ~1e-2 rad, more than a bf16 step), the library's cos / sin reduce it exactly,
 // and the result is rounded once to the arithmetic of the rotation.
-void segment_trig(const Geometry& g, int64_t delta, float* out)
+void segment_trig(const Geometry& g, const double* theta_j, int64_t delta, float* out)
 {
     const int half = g.rope_dim / 2;
     for (int j = 0; j < half; ++j) {
-        const double theta_j = std::pow(g.theta, -2.0 * (double)j / (double)g.rope_dim);
-        const double phi = (double)delta * theta_j;
-        const double c = std::cos(phi), s = std::sin(phi);
+        const double phi = (double)delta * theta_j[j];
+        double s, c;
+        sincos(phi, &s, &c);
         if (g.precision == LEYLINE_ROTATE_BF16_NAIVE) {
             out[2 * j] = bf16_nearest(c);
             out[2 * j + 1] = bf16_nearest(s);
@@ -159,6 +159,8 @@ int plan_requests(const Geometry& g, const int64_t* seq_lens_host, int32_t max_b
     const int64_t B = g.block_size;
     plan->reindex = reindex;
     int64_t tiles = 0, commit = 0, pops = 0, pushes = 0;
+    std::vector<double> theta_j(g.rope_dim / 2);  // theta^(-2j/d) in fp64
+    for (int j = 0; j < g.rope_dim / 2; ++j) theta_j[j] = std::pow(g.theta, -2.0 * (double)j / (double)g.rope_dim);
     leyline_stats_t& st = plan->stats;
     for (int32_t i = 0; i < n;) {
         const int32_t req = dirs[order[i]].req;
@@ -224,7 +226,7 @@ int plan_requests(const Geometry& g, const int64_t* seq_lens_host, int32_t max_b
                 if (A != 0 && !lazy) {
                     s.trig = plan->n_trig++;
                     plan->trig.resize((size_t)plan->n_trig * g.rope_dim);
-                    segment_trig(g, A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
+                    segment_trig(g, theta_j.data(), A, plan->trig.data() + (size_t)s.trig * g.rope_dim);
                 }
                 plan->segs.push_back(s);
                 st.downstream_slots += run_end - d->s_end;
