@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, valid only for the kernel code it was taken on (kernel_sha)
 # (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.9 MB; the
 # rest of the 210.9 MB written was still in L2 when the single captured launch ended).
-NCU_TRAFFIC = {"kernel_sha256": "e0dd899d192707f2a13342a41d3a19ed8d95cbfbc7d21de95b37691aacf26d4f",
-               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210918656 + 160857344}}
+NCU_TRAFFIC = {"kernel_sha256": "e6b02bceef6cc35876cb24000d25a55d08e76b5912e7f7676d7ef9c58132c026",
+               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210927616 + 161605888}}
 
 
 def parse():
@@ -105,12 +105,17 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("leyline_device.cuh", "leyline_move.cu", "leyline_reindex.cu", "leyline_read.cu",
+                  "leyline_plan.h", "leyline_internal.h")
+
+
 def kernel_sha():
-    """sha256 of the kernel source with comments and whitespace runs removed: a change to
+    """sha256 of the kernel sources with comments and whitespace runs removed: a change to
     the code invalidates stored ncu counters, a change to a comment does not."""
-    p = os.path.join(ROOT, "rope_rotation_gb300", "csrc", "leyline_kernels.cu")
-    with open(p) as f:
-        text = f.read()
+    text = ""
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "rope_rotation_gb300", "csrc", name)) as f:
+            text += f.read() + "\n"
     text = re.sub(r"//[^\n]*", "", text)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()

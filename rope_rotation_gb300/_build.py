@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libleyline.so")
-SOURCES = ["leyline_kernels.cu", "leyline_planner.cpp", "leyline_pool.cpp", "leyline_noalloc.cu"]
+SOURCES = ["leyline_move.cu", "leyline_reindex.cu", "leyline_read.cu", "leyline_planner.cpp", "leyline_pool.cpp",
+           "leyline_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

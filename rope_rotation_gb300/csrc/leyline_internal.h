@@ -92,8 +92,13 @@ struct SpliceArgs {
     Geometry g;
 };
 
-// Launchers (leyline_kernels.cu).  Each returns the cudaError_t of the launches as int.
+// Launchers (leyline_move.cu, leyline_reindex.cu, leyline_read.cu).  Each returns the
+// cudaError_t of the launches as int.
 int launch_init_queue(int32_t* q, int64_t num_pages, void* stream);
+// Enqueue a re-indexed call's kernels (prep, rows of R, fresh rows, rotation, commit):
+// leyline_reindex.cu.  launch_splice calls it for plans with reindex set.
+int launch_reindex_call(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stream, cudaEvent_t t0,
+                        cudaEvent_t t1);
 // Enqueue move+rotate then commit.  pp != nullptr: the plan travels in pp (a.reqs,
 // a.segs, a.trig unused); else it is read from a.reqs / a.segs / a.trig.  With
 // timing events, they bracket the move+rotate kernel.

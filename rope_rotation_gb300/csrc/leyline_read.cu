@@ -1,0 +1,226 @@
+// leyline_read.cu -- reads and bookkeeping kernels of the GB300 Leyline splice library
+// (sm_103a): the free-page ring's initial fill, gathers of logical rows (lazy pools turn
+// each row's bands by its pending count on the way out), materialize, pending clears.
+//
+// "Leyline: KV Cache Directives for Agentic Inference", section 2.2: R(a) R(b) = R(a + b),
+// so a lazy pool's summed turn is applied once when a row is read.
+#include "leyline_device.cuh"
+
+namespace leyline {
+namespace {
+
+__global__ void init_queue_kernel(int32_t* q, long long num_pages)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * num_pages;
+         i += (long long)gridDim.x * blockDim.x)
+        q[i] = i < num_pages ? (int32_t)i : -1;
+}
+
+// Gather logical rows [t0, t1) of one request and layer into a contiguous buffer.
+__global__ void gather_kernel(const uint4* kv, const int32_t* table_row, const Geometry g, long long layer,
+                              long long t0, long long n, uint4* out, int32_t* status)
+{
+    const long long row_vecs = g.row_vecs, lv = g.latent_vecs, B = g.block_size;
+    const long long total = n * row_vecs;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long r = i / row_vecs, c = i - r * row_vecs;
+        const long long t = t0 + r;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= g.num_pages) {
+            raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        const long long slot = (long long)page * B + t % B;
+        out[i] = c < lv ? kv[lat_off(g, layer, slot) + c] : kv[band_off(g, layer, slot) + (c - lv)];
+    }
+}
+
+// -------------------------------------------------------------------------
+// Lazy pools.  cos / sin of pending * theta_j: the angle is formed in fp64 and the
+// fp64 sincos reduces it, then it is rounded once to the rotation's arithmetic,
+// exactly as the host does for an eager splice.
+__device__ __forceinline__ void pending_trig(int pend, double theta_j, bool bf16, float& c, float& s)
+{
+    double sd, cd;
+    sincos((double)pend * theta_j, &sd, &cd);
+    if (bf16) {
+        c = __bfloat162float(__double2bfloat16(cd));
+        s = __bfloat162float(__double2bfloat16(sd));
+    } else {
+        c = (float)cd;
+        s = (float)sd;
+    }
+}
+
+// cos / sin of the pairs of item q of a band: 8 pairs j = 8q.. (half-split) or 4
+// pairs j = 4q.. (interleaved).
+template <int kLayout>
+__device__ __forceinline__ void item_trig(int pend, int q, const double* theta_j, bool bf16, float* c, float* s)
+{
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;
+#pragma unroll
+    for (int w = 0; w < kPairs; ++w) pending_trig(pend, theta_j[kPairs * q + w], bf16, c[w], s[w]);
+}
+
+// Item q of the band at `band` (x at q, y at q + head_vecs / 2 for half-split),
+// turned by (c, s) and written to `dst`.
+template <int kLayout>
+__device__ __forceinline__ void turn_item(const uint4* band, uint4* dst, int q, int hv, bool bf16, const float* c,
+                                          const float* s)
+{
+    if (kLayout == 0) {
+        uint4 x = band[q], y = band[q + hv / 2];
+        if (bf16) rotate_half_split<true>(x, y, c, s);
+        else rotate_half_split<false>(x, y, c, s);
+        dst[q] = x;
+        dst[q + hv / 2] = y;
+    } else {
+        uint4 x = band[q];
+        if (bf16) rotate_interleaved<true>(x, c, s);
+        else rotate_interleaved<false>(x, c, s);
+        dst[q] = x;
+    }
+}
+
+// Gather from a lazy pool: one warp per row.  The latent is copied; item q of each
+// rope band is turned by the slot's pending count on the way out.
+template <int kLayout>
+__global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, const Geometry g, long long layer,
+                                   long long t0, long long n, uint4* out, const int32_t* pending,
+                                   const double* theta_j, int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    const int hv = g.head_vecs;
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long r = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; r < n; r += warps) {
+        const long long t = t0 + r;
+        const long long B = g.block_size;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= g.num_pages) {
+            if (lane == 0) raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        const long long slot = (long long)page * B + t % B;
+        const uint4* lat = kv + lat_off(g, layer, slot);
+        const uint4* bands = kv + band_off(g, layer, slot);
+        uint4* o = out + r * g.row_vecs;
+        for (int c = lane; c < g.latent_vecs; c += 32) o[c] = lat[c];
+        const int pend = pending[slot];
+        for (int it = lane; it < g.rope_heads * head_items; it += 32) {
+            const int head = it / head_items, q = it - head * head_items;
+            const uint4* band = bands + head * hv;
+            uint4* dst = o + g.latent_vecs + head * hv;
+            if (pend == 0) {
+                dst[q] = band[q];
+                if (kLayout == 0) dst[q + hv / 2] = band[q + hv / 2];
+                continue;
+            }
+            float c[8], s[8];
+            item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
+            turn_item<kLayout>(band, dst, q, hv, bf16, c, s);
+        }
+    }
+}
+
+// Materialize a lazy request: one warp per row.  Lanes take the row's (layer,
+// band item) pairs in turn, so the pair group q of a lane, and the cos / sin held
+// for it, change only when the items per layer do not divide 32.  The count is
+// read before and cleared after every layer of the row is turned in place.
+template <int kLayout>
+__global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Geometry g, long long len,
+                                   int32_t* pending, const double* theta_j, int32_t* status)
+{
+    const int lane = threadIdx.x & 31;
+    const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+    const int hv = g.head_vecs;
+    const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const int items = g.rope_heads * head_items;  // per layer
+    const long long warps = (long long)gridDim.x * (blockDim.x / 32);
+    for (long long t = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; t < len; t += warps) {
+        const long long B = g.block_size;
+        const int page = table_row[t / B];
+        if (page < 0 || page >= g.num_pages) {
+            if (lane == 0) raise_status(status, ST_BAD_PAGE);
+            continue;
+        }
+        const long long slot = (long long)page * B + t % B;
+        const int pend = pending[slot];
+        if (pend == 0) continue;
+        float c[8], s[8];
+        int have_q = -1;
+        for (long long idx = lane; idx < (long long)g.num_layers * items; idx += 32) {
+            const long long layer = idx / items;
+            const int it = (int)(idx - layer * items);
+            const int head = it / head_items, q = it - head * head_items;
+            if (q != have_q) {
+                item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
+                have_q = q;
+            }
+            uint4* band = kv + band_off(g, layer, slot) + head * hv;
+            turn_item<kLayout>(band, band, q, hv, bf16, c, s);
+        }
+        __syncwarp();
+        if (lane == 0) pending[slot] = 0;
+    }
+}
+
+__global__ void clear_pending_kernel(int32_t* pending, const int32_t* page_ids, long long n, int block_size)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n * block_size;
+         i += (long long)gridDim.x * blockDim.x)
+        pending[(long long)page_ids[i / block_size] * block_size + i % block_size] = 0;
+}
+
+}  // namespace
+
+int launch_init_queue(int32_t* q, int64_t num_pages, void* stream)
+{
+    init_queue_kernel<<<grid_for(2 * num_pages, 256, 4096), 256, 0, (cudaStream_t)stream>>>(q, num_pages);
+    return (int)cudaGetLastError();
+}
+
+int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
+                  int64_t t1, void* out, int32_t* status, void* stream)
+{
+    const long long n = t1 - t0;
+    if (n <= 0) return 0;
+    gather_kernel<<<grid_for(n * g.row_vecs, 256, 8192), 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint4*>(kv), table_row, g, layer, t0, n, static_cast<uint4*>(out), status);
+    return (int)cudaGetLastError();
+}
+
+int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
+                       int64_t t1, void* out, const int32_t* pending, const double* theta_j, int32_t* status,
+                       void* stream)
+{
+    const long long n = t1 - t0;
+    if (n <= 0) return 0;
+    auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? gather_lazy_kernel<0> : gather_lazy_kernel<1>;
+    k<<<grid_for(n * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(kv), table_row, g,
+                                                                      layer, t0, n, static_cast<uint4*>(out),
+                                                                      pending, theta_j, status);
+    return (int)cudaGetLastError();
+}
+
+int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
+                       const double* theta_j, int32_t* status, void* stream)
+{
+    if (len <= 0) return 0;
+    auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
+    k<<<grid_for(len * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
+                                                                        pending, theta_j, status);
+    return (int)cudaGetLastError();
+}
+
+int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream)
+{
+    if (n <= 0) return 0;
+    clear_pending_kernel<<<grid_for(n * block_size, 256, 4096), 256, 0, (cudaStream_t)stream>>>(pending, page_ids, n,
+                                                                                             block_size);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace leyline
