@@ -208,6 +208,17 @@ def host_plan_us(w, flags: int, reps: int = 50) -> float:
 
 # ---------------------------------------------------------------- our arm ---
 
+# The value leg times the device (the metric runs from the first kernel of the first
+# timed step to the last kernel of the last): before its first event the stream is held
+# by a short spin, so that the host has queued steps when the timed region starts and
+# the region holds the K steps' GPU work alone.  The e2e leg has no head start.
+HEAD_START_CYCLES = 2_000_000  # about 1 ms at 2 GHz
+
+
+def hold_stream(torch):
+    torch.cuda._sleep(HEAD_START_CYCLES)
+
+
 def run_ours(args, rank, world, local):
     import torch
     import __graft_entry__
@@ -251,11 +262,23 @@ def run_ours(args, rank, world, local):
             repl_dev[d.key] = t
             repl_host[d.key] = t.cpu().pin_memory()
 
+    # each step's directives: one checked template per source of R (directive_batch), of
+    # which a step changes only the request ids
+    templates = {}
+
     def dirs_for(g, repl_map):
-        return [leyline.directive(g * C + d.req, d.s_start, d.s_end, repl_map.get(d.key), n_repl=d.n_repl)
-                for d in w.steps[0]]
+        key = id(repl_map)
+        if key not in templates:
+            templates[key] = leyline.directive_batch([d.req for d in w.steps[0]], [d.s_start for d in w.steps[0]],
+                                                     [d.s_end for d in w.steps[0]],
+                                                     [repl_map.get(d.key) for d in w.steps[0]],
+                                                     n_repl=[d.n_repl for d in w.steps[0]])
+        b = templates[key].copy()
+        b["req"] += g * C
+        return b
 
     stream = torch.cuda.current_stream()
+    stream_ptr = stream.cuda_stream
     # warm-up
     for g in range(W):
         cache.splice(dirs_for(g, repl_dev))
@@ -276,14 +299,18 @@ def run_ours(args, rank, world, local):
         leyline.leyline_kernel_timing_enable(cache.pool, True)
     barrier()
     torch.cuda.synchronize()
+    hold_stream(torch)
     ev0.record(stream)
+    t_host = time.perf_counter()
     for k in range(K):
-        cache.splice(dirs_for(W + k, repl_dev))
+        cache.splice(dirs_for(W + k, repl_dev), stream_ptr)
+    enqueue_us = (time.perf_counter() - t_host) * 1e6 / K
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
     cache.check_status()
+    last = cache.last_stats()
 
     if not args.single_leg:
         # kernel leg: the same steps on fresh requests, with events around move+rotate
@@ -378,6 +405,8 @@ def run_ours(args, rank, world, local):
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
                    "l2": "inputs larger than L2: each step splices its own pre-filled request",
+                   "timing": "value: CUDA events around K steps queued behind a ~1 ms spin on the stream "
+                             "(device time of the steps); e2e: events around the steps with no head start",
                    "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
                    + (", re-index" if reindexed else "") + (", split rope" if args.split else ""),
                    "move_kernel": ("rotate_in_place" if reindexed
@@ -387,6 +416,10 @@ def run_ours(args, rank, world, local):
         "slot_layers_per_s": value * w.num_layers,
         "host_plan_us": host_plan_us(w, (leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
                                      | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)),
+        # host side of the timed steps: the Python loop per step, and the library's own
+        # account of its last call (leyline_stats_t host_ns, resolve_ns, plan_ns)
+        "host": {"enqueue_us_per_step": enqueue_us, "splice_call_us": last["host_ns"] / 1e3,
+                 "resolve_us": last["resolve_ns"] / 1e3, "plan_us": last["plan_ns"] / 1e3},
         "clocks": clocks,
         "gpu_launches": K * st["kernels_launched"],
         "roofline": {"kernel": kernel_name, "bound": "hbm", "achieved": achieved, "peak": peak,

@@ -188,6 +188,11 @@ typedef struct {
     int32_t kernels_launched;  /* kernels this call enqueued */
     int32_t reindexed;         /* 1: the call kept survivors in their pages (LEYLINE_POOL_REINDEX) */
     int32_t reserved;
+    /* Host time of the call (leyline_splice, leyline_splice_noalloc; 0 from the dry run),
+     * in nanoseconds of the host's monotonic clock: */
+    int64_t host_ns;           /* the whole call, from entry to return (kernels are enqueued, not waited for) */
+    int64_t resolve_ns;        /* classifying the directives' pointers to rows of R */
+    int64_t plan_ns;           /* the host planner */
 } leyline_stats_t;
 
 /* -------------------------------------------------------------- pool ---- */
@@ -304,7 +309,8 @@ int leyline_sync_status(leyline_pool_t* pool);
 /* Kernel timing for benchmarks.  While enabled, each splice records CUDA events
  * on its stream around its move+rotate kernel.  leyline_kernel_timing_read waits
  * for them and returns the summed kernel time (ms) and the number of timed
- * launches since the last enable, then keeps timing. */
+ * launches since the last enable, then keeps timing.  Enabling creates the events
+ * of the first 256 timed calls at once, so that those calls create none. */
 int leyline_kernel_timing_enable(leyline_pool_t* pool, int32_t enable);
 int leyline_kernel_timing_read(leyline_pool_t* pool, double* total_ms, int32_t* launches);
 

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <cstdint>
 #include <string>
 #include <utility>
@@ -122,6 +123,18 @@ int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, i
 // link (NVLink-C2C on Grace hosts).  Pageable host memory and memory of another
 // device are refused (LEYLINE_ERR_INVALID_ARG, message naming `what`).
 int resolve_access(const void* ptr, int device, const char* what, void** alias, bool* is_host);
+
+// Host time of a splice call, reported in leyline_stats_t.
+using HostClock = std::chrono::steady_clock::time_point;
+inline HostClock host_now() { return std::chrono::steady_clock::now(); }
+inline void set_host_times(leyline_stats_t* st, HostClock enter, HostClock resolved, HostClock planned)
+{
+    using std::chrono::duration_cast;
+    using std::chrono::nanoseconds;
+    st->host_ns = duration_cast<nanoseconds>(host_now() - enter).count();
+    st->resolve_ns = duration_cast<nanoseconds>(resolved - enter).count();
+    st->plan_ns = duration_cast<nanoseconds>(planned - resolved).count();
+}
 // resolve_access for every directive's rows of R.  *out points at the directives
 // to plan from: `dirs` itself, or a copy in *work with aliases substituted.
 // *host_rows is set when any rows of R live in host memory.

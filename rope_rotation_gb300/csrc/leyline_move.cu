@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
                                                                 const __grid_constant__ PlanSrc plan)
 {
     constexpr int kRopeVecs = 8;
+    constexpr int kWarps = kMoveThreads / 32;
     __shared__ RowDesc desc[kTileRows];
     wait_for_previous_grid();
     allow_next_grid();
@@ -47,12 +48,30 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
     float cs[8], sn[8];
     int trig = -1;
 
-    long long u0, u1;
-    my_units(a.total_tiles * L, u0, u1);
+    // The split is by warp unit (one warp's two rows of a tile in one layer): CTA runs
+    // then differ by one warp unit, not by a whole (tile, layer) unit, so the CTAs that
+    // finish last hold 1/8 of a unit more work than the rest.  A warp outside this
+    // CTA's run skips the unit's loads and stores but still joins its barriers.
+    // The run is walked with 32-bit counters: k counts its units, and (tile, layer)
+    // advance by one layer per unit.  Units [k_first, k_last) are this warp's.
+    int n, k_first, k_last, layer;
+    long long tile;
+    {
+        long long w0, w1;
+        my_units(a.total_tiles * L * kWarps, w0, w1);
+        const long long u0 = w0 / kWarps, u1 = (w1 + kWarps - 1) / kWarps;
+        n = (int)(u1 - u0);
+        k_first = warp >= (int)(w0 - u0 * kWarps) ? 0 : 1;
+        k_last = warp < (int)(w1 - (u1 - 1) * kWarps) ? n : n - 1;
+        tile = u0 / L;
+        layer = (int)(u0 - tile * L);
+    }
     long long cur_tile = -1;
-    for (long long u = u0; u < u1; ++u) {
-        const long long tile = u / L;
-        const long long layer = u - tile * L;
+    for (int k = 0; k < n; ++k, ++layer) {
+        if (layer == L) {
+            layer = 0;
+            ++tile;
+        }
         if (tile != cur_tile) {
             __syncthreads();
             if (threadIdx.x < kTileRows) desc[threadIdx.x] = make_desc(a, pv, tile, threadIdx.x);
@@ -70,33 +89,35 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
                 }
             }
         }
+        const bool mine = k >= k_first && k < k_last;
         const RowDesc d0 = desc[warp * kRowsPerWarp];
         const RowDesc d1 = desc[warp * kRowsPerWarp + 1];
+        const bool has0 = mine && d0.src != nullptr, has1 = mine && d1.src != nullptr;
         uint4 v[4];
-        if (d0.src) {
+        if (has0) {
             const uint4* s0 = d0.src + layer * d0.src_lstride;
             v[0] = ld_stream(s0 + lane);
             v[1] = ld_stream(s0 + lane + 32);
         }
-        if (d1.src) {
+        if (has1) {
             const uint4* s1 = d1.src + layer * d1.src_lstride;
             v[2] = ld_stream(s1 + lane);
             v[3] = ld_stream(s1 + lane + 32);
         }
         const RowDesc dr = rope_lane ? desc[rope_row] : d0;
-        const bool do_rope = rope_lane && dr.src != nullptr;
+        const bool do_rope = mine && rope_lane && dr.src != nullptr;
         uint4 rx, ry;
         if (do_rope) {
             const uint4* rs = dr.src_band + layer * dr.band_lstride;
             rx = ld_stream(rs + rope_q);
             if (kLayout == 0) ry = ld_stream(rs + rope_q + kRopeVecs / 2);
         }
-        if (d0.src) {
+        if (has0) {
             uint4* t0 = d0.dst + layer * lat_layer;
             st_stream(t0 + lane, v[0]);
             st_stream(t0 + lane + 32, v[1]);
         }
-        if (d1.src) {
+        if (has1) {
             uint4* t1 = d1.dst + layer * lat_layer;
             st_stream(t1 + lane, v[2]);
             st_stream(t1 + lane + 32, v[3]);

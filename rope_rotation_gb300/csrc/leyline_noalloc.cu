@@ -74,6 +74,7 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
                                       int32_t n, void* stream_v)
 {
     clear_error();
+    const HostClock t_enter = host_now();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
     if (!bt || !bt->table || !bt->seq_lens_dev || !bt->seq_lens_host || bt->num_reqs < 0 || bt->max_blocks < 0)
         return set_error(LEYLINE_ERR_INVALID_ARG, "incomplete block table");
@@ -85,12 +86,15 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     bool host_rows = false;
     int rc = resolve_repl_rows(dirs, n, p->device, &resolved, &use, &host_rows);
     if (rc != LEYLINE_OK) return rc;
+    const HostClock t_resolved = host_now();
     Plan plan;
     const int64_t free_now = p->q_tail - p->q_head;
     rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
+    const HostClock t_planned = host_now();
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
+        set_host_times(&p->last_stats, t_enter, t_resolved, t_planned);
         return LEYLINE_OK;
     }
     if (free_now - plan.total_pop + plan.total_push > p->g.num_pages)
@@ -187,5 +191,6 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     p->q_head += plan.total_pop;
     p->q_tail += plan.total_push;
     p->last_stats = plan.stats;
+    set_host_times(&p->last_stats, t_enter, t_resolved, t_planned);
     return LEYLINE_OK;
 }

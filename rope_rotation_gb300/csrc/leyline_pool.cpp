@@ -39,6 +39,9 @@ namespace {
 
 constexpr size_t kPlanSlotBytes = 64 << 10;  // pinned plan staging per slot (grown on demand)
 
+// Timing event pairs created when kernel timing is switched on (more are made on demand).
+constexpr size_t kTimingEventsUpFront = 256;
+
 struct DeviceGuard {
     int prev = -1;
     bool ok = false;
@@ -337,6 +340,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
                    void* stream_v)
 {
     clear_error();
+    const HostClock t_enter = host_now();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
     if (!bt || !bt->table || !bt->seq_lens_dev || !bt->seq_lens_host || bt->num_reqs < 0 || bt->max_blocks < 0)
         return set_error(LEYLINE_ERR_INVALID_ARG, "incomplete block table");
@@ -348,12 +352,15 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     bool host_rows = false;
     int rc = resolve_repl_rows(dirs, n, p->device, &resolved, &use, &host_rows);
     if (rc != LEYLINE_OK) return rc;
+    const HostClock t_resolved = host_now();
     Plan plan;
     const int64_t free_now = p->q_tail - p->q_head;
     rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
     if (rc != LEYLINE_OK) return rc;
+    const HostClock t_planned = host_now();
     if (plan.reqs.empty()) {
         p->last_stats = plan.stats;
+        set_host_times(&p->last_stats, t_enter, t_resolved, t_planned);
         return LEYLINE_OK;
     }
     if (free_now - plan.total_pop + plan.total_push > p->g.num_pages)
@@ -457,8 +464,11 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     if (p->timing) {
         if (p->tev_used == p->tev.size()) {
             cudaEvent_t x, y;
-            if (cudaEventCreate(&x) != cudaSuccess || cudaEventCreate(&y) != cudaSuccess)
+            if (cudaEventCreate(&x) != cudaSuccess) return set_error(LEYLINE_ERR_CUDA, "creating timing events");
+            if (cudaEventCreate(&y) != cudaSuccess) {
+                cudaEventDestroy(x);
                 return set_error(LEYLINE_ERR_CUDA, "creating timing events");
+            }
             p->tev.emplace_back(x, y);
         }
         t0 = p->tev[p->tev_used].first;
@@ -478,6 +488,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     p->q_head += plan.total_pop;
     p->q_tail += plan.total_push;
     p->last_stats = plan.stats;
+    set_host_times(&p->last_stats, t_enter, t_resolved, t_planned);
     return LEYLINE_OK;
 }
 
@@ -569,6 +580,19 @@ int leyline_kernel_timing_enable(leyline_pool_t* p, int32_t enable)
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
     p->timing = enable != 0;
     p->tev_used = 0;
+    if (p->timing && p->tev.size() < kTimingEventsUpFront) {
+        // created now, so that the timed calls themselves create no events
+        DeviceGuard guard(p->device);
+        while (p->tev.size() < kTimingEventsUpFront) {
+            cudaEvent_t x, y;
+            if (cudaEventCreate(&x) != cudaSuccess) return set_error(LEYLINE_ERR_CUDA, "creating timing events");
+            if (cudaEventCreate(&y) != cudaSuccess) {
+                cudaEventDestroy(x);
+                return set_error(LEYLINE_ERR_CUDA, "creating timing events");
+            }
+            p->tev.emplace_back(x, y);
+        }
+    }
     return LEYLINE_OK;
 }
 

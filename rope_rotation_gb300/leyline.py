@@ -75,7 +75,8 @@ class Stats(ctypes.Structure):
                 ("moved_bytes", ctypes.c_int64), ("pages_popped", ctypes.c_int64),
                 ("pages_pushed", ctypes.c_int64), ("requests_touched", ctypes.c_int32),
                 ("kernels_launched", ctypes.c_int32), ("reindexed", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("reserved", ctypes.c_int32), ("host_ns", ctypes.c_int64), ("resolve_ns", ctypes.c_int64),
+                ("plan_ns", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -218,38 +219,83 @@ class Tables:
                              int(table.shape[0]), int(table.shape[1]))
 
 
+def _repl_ptr(repl, n_repl: Optional[int]):
+    """(n_repl, address) of a directive's rows of R, checked as the library will read them."""
+    if repl is None:
+        return (0 if n_repl is None else n_repl), None
+    shape = repl.shape
+    if n_repl is None:
+        n_repl = int(shape[1]) if len(shape) == 3 else -1
+    if len(shape) != 3 or int(shape[1]) < n_repl:
+        raise ValueError(f"repl: shape {tuple(shape)}, expected [num_layers][>= {n_repl}][row]")
+    if int(shape[1]) != n_repl:
+        raise ValueError(f"repl: {int(shape[1])} rows per layer but n_repl = {n_repl}; the layer stride "
+                         "of R is n_repl rows, so pass R with exactly n_repl rows per layer")
+    return n_repl, _rows_ptr(repl, "repl")
+
+
 def directive(req: int, s_start: int, s_end: int, repl=None, n_repl: Optional[int] = None,
               mode: int = LEYLINE_AMORTIZE) -> Directive:
     """repl: bf16 tensor [num_layers][n_repl][row], contiguous, on the pool's GPU or in pinned host
     memory (read in place by the kernel), or None."""
-    if n_repl is None:
-        n_repl = 0 if repl is None else int(repl.shape[1])
-    if repl is None:
-        return Directive(req, mode, s_start, s_end, n_repl, 0, None)
-    if repl.dim() != 3 or int(repl.shape[1]) < n_repl:
-        raise ValueError(f"repl: shape {tuple(repl.shape)}, expected [num_layers][>= {n_repl}][row]")
-    if int(repl.shape[1]) != n_repl:
-        raise ValueError(f"repl: {int(repl.shape[1])} rows per layer but n_repl = {n_repl}; the layer stride "
-                         "of R is n_repl rows, so pass R with exactly n_repl rows per layer")
-    return Directive(req, mode, s_start, s_end, n_repl, 0, _rows_ptr(repl, "repl"))
+    n_repl, ptr = _repl_ptr(repl, n_repl)
+    return Directive(req, mode, s_start, s_end, n_repl, 0, ptr)
 
 
-def _dir_array(dirs: Sequence[Directive]):
-    arr = (Directive * max(len(dirs), 1))(*dirs)
-    return arr
+# leyline_directive_t as a numpy record: a structured array of it is a C array of
+# directives, which the splice calls take without per-element marshalling.
+DIRECTIVE_DTYPE = np.dtype([("req", "<i4"), ("mode", "<i4"), ("s_start", "<i8"), ("s_end", "<i8"),
+                            ("n_repl", "<i4"), ("reserved", "<i4"), ("repl_rows", "<u8")], align=True)
+assert DIRECTIVE_DTYPE.itemsize == ctypes.sizeof(Directive)
+assert all(DIRECTIVE_DTYPE.fields[n][1] == getattr(Directive, n).offset for n, _ in Directive._fields_)
+
+
+def directive_batch(req, s_start, s_end, repl: Optional[Sequence] = None, n_repl=None,
+                    mode=LEYLINE_AMORTIZE) -> np.ndarray:
+    """Many directives at once: req, s_start, s_end (and n_repl, mode) are equal-length
+    sequences or scalars; repl is a sequence of tensors or None, checked as directive()
+    checks one.  Returns a structured array of DIRECTIVE_DTYPE that the splice calls take
+    as is; its fields can be changed in place (numpy) between calls."""
+    req = np.atleast_1d(np.asarray(req, dtype=np.int64))
+    n = req.size
+    out = np.zeros(n, dtype=DIRECTIVE_DTYPE)
+    out["req"] = req
+    out["s_start"] = np.broadcast_to(np.asarray(s_start, dtype=np.int64), n)
+    out["s_end"] = np.broadcast_to(np.asarray(s_end, dtype=np.int64), n)
+    out["mode"] = np.broadcast_to(np.asarray(mode, dtype=np.int64), n)
+    rows = [None] * n if repl is None else list(repl)
+    if len(rows) != n:
+        raise ValueError(f"repl: {len(rows)} entries for {n} directives")
+    counts = [None] * n if n_repl is None else [int(c) for c in np.broadcast_to(np.asarray(n_repl), n)]
+    checked = [_repl_ptr(t, c) for t, c in zip(rows, counts)]
+    out["n_repl"] = [c for c, _ in checked]
+    out["repl_rows"] = [p or 0 for _, p in checked]
+    return out
+
+
+def _dir_array(dirs):
+    """(pointer argument, count) for a sequence of Directive or a DIRECTIVE_DTYPE array."""
+    if isinstance(dirs, np.ndarray):
+        if dirs.dtype != DIRECTIVE_DTYPE or dirs.ndim != 1 or not dirs.flags.c_contiguous:
+            raise ValueError("directive arrays must be 1-D, contiguous and of DIRECTIVE_DTYPE")
+        if dirs.size == 0:
+            return (Directive * 1)(), 0
+        return dirs.ctypes.data_as(ctypes.POINTER(Directive)), int(dirs.size)
+    return (Directive * max(len(dirs), 1))(*dirs), len(dirs)
 
 
 # ---------------------------------------------------------------- splice ----
 
-def leyline_splice(pool, tables: Tables, dirs: Sequence[Directive], stream=None) -> None:
-    arr = _dir_array(dirs)
-    _check(load().leyline_splice(pool, ctypes.byref(tables.bt), arr, len(dirs), _stream_ptr(stream)))
+def leyline_splice(pool, tables: Tables, dirs, stream=None) -> None:
+    """dirs: a sequence of Directive (directive()) or a DIRECTIVE_DTYPE array (directive_batch())."""
+    arr, n = _dir_array(dirs)
+    _check(load().leyline_splice(pool, ctypes.byref(tables.bt), arr, n, _stream_ptr(stream)))
 
 
-def leyline_splice_noalloc(pool, tables: Tables, dirs: Sequence[Directive], stream=None) -> None:
+def leyline_splice_noalloc(pool, tables: Tables, dirs, stream=None) -> None:
     """leyline_splice with its scratch in the library's static device array (no allocation)."""
-    arr = _dir_array(dirs)
-    _check(load().leyline_splice_noalloc(pool, ctypes.byref(tables.bt), arr, len(dirs), _stream_ptr(stream)))
+    arr, n = _dir_array(dirs)
+    _check(load().leyline_splice_noalloc(pool, ctypes.byref(tables.bt), arr, n, _stream_ptr(stream)))
 
 
 def leyline_splice_plan(desc: PoolDesc, seq_lens_host, max_blocks: int, dirs: Sequence[Directive],
@@ -258,10 +304,10 @@ def leyline_splice_plan(desc: PoolDesc, seq_lens_host, max_blocks: int, dirs: Se
     lens = np.ascontiguousarray(seq_lens_host, dtype=np.int64)
     out = np.empty(max(lens.size, 1), dtype=np.int64)
     st = Stats()
-    arr = _dir_array(dirs)
+    arr, n = _dir_array(dirs)
     p64 = ctypes.POINTER(ctypes.c_int64)
     _check(load().leyline_splice_plan(ctypes.byref(desc), lens.ctypes.data_as(p64), lens.size, max_blocks, arr,
-                                      len(dirs), free_pages, ctypes.byref(st), out.ctypes.data_as(p64)))
+                                      n, free_pages, ctypes.byref(st), out.ctypes.data_as(p64)))
     return st, out[:lens.size]
 
 

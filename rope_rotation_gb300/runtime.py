@@ -117,7 +117,8 @@ class PagedCache:
         row = self.table[req].cpu().numpy().astype(np.int64)
         return row[t // self.block_size] * self.block_size + t % self.block_size
 
-    def splice(self, dirs: Sequence[leyline.Directive], stream=None) -> None:
+    def splice(self, dirs, stream=None) -> None:
+        """dirs: a list of leyline.directive() or one leyline.directive_batch() array."""
         leyline.leyline_splice(self.pool, self.tables, dirs, stream)
 
     def gather(self, req: int, layer: int, t0: int, t1: int, out=None, stream=None):

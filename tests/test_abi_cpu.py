@@ -208,3 +208,50 @@ def test_binding_refuses_tensors_it_cannot_pass_as_rows(L):
                     (torch.zeros((3, 576), dtype=torch.bfloat16), {})]:
         with pytest.raises(ValueError):
             L.directive(0, 1, 2, bad, **kw)
+
+
+def test_directive_batch_is_the_c_directive_array(L):
+    """directive_batch() builds the same bytes as a C array of directive() results, and the
+    planner returns the same work and lengths for either form."""
+    import torch
+    w = configs.by_name("cfg3")
+    step = w.steps[0]
+    R = {d.key: torch.zeros(2, d.n_repl, 576, dtype=torch.bfloat16) for d in step if d.n_repl}
+    one = [L.directive(d.req, d.s_start, d.s_end, R.get(d.key), n_repl=d.n_repl) for d in step]
+    batch = L.directive_batch([d.req for d in step], [d.s_start for d in step], [d.s_end for d in step],
+                              [R.get(d.key) for d in step], n_repl=[d.n_repl for d in step])
+    assert batch.tobytes() == bytes((L.Directive * len(one))(*one))
+    desc = L.pool_desc(w.num_layers, w.block_size, 1 << 30)
+    mb = max(-(-(x + 200) // w.block_size) for x in w.lengths)
+    st1, len1 = L.leyline_splice_plan(desc, np.array(w.lengths), mb, one)
+    st2, len2 = L.leyline_splice_plan(desc, np.array(w.lengths), mb, batch)
+    assert st1.as_dict() == st2.as_dict() and list(len1) == list(len2)
+    assert st1.downstream_slots > 0
+    # fields edited in place between calls: the request ids of the next batch of requests
+    moved = batch.copy()
+    moved["req"] += 1
+    st3, len3 = L.leyline_splice_plan(desc, np.array([0] + list(w.lengths)), mb, moved)
+    assert st3.downstream_slots == st1.downstream_slots and list(len3[1:]) == list(len1)
+    # modes broadcast; an empty batch is a no-op
+    ev = L.directive_batch([0, 1], [5, 9], [7, 9], None, mode=L.LEYLINE_EVICT)
+    assert list(ev["mode"]) == [L.LEYLINE_EVICT] * 2 and list(ev["n_repl"]) == [0, 0]
+    st0, len0 = L.leyline_splice_plan(desc, np.array([30, 40]), 16, L.directive_batch([], [], []))
+    assert st0.requests_touched == 0 and list(len0) == [30, 40]
+
+
+def test_directive_batch_refusals(L):
+    import torch
+    with pytest.raises(ValueError):  # rows of R must be bf16
+        L.directive_batch([0], [0], [1], [torch.zeros(2, 3, 576)])
+    with pytest.raises(ValueError):  # exactly n_repl rows per layer
+        L.directive_batch([0], [0], [1], [torch.zeros(2, 3, 576, dtype=torch.bfloat16)], n_repl=2)
+    with pytest.raises(ValueError):  # one entry of repl per directive
+        L.directive_batch([0, 1], [0, 0], [1, 1], [None])
+    with pytest.raises(ValueError):  # contiguous rows only
+        L.directive_batch([0], [0], [1], [torch.zeros(2, 576, 3, dtype=torch.bfloat16).transpose(1, 2)])
+    good = L.directive_batch([0, 1, 0, 1], [0, 0, 2, 2], [1, 1, 3, 3])
+    desc = L.pool_desc(4, 16, 1 << 20)
+    same_size = np.zeros(2, dtype=[(f, "<i8") for f in "abcde"])  # 40 bytes, another record
+    for bad in (good[::2], same_size, np.zeros(2, dtype=np.int64)):
+        with pytest.raises(ValueError):
+            L.leyline_splice_plan(desc, np.array([10, 10]), 8, bad)

@@ -281,8 +281,9 @@ def test_gqa_rows(layout, B, flags):
 # Many calls in flight: plans too large for a kernel parameter are staged through a
 # ring of pinned slots, so the host enqueues call after call without waiting; the
 # final caches must equal the oracle's chain.
-@pytest.mark.parametrize("flags", [0, REINDEX])
-def test_many_calls_in_flight_with_uploaded_plans(flags):
+@pytest.mark.parametrize("flags,batch", [(0, False), (REINDEX, False), (0, True), (REINDEX, True)])
+def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
+    """batch: the directives go in as one directive_batch() record array per call."""
     import torch
     from rope_rotation_gb300 import leyline
     rng = np.random.default_rng(77)
@@ -309,7 +310,13 @@ def test_many_calls_in_flight_with_uploaded_plans(flags):
     for step in steps:  # no synchronisation between calls
         dirs, k = H.gpu_directives(w, step)
         keep.append(k)
+        if batch:
+            dirs = leyline.directive_batch([d.req for d in step], [d.s_start for d in step],
+                                           [d.s_end for d in step], k, n_repl=[d.n_repl for d in step],
+                                           mode=[d.mode for d in step])
         cache.splice(dirs)
+        st = cache.last_stats()  # the library's account of its host time for this call
+        assert st["host_ns"] >= st["resolve_ns"] + st["plan_ns"] and st["plan_ns"] > 0
     torch.cuda.synchronize()
     cache.check_status()
     state = H.oracle_state(w)
