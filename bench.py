@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # capture, valid only for the kernel code it was taken on (kernel_sha)
 # (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.9 MB; the
 # rest of the 210.9 MB written was still in L2 when the single captured launch ended).
-NCU_TRAFFIC = {"kernel_sha256": "e6b02bceef6cc35876cb24000d25a55d08e76b5912e7f7676d7ef9c58132c026",
-               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210927616 + 161605888}}
+NCU_TRAFFIC = {"kernel_sha256": "19d520470faab6e3ea43a79c15439d1955f5ef2bd1b651464bc19bb1f1f8a00d",
+               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210919424 + 161109248}}
 
 
 def parse():
