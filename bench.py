@@ -357,7 +357,7 @@ def run_ours(args, rank, world, local):
             if args.e2e_copy:
                 for k2, v in repl_host.items():
                     rbuf[k2].copy_(v, non_blocking=True)
-            cache.splice(dirs_for(g, src))
+            cache.splice(dirs_for(g, src), stream_ptr)
             out_tab[k].copy_(cache.table[g * C:(g + 1) * C], non_blocking=True)
             out_len[k].copy_(cache.seq_lens_dev[g * C:(g + 1) * C], non_blocking=True)
         e1.record(stream)

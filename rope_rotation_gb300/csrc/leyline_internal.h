@@ -89,7 +89,7 @@ struct SpliceArgs {
     int32_t max_blocks;
     int32_t move_kernel;      // MoveKernel
     int32_t reindex;          // 1: prep + in-place rotation + staged commit
-    int32_t pad2;
+    int32_t prep_ctas;        // re-index: CTAs of the prep part of the prep + rows-of-R launch
     Geometry g;
 };
 

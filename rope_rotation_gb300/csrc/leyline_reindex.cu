@@ -13,80 +13,79 @@ namespace {
 // Re-index mode (pool flag LEYLINE_POOL_REINDEX; block size 1, or a call whose
 // directives all lie on block boundaries): a surviving downstream block keeps its
 // page.  Up to four kernels, each a programmatic dependent of the one before:
-//   prep          stages the page of every rewritten table entry (the kept block's
-//                 old page, or a fresh page for a block of R) and returns the pages
-//                 of dropped blocks to the ring; it reads the old table and writes
-//                 only the staging array and the ring's push region;
-//   rows of R     copies the call's rows of R into their fresh pages (if any);
+//   prep + R      one launch of two parts.  Prep CTAs stage the page of every
+//                 rewritten table entry (the kept block's old page, or a fresh page)
+//                 and return the pages of dropped blocks to the ring; they read the old
+//                 table and write only the staging array, the ring's push region and
+//                 (lazy pools) the counts of kept and returned pages.  The other CTAs
+//                 copy the call's rows of R into their fresh pages, which they find in
+//                 the ring's pop region by prep's own rule, so the parts do not wait on
+//                 each other;
+//   fresh rows    survivor and prefix rows of boundary blocks into their staged fresh
+//                 pages (if any);
 //   rotate        turns the rope bands of every turned row in place (128 bytes read
 //                 and written per band and layer; the latent is not touched; if any);
 //   commit        installs the staged entries, clears entries past the new end,
 //                 writes the new length.
-template <class PlanSrc>
-__global__ void prep_reindex(const __grid_constant__ SpliceArgs a, const __grid_constant__ PlanSrc plan)
+// One prep item i: the page of new block i of its request (the kept block's old page,
+// or its fresh page), or the return of one dropped old block to the ring.
+__device__ __forceinline__ void prep_item(const SpliceArgs& a, const PlanView& pv, long long i)
 {
-    wait_for_previous_grid();
-    allow_next_grid();
-    const PlanView pv = plan_view(a, plan);
-    const long long stride = (long long)gridDim.x * blockDim.x;
     const long long B = a.g.block_size;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_prep; i += stride) {
-        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_PREP)];
-        const long long k = i - rp.prep_begin;
-        const long long blocks = (rp.new_len + B - 1) / B - rp.b0;  // new blocks from b0 on
-        const int32_t* trow = a.table + (long long)rp.req * a.max_blocks;
-        if (k < blocks) {
-            const long long jb = rp.b0 + k;  // new block
-            const long long p = jb * B;      // its first row
-            const long long valid = rp.new_len - p < B ? rp.new_len - p : B;
-            const Seg* sg = pv.segs + rp.seg_begin;
-            const Seg s = sg[find_seg(sg, rp.seg_count, p)];
-            int page;
-            if (jb >= s.kb0 && jb < s.kb1) {  // kept: the old block holding exactly these rows
-                const long long ob = (s.src_start + (p - s.new_start)) / B;
-                page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
-                if (page < 0 || page >= a.g.num_pages) {
-                    raise_status(a.status, ST_BAD_PAGE);
-                    page = -1;
-                }
-                if (a.pending && page >= 0 && s.turn != 0)  // the valid slots turn; the others stay 0
-                    for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] += s.turn;
-            } else {  // fresh: the new block's position among the request's fresh blocks
-                const long long kept_before = s.kept_before + (jb < s.kb0 ? 0 : (long long)s.kb1 - s.kb0);
-                page = a.free_q[ring(a.pop_base + rp.pop_off + (k - kept_before), a.q_cap)];
-                if (page < 0 || page >= a.g.num_pages) {
-                    raise_status(a.status, ST_BAD_FRESH);
-                    page = -1;
-                }
-            }
-            a.stage[rp.stage_begin + k] = page;
-        } else {
-            const long long j = k - blocks;  // j-th returned old block of the request
-            const Seg* dg = pv.segs + rp.drop_seg_begin;
-            int q = 0;
-            for (int x = 1; x < rp.drop_seg_count; ++x)
-                if (dg[x].aux <= j) q = x;
-            const long long ob = dg[q].src_start + (j - dg[q].aux);
-            int page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
+    const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_PREP)];
+    const long long k = i - rp.prep_begin;
+    const long long blocks = (rp.new_len + B - 1) / B - rp.b0;  // new blocks from b0 on
+    const int32_t* trow = a.table + (long long)rp.req * a.max_blocks;
+    if (k < blocks) {
+        const long long jb = rp.b0 + k;  // new block
+        const long long p = jb * B;      // its first row
+        const long long valid = rp.new_len - p < B ? rp.new_len - p : B;
+        const Seg* sg = pv.segs + rp.seg_begin;
+        const Seg s = sg[find_seg(sg, rp.seg_count, p)];
+        int page;
+        if (jb >= s.kb0 && jb < s.kb1) {  // kept: the old block holding exactly these rows
+            const long long ob = (s.src_start + (p - s.new_start)) / B;
+            page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
             if (page < 0 || page >= a.g.num_pages) {
-                raise_status(a.status, ST_BAD_OLD);
+                raise_status(a.status, ST_BAD_PAGE);
                 page = -1;
             }
-            a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
-            // a free page carries no pending turn; when the fresh-rows kernel still reads
-            // survivors from the request's returned pages, the commit clears them instead
-            if (a.pending && page >= 0 && rp.fresh_seg_count == 0)
-                for (long long sl = 0; sl < B; ++sl) a.pending[(long long)page * B + sl] = 0;
+            if (a.pending && page >= 0 && s.turn != 0)  // the valid slots turn; the others stay 0
+                for (long long sl = 0; sl < valid; ++sl) a.pending[(long long)page * B + sl] += s.turn;
+        } else {  // fresh: the new block's position among the request's fresh blocks
+            const long long kept_before = s.kept_before + (jb < s.kb0 ? 0 : (long long)s.kb1 - s.kb0);
+            page = a.free_q[ring(a.pop_base + rp.pop_off + (k - kept_before), a.q_cap)];
+            if (page < 0 || page >= a.g.num_pages) {
+                raise_status(a.status, ST_BAD_FRESH);
+                page = -1;
+            }
         }
+        a.stage[rp.stage_begin + k] = page;
+    } else {
+        const long long j = k - blocks;  // j-th returned old block of the request
+        const Seg* dg = pv.segs + rp.drop_seg_begin;
+        int q = 0;
+        for (int x = 1; x < rp.drop_seg_count; ++x)
+            if (dg[x].aux <= j) q = x;
+        const long long ob = dg[q].src_start + (j - dg[q].aux);
+        int page = (ob >= 0 && ob < a.max_blocks) ? trow[ob] : -1;
+        if (page < 0 || page >= a.g.num_pages) {
+            raise_status(a.status, ST_BAD_OLD);
+            page = -1;
+        }
+        a.free_q[ring(a.push_base + rp.push_off + j, a.q_cap)] = page;
+        // a free page carries no pending turn; when the fresh-rows kernel still reads
+        // survivors from the request's returned pages, the commit clears them instead
+        if (a.pending && page >= 0 && rp.fresh_seg_count == 0)
+            for (long long sl = 0; sl < B; ++sl) a.pending[(long long)page * B + sl] = 0;
     }
 }
 
-
 // Re-index mode writes fresh rows and turns kept bands.
-//   copy_repl_reindex: the call's rows of R form one list; items of (row, 8 layers)
-//   are spread over every warp of the grid, a lane moving every 32nd vector of the
-//   row with four loads in flight.  A row of R moves 9 times the bytes of a turned
-//   band, so rows of R are not tied to one CTA's share of the tiles.
+//   prep_repl_reindex (its row-of-R part): the call's rows of R form one list; items
+//   of (row, 8 layers) are spread over every warp of its CTAs, a lane moving every
+//   32nd vector of the row with four loads in flight.  A row of R moves 9 times the
+//   bytes of a turned band, so rows of R are not tied to one CTA's share of the tiles.
 //   copy_fresh_reindex: the other rows of blocks that get fresh pages (survivors and
 //   prefix rows of boundary blocks), likewise spread over warps, read through the old
 //   table and turned by their segment's cos/sin.
@@ -109,64 +108,88 @@ __host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, i
     return l > 0 ? l : 1;
 }
 
-// Rows of R of a re-indexed call into their fresh pages (the pages prep staged).
+// One row-of-R item: row rrow of the call's rows of R, layers [l0, l0 + kFreshLayers),
+// moved by one warp into the row's fresh page.  The page is the one prep stages for
+// the row's block (a block holding a row of R is never kept): the block's position
+// among its request's fresh blocks, read from the ring's pop region.
+__device__ __forceinline__ void repl_item(const SpliceArgs& a, const PlanView& pv, long long rrow, long long l0,
+                                          int lane)
+{
+    const long long L = a.g.num_layers;
+    const int row_vecs = a.g.row_vecs, lv = a.g.latent_vecs;
+    uint4* kv = static_cast<uint4*>(a.kv);
+    const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, rrow, BY_REPL)];
+    long long j = rrow - rp.repl_begin;  // row within the request's rows of R
+    const Seg* sg = pv.segs + rp.seg_begin;
+    int k = -1;
+    for (int q = 0; q < rp.seg_count && k < 0; ++q) {
+        if (sg[q].kind != SEG_REPL) continue;
+        if (j < sg[q].n_repl) k = q;
+        else j -= sg[q].n_repl;
+    }
+    if (k < 0) {
+        if (lane == 0) raise_status(a.status, ST_BAD_FRESH);
+        return;
+    }
+    const Seg s = sg[k];
+    const long long p = s.new_start + j;  // rows fit 32 bits (the planner checks lengths)
+    const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
+    const Seg sb = sg[find_seg(sg, rp.seg_count, (long long)pb * B)];  // segment of the block's first row
+    const long long kept_before = sb.kept_before + ((long long)pb < sb.kb0 ? 0 : (long long)sb.kb1 - sb.kb0);
+    const int page = a.free_q[ring(a.pop_base + rp.pop_off + ((long long)pb - rp.b0 - kept_before), a.q_cap)];
+    if (page < 0 || page >= a.g.num_pages) {
+        if (lane == 0) raise_status(a.status, ST_BAD_FRESH);
+        return;
+    }
+    const long long slot = (long long)page * B + ((unsigned)p - pb * B);
+    if (a.pending && l0 == 0 && lane == 0) a.pending[slot] = 0;  // R is encoded at its final position
+    const long long rstride = (long long)s.n_repl * row_vecs;
+    const uint4* src = static_cast<const uint4*>(s.repl) + j * row_vecs;
+    const long long l1 = l0 + kFreshLayers < L ? l0 + kFreshLayers : L;
+    for (long long layer = l0; layer < l1; ++layer) {
+        for (int c0 = 0; c0 < row_vecs; c0 += 4 * 32) {
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = c0 + 32 * q + lane;
+                if (c < row_vecs) v[q] = ld_stream(src + layer * rstride + c);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int c = c0 + 32 * q + lane;
+                if (c < row_vecs)
+                    st_stream(kv + (c < lv ? lat_off(a.g, layer, slot) + c : band_off(a.g, layer, slot) + (c - lv)),
+                              v[q]);
+            }
+        }
+    }
+}
+
+// Prep and the rows of R in one launch: CTAs [0, a.prep_ctas) take the prep items
+// (one per thread), the others the row-of-R items (one per warp).  The two parts
+// write disjoint memory (staging array, ring push region and the counts of kept and
+// returned pages; fresh pages and their counts), so neither waits for the other.
 template <class PlanSrc>
-__global__ void __launch_bounds__(kMoveThreads) copy_repl_reindex(const __grid_constant__ SpliceArgs a,
+__global__ void __launch_bounds__(kMoveThreads) prep_repl_reindex(const __grid_constant__ SpliceArgs a,
                                                                   const __grid_constant__ PlanSrc plan)
 {
     wait_for_previous_grid();
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
+    const long long prep_ctas = a.prep_ctas;
+    if ((long long)blockIdx.x < prep_ctas) {
+        const long long stride = prep_ctas * blockDim.x;
+        for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < a.total_prep; i += stride)
+            prep_item(a, pv, i);
+        return;
+    }
     const int lane = threadIdx.x & 31;
-    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    const long long L = a.g.num_layers;
-    const int chunks = (int)((L + kFreshLayers - 1) / kFreshLayers);
-    const int row_vecs = a.g.row_vecs, lv = a.g.latent_vecs;
-    uint4* kv = static_cast<uint4*>(a.kv);
+    const long long gw = (((long long)blockIdx.x - prep_ctas) * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = (((long long)gridDim.x - prep_ctas) * blockDim.x) >> 5;
+    const long long chunks = (a.g.num_layers + kFreshLayers - 1) / kFreshLayers;
     for (long long w = gw; w < a.total_repl * chunks; w += nw) {
         const long long rrow = w / chunks;
-        const long long l0 = (w - rrow * chunks) * kFreshLayers;
-        const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, rrow, BY_REPL)];
-        long long j = rrow - rp.repl_begin;  // row within the request's rows of R
-        const Seg* sg = pv.segs + rp.seg_begin;
-        int k = -1;
-        for (int q = 0; q < rp.seg_count && k < 0; ++q) {
-            if (sg[q].kind != SEG_REPL) continue;
-            if (j < sg[q].n_repl) k = q;
-            else j -= sg[q].n_repl;
-        }
-        if (k < 0) {
-            if (lane == 0) raise_status(a.status, ST_BAD_FRESH);
-            continue;
-        }
-        const Seg s = sg[k];
-        const long long p = s.new_start + j;  // rows fit 32 bits (the planner checks lengths)
-        const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
-        const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
-        if (page < 0 || page >= a.g.num_pages) continue;  // prep has recorded a bad fresh page
-        const long long slot = (long long)page * B + ((unsigned)p - pb * B);
-        if (a.pending && l0 == 0 && lane == 0) a.pending[slot] = 0;  // R is encoded at its final position
-        const long long rstride = (long long)s.n_repl * row_vecs;
-        const uint4* src = static_cast<const uint4*>(s.repl) + j * row_vecs;
-        const long long l1 = l0 + kFreshLayers < L ? l0 + kFreshLayers : L;
-        for (long long layer = l0; layer < l1; ++layer) {
-            for (int c0 = 0; c0 < row_vecs; c0 += 4 * 32) {
-                uint4 v[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int c = c0 + 32 * q + lane;
-                    if (c < row_vecs) v[q] = ld_stream(src + layer * rstride + c);
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int c = c0 + 32 * q + lane;
-                    if (c < row_vecs)
-                        st_stream(kv + (c < lv ? lat_off(a.g, layer, slot) + c : band_off(a.g, layer, slot) + (c - lv)),
-                                  v[q]);
-                }
-            }
-        }
+        repl_item(a, pv, rrow, (w - rrow * chunks) * kFreshLayers, lane);
     }
 }
 
@@ -470,8 +493,16 @@ template <class PlanSrc>
 int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStream_t s, cudaEvent_t t0, cudaEvent_t t1)
 {
     cudaError_t e = cudaSuccess;
-    if (a.total_prep > 0)
-        e = launch_dependent(prep_reindex<PlanSrc>, grid_for(a.total_prep, 256, 8192), 256, s, a, plan);
+    // prep and the rows of R: one launch, prep CTAs first
+    const int prep_ctas = a.total_prep > 0 ? grid_for(a.total_prep, kMoveThreads, 8192) : 0;
+    const long long repl_items = a.total_repl * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
+    const int repl_ctas = repl_items > 0 ? grid_for(repl_items * 32, kMoveThreads, 8192) : 0;
+    if (t0) e = cudaEventRecord(t0, s);
+    if (e == cudaSuccess && prep_ctas + repl_ctas > 0) {
+        SpliceArgs b = a;
+        b.prep_ctas = prep_ctas;
+        e = launch_dependent(prep_repl_reindex<PlanSrc>, prep_ctas + repl_ctas, kMoveThreads, s, b, plan);
+    }
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
     const int ipr = a.g.rope_heads * (split ? a.g.head_vecs / 2 : a.g.head_vecs);
@@ -480,12 +511,6 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const int lpu = reindex_layers_per_unit(per_layer, mla ? 1 : kMaxItems);
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);
-    if (e == cudaSuccess && t0) e = cudaEventRecord(t0, s);
-    if (e == cudaSuccess && a.total_repl > 0) {  // rows of R: items of (row, kFreshLayers layers), a warp each
-        const long long items = a.total_repl * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
-        e = launch_dependent(copy_repl_reindex<PlanSrc>, grid_for(items * 32, kMoveThreads, 8192), kMoveThreads, s,
-                             a, plan);
-    }
     if (e == cudaSuccess && a.total_fresh > 0) {  // other fresh rows: items of (row, kFreshLayers layers)
         const long long items = a.total_fresh * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
         const int fgrid = grid_for(items * 32, kMoveThreads, 8192);

@@ -125,6 +125,11 @@ def gpu_directives(w: Workload, step: list[Dir]):
     return dirs, repl
 
 
+def work_stats(cache) -> dict:
+    """The last call's work accounting, without its host timings (which differ call to call)."""
+    return {k: v for k, v in cache.last_stats().items() if not k.endswith("_ns")}
+
+
 def logical_rows(cache, req: int, length: int) -> np.ndarray:
     """All layers of one request gathered through the C ABI, as uint16 [layers][L][row]."""
     import torch

@@ -39,7 +39,7 @@ def _run(w, cache):
         torch.cuda.synchronize()
         cache.check_status()
         del keep
-    return cache.last_stats()
+    return H.work_stats(cache)
 
 
 @pytest.mark.parametrize("B,flags,layout,precision,heads,rope", [
@@ -73,7 +73,7 @@ def test_block_reindex_split_equals_whole_rows():
             torch.cuda.synchronize()
             c.check_status()
             del keep
-        assert whole.last_stats() == split.last_stats()
+        assert H.work_stats(whole) == H.work_stats(split)
     for r in range(w.num_reqs):
         n = int(whole.seq_lens_host[r])
         assert np.array_equal(H.logical_rows(whole, r, n), H.logical_rows(split, r, n))
