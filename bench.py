@@ -54,6 +54,8 @@ def parse():
                     help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
     ap.add_argument("--lazy", action="store_true",
                     help="lazy pools: splices count pending turns instead of rotating (LEYLINE_POOL_LAZY)")
+    ap.add_argument("--read", action="store_true",
+                    help="lazy pools: also time leyline_materialize of the timed steps' requests")
     ap.add_argument("--split", action="store_true",
                     help="latents and rope bands in two arrays (LEYLINE_POOL_SPLIT_ROPE)")
     ap.add_argument("--e2e-copy", action="store_true",
@@ -370,6 +372,31 @@ def run_ours(args, rank, world, local):
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h,
                "inputs": "rows of R copied to device buffers, then spliced" if args.e2e_copy
                else "rows of R read in place from pinned host memory by the move kernel"}
+    lazy_read = None
+    if args.lazy and args.read:
+        # the cost a lazy pool defers to its reads: materialize each request of the value
+        # leg's timed steps (every pending band turned in place once, counts cleared)
+        reqs = [g * C + r for g in range(W, W + K) for r in range(C)]
+        pend = cache.pending().view(-1)
+        turned = 0
+        for q in reqs:
+            t = torch.arange(int(cache.seq_lens_host[q]), device=dev)
+            slots = cache.table[q][t // B].long() * B + t % B
+            turned += int((pend[slots] != 0).sum())
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        hold_stream(torch)
+        r0.record(stream)
+        for q in reqs:
+            cache.materialize(q, stream_ptr)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        cache.check_status()
+        read_ms = r0.elapsed_time(r1)
+        band_bytes = 2 * w.num_layers * w.rope_heads * w.rope_dim * 2  # read + write per turned slot
+        lazy_read = {"op": "leyline_materialize", "requests": len(reqs), "turned_slots": turned,
+                     "ms": read_ms, "slots_per_s": turned / (read_ms / 1e3),
+                     "algorithmic_gbps": turned * band_bytes / (read_ms / 1e3) / 1e9}
     clocks = sampler.stop()
 
     # max over ranks
@@ -429,6 +456,8 @@ def run_ours(args, rank, world, local):
                      "launch_ms": k2_avg_s * 1e3, "launches_timed": k2_n,
                      "algorithmic_bytes_per_launch": st["algorithmic_bytes"]},
     }
+    if lazy_read:
+        line["lazy_read"] = lazy_read
     if e2e:
         line["e2e"] = {"value": slots / (e2e["ms"] / 1e3), "unit": "slots/s", "h2d_bytes_per_step": e2e["h2d"],
                        "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": e2e["ms"] / K,

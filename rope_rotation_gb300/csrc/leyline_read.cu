@@ -53,14 +53,45 @@ __device__ __forceinline__ void pending_trig(int pend, double theta_j, bool bf16
     }
 }
 
+// The read kernels run one warp per row.  A warp forms the cos / sin of every pair
+// of a band once per pending count -- a lane per pair, into the warp's slice of
+// shared memory -- and keeps them while the count stays the same (after a splice a
+// segment's survivors share one count); each lane then reads the pairs of its items.
+constexpr int kReadThreads = 256;
+constexpr int kMaxPairs = 128;  // rope_dim <= 256
+
+struct WarpTrig {
+    float2* cs;     // this warp's [kMaxPairs] (cos, sin)
+    int pend = 0;   // count the slice holds
+    bool valid = false;
+
+    __device__ __forceinline__ void ensure(int count, const double* theta_j, int half, bool bf16)
+    {
+        if (valid && count == pend) return;  // warp-uniform: the count is the row's
+        __syncwarp();                        // lanes are done reading the previous count's values
+        for (int j = threadIdx.x & 31; j < half; j += 32) {
+            float c, s;
+            pending_trig(count, theta_j[j], bf16, c, s);
+            cs[j] = make_float2(c, s);
+        }
+        __syncwarp();
+        pend = count;
+        valid = true;
+    }
+};
+
 // cos / sin of the pairs of item q of a band: 8 pairs j = 8q.. (half-split) or 4
 // pairs j = 4q.. (interleaved).
 template <int kLayout>
-__device__ __forceinline__ void item_trig(int pend, int q, const double* theta_j, bool bf16, float* c, float* s)
+__device__ __forceinline__ void item_trig(const float2* cs, int q, float* c, float* s)
 {
     constexpr int kPairs = kLayout == 0 ? 8 : 4;
 #pragma unroll
-    for (int w = 0; w < kPairs; ++w) pending_trig(pend, theta_j[kPairs * q + w], bf16, c[w], s[w]);
+    for (int w = 0; w < kPairs; ++w) {
+        const float2 v = cs[kPairs * q + w];
+        c[w] = v.x;
+        s[w] = v.y;
+    }
 }
 
 // Item q of the band at `band` (x at q, y at q + head_vecs / 2 for half-split),
@@ -90,10 +121,14 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
                                    long long t0, long long n, uint4* out, const int32_t* pending,
                                    const double* theta_j, int32_t* status)
 {
+    __shared__ float2 trig_smem[kReadThreads / 32][kMaxPairs];
     const int lane = threadIdx.x & 31;
     const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const int hv = g.head_vecs;
     const int head_items = kLayout == 0 ? hv / 2 : hv;
+    const int half = g.rope_dim / 2;
+    WarpTrig wt;
+    wt.cs = trig_smem[threadIdx.x / 32];
     const long long warps = (long long)gridDim.x * (blockDim.x / 32);
     for (long long r = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; r < n; r += warps) {
         const long long t = t0 + r;
@@ -109,6 +144,7 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
         uint4* o = out + r * g.row_vecs;
         for (int c = lane; c < g.latent_vecs; c += 32) o[c] = lat[c];
         const int pend = pending[slot];
+        if (pend != 0) wt.ensure(pend, theta_j, half, bf16);
         for (int it = lane; it < g.rope_heads * head_items; it += 32) {
             const int head = it / head_items, q = it - head * head_items;
             const uint4* band = bands + head * hv;
@@ -119,25 +155,32 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
                 continue;
             }
             float c[8], s[8];
-            item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
+            item_trig<kLayout>(wt.cs, q, c, s);
             turn_item<kLayout>(band, dst, q, hv, bf16, c, s);
         }
     }
 }
 
-// Materialize a lazy request: one warp per row.  Lanes take the row's (layer,
-// band item) pairs in turn, so the pair group q of a lane, and the cos / sin held
-// for it, change only when the items per layer do not divide 32.  The count is
-// read before and cleared after every layer of the row is turned in place.
+// Materialize a lazy request: one warp per row, its lanes walking the row's (layer,
+// band item) pairs.  When the items per layer divide 32 -- MLA bands, and 1, 2, 4 or 8
+// GQA heads -- a lane's item is the same in every layer, so its cos / sin are read
+// once per row and two layers' loads are in flight before either layer's stores.  The
+// count is read before and cleared after every layer of the row is turned in place.
 template <int kLayout>
 __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Geometry g, long long len,
                                    int32_t* pending, const double* theta_j, int32_t* status)
 {
+    __shared__ float2 trig_smem[kReadThreads / 32][kMaxPairs];
     const int lane = threadIdx.x & 31;
     const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const int hv = g.head_vecs;
     const int head_items = kLayout == 0 ? hv / 2 : hv;
     const int items = g.rope_heads * head_items;  // per layer
+    const int half = g.rope_dim / 2;
+    const long long n_it = (long long)g.num_layers * items;
+    const bool fixed_item = 32 % items == 0;
+    WarpTrig wt;
+    wt.cs = trig_smem[threadIdx.x / 32];
     const long long warps = (long long)gridDim.x * (blockDim.x / 32);
     for (long long t = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; t < len; t += warps) {
         const long long B = g.block_size;
@@ -149,18 +192,57 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Ge
         const long long slot = (long long)page * B + t % B;
         const int pend = pending[slot];
         if (pend == 0) continue;
+        wt.ensure(pend, theta_j, half, bf16);
         float c[8], s[8];
-        int have_q = -1;
-        for (long long idx = lane; idx < (long long)g.num_layers * items; idx += 32) {
-            const long long layer = idx / items;
-            const int it = (int)(idx - layer * items);
+        if (fixed_item) {
+            const int it = lane % items;
             const int head = it / head_items, q = it - head * head_items;
-            if (q != have_q) {
-                item_trig<kLayout>(pend, q, theta_j, bf16, c, s);
-                have_q = q;
+            item_trig<kLayout>(wt.cs, q, c, s);
+            for (long long idx = lane; idx < n_it; idx += 64) {
+                const bool two = idx + 32 < n_it;
+                uint4* b0 = kv + band_off(g, idx / items, slot) + head * hv;
+                uint4* b1 = kv + band_off(g, (idx + 32) / items, slot) + head * hv;
+                uint4 x0 = b0[q], y0, x1, y1;
+                if (kLayout == 0) y0 = b0[q + hv / 2];
+                if (two) {
+                    x1 = b1[q];
+                    if (kLayout == 0) y1 = b1[q + hv / 2];
+                }
+                if (kLayout == 0) {
+                    if (bf16) rotate_half_split<true>(x0, y0, c, s);
+                    else rotate_half_split<false>(x0, y0, c, s);
+                    b0[q] = x0;
+                    b0[q + hv / 2] = y0;
+                    if (two) {
+                        if (bf16) rotate_half_split<true>(x1, y1, c, s);
+                        else rotate_half_split<false>(x1, y1, c, s);
+                        b1[q] = x1;
+                        b1[q + hv / 2] = y1;
+                    }
+                } else {
+                    if (bf16) rotate_interleaved<true>(x0, c, s);
+                    else rotate_interleaved<false>(x0, c, s);
+                    b0[q] = x0;
+                    if (two) {
+                        if (bf16) rotate_interleaved<true>(x1, c, s);
+                        else rotate_interleaved<false>(x1, c, s);
+                        b1[q] = x1;
+                    }
+                }
             }
-            uint4* band = kv + band_off(g, layer, slot) + head * hv;
-            turn_item<kLayout>(band, band, q, hv, bf16, c, s);
+        } else {
+            int have_q = -1;
+            for (long long idx = lane; idx < n_it; idx += 32) {
+                const long long layer = idx / items;
+                const int it = (int)(idx - layer * items);
+                const int head = it / head_items, q = it - head * head_items;
+                if (q != have_q) {
+                    item_trig<kLayout>(wt.cs, q, c, s);
+                    have_q = q;
+                }
+                uint4* band = kv + band_off(g, layer, slot) + head * hv;
+                turn_item<kLayout>(band, band, q, hv, bf16, c, s);
+            }
         }
         __syncwarp();
         if (lane == 0) pending[slot] = 0;
@@ -199,7 +281,7 @@ int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry&
     const long long n = t1 - t0;
     if (n <= 0) return 0;
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? gather_lazy_kernel<0> : gather_lazy_kernel<1>;
-    k<<<grid_for(n * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(kv), table_row, g,
+    k<<<grid_for(n * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(kv), table_row, g,
                                                                       layer, t0, n, static_cast<uint4*>(out),
                                                                       pending, theta_j, status);
     return (int)cudaGetLastError();
@@ -210,7 +292,7 @@ int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, in
 {
     if (len <= 0) return 0;
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
-    k<<<grid_for(len * 32, 256, 8192), 256, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
+    k<<<grid_for(len * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
                                                                         pending, theta_j, status);
     return (int)cudaGetLastError();
 }
