@@ -170,10 +170,10 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workload --
 
-def workload(name: str, layers: int = 0):
+def workload(name: str, layers: int = 0, chain_ok: bool = False):
     from synth import configs
     w = configs.by_name(name)
-    if len(w.steps) != 1:
+    if len(w.steps) != 1 and not chain_ok:
         raise SystemExit(f"workload {name} is a multi-step chain; bench runs single-call workloads")
     if layers > 0:
         w.num_layers = layers
@@ -468,6 +468,136 @@ def run_ours(args, rank, world, local):
 
 # -------------------------------------------------------------- CPU oracle --
 
+def run_chain(args, rank, world, local):
+    """A workload of successive splices of one request (the 64-splice chain): a step is the
+    whole chain on a fresh copy of the request, its splices enqueued back to back (each one
+    planned on the lengths the one before left).  Value: downstream slots of all splices per
+    second; the roofline kernel is timed around every splice's move (or rotate) kernel."""
+    import torch
+    import __graft_entry__
+    from rope_rotation_gb300 import leyline
+    from rope_rotation_gb300.runtime import PagedCache
+    from synth import fill
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = workload(args.workload, args.layers, chain_ok=True)
+    K, W = args.steps, args.warmup
+    assert w.num_reqs == 1 and all(len(step) == 1 for step in w.steps), "one request, one directive per splice"
+    L0, B = w.lengths[0], w.block_size
+    nb = -(-max(L0, max(d.s_start + d.n_repl for step in w.steps for d in step)) // B) + 1
+    groups = W + K
+    flags = ((leyline.LEYLINE_POOL_REINDEX if args.reindex else 0) | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)
+             | (leyline.LEYLINE_POOL_SPLIT_ROPE if args.split else 0))
+    # every chain copy's pages, plus one request's worth for the fresh pages a rewrite takes
+    cache = PagedCache(w.num_layers, B, (groups + 1) * nb, groups, nb, w.latent_dim, w.rope_dim, w.theta, flags=flags)
+    seed = rank_seed(w.seed, rank)
+    for g in range(groups):
+        cache.add_request(g, L0)
+        fill.fill_request(cache, seed, g, L0)
+    tmpl = []
+    for step in w.steps:
+        d = step[0]
+        r = fill.repl_tensor(seed, 0, d.key, w.num_layers, d.n_repl, cache.row, dev) if d.n_repl else None
+        tmpl.append((leyline.directive_batch([0], [d.s_start], [d.s_end], [r], n_repl=[d.n_repl],
+                                             mode=[d.mode]), r))
+    stream = torch.cuda.current_stream()
+    stream_ptr = stream.cuda_stream
+
+    def chain(g, stats=None):
+        for t, _ in tmpl:
+            b = t.copy()
+            b["req"] = g
+            cache.splice(b, stream_ptr)
+            if stats is not None:
+                for k, v in cache.last_stats().items():
+                    stats[k] = stats.get(k, 0) + v
+
+    per_chain = {}
+    for g in range(W):
+        chain(g, per_chain if g == 0 else None)
+    if W == 0:
+        raise SystemExit("a chain needs at least one warm-up chain (its work counts come from it)")
+    torch.cuda.synchronize()
+    cache.check_status()
+    n_splices = len(tmpl)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    leyline.leyline_kernel_timing_enable(cache.pool, True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    hold_stream(torch)
+    ev0.record(stream)
+    t_host = time.perf_counter()
+    for g in range(W, W + K):
+        chain(g)
+    enqueue_us = (time.perf_counter() - t_host) * 1e6 / K
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    cache.check_status()
+    k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
+    leyline.leyline_kernel_timing_enable(cache.pool, False)
+    clocks = sampler.stop()
+    (elapsed_ms,) = reduce_max_over_ranks([elapsed_ms], world, dev)
+    value = job_value(per_chain["downstream_slots"], K, world, elapsed_ms)
+    peak, peak_kind = measured_peaks()
+    # per launch: the chain's algorithmic bytes spread over its timed launches
+    achieved = per_chain["algorithmic_bytes"] * K / (k2_ms / 1e3) / 1e9 if k2_ms > 0 else 0.0
+    reindexed = per_chain["reindexed"] > 0
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "slots/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": elapsed_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.num_layers, "tokens": L0, "block_size": B,
+                   "latent_dim": w.latent_dim, "rope_dim": w.rope_dim, "storage": "bf16",
+                   "splices_per_step": n_splices,
+                   "step": "the whole chain of successive splices on a fresh copy of the request",
+                   "downstream_slots_per_step": per_chain["downstream_slots"],
+                   "repl_slots_per_step": per_chain["repl_slots"],
+                   "algorithmic_bytes_per_step": per_chain["algorithmic_bytes"],
+                   "reindexed_splices": per_chain["reindexed"],
+                   "l2": "inputs larger than L2: each chain splices its own pre-filled request",
+                   "timing": "CUDA events around K chains queued behind a ~1 ms spin on the stream",
+                   "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
+                   + (", re-index" if args.reindex else "") + (", split rope" if args.split else ""),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gbps_step": per_chain["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
+        "slot_layers_per_s": value * w.num_layers,
+        "host": {"enqueue_us_per_step": enqueue_us, "enqueue_us_per_splice": enqueue_us / n_splices},
+        "clocks": clocks,
+        "gpu_launches": K * per_chain["kernels_launched"],
+        "roofline": {"kernel": "rotate_in_place" if reindexed else "move_rotate_vector", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "launch_ms": k2_ms / max(k2_n, 1), "launches_timed": k2_n,
+                     "algorithmic_bytes_per_launch": per_chain["algorithmic_bytes"] / n_splices},
+    }
+    cache.close()
+    return line, w
+
+
 def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
     """Time the fp64 oracle (single thread, as it stands) on whole calls of the workload,
     repeated until about budget_s seconds of CPU work."""
@@ -535,9 +665,11 @@ def main():
         if line is not None:
             print(json.dumps(line), flush=True)
         return
-    line, w = run_ours(args, rank, world, local)
+    from synth import configs
+    is_chain = len(configs.by_name(args.workload).steps) > 1
+    line, w = (run_chain if is_chain else run_ours)(args, rank, world, local)
     if rank == 0:
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and not is_chain:
             cb, _ = cpu_oracle_sample(w, args.cpu_seconds)
             line["cpu_baseline"] = cb
         print(json.dumps(line), flush=True)
