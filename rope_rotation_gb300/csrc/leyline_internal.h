@@ -107,14 +107,14 @@ int launch_splice(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stre
                   cudaEvent_t t1);
 int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
                   int64_t t1, void* out, int32_t* status, void* stream);
-// Lazy pools: gather turning each row's rope bands by its pending count; theta_j is
-// the device table of theta^(-2j/rope_dim) (fp64, rope_dim / 2 entries).
+// Lazy pools: gather turning each row's rope bands by its pending count; turn is the
+// pool's device turn table (see kTurnSpan below).
 int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
-                       int64_t t1, void* out, const int32_t* pending, const double* theta_j, int32_t* status,
+                       int64_t t1, void* out, const int32_t* pending, const double* turn, int32_t* status,
                        void* stream);
 // Lazy pools: turn rows [0, len) of one request by their pending counts, in place, and clear the counts.
 int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
-                       const double* theta_j, int32_t* status, void* stream);
+                       const double* turn, int32_t* status, void* stream);
 // Lazy pools: set the pending counts of n pages (device ids) to 0.
 int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream);
 // Device access to a caller buffer.  Memory of `device` and managed memory are
@@ -123,6 +123,15 @@ int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, i
 // link (NVLink-C2C on Grace hosts).  Pageable host memory and memory of another
 // device are refused (LEYLINE_ERR_INVALID_ARG, message naming `what`).
 int resolve_access(const void* ptr, int device, const char* what, void** alias, bool* is_host);
+
+// Lazy pools' turn table (device, fp64), read by the kernels that apply pending
+// counts: theta_j for the `half` pairs (padded to an even count), then
+//   lo[j][m] = (cos, sin)(m * theta_j)              m < kTurnSpan
+//   hi[j][m] = (cos, sin)(m * kTurnSpan * theta_j)  m < kTurnSpan
+// so that a count p < kTurnSpan^2 turns by the product of hi[j][p / kTurnSpan] and
+// lo[j][p % kTurnSpan] (angle addition) instead of a sincos.
+constexpr int kTurnSpan = 2048;
+inline size_t turn_table_doubles(int half) { return (size_t)(half + 1) / 2 * 2 + (size_t)4 * half * kTurnSpan; }
 
 // Host time of a splice call, reported in leyline_stats_t.
 using HostClock = std::chrono::steady_clock::time_point;
@@ -163,7 +172,7 @@ struct leyline_pool {
     int32_t move_kernel = 0;  // MoveKernel used by this pool
     int32_t* d_stage = nullptr;  // re-index: staged table entries
     int32_t* d_pending = nullptr;  // lazy: pending turns per slot
-    double* d_theta_j = nullptr;   // lazy: theta_j table for readers
+    double* d_theta_j = nullptr;   // lazy: the readers' turn table (layout at kTurnSpan)
     size_t d_stage_cap = 0;      // entries
     int32_t* d_queue = nullptr;  // free-page ring, 2 * num_pages entries
     int64_t q_cap = 0;

@@ -197,11 +197,25 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         const size_t slots = (size_t)g.num_pages * (size_t)g.block_size;
         e = cudaMalloc(&p->d_pending, sizeof(int32_t) * slots);
         if (e == cudaSuccess) e = cudaMemset(p->d_pending, 0, sizeof(int32_t) * slots);
-        std::vector<double> th(g.rope_dim / 2);
-        for (int j = 0; j < g.rope_dim / 2; ++j) th[j] = std::pow(g.theta, -2.0 * j / g.rope_dim);
-        if (e == cudaSuccess) e = cudaMalloc(&p->d_theta_j, sizeof(double) * th.size());
+        // the readers' turn table: theta_j, then cos / sin of m theta_j and m kTurnSpan theta_j
+        const int half = g.rope_dim / 2;
+        std::vector<double> tt(turn_table_doubles(half), 0.0);
+        double* lo = tt.data() + (half + 1) / 2 * 2;
+        double* hi = lo + (size_t)2 * half * kTurnSpan;
+        for (int j = 0; j < half; ++j) {
+            const double th = std::pow(g.theta, -2.0 * j / g.rope_dim);
+            tt[j] = th;
+            for (int m = 0; m < kTurnSpan; ++m) {
+                const double a = (double)m * th, b = (double)((int64_t)m * kTurnSpan) * th;
+                lo[2 * ((size_t)j * kTurnSpan + m)] = std::cos(a);
+                lo[2 * ((size_t)j * kTurnSpan + m) + 1] = std::sin(a);
+                hi[2 * ((size_t)j * kTurnSpan + m)] = std::cos(b);
+                hi[2 * ((size_t)j * kTurnSpan + m) + 1] = std::sin(b);
+            }
+        }
+        if (e == cudaSuccess) e = cudaMalloc(&p->d_theta_j, sizeof(double) * tt.size());
         if (e == cudaSuccess)
-            e = cudaMemcpy(p->d_theta_j, th.data(), sizeof(double) * th.size(), cudaMemcpyHostToDevice);
+            e = cudaMemcpy(p->d_theta_j, tt.data(), sizeof(double) * tt.size(), cudaMemcpyHostToDevice);
     }
     if (e == cudaSuccess) e = (cudaError_t)launch_init_queue(p->d_queue, g.num_pages, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

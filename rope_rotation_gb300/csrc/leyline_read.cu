@@ -37,13 +37,27 @@ __global__ void gather_kernel(const uint4* kv, const int32_t* table_row, const G
 }
 
 // -------------------------------------------------------------------------
-// Lazy pools.  cos / sin of pending * theta_j: the angle is formed in fp64 and the
-// fp64 sincos reduces it, then it is rounded once to the rotation's arithmetic,
-// exactly as the host does for an eager splice.
-__device__ __forceinline__ void pending_trig(int pend, double theta_j, bool bf16, float& c, float& s)
+// Lazy pools.  cos / sin of pending * theta_j, formed in fp64 and rounded once to the
+// rotation's arithmetic, as the host does for an eager splice.  A count below
+// kTurnSpan^2 in magnitude takes the angle-addition product of the pool's two turn
+// tables (R(a) R(b) = R(a + b): 2 loads and 6 fp64 operations); a larger one, fp64
+// sincos of the angle.
+__device__ __forceinline__ void pending_trig(int pend, const double* turn, int half, int j, bool bf16, float& c,
+                                             float& s)
 {
+    const long long a = pend < 0 ? -(long long)pend : (long long)pend;
     double sd, cd;
-    sincos((double)pend * theta_j, &sd, &cd);
+    if (a < (long long)kTurnSpan * kTurnSpan) {
+        const double2* lo = reinterpret_cast<const double2*>(turn + (half + 1) / 2 * 2);
+        const double2* hi = lo + (size_t)half * kTurnSpan;
+        const double2 l = lo[(size_t)j * kTurnSpan + (a % kTurnSpan)];
+        const double2 h = hi[(size_t)j * kTurnSpan + (a / kTurnSpan)];
+        cd = fma(h.x, l.x, -(h.y * l.y));
+        sd = fma(h.y, l.x, h.x * l.y);
+        if (pend < 0) sd = -sd;
+    } else {
+        sincos((double)pend * turn[j], &sd, &cd);
+    }
     if (bf16) {
         c = __bfloat162float(__double2bfloat16(cd));
         s = __bfloat162float(__double2bfloat16(sd));
@@ -65,13 +79,13 @@ struct WarpTrig {
     int pend = 0;   // count the slice holds
     bool valid = false;
 
-    __device__ __forceinline__ void ensure(int count, const double* theta_j, int half, bool bf16)
+    __device__ __forceinline__ void ensure(int count, const double* turn, int half, bool bf16)
     {
         if (valid && count == pend) return;  // warp-uniform: the count is the row's
         __syncwarp();                        // lanes are done reading the previous count's values
         for (int j = threadIdx.x & 31; j < half; j += 32) {
             float c, s;
-            pending_trig(count, theta_j[j], bf16, c, s);
+            pending_trig(count, turn, half, j, bf16, c, s);
             cs[j] = make_float2(c, s);
         }
         __syncwarp();
@@ -119,7 +133,7 @@ __device__ __forceinline__ void turn_item(const uint4* band, uint4* dst, int q, 
 template <int kLayout>
 __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, const Geometry g, long long layer,
                                    long long t0, long long n, uint4* out, const int32_t* pending,
-                                   const double* theta_j, int32_t* status)
+                                   const double* turn, int32_t* status)
 {
     __shared__ float2 trig_smem[kReadThreads / 32][kMaxPairs];
     const int lane = threadIdx.x & 31;
@@ -144,7 +158,7 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
         uint4* o = out + r * g.row_vecs;
         for (int c = lane; c < g.latent_vecs; c += 32) o[c] = lat[c];
         const int pend = pending[slot];
-        if (pend != 0) wt.ensure(pend, theta_j, half, bf16);
+        if (pend != 0) wt.ensure(pend, turn, half, bf16);
         for (int it = lane; it < g.rope_heads * head_items; it += 32) {
             const int head = it / head_items, q = it - head * head_items;
             const uint4* band = bands + head * hv;
@@ -168,7 +182,7 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
 // count is read before and cleared after every layer of the row is turned in place.
 template <int kLayout>
 __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Geometry g, long long len,
-                                   int32_t* pending, const double* theta_j, int32_t* status)
+                                   int32_t* pending, const double* turn, int32_t* status)
 {
     __shared__ float2 trig_smem[kReadThreads / 32][kMaxPairs];
     const int lane = threadIdx.x & 31;
@@ -192,22 +206,32 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Ge
         const long long slot = (long long)page * B + t % B;
         const int pend = pending[slot];
         if (pend == 0) continue;
-        wt.ensure(pend, theta_j, half, bf16);
         float c[8], s[8];
         if (fixed_item) {
             const int it = lane % items;
             const int head = it / head_items, q = it - head * head_items;
-            item_trig<kLayout>(wt.cs, q, c, s);
-            for (long long idx = lane; idx < n_it; idx += 64) {
-                const bool two = idx + 32 < n_it;
-                uint4* b0 = kv + band_off(g, idx / items, slot) + head * hv;
-                uint4* b1 = kv + band_off(g, (idx + 32) / items, slot) + head * hv;
-                uint4 x0 = b0[q], y0, x1, y1;
-                if (kLayout == 0) y0 = b0[q + hv / 2];
+            uint4 x0, y0, x1, y1;
+            uint4 *b0 = nullptr, *b1 = nullptr;
+            bool one = false, two = false;
+            auto load = [&](long long idx) {
+                one = idx < n_it;
+                two = idx + 32 < n_it;
+                b0 = kv + band_off(g, idx / items, slot) + head * hv;
+                b1 = kv + band_off(g, (idx + 32) / items, slot) + head * hv;
+                if (one) {
+                    x0 = b0[q];
+                    if (kLayout == 0) y0 = b0[q + hv / 2];
+                }
                 if (two) {
                     x1 = b1[q];
                     if (kLayout == 0) y1 = b1[q + hv / 2];
                 }
+            };
+            load(lane);  // the first two layers' loads are in flight while the cos / sin form
+            wt.ensure(pend, turn, half, bf16);
+            item_trig<kLayout>(wt.cs, q, c, s);
+            for (long long idx = lane; idx < n_it; idx += 64) {
+                if (idx != lane) load(idx);
                 if (kLayout == 0) {
                     if (bf16) rotate_half_split<true>(x0, y0, c, s);
                     else rotate_half_split<false>(x0, y0, c, s);
@@ -231,6 +255,7 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Ge
                 }
             }
         } else {
+            wt.ensure(pend, turn, half, bf16);
             int have_q = -1;
             for (long long idx = lane; idx < n_it; idx += 32) {
                 const long long layer = idx / items;
@@ -275,7 +300,7 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
 }
 
 int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
-                       int64_t t1, void* out, const int32_t* pending, const double* theta_j, int32_t* status,
+                       int64_t t1, void* out, const int32_t* pending, const double* turn, int32_t* status,
                        void* stream)
 {
     const long long n = t1 - t0;
@@ -283,17 +308,17 @@ int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry&
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? gather_lazy_kernel<0> : gather_lazy_kernel<1>;
     k<<<grid_for(n * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(static_cast<const uint4*>(kv), table_row, g,
                                                                       layer, t0, n, static_cast<uint4*>(out),
-                                                                      pending, theta_j, status);
+                                                                      pending, turn, status);
     return (int)cudaGetLastError();
 }
 
 int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
-                       const double* theta_j, int32_t* status, void* stream)
+                       const double* turn, int32_t* status, void* stream)
 {
     if (len <= 0) return 0;
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
     k<<<grid_for(len * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
-                                                                        pending, theta_j, status);
+                                                                        pending, turn, status);
     return (int)cudaGetLastError();
 }
 
