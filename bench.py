@@ -36,10 +36,17 @@ METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 
 FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic (read + write bytes) of a kernel on a workload, from an ncu
 # capture, valid only for the kernel code it was taken on (kernel_sha)
-# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.9 MB; the
+# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.4 MB; the
 # rest of the 210.9 MB written was still in L2 when the single captured launch ended).
-NCU_TRAFFIC = {"kernel_sha256": "19d520470faab6e3ea43a79c15439d1955f5ef2bd1b651464bc19bb1f1f8a00d",
-               "launches": {("dsv2lite-27L-32k-B16", "move_rotate_vector"): 210919424 + 161109248}}
+NCU_TRAFFIC = {
+    ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
+        "kernel_sha256": "92c349f1781b1cb413ac12fb86d4b09939cd22955b2d306a6c7b0d9c1be4c988",
+        "bytes": 210919424 + 161417216},
+    # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
+    ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
+        "kernel_sha256": "2dda5e72b1ee8fb4f37f6bad7407700eb6a1a3119b5d5fdc3df1873517dbe975",
+        "bytes": 130895104 + 73753600},
+}
 
 
 def parse():
@@ -107,15 +114,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("leyline_device.cuh", "leyline_move.cu", "leyline_reindex.cu", "leyline_read.cu",
-                  "leyline_plan.h", "leyline_internal.h")
+# The sources each timed kernel is compiled from: the shared headers and its own file.
+KERNEL_COMMON = ("leyline_device.cuh", "leyline_plan.h", "leyline_internal.h")
+KERNEL_FILES = {"move_rotate": "leyline_move.cu", "rotate_in_place": "leyline_reindex.cu",
+                "materialize": "leyline_read.cu"}
 
 
-def kernel_sha():
-    """sha256 of the kernel sources with comments and whitespace runs removed: a change to
-    the code invalidates stored ncu counters, a change to a comment does not."""
+def kernel_sha(kernel: str = "move_rotate"):
+    """sha256 of one kernel's sources with comments and whitespace runs removed: a change to
+    its code invalidates its stored ncu counters, a change to a comment or to another
+    kernel's file does not."""
     text = ""
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_COMMON + (KERNEL_FILES[kernel],):
         with open(os.path.join(ROOT, "rope_rotation_gb300", "csrc", name)) as f:
             text += f.read() + "\n"
     text = re.sub(r"//[^\n]*", "", text)
@@ -411,8 +421,10 @@ def run_ours(args, rank, world, local):
     achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
     kernel_name = "rotate_in_place" if reindexed else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")
     traffic = None
-    if NCU_TRAFFIC["kernel_sha256"] == kernel_sha() and not args.lazy and not args.split:
-        traffic = NCU_TRAFFIC["launches"].get((w.name, kernel_name))
+    stored = NCU_TRAFFIC.get((w.name, kernel_name))
+    if stored and not args.lazy and not args.split and stored["kernel_sha256"] == kernel_sha(
+            "rotate_in_place" if reindexed else "move_rotate"):
+        traffic = stored["bytes"]
     line = {
         "metric": METRIC,
         "value": value,
