@@ -27,7 +27,15 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-OUT = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "gpurun_out")
+# the drift records are written where LEYLINE_RESULTS_DIR points (not written when unset)
+OUT = os.environ.get("LEYLINE_RESULTS_DIR", "")
+
+
+def _record(name: str, rec: dict) -> None:
+    if OUT:
+        os.makedirs(OUT, exist_ok=True)
+        with open(os.path.join(OUT, name), "w") as f:
+            json.dump(rec, f, indent=1)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -163,9 +171,7 @@ def test_chain_64_drift():
     report["max_moves"] = int(np.max(moves))
     assert gpu_vals["fp32"] < gpu_vals["bf16"]
     assert gpu_vals["fp32"] < 2e-2
-    os.makedirs(OUT, exist_ok=True)
-    with open(os.path.join(OUT, "chain_drift.json"), "w") as f:
-        json.dump(report, f, indent=1)
+    _record("chain_drift.json", report)
     print("chain drift:", report)
 
 
@@ -226,8 +232,6 @@ def test_chain_64_lazy_drift():
               "lazy_drift_rel_l2": float(np.linalg.norm(g - t) / np.linalg.norm(t)),
               "lazy_elements_off_by_floor_clause": c["floor_used"], "lazy_max_bf16_steps": c["max_steps"],
               "last_splice_algorithmic_bytes": int(stats["algorithmic_bytes"])}
-    os.makedirs(OUT, exist_ok=True)
-    with open(os.path.join(OUT, "chain_drift_lazy.json"), "w") as f:
-        json.dump(report, f, indent=1)
+    _record("chain_drift_lazy.json", report)
     print("lazy chain drift:", report)
     assert report["lazy_drift_rel_l2"] < 1e-3
