@@ -48,7 +48,7 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
 
 // A plan small enough to travel as a kernel parameter (__grid_constant__): no
 // host-to-device copy and no plan buffer on the path.
-constexpr int kParamReqs = 8;  // 104 bytes each
+constexpr int kParamReqs = 8;  // 128 bytes each
 constexpr int kParamSegs = 24;
 constexpr int kParamTrigFloats = 640;  // 10 rotated segments of a 64-wide rope band
 struct alignas(16) ParamPlan {
