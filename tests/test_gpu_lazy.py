@@ -358,3 +358,43 @@ def test_lazy_chain_drift_single_rounding():
     c = H.compare_kpe(got[:, keep, w.latent_dim:].reshape(-1, w.rope_dim), exact.reshape(-1, w.rope_dim), 0)
     assert c["rel_l2"] < 1e-3 and max(rel) < 1e-3
     cache.close()
+
+
+@pytest.mark.parametrize("precision,layout", [(0, 0), (0, 1), (1, 0)])
+def test_large_counts_across_the_turn_table(precision, layout):
+    """Counts written straight into the pending array (the pointer leyline_pending_ptr hands to
+    readers), chosen across the readers' turn table: single table steps, the 2048 boundary, the
+    table's last count 2048^2 - 1, the sincos path beyond it, and the int32 extremes.  A gather
+    equals the oracle's re-encoding by the count within one rounding (the bf16 arm bit-exact),
+    and materialize stores exactly what the gather returned."""
+    import torch
+    S = 2048
+    counts = [0, 1, -1, 2047, S, -(S + 1), 2 * S - 1, 123456, -987654, S * S - 1, -(S * S - 1), S * S,
+              -(S * S), 10 ** 7, -(10 ** 8), 2 ** 31 - 1, -(2 ** 31 - 1), -(2 ** 31)]
+    L = 4 * len(counts)
+    w = Workload(f"lazy-large-p{precision}-l{layout}", 2, 1, [L], [], seed=61)
+    cache = H.make_cache(w, pair_layout=layout, precision=precision, flags=LAZY)
+    pend_of_row = np.array([counts[t % len(counts)] for t in range(L)], dtype=np.int64)
+    pages = cache.table[0, :L].long()
+    cache.pending()[pages, 0] = torch.tensor(pend_of_row, dtype=torch.int32, device=cache.device)
+    torch.cuda.synchronize()
+    stored = _raw_rows(cache, 0, L)
+    got = H.logical_rows(cache, 0, L)
+    lat = w.latent_dim
+    assert np.array_equal(got[:, :, :lat], stored[:, :, :lat])
+    zero = pend_of_row == 0
+    assert np.array_equal(got[:, zero], stored[:, zero])
+    bands = stored[:, ~zero, lat:].reshape(w.num_layers, -1, w.rope_heads, w.rope_dim)
+    p = np.broadcast_to(pend_of_row[~zero][None, :, None], bands.shape[:3]).reshape(-1)
+    if precision == 0:
+        want = oracle.rerotate(bands, 0, p, w.theta, layout)
+    else:
+        want = oracle.rotate_bf16only(bands, p, w.theta, layout)
+    H.compare_kpe(got[:, ~zero, lat:].reshape(-1, w.rope_dim), want.reshape(-1, w.rope_dim), layout,
+                  exact=precision != 0)
+    cache.materialize(0)
+    torch.cuda.synchronize()
+    cache.check_status()
+    assert not _pending_of(cache, 0, L).any()
+    assert np.array_equal(_raw_rows(cache, 0, L), got), "materialize stored other bits than the gather returned"
+    cache.close()
