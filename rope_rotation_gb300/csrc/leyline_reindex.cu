@@ -410,6 +410,59 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
             cur_tile = tile;
         }
         const long long layer0 = grp * lpu;
+        if (kItems == 1) {
+            // one item per thread: when the next unit is the same tile's next layer group,
+            // both units' loads are issued before either unit's stores
+            const bool two = grp + 1 < groups && u + 1 < u1;
+            uint4* band = n_items ? band_s[it_row[0]] : nullptr;
+            const long long la = layer0 + it_lo[0], lb = la + lpu;
+            const bool da = band && la < L, db = two && band && lb < L;
+            uint4* ra = band + la * a.g.rope_layer_vecs + it_off[0];
+            uint4* rb = band + lb * a.g.rope_layer_vecs + it_off[0];
+            uint4 xa, ya, xb, yb;
+            if (da) {
+                xa = ld_rw(ra);
+                if (kLayout == 0) ya = ld_rw(ra + hv / 2);
+            }
+            if (db) {
+                xb = ld_rw(rb);
+                if (kLayout == 0) yb = ld_rw(rb + hv / 2);
+            }
+            if (da || db) {
+                float cs[8], sn[8];
+                const float* tp = &trig_s[2 * kPairs * it_q[0]];
+#pragma unroll
+                for (int w = 0; w < kPairs; ++w) {
+                    cs[w] = tp[2 * w];
+                    sn[w] = tp[2 * w + 1];
+                }
+                if (kLayout == 0) {
+                    if (da) {
+                        rotate_half_split<kBf16>(xa, ya, cs, sn);
+                        st_stream(ra, xa);
+                        st_stream(ra + hv / 2, ya);
+                    }
+                    if (db) {
+                        rotate_half_split<kBf16>(xb, yb, cs, sn);
+                        st_stream(rb, xb);
+                        st_stream(rb + hv / 2, yb);
+                    }
+                } else {
+                    if (da) {
+                        rotate_interleaved<kBf16>(xa, cs, sn);
+                        st_stream(ra, xa);
+                    }
+                    if (db) {
+                        rotate_interleaved<kBf16>(xb, cs, sn);
+                        st_stream(rb, xb);
+                    }
+                }
+            }
+            if (two) {
+                ++u;
+                ++grp;
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < kItems; ++k) {
             if (k >= n_items) break;
@@ -434,6 +487,7 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_p
                 rotate_interleaved<kBf16>(x, cs, sn);
                 st_stream(r, x);
             }
+        }
         }
         if (++grp == groups) {
             grp = 0;
