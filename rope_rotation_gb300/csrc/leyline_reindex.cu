@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(kMoveThreads, 3) copy_fresh_reindex(const __gr
 // kItems: work items per thread.  1 for the MLA row (16 rows x 4 or 8 items per
 // layer: a unit covers 4 or 2 layers), with 8 CTAs per SM; kMaxItems for wider rows.
 template <int kLayout, bool kBf16, int kItems, class PlanSrc>
-__global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 8 : 2) rotate_in_place(const __grid_constant__ SpliceArgs a,
+__global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 5 : 2) rotate_in_place(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
     __shared__ uint4* band_s[kTileRows];                  // the tile's rows' bands (layer 0); nullptr: none
