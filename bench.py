@@ -44,8 +44,8 @@ NCU_TRAFFIC = {
         "bytes": 210919424 + 161417216},
     # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "2dda5e72b1ee8fb4f37f6bad7407700eb6a1a3119b5d5fdc3df1873517dbe975",
-        "bytes": 130895104 + 73753600},
+        "kernel_sha256": "5ba3a9abeb3f46e44c7dcad015ecef6c27407682827c20d2730764d775cf1986",
+        "bytes": 130892800 + 75437056},
 }
 
 
