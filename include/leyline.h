@@ -187,7 +187,8 @@ typedef struct {
     int32_t requests_touched;
     int32_t kernels_launched;  /* kernels this call enqueued */
     int32_t reindexed;         /* 1: the call kept survivors in their pages (LEYLINE_POOL_REINDEX) */
-    int32_t reserved;
+    int32_t overlapped;        /* 1: the call's move kernel may start before the previous call's work
+                                  on the stream ends (see leyline_splice) */
     /* Host time of the call (leyline_splice, leyline_splice_noalloc; 0 from the dry run),
      * in nanoseconds of the host's monotonic clock: */
     int64_t host_ns;           /* the whole call, from entry to return (kernels are enqueued, not waited for) */

@@ -90,6 +90,9 @@ struct SpliceArgs {
     int32_t move_kernel;      // MoveKernel
     int32_t reindex;          // 1: prep + in-place rotation + staged commit
     int32_t prep_ctas;        // re-index: CTAs of the prep part of the prep + rows-of-R launch
+    int32_t overlap_prev;     // 1: the move kernel starts without waiting for the previous kernel
+                              // and waits for it at its end (the host has ruled out hazards)
+    int32_t pad3;
     Geometry g;
 };
 
@@ -196,4 +199,12 @@ struct leyline_pool {
     bool timing = false;
     std::vector<std::pair<cudaEvent_t, cudaEvent_t>> tev;
     size_t tev_used = 0;
+    // Rewrite splices enqueued back to back on one stream may overlap: a call's move kernel
+    // may start while the calls before it still run.  The window holds the calls that may
+    // still run: those since the last call whose move kernel waited at its start.
+    static constexpr int kOverlapWindow = 8;
+    bool window_open = false;          // the last work on last_stream was a rewrite splice's commit
+    int window_calls = 0;
+    int64_t window_tail = 0;           // ring tail when the window's first call was planned
+    std::vector<int32_t> window_reqs;  // requests the window's calls rewrite
 };

@@ -13,8 +13,11 @@
 //                free-page ring.
 // The commit kernel is launched as a programmatic dependent of move+rotate, so its
 // launch overlaps the move; it waits (griddepcontrol.wait) for the move to finish
-// before it touches the table.  The path is bandwidth-bound (about 64 fp32 FMAs per
-// 2304 bytes moved), so it uses no tensor cores.
+// before it touches the table.  Calls enqueued back to back may overlap as well: when
+// the host has shown that a call shares no request with the calls still running and
+// takes no page they returned, its move kernel starts before they end (SpliceArgs::
+// overlap_prev).  The path is bandwidth-bound (about 64 fp32 FMAs per 2304 bytes
+// moved), so it uses no tensor cores.
 #include "leyline_device.cuh"
 
 namespace leyline {
@@ -34,7 +37,10 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
     constexpr int kRopeVecs = 8;
     constexpr int kWarps = kMoveThreads / 32;
     __shared__ RowDesc desc[kTileRows];
-    wait_for_previous_grid();
+    // An overlapped call (a.overlap_prev) reads nothing the calls still running write, so it
+    // starts at once and waits for the previous kernel only at its end, which keeps the
+    // completion of calls in stream order.
+    if (!a.overlap_prev) wait_for_previous_grid();
     allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,6 +140,7 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
             }
         }
     }
+    if (a.overlap_prev) wait_for_previous_grid();
 }
 
 // -------------------------------------------------------------------------
@@ -477,6 +484,10 @@ template <class PlanSrc>
 __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_constant__ SpliceArgs a,
                                                                 const __grid_constant__ PlanSrc plan)
 {
+    // The next call's first kernel may launch at once: it waits for this grid before it
+    // reads anything, unless the host has let it overlap (it then reads nothing this
+    // grid writes).
+    allow_next_grid();
     const PlanView pv = plan_view(a, plan);
     const long long stride = (long long)gridDim.x * blockDim.x;
     long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
@@ -490,7 +501,6 @@ __global__ void __launch_bounds__(kCommitThreads) commit_kernel(const __grid_con
         if (k < rp->n_new) fresh = a.free_q[ring(a.pop_base + rp->pop_off + k, a.q_cap)];
     }
     wait_for_previous_grid();
-    allow_next_grid();
     while (i < a.total_commit) {
         int32_t* row = a.table_w + (long long)rp->req * a.max_blocks + rp->b0;
         if (k == 0) a.seq_lens_dev[rp->req] = (int32_t)rp->new_len;

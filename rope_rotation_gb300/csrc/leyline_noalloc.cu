@@ -186,6 +186,7 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     if (e != cudaSuccess) return cuda_fail(e, "recording completion event");
     p->has_work = true;
     p->last_stream = stream;
+    p->window_open = false;  // this entry point does not overlap; the next splice waits for it
 
     for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
     p->q_head += plan.total_pop;

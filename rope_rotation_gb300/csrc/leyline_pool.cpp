@@ -283,6 +283,7 @@ int leyline_alloc_pages(leyline_pool_t* p, int32_t n, int32_t* ids)
 {
     clear_error();
     if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (n > p->q_tail - p->q_head) return set_error(LEYLINE_ERR_NO_PAGES, "not enough free pages");
     if (n == 0) return LEYLINE_OK;
     DeviceGuard guard(p->device);
@@ -305,6 +306,7 @@ int leyline_free_pages(leyline_pool_t* p, int32_t n, const int32_t* ids)
 {
     clear_error();
     if (!p || n < 0 || (n > 0 && !ids)) return set_error(LEYLINE_ERR_INVALID_ARG, "bad arguments");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (p->q_tail - p->q_head + n > p->g.num_pages)
         return set_error(LEYLINE_ERR_INVALID_ARG, "more pages returned than the pool holds");
     for (int32_t i = 0; i < n; ++i)
@@ -493,15 +495,46 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
                                     : a.move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
                                                                  : p->move_blocks_per_sm);
+    // Overlap with the calls before it.  A rewrite whose plan travels as a kernel parameter
+    // and whose move runs in the MLA vector kernel may start before the calls still running
+    // (the window) end, when on the same stream it rewrites no request they rewrite and
+    // takes only pages that were on the free list before the window's first call returned
+    // any: it then reads nothing they write and writes nothing they read.
+    const bool mla = p->g.latent_vecs == 64 && p->g.rope_vecs == 8 && p->g.rope_heads == 1;
+    const bool vector_mla = mla && !(a.move_kernel == MOVE_BULK && !(p->g.flags & LEYLINE_POOL_SPLIT_ROPE));
+    const bool chainable = !plan.reindex && in_params && !p->timing && vector_mla && plan.total_tiles > 0 &&
+                           plan.total_commit > 0;
+    bool overlap = chainable && p->window_open && p->has_work && stream == p->last_stream &&
+                   p->window_calls < leyline_pool::kOverlapWindow && p->q_head + plan.total_pop <= p->window_tail;
+    for (size_t r = 0; overlap && r < plan.reqs.size(); ++r)
+        if (std::find(p->window_reqs.begin(), p->window_reqs.end(), plan.reqs[r].req) != p->window_reqs.end())
+            overlap = false;
+    a.overlap_prev = overlap ? 1 : 0;
     int err = launch_splice(a, in_params ? &pp : nullptr, grid, stream, t0, t1);
-    if (err != 0) return cuda_error((cudaError_t)err, "launching the splice kernels");
+    if (err != 0) {
+        p->window_open = false;
+        return cuda_error((cudaError_t)err, "launching the splice kernels");
+    }
     rc = mark_done(p, stream);
     if (rc != LEYLINE_OK) return rc;
+    if (chainable) {
+        if (!overlap) {  // this call waited for everything before it: a new window opens
+            p->window_open = true;
+            p->window_calls = 0;
+            p->window_tail = p->q_tail;
+            p->window_reqs.clear();
+        }
+        ++p->window_calls;
+        for (const ReqPlan& rp : plan.reqs) p->window_reqs.push_back(rp.req);
+    } else {
+        p->window_open = false;
+    }
 
     for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
     p->q_head += plan.total_pop;
     p->q_tail += plan.total_push;
     p->last_stats = plan.stats;
+    p->last_stats.overlapped = overlap ? 1 : 0;
     set_host_times(&p->last_stats, t_enter, t_resolved, t_planned);
     return LEYLINE_OK;
 }
@@ -518,6 +551,7 @@ int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t r
 {
     clear_error();
     if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (req < 0 || req >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
     if (layer < 0 || layer >= p->g.num_layers) return set_error(LEYLINE_ERR_INVALID_ARG, "layer out of range");
     if (t0 < 0 || t0 > t1 || t1 > bt->seq_lens_host[req] || t1 > (int64_t)bt->max_blocks * p->g.block_size)
@@ -544,6 +578,7 @@ int leyline_materialize(leyline_pool_t* p, const leyline_block_table_t* bt, int3
 {
     clear_error();
     if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (!p->d_pending) return set_error(LEYLINE_ERR_INVALID_ARG, "the pool was not created with LEYLINE_POOL_LAZY");
     if (req < 0 || req >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
     const int64_t len = bt->seq_lens_host[req];
@@ -574,6 +609,7 @@ int leyline_sync_status(leyline_pool_t* p)
 {
     clear_error();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     DeviceGuard guard(p->device);
     int rc = wait_pool(p);
     if (rc != LEYLINE_OK) return rc;
@@ -592,6 +628,7 @@ int leyline_sync_status(leyline_pool_t* p)
 int leyline_kernel_timing_enable(leyline_pool_t* p, int32_t enable)
 {
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
     p->timing = enable != 0;
     p->tev_used = 0;
     if (p->timing && p->tev.size() < kTimingEventsUpFront) {

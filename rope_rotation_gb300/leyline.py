@@ -75,7 +75,7 @@ class Stats(ctypes.Structure):
                 ("moved_bytes", ctypes.c_int64), ("pages_popped", ctypes.c_int64),
                 ("pages_pushed", ctypes.c_int64), ("requests_touched", ctypes.c_int32),
                 ("kernels_launched", ctypes.c_int32), ("reindexed", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("host_ns", ctypes.c_int64), ("resolve_ns", ctypes.c_int64),
+                ("overlapped", ctypes.c_int32), ("host_ns", ctypes.c_int64), ("resolve_ns", ctypes.c_int64),
                 ("plan_ns", ctypes.c_int64)]
 
     def as_dict(self) -> dict:

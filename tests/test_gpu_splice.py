@@ -167,6 +167,7 @@ def test_evict_and_mixed_modes(B, move_kernel):
 # Re-index mode (block size 1, LEYLINE_POOL_REINDEX): survivors keep their pages, only
 # the table entries move and rope bands turn in place.
 REINDEX = 1
+LAZY = 2
 
 
 def test_reindex_edge_grid():
@@ -337,5 +338,98 @@ def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
         # each row may have been turned by up to 20 calls: the chain allowance covers it
         H.compare_kpe(got[:, :, lat:].reshape(-1, w.rope_dim), state[r][:, :, lat:].reshape(-1, w.rope_dim), 0,
                       turns=np.full(got.shape[0] * got.shape[1], 20))
+    del keep
+    cache.close()
+
+
+# ------------------------------------------------------------------------------
+# Calls that overlap: a rewrite call's move kernel may start before the calls still running
+# end, when it rewrites none of their requests and takes no page they returned.  The
+# schedule below mixes calls that qualify with calls that share a request with the window
+# or need pages the window returned (a tight pool); the flag each call reports must follow
+# that rule, and every request must end equal to the oracle's chain.
+@pytest.mark.parametrize("flags", [0, LAZY])
+def test_consecutive_calls_overlap_only_when_safe(flags):
+    import torch
+    from rope_rotation_gb300 import leyline
+    rng = np.random.default_rng(91)
+    n_req, B, window_max = 12, 16, 8
+    lengths = [int(rng.integers(300, 700)) for _ in range(n_req)]
+    lens = list(lengths)
+    steps, key = [], 0
+    for c in range(24):
+        reqs = [(2 * c) % n_req, (2 * c + 1) % n_req] if c % 5 != 4 else [(2 * c - 1) % n_req]
+        step = []
+        for r in reqs:
+            L = lens[r]
+            s = int(rng.integers(0, L // 2))
+            e = s + int(rng.integers(20, 120))
+            n = int(rng.integers(0, 5))
+            step.append(Dir(r, s, e, n, key))
+            key += 1
+            lens[r] = L + n - (e - s)
+        steps.append(step)
+    w = Workload(f"overlap-f{flags}", 2, B, lengths, steps, seed=92)
+    cache = H.make_cache(w, slack_pages=4, flags=flags)
+    keep, flags_seen = [], []
+    # the rule, restated: the window holds the calls since the last one that waited
+    q_head = sum(-(-L // B) for L in lengths)
+    q_tail = cache.num_pages
+    window_tail, window_reqs, window_calls, window_open = 0, set(), 0, False
+    want = []
+    for step in steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        cache.splice(dirs)
+        st = cache.last_stats()
+        rq = {d.req for d in step}
+        ok = (window_open and window_calls < window_max and not (rq & window_reqs)
+              and q_head + st["pages_popped"] <= window_tail)
+        want.append(int(ok))
+        flags_seen.append(st["overlapped"])
+        if not ok:
+            window_open, window_calls, window_tail, window_reqs = True, 0, q_tail, set()
+        window_calls += 1
+        window_reqs |= rq
+        q_head += st["pages_popped"]
+        q_tail += st["pages_pushed"]
+    torch.cuda.synchronize()
+    cache.check_status()
+    assert flags_seen == want, f"overlap flags {flags_seen} != rule {want}"
+    assert 0 < sum(flags_seen) < len(steps), "the schedule should mix overlapped and waiting calls"
+    if flags & LAZY:
+        # a lazy pool stores bits and counts: both exact against the oracle's slot maps
+        import test_gpu_lazy as TL
+        st = TL.LazyState(w)
+        lens_now = np.array(w.lengths, dtype=np.int64)
+        for step in steps:
+            st.apply(w, step, lens_now)
+            lens_now = np.array([b.shape[1] for b in st.base], dtype=np.int64)
+        for r in range(n_req):
+            n = int(cache.seq_lens_host[r])
+            assert n == st.base[r].shape[1]
+            assert np.array_equal(TL._raw_rows(cache, r, n), st.base[r]), f"request {r}: stored bits differ"
+            assert np.array_equal(TL._pending_of(cache, r, n), st.pend[r]), f"request {r}: counts differ"
+        TL._check_free_pages_clear(cache)
+        del keep
+        cache.close()
+        return
+    state = H.oracle_state(w)
+    import oracle
+    import synth
+    for step in steps:
+        for r in {d.req for d in step}:
+            ds = [d for d in step if d.req == r]
+            reps = [synth.repl_rows(w.seed, r, d.key, w.num_layers, d.n_repl, w.row_elems) for d in ds]
+            state[r] = oracle.splice_request(state[r], [(d.s_start, d.s_end, d.n_repl) for d in ds], reps,
+                                             w.latent_dim, w.theta, 0)
+    for r in range(n_req):
+        n = int(cache.seq_lens_host[r])
+        assert n == state[r].shape[1]
+        got = H.logical_rows(cache, r, n)
+        lat = w.latent_dim
+        assert np.array_equal(got[:, :, :lat], state[r][:, :, :lat])
+        H.compare_kpe(got[:, :, lat:].reshape(-1, w.rope_dim), state[r][:, :, lat:].reshape(-1, w.rope_dim), 0,
+                      turns=np.full(got.shape[0] * got.shape[1], len(steps)))
     del keep
     cache.close()
