@@ -466,7 +466,11 @@ def run_ours(args, rank, world, local):
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms": k2_avg_s * 1e3, "launches_timed": k2_n,
-                     "algorithmic_bytes_per_launch": st["algorithmic_bytes"]},
+                     "algorithmic_bytes_per_launch": st["algorithmic_bytes"],
+                     # the value leg's steps: consecutive calls overlap there, which the
+                     # per-launch events of the kernel leg rule out
+                     "step_achieved": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9,
+                     "step_frac": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak},
     }
     if lazy_read:
         line["lazy_read"] = lazy_read

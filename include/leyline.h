@@ -235,6 +235,12 @@ int64_t leyline_free_page_count(const leyline_pool_t* pool);
  * kernels (move+rotate, then commit).  The plan travels as a kernel parameter
  * when it has at most 8 requests, 24 segments and 10 rotated segments;
  * otherwise it is uploaded first with one host-to-device copy.
+ * Calls enqueued back to back on one stream keep stream order for everything
+ * the caller can observe, but the library may let a call's kernels start
+ * before the previous calls' kernels end: only for a rewrite whose plan is a
+ * kernel parameter, which shares no request with the calls that may still run
+ * and takes no page they returned (stats: overlapped).  Any other work on the
+ * stream between two calls, or a call on another stream, orders them fully.
  * Errors (nothing is enqueued or changed): INVALID_ARG, INVALID_DIRECTIVE,
  * OVERLAP, UNSUPPORTED_MODE (FORGET: the caller re-prefills, section 2.1),
  * CAPACITY, NO_PAGES.  CUDA: a launch failed after validation; the pool must
