@@ -36,12 +36,12 @@ METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 
 FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic (read + write bytes) of a kernel on a workload, from an ncu
 # capture, valid only for the kernel code it was taken on (kernel_sha)
-# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.4 MB; the
+# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.1 MB; the
 # rest of the 210.9 MB written was still in L2 when the single captured launch ended).
 NCU_TRAFFIC = {
     ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
-        "kernel_sha256": "92c349f1781b1cb413ac12fb86d4b09939cd22955b2d306a6c7b0d9c1be4c988",
-        "bytes": 210919424 + 161417216},
+        "kernel_sha256": "76c7e7f44dd7ef590c44de8219af8efe598167dc0c6ef02474a2b9be92b6a660",
+        "bytes": 210918912 + 161064704},
     # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
         "kernel_sha256": "5ba3a9abeb3f46e44c7dcad015ecef6c27407682827c20d2730764d775cf1986",
