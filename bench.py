@@ -44,8 +44,8 @@ NCU_TRAFFIC = {
         "bytes": 210918912 + 161064704},
     # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "5ba3a9abeb3f46e44c7dcad015ecef6c27407682827c20d2730764d775cf1986",
-        "bytes": 130892800 + 75437056},
+        "kernel_sha256": "2d7517d189d93b0a50478fd95ba3c605c4f05540a7e8e380a390b1ef1cf6ff2b",
+        "bytes": 130889984 + 75299584},
 }
 
 
