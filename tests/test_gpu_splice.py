@@ -168,6 +168,7 @@ def test_evict_and_mixed_modes(B, move_kernel):
 # the table entries move and rope bands turn in place.
 REINDEX = 1
 LAZY = 2
+SPLIT = 4
 
 
 def test_reindex_edge_grid():
@@ -348,10 +349,12 @@ def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
 # schedule below mixes calls that qualify with calls that share a request with the window
 # or need pages the window returned (a tight pool); the flag each call reports must follow
 # that rule, and every request must end equal to the oracle's chain.
-@pytest.mark.parametrize("flags", [0, LAZY])
-def test_consecutive_calls_overlap_only_when_safe(flags):
+@pytest.mark.parametrize("flags,kernel", [(0, "vector"), (LAZY, "vector"), (SPLIT, "vector"), (0, "bulk")])
+def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
+    """The bulk (TMA) move kernel always waits for the calls before it."""
     import torch
     from rope_rotation_gb300 import leyline
+    monkeypatch.setenv("LEYLINE_MOVE_KERNEL", kernel)
     rng = np.random.default_rng(91)
     n_req, B, window_max = 12, 16, 8
     lengths = [int(rng.integers(300, 700)) for _ in range(n_req)]
@@ -383,11 +386,13 @@ def test_consecutive_calls_overlap_only_when_safe(flags):
         cache.splice(dirs)
         st = cache.last_stats()
         rq = {d.req for d in step}
-        ok = (window_open and window_calls < window_max and not (rq & window_reqs)
+        ok = (kernel == "vector" and window_open and window_calls < window_max and not (rq & window_reqs)
               and q_head + st["pages_popped"] <= window_tail)
         want.append(int(ok))
         flags_seen.append(st["overlapped"])
-        if not ok:
+        if kernel != "vector":
+            window_open = False
+        elif not ok:
             window_open, window_calls, window_tail, window_reqs = True, 0, q_tail, set()
         window_calls += 1
         window_reqs |= rq
@@ -396,7 +401,8 @@ def test_consecutive_calls_overlap_only_when_safe(flags):
     torch.cuda.synchronize()
     cache.check_status()
     assert flags_seen == want, f"overlap flags {flags_seen} != rule {want}"
-    assert 0 < sum(flags_seen) < len(steps), "the schedule should mix overlapped and waiting calls"
+    if kernel == "vector":
+        assert 0 < sum(flags_seen) < len(steps), "the schedule should mix overlapped and waiting calls"
     if flags & LAZY:
         # a lazy pool stores bits and counts: both exact against the oracle's slot maps
         import test_gpu_lazy as TL
