@@ -105,7 +105,13 @@ typedef enum { LEYLINE_ROTATE_FP32 = 0, LEYLINE_ROTATE_BF16_NAIVE = 1 } leyline_
  * and clears it, and attention kernels can read the counts through
  * leyline_pending_ptr.  A band is then rounded to bf16 once per read instead of
  * once per splice (section 4.3: the drift of repeated bf16 rotation), and with
- * LEYLINE_POOL_REINDEX a splice moves no cache bytes for survivors at all. */
+ * LEYLINE_POOL_REINDEX a splice moves no cache bytes for survivors at all.
+ * Readers form the cos and sin of pending * theta_j in fp64 and round them once
+ * to the rotation's precision, as an eager splice does for its Delta: for
+ * |pending| < 2^22 as the angle-addition product of cos/sin(hi * 2048 * theta_j)
+ * and cos/sin(lo * theta_j) (pending = hi * 2048 + lo), else by fp64 sincos of
+ * the angle.  An attention kernel that applies the counts itself matches
+ * leyline_gather when it does the same. */
 #define LEYLINE_POOL_LAZY 2
 /* LEYLINE_POOL_SPLIT_ROPE: the pool buffer holds the latents and the rope bands in
  * two arrays instead of whole rows: bf16 latent[num_layers][num_pages][block_size]
@@ -158,7 +164,10 @@ typedef enum { LEYLINE_AMORTIZE = 0, LEYLINE_FORGET = 1, LEYLINE_EVICT = 2 } ley
 /* One directive D = (s_start, s_end, R, m) for request `req` (section 2.1).
  * [s_start, s_end) is half-open, in the request's coordinates before the call;
  * several directives of one request must not overlap and must have distinct
- * s_start.  repl_rows: device bf16 [num_layers][n_repl][row] (row as in the pool),
+ * s_start.  repl_rows: bf16 [num_layers][n_repl][row] (row as in the pool) in
+ * device memory of the pool's GPU or in pinned host memory (cudaHostAlloc or
+ * cudaHostRegister; the kernel reads it in place over the host link), 16-byte
+ * aligned; pageable memory is refused with INVALID_ARG.  These are
  * the rows of R already encoded at their final positions s_start + D_before + i
  * (D_before = the summed Delta of the request's directives left of this one),
  * as prefill writes them (section 2.3); they are copied bit for bit and must stay
@@ -284,10 +293,12 @@ int leyline_last_stats(const leyline_pool_t* pool, leyline_stats_t* out);
 /* -------------------------------------------------------------- gather ---- */
 
 /* Copy the logical rows [t0, t1) of request `req`, layer `layer` into out_dev
- * (device bf16 [t1 - t0][row], 16-byte aligned), reading
+ * (bf16 [t1 - t0][row], 16-byte aligned, in device memory of the pool's GPU or in
+ * pinned host memory, which the kernel writes in place), reading
  * through the block table.  In a LEYLINE_POOL_LAZY pool each row's rope bands
  * are turned by the row's pending count on the way out.  Asynchronous on `stream`.
- * Errors: INVALID_ARG (range outside [0, seq_lens_host[req]], bad layer/req). */
+ * Errors: INVALID_ARG (range outside [0, seq_lens_host[req]], bad layer/req,
+ * pageable or foreign-device output). */
 int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, int32_t layer,
                    int64_t t0, int64_t t1, void* out_dev, void* stream);
 
