@@ -349,31 +349,16 @@ def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
 # schedule below mixes calls that qualify with calls that share a request with the window
 # or need pages the window returned (a tight pool); the flag each call reports must follow
 # that rule, and every request must end equal to the oracle's chain.
-@pytest.mark.parametrize("flags,kernel", [(0, "vector"), (LAZY, "vector"), (SPLIT, "vector"), (0, "bulk")])
-def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
-    """The bulk (TMA) move kernel always waits for the calls before it."""
+def _run_overlapping_calls(w: Workload, flags: int, kernel: str, slack: int, window_max: int = 8) -> list:
+    """Enqueue every step of w with no synchronisation, check each call's overlap flag against
+    the rule, and the final caches against the oracle (eager pools: its chain; lazy pools: the
+    stored bits and counts, exactly).  Returns the flags."""
     import torch
-    from rope_rotation_gb300 import leyline
-    monkeypatch.setenv("LEYLINE_MOVE_KERNEL", kernel)
-    rng = np.random.default_rng(91)
-    n_req, B, window_max = 12, 16, 8
-    lengths = [int(rng.integers(300, 700)) for _ in range(n_req)]
-    lens = list(lengths)
-    steps, key = [], 0
-    for c in range(24):
-        reqs = [(2 * c) % n_req, (2 * c + 1) % n_req] if c % 5 != 4 else [(2 * c - 1) % n_req]
-        step = []
-        for r in reqs:
-            L = lens[r]
-            s = int(rng.integers(0, L // 2))
-            e = s + int(rng.integers(20, 120))
-            n = int(rng.integers(0, 5))
-            step.append(Dir(r, s, e, n, key))
-            key += 1
-            lens[r] = L + n - (e - s)
-        steps.append(step)
-    w = Workload(f"overlap-f{flags}", 2, B, lengths, steps, seed=92)
-    cache = H.make_cache(w, slack_pages=4, flags=flags)
+    B = w.block_size
+    lengths = list(w.lengths)
+    steps = w.steps
+    n_req = w.num_reqs
+    cache = H.make_cache(w, slack_pages=slack, flags=flags)
     keep, flags_seen = [], []
     # the rule, restated: the window holds the calls since the last one that waited
     q_head = sum(-(-L // B) for L in lengths)
@@ -401,8 +386,6 @@ def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
     torch.cuda.synchronize()
     cache.check_status()
     assert flags_seen == want, f"overlap flags {flags_seen} != rule {want}"
-    if kernel == "vector":
-        assert 0 < sum(flags_seen) < len(steps), "the schedule should mix overlapped and waiting calls"
     if flags & LAZY:
         # a lazy pool stores bits and counts: both exact against the oracle's slot maps
         import test_gpu_lazy as TL
@@ -419,7 +402,7 @@ def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
         TL._check_free_pages_clear(cache)
         del keep
         cache.close()
-        return
+        return flags_seen
     state = H.oracle_state(w)
     import oracle
     import synth
@@ -439,3 +422,64 @@ def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
                       turns=np.full(got.shape[0] * got.shape[1], len(steps)))
     del keep
     cache.close()
+    return flags_seen
+
+
+@pytest.mark.parametrize("flags,kernel", [(0, "vector"), (LAZY, "vector"), (SPLIT, "vector"), (0, "bulk")])
+def test_consecutive_calls_overlap_only_when_safe(flags, kernel, monkeypatch):
+    """A fixed schedule: pairs of requests in turn, every fifth call one request of the call
+    before it, a tight pool.  The bulk (TMA) move kernel always waits for the calls before it."""
+    monkeypatch.setenv("LEYLINE_MOVE_KERNEL", kernel)
+    rng = np.random.default_rng(91)
+    n_req, B = 12, 16
+    lengths = [int(rng.integers(300, 700)) for _ in range(n_req)]
+    lens = list(lengths)
+    steps, key = [], 0
+    for c in range(24):
+        reqs = [(2 * c) % n_req, (2 * c + 1) % n_req] if c % 5 != 4 else [(2 * c - 1) % n_req]
+        step = []
+        for r in reqs:
+            L = lens[r]
+            s = int(rng.integers(0, L // 2))
+            e = s + int(rng.integers(20, 120))
+            n = int(rng.integers(0, 5))
+            step.append(Dir(r, s, e, n, key))
+            key += 1
+            lens[r] = L + n - (e - s)
+        steps.append(step)
+    w = Workload(f"overlap-f{flags}", 2, B, lengths, steps, seed=92)
+    seen = _run_overlapping_calls(w, flags, kernel, slack=4)
+    if kernel == "vector":
+        assert 0 < sum(seen) < len(steps), "the schedule should mix overlapped and waiting calls"
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_overlapping_calls_fuzz(seed, monkeypatch):
+    """Random schedules: 30 calls of 1-2 random requests with 1-2 directives each (so every
+    plan is a kernel parameter), random block sizes, pool slack and pool modes."""
+    monkeypatch.setenv("LEYLINE_MOVE_KERNEL", "vector")
+    rng = np.random.default_rng(1000 + seed)
+    flags = [0, LAZY, SPLIT, LAZY | SPLIT][seed % 4]
+    n_req = int(rng.integers(4, 14))
+    B = int(rng.choice([1, 4, 16]))
+    lengths = [int(rng.integers(200, 600)) for _ in range(n_req)]
+    lens = list(lengths)
+    steps, key = [], 0
+    for _ in range(30):
+        reqs = rng.choice(n_req, size=int(rng.integers(1, 3)), replace=False)
+        step = []
+        for r in sorted(int(x) for x in reqs):
+            L = lens[r]
+            k = int(rng.integers(1, 3))
+            cuts = sorted(int(x) for x in rng.choice(np.arange(1, L), size=2 * k, replace=False))
+            for j in range(k):
+                s, e = cuts[2 * j], cuts[2 * j + 1]
+                e = min(e, s + max(L // 6, 1))
+                n = int(rng.integers(0, 7))
+                step.append(Dir(r, s, e, n, key))
+                key += 1
+                L += n - (e - s)
+            lens[r] = L
+        steps.append(step)
+    w = Workload(f"overlap-fuzz-{seed}", int(rng.integers(1, 3)), B, lengths, steps, seed=2000 + seed)
+    _run_overlapping_calls(w, flags, "vector", slack=int(rng.integers(0, 40)))
