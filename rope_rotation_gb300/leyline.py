@@ -89,12 +89,12 @@ _SIGNATURES = {
     "leyline_alloc_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "leyline_free_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "leyline_free_page_count": (ctypes.c_int64, [_vp]),
-    "leyline_splice": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(Directive), ctypes.c_int32,
-                                      _vp]),
-    "leyline_splice_noalloc": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(Directive),
-                                              ctypes.c_int32, _vp]),
+    # the directives go in as a plain address: a ctypes array of Directive or a
+    # DIRECTIVE_DTYPE record array (its data pointer)
+    "leyline_splice": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), _vp, ctypes.c_int32, _vp]),
+    "leyline_splice_noalloc": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), _vp, ctypes.c_int32, _vp]),
     "leyline_splice_plan": (ctypes.c_int, [ctypes.POINTER(PoolDesc), ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
-                                           ctypes.c_int32, ctypes.POINTER(Directive), ctypes.c_int32, ctypes.c_int64,
+                                           ctypes.c_int32, _vp, ctypes.c_int32, ctypes.c_int64,
                                            ctypes.POINTER(Stats), ctypes.POINTER(ctypes.c_int64)]),
     "leyline_last_stats": (ctypes.c_int, [_vp, ctypes.POINTER(Stats)]),
     "leyline_gather": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, ctypes.c_int32,
@@ -274,13 +274,14 @@ def directive_batch(req, s_start, s_end, repl: Optional[Sequence] = None, n_repl
 
 
 def _dir_array(dirs):
-    """(pointer argument, count) for a sequence of Directive or a DIRECTIVE_DTYPE array."""
+    """(address argument, count) for a sequence of Directive or a DIRECTIVE_DTYPE array; the
+    caller keeps `dirs` alive for the call."""
     if isinstance(dirs, np.ndarray):
         if dirs.dtype != DIRECTIVE_DTYPE or dirs.ndim != 1 or not dirs.flags.c_contiguous:
             raise ValueError("directive arrays must be 1-D, contiguous and of DIRECTIVE_DTYPE")
         if dirs.size == 0:
             return (Directive * 1)(), 0
-        return dirs.ctypes.data_as(ctypes.POINTER(Directive)), int(dirs.size)
+        return dirs.ctypes.data, int(dirs.size)
     return (Directive * max(len(dirs), 1))(*dirs), len(dirs)
 
 
