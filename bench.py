@@ -324,6 +324,8 @@ def run_ours(args, rank, world, local):
     cache.check_status()
     last = cache.last_stats()
 
+    kernel_leg_ms = elapsed_ms  # --single-leg: the value leg carries the kernel events
+    kl0, kl1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if not args.single_leg:
         # kernel leg: the same steps on fresh requests, with events around move+rotate
         base = W + K
@@ -333,10 +335,14 @@ def run_ours(args, rank, world, local):
         leyline.leyline_kernel_timing_enable(cache.pool, True)
         barrier()
         torch.cuda.synchronize()
+        hold_stream(torch)
+        kl0.record(stream)
         for k in range(K):
             cache.splice(dirs_for(base + W + k, repl_dev))
+        kl1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        kernel_leg_ms = kl0.elapsed_time(kl1)
     k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
     leyline.leyline_kernel_timing_enable(cache.pool, False)
     cache.check_status()
@@ -470,7 +476,10 @@ def run_ours(args, rank, world, local):
                      # the value leg's steps: consecutive calls overlap there, which the
                      # per-launch events of the kernel leg rule out
                      "step_achieved": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9,
-                     "step_frac": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak},
+                     "step_frac": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak,
+                     # the kernel's share of the kernel leg's own steps (serialised like an ncu
+                     # launch list, so the two shares compare)
+                     "launch_share": k2_ms / kernel_leg_ms if kernel_leg_ms > 0 else None},
     }
     if lazy_read:
         line["lazy_read"] = lazy_read
