@@ -617,7 +617,10 @@ def run_chain(args, rank, world, local):
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "launch_ms": k2_ms / max(k2_n, 1), "launches_timed": k2_n,
-                     "algorithmic_bytes_per_launch": per_chain["algorithmic_bytes"] / n_splices},
+                     "algorithmic_bytes_per_launch": per_chain["algorithmic_bytes"] / n_splices,
+                     "step_achieved": per_chain["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9,
+                     "step_frac": per_chain["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak,
+                     "launch_share": k2_ms / elapsed_ms if elapsed_ms > 0 else None},
     }
     cache.close()
     return line, w
