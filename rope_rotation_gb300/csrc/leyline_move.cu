@@ -23,6 +23,16 @@
 namespace leyline {
 namespace {
 
+// A 16-byte value from lane ^ m of the warp (every lane must take part).
+__device__ __forceinline__ uint4 shfl_xor_vec(uint4 v, int m)
+{
+    v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+    v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+    v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+    v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+    return v;
+}
+
 // -------------------------------------------------------------------------
 // Move+rotate, MLA shape (latent 512 = 64 vectors, rope 64 = 8 vectors).
 // Work unit = (16-row tile, layer); a CTA takes a contiguous run of units, so it
@@ -47,10 +57,13 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
     const long long L = a.g.num_layers;
     const long long lat_layer = a.g.lat_layer_vecs, rope_layer = a.g.rope_layer_vecs;
     const int half = 4 * kRopeVecs;  // pairs per row
-    constexpr int kRopeLanesPerRow = kLayout == 0 ? kRopeVecs / 2 : kRopeVecs;  // 4 or 8
+    // 8 lanes per row's band, one 16-byte chunk each: a warp's loads cover whole lines
+    // (half-split: the partner half comes from lane ^ 4)
+    constexpr int kRopeLanesPerRow = kRopeVecs;
     const bool rope_lane = lane < kRowsPerWarp * kRopeLanesPerRow;
     const int rope_row = warp * kRowsPerWarp + lane / kRopeLanesPerRow;
-    const int rope_q = lane % kRopeLanesPerRow;
+    const int rope_c = lane % kRopeLanesPerRow;                 // this lane's chunk
+    const int rope_q = kLayout == 0 ? rope_c % (kRopeVecs / 2) : rope_c;  // its pair group
     float cs[8], sn[8];
     int trig = -1;
 
@@ -112,12 +125,12 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
         }
         const RowDesc dr = rope_lane ? desc[rope_row] : d0;
         const bool do_rope = mine && rope_lane && dr.src != nullptr;
-        uint4 rx, ry;
+        uint4 rx = make_uint4(0u, 0u, 0u, 0u);
         if (do_rope) {
             const uint4* rs = dr.src_band + layer * dr.band_lstride;
-            rx = ld_stream(rs + rope_q);
-            if (kLayout == 0) ry = ld_stream(rs + rope_q + kRopeVecs / 2);
+            rx = ld_stream(rs + rope_c);
         }
+        const uint4 rp = kLayout == 0 ? shfl_xor_vec(rx, kRopeVecs / 2) : rx;  // every lane takes part
         if (has0) {
             uint4* t0 = d0.dst + layer * lat_layer;
             st_stream(t0 + lane, v[0]);
@@ -131,12 +144,13 @@ __global__ void __launch_bounds__(kMoveThreads, 3) move_rotate_mla(const __grid_
         if (do_rope) {
             uint4* rd = dr.dst_band + layer * rope_layer;
             if (kLayout == 0) {
-                if (trig >= 0) rotate_half_split<kBf16>(rx, ry, cs, sn);
-                st_stream(rd + rope_q, rx);
-                st_stream(rd + rope_q + kRopeVecs / 2, ry);
+                const bool hi = rope_c >= kRopeVecs / 2;  // this lane holds the y half
+                uint4 x = hi ? rp : rx, y = hi ? rx : rp;
+                if (trig >= 0) rotate_half_split<kBf16>(x, y, cs, sn);
+                st_stream(rd + rope_c, hi ? y : x);
             } else {
                 if (trig >= 0) rotate_interleaved<kBf16>(rx, cs, sn);
-                st_stream(rd + rope_q, rx);
+                st_stream(rd + rope_c, rx);
             }
         }
     }
