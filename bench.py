@@ -36,12 +36,12 @@ METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 
 FALLBACK_HBM_GBS = 6800.0
 # Per-launch DRAM traffic (read + write bytes) of a kernel on a workload, from an ncu
 # capture, valid only for the kernel code it was taken on (kernel_sha)
-# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 161.1 MB; the
+# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.8 MB; the
 # rest of the 210.9 MB written was still in L2 when the single captured launch ended).
 NCU_TRAFFIC = {
     ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
-        "kernel_sha256": "76c7e7f44dd7ef590c44de8219af8efe598167dc0c6ef02474a2b9be92b6a660",
-        "bytes": 210918912 + 161064704},
+        "kernel_sha256": "cb5ffd94aae258a0a13a19b61dad06767e0bff66acc83ae01ddca7f255930f65",
+        "bytes": 210919168 + 160825344},
     # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
         "kernel_sha256": "2d7517d189d93b0a50478fd95ba3c605c4f05540a7e8e380a390b1ef1cf6ff2b",
