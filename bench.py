@@ -403,14 +403,13 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         hold_stream(torch)
         r0.record(stream)
-        for q in reqs:
-            cache.materialize(q, stream_ptr)
+        cache.materialize_requests(reqs, stream_ptr)
         r1.record(stream)
         torch.cuda.synchronize()
         cache.check_status()
         read_ms = r0.elapsed_time(r1)
         band_bytes = 2 * w.num_layers * w.rope_heads * w.rope_dim * 2  # read + write per turned slot
-        lazy_read = {"op": "leyline_materialize", "requests": len(reqs), "turned_slots": turned,
+        lazy_read = {"op": "leyline_materialize_requests", "requests": len(reqs), "turned_slots": turned,
                      "ms": read_ms, "slots_per_s": turned / (read_ms / 1e3),
                      "algorithmic_gbps": turned * band_bytes / (read_ms / 1e3) / 1e9}
     clocks = sampler.stop()

@@ -310,6 +310,12 @@ int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_
  * pool, bad request). */
 int leyline_materialize(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, void* stream);
 
+/* leyline_materialize for the n requests reqs[0..n) (host array, distinct ids), in one
+ * launch per 64 requests: their rows form one list, so the launches are few and full.
+ * Errors: INVALID_ARG (not a lazy pool, a request out of range or listed twice). */
+int leyline_materialize_requests(leyline_pool_t* pool, const leyline_block_table_t* bt, const int32_t* reqs,
+                                 int32_t n, void* stream);
+
 /* LEYLINE_POOL_LAZY pools: device pointer to the pending counts, int32
  * [num_pages][block_size] (the count of the slot at position t of a request is
  * at page * block_size + t % block_size, page = table[t / block_size]).  Owned by

@@ -115,9 +115,19 @@ int launch_gather(const void* kv, const int32_t* table_row, const Geometry& g, i
 int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry& g, int32_t layer, int64_t t0,
                        int64_t t1, void* out, const int32_t* pending, const double* turn, int32_t* status,
                        void* stream);
-// Lazy pools: turn rows [0, len) of one request by their pending counts, in place, and clear the counts.
-int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
-                       const double* turn, int32_t* status, void* stream);
+// Lazy pools: the requests one materialize launch turns, and the cumulative ends of their
+// rows in the launch's flat row list (request k holds rows [row_end[k - 1], row_end[k])).
+constexpr int kMaterializeReqs = 64;
+struct MaterializeSet {
+    int32_t n;
+    int32_t pad;
+    int32_t req[kMaterializeReqs];
+    int64_t row_end[kMaterializeReqs];
+};
+// Lazy pools: turn every row of the set's requests by its pending count, in place, and
+// clear the counts; table is the block table [num_reqs][max_blocks].
+int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const MaterializeSet& set,
+                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status, void* stream);
 // Lazy pools: set the pending counts of n pages (device ids) to 0.
 int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream);
 // Device access to a caller buffer.  Memory of `device` and managed memory are

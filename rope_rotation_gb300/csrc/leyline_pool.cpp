@@ -574,25 +574,52 @@ int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t r
     return mark_done(p, stream);
 }
 
-int leyline_materialize(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t req, void* stream_v)
+int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t* bt, const int32_t* reqs, int32_t n,
+                                 void* stream_v)
 {
     clear_error();
-    if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    if (!p || !bt || !bt->table || !bt->seq_lens_host || n < 0 || (n > 0 && !reqs))
+        return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
     p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (!p->d_pending) return set_error(LEYLINE_ERR_INVALID_ARG, "the pool was not created with LEYLINE_POOL_LAZY");
-    if (req < 0 || req >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
-    const int64_t len = bt->seq_lens_host[req];
-    if (len < 0 || len > (int64_t)bt->max_blocks * p->g.block_size)
-        return set_error(LEYLINE_ERR_INVALID_ARG, "seq_len outside the block table");
-    if (len == 0) return LEYLINE_OK;
+    std::vector<int32_t> seen(reqs, reqs + n);
+    std::sort(seen.begin(), seen.end());
+    for (int32_t k = 0; k < n; ++k) {
+        if (seen[k] < 0 || seen[k] >= bt->num_reqs) return set_error(LEYLINE_ERR_INVALID_ARG, "request out of range");
+        if (k > 0 && seen[k] == seen[k - 1])  // two warps would turn the same rows
+            return set_error(LEYLINE_ERR_INVALID_ARG, "a request appears twice");
+        const int64_t len = bt->seq_lens_host[seen[k]];
+        if (len < 0 || len > (int64_t)bt->max_blocks * p->g.block_size)
+            return set_error(LEYLINE_ERR_INVALID_ARG, "seq_len outside the block table");
+    }
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
     int rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
-    int err = launch_materialize(p->kv, bt->table + (int64_t)req * bt->max_blocks, p->g, len, p->d_pending,
-                                 p->d_theta_j, p->d_status, stream);
-    if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
-    return mark_done(p, stream);
+    bool launched = false;
+    for (int32_t k0 = 0; k0 < n; k0 += kMaterializeReqs) {  // up to kMaterializeReqs requests per launch
+        MaterializeSet set{};
+        int64_t rows = 0;
+        for (int32_t k = k0; k < n && k < k0 + kMaterializeReqs; ++k) {
+            const int64_t len = bt->seq_lens_host[reqs[k]];
+            if (len == 0) continue;
+            rows += len;
+            set.req[set.n] = reqs[k];
+            set.row_end[set.n] = rows;
+            ++set.n;
+        }
+        if (set.n == 0) continue;
+        int err = launch_materialize(p->kv, bt->table, bt->max_blocks, set, p->g, p->d_pending, p->d_theta_j,
+                                     p->d_status, stream);
+        if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
+        launched = true;
+    }
+    return launched ? mark_done(p, stream) : LEYLINE_OK;
+}
+
+int leyline_materialize(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t req, void* stream_v)
+{
+    return leyline_materialize_requests(p, bt, &req, 1, stream_v);
 }
 
 int32_t* leyline_pending_ptr(leyline_pool_t* p)

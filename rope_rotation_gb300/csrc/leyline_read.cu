@@ -175,14 +175,16 @@ __global__ void gather_lazy_kernel(const uint4* kv, const int32_t* table_row, co
     }
 }
 
-// Materialize a lazy request: one warp per row, its lanes walking the row's (layer,
-// band item) pairs.  When the items per layer divide 32 -- MLA bands, and 1, 2, 4 or 8
+// Materialize lazy requests: the rows of the set's requests form one list, one warp per
+// row (its request found by binary search over the cumulative row ends), its lanes walking
+// the row's (layer, band item) pairs.  When the items per layer divide 32 -- MLA bands, and 1, 2, 4 or 8
 // GQA heads -- a lane's item is the same in every layer, so its cos / sin are read
 // once per row and two layers' loads are in flight before either layer's stores.  The
 // count is read before and cleared after every layer of the row is turned in place.
 template <int kLayout>
-__global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Geometry g, long long len,
-                                   int32_t* pending, const double* turn, int32_t* status)
+__global__ void materialize_kernel(uint4* kv, const int32_t* table, int max_blocks,
+                                   const __grid_constant__ MaterializeSet set, const Geometry g, int32_t* pending,
+                                   const double* turn, int32_t* status)
 {
     __shared__ float2 trig_smem[kReadThreads / 32][kMaxPairs];
     const int lane = threadIdx.x & 31;
@@ -196,7 +198,16 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table_row, const Ge
     WarpTrig wt;
     wt.cs = trig_smem[threadIdx.x / 32];
     const long long warps = (long long)gridDim.x * (blockDim.x / 32);
-    for (long long t = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; t < len; t += warps) {
+    const long long rows = set.row_end[set.n - 1];
+    for (long long f = blockIdx.x * (long long)(blockDim.x / 32) + threadIdx.x / 32; f < rows; f += warps) {
+        int lo = 0, hi = set.n - 1;  // first request whose rows end after f
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (set.row_end[mid] > f) hi = mid;
+            else lo = mid + 1;
+        }
+        const long long t = f - (lo ? set.row_end[lo - 1] : 0);
+        const int32_t* table_row = table + (long long)set.req[lo] * max_blocks;
         const long long B = g.block_size;
         const int page = table_row[t / B];
         if (page < 0 || page >= g.num_pages) {
@@ -312,13 +323,14 @@ int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry&
     return (int)cudaGetLastError();
 }
 
-int launch_materialize(void* kv, const int32_t* table_row, const Geometry& g, int64_t len, int32_t* pending,
-                       const double* turn, int32_t* status, void* stream)
+int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const MaterializeSet& set,
+                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status, void* stream)
 {
-    if (len <= 0) return 0;
+    if (set.n <= 0 || set.row_end[set.n - 1] <= 0) return 0;
+    const long long rows = set.row_end[set.n - 1];
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
-    k<<<grid_for(len * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(static_cast<uint4*>(kv), table_row, g, len,
-                                                                        pending, turn, status);
+    k<<<grid_for(rows * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<uint4*>(kv), table, max_blocks, set, g, pending, turn, status);
     return (int)cudaGetLastError();
 }
 

@@ -100,6 +100,8 @@ _SIGNATURES = {
     "leyline_gather": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int64, ctypes.c_int64, _vp, _vp]),
     "leyline_materialize": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.c_int32, _vp]),
+    "leyline_materialize_requests": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), ctypes.POINTER(ctypes.c_int32),
+                                                    ctypes.c_int32, _vp]),
     "leyline_pending_ptr": (ctypes.c_void_p, [_vp]),
     "leyline_sync_status": (ctypes.c_int, [_vp]),
     "leyline_kernel_timing_enable": (ctypes.c_int, [_vp, ctypes.c_int32]),
@@ -326,6 +328,14 @@ def leyline_gather(pool, tables: Tables, req: int, layer: int, t0: int, t1: int,
 
 def leyline_materialize(pool, tables: Tables, req: int, stream=None) -> None:
     _check(load().leyline_materialize(pool, ctypes.byref(tables.bt), req, _stream_ptr(stream)))
+
+
+def leyline_materialize_requests(pool, tables: Tables, reqs, stream=None) -> None:
+    """leyline_materialize for several distinct requests, in one launch per 64 of them."""
+    a = np.ascontiguousarray(reqs, dtype=np.int32)
+    _check(load().leyline_materialize_requests(pool, ctypes.byref(tables.bt),
+                                               a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), a.size,
+                                               _stream_ptr(stream)))
 
 
 def leyline_pending_ptr(pool) -> int:

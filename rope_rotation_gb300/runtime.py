@@ -130,6 +130,10 @@ class PagedCache:
     def materialize(self, req: int, stream=None) -> None:
         leyline.leyline_materialize(self.pool, self.tables, req, stream)
 
+    def materialize_requests(self, reqs, stream=None) -> None:
+        """materialize several distinct requests in one launch per 64 of them."""
+        leyline.leyline_materialize_requests(self.pool, self.tables, reqs, stream)
+
     def pending(self):
         """Pending counts [num_pages][block_size] of a lazy pool, as a torch view (None otherwise)."""
         addr = leyline.leyline_pending_ptr(self.pool)

@@ -398,3 +398,45 @@ def test_large_counts_across_the_turn_table(precision, layout):
     assert not _pending_of(cache, 0, L).any()
     assert np.array_equal(_raw_rows(cache, 0, L), got), "materialize stored other bits than the gather returned"
     cache.close()
+
+
+@pytest.mark.parametrize("B", [16, 1])
+def test_materialize_requests_equals_one_at_a_time(B):
+    """Many requests in one call turn every row exactly as materializing them one by one does
+    (two pools given the same splices); a request listed twice is refused."""
+    import torch
+    from rope_rotation_gb300 import leyline
+    rng = np.random.default_rng(71)
+    n_req = 70  # more than one launch's 64 requests
+    lengths = [int(rng.integers(40, 160)) for _ in range(n_req)]
+    step, key = [], 0
+    for r in range(n_req):
+        L = lengths[r]
+        if r % 9 == 4:
+            continue  # a request with nothing pending
+        s = int(rng.integers(0, L // 2))
+        step.append(Dir(r, s, s + int(rng.integers(1, L // 3)), int(rng.integers(0, 4)), key))
+        key += 1
+    w = Workload(f"mat-many-B{B}", 2, B, lengths, [step], seed=72)
+    one = H.make_cache(w, flags=LAZY)
+    many = H.make_cache(w, flags=LAZY)
+    for c in (one, many):
+        dirs, keep = H.gpu_directives(w, step)
+        c.splice(dirs)
+        torch.cuda.synchronize()
+        del keep
+    order = [int(x) for x in rng.permutation(n_req)]
+    for r in order:
+        one.materialize(r)
+    many.materialize_requests(order)
+    torch.cuda.synchronize()
+    one.check_status()
+    many.check_status()
+    for r in range(n_req):
+        L = int(one.seq_lens_host[r])
+        assert np.array_equal(_raw_rows(one, r, L), _raw_rows(many, r, L)), f"request {r} differs"
+        assert not _pending_of(many, r, L).any()
+    with pytest.raises(leyline.LeylineError):
+        many.materialize_requests([3, 5, 3])
+    one.close()
+    many.close()
