@@ -231,6 +231,41 @@ int leyline_free_pages(leyline_pool_t* pool, int32_t n, const int32_t* page_ids_
 /* Number of free pages as seen at enqueue time (negative code on a NULL pool). */
 int64_t leyline_free_page_count(const leyline_pool_t* pool);
 
+/* Checkpoint and rollback of the pool's page accounting.  A rewrite splice
+ * (section 2.3's rotation kernel, run out of place) only reads its source pages
+ * and hands them back to the free-page list, so until those pages are taken
+ * again the cache before the splice still exists; these two calls get it back,
+ * to repeat a splice on the same input (benchmark repeats: section 2.3 gives no
+ * other way to run the same edit twice) or to drop a splice whose edit was
+ * rejected.  The pages say nothing about undoing a splice.
+ *
+ * leyline_pool_checkpoint saves the free-page list, its positions and, in a
+ * LEYLINE_POOL_LAZY pool, the pending counts, into device memory the pool
+ * allocates on the first checkpoint (4 bytes per ring entry, 2 * num_pages, plus
+ * 4 bytes per slot in lazy pools) and keeps until destroyed.  A later checkpoint
+ * replaces it.  Enqueued on `stream` after the pool's earlier work.
+ * Errors: INVALID_ARG (null pool), CUDA.
+ *
+ * leyline_pool_rollback puts the saved accounting back (enqueued on `stream`):
+ * pages taken since the checkpoint are free again and pages returned since are
+ * owned again.  The block table and the lengths are the caller's: the caller
+ * restores them too (table, seq_lens_dev and seq_lens_host as they were at the
+ * checkpoint), after the pool's work on the stream.  Refused, with nothing
+ * changed (INVALID_ARG), when
+ *   - the pool has no checkpoint;
+ *   - a page returned since the checkpoint has been taken again (its rows may
+ *     have been overwritten): the splices since the checkpoint took more pages
+ *     than were free at the checkpoint;
+ *   - stored rope bands were turned in place since the checkpoint (a re-index
+ *     splice of an eager pool, or leyline_materialize), unless flags holds
+ *     LEYLINE_ROLLBACK_ACCEPT_TURNED: the accounting is then restored but those
+ *     bands stay turned (benchmark repeats, where the work and not the values
+ *     matters).
+ * Errors: INVALID_ARG, CUDA. */
+#define LEYLINE_ROLLBACK_ACCEPT_TURNED 1
+int leyline_pool_checkpoint(leyline_pool_t* pool, void* stream);
+int leyline_pool_rollback(leyline_pool_t* pool, int32_t flags, void* stream);
+
 /* -------------------------------------------------------------- splice ---- */
 
 /* Apply n AMORTIZE directives (any mix of requests) as one composed pass per
@@ -273,7 +308,9 @@ int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leylin
  * wait for earlier work on `stream`.  Same arguments, results and error codes
  * as leyline_splice, plus SCRATCH when the call's plan exceeds 4 MiB (with a
  * 64-wide rope band, about 12,000 directives that shift their downstream
- * rows): split the directives over several calls. */
+ * rows): split the directives over several calls.  While kernel timing is on
+ * (leyline_kernel_timing_enable), a call is timed with the events created when
+ * timing was switched on; calls beyond those 256 are not timed. */
 int leyline_splice_noalloc(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
                            int32_t n, void* stream);
 

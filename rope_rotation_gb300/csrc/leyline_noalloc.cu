@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "leyline_internal.h"
+#include "leyline_pool_state.h"
 
 using namespace leyline;
 
@@ -180,13 +181,22 @@ extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* 
     const int grid = p->sm_count * (plan.reindex                    ? p->reindex_blocks_per_sm
                                     : a.move_kernel == MOVE_BULK ? p->bulk_blocks_per_sm
                                                                  : p->move_blocks_per_sm);
-    int err = launch_splice(a, nullptr, grid, stream, nullptr, nullptr);
+    // kernel timing uses the events leyline_kernel_timing_enable created up front; a call
+    // past those goes untimed rather than create more
+    cudaEvent_t t0 = nullptr, t1 = nullptr;
+    if (p->timing && p->tev_used < p->tev.size()) {
+        t0 = p->tev[p->tev_used].first;
+        t1 = p->tev[p->tev_used].second;
+        ++p->tev_used;
+    }
+    int err = launch_splice(a, nullptr, grid, stream, t0, t1);
     if (err != 0) return cuda_fail((cudaError_t)err, "launching the splice kernels");
     e = cudaEventRecord(p->done, stream);
     if (e != cudaSuccess) return cuda_fail(e, "recording completion event");
     p->has_work = true;
     p->last_stream = stream;
     p->window_open = false;  // this entry point does not overlap; the next splice waits for it
+    if (plan.reindex && !p->d_pending) p->ckpt_turned = true;  // bands turned in place
 
     for (const ReqPlan& rp : plan.reqs) bt->seq_lens_host[rp.req] = rp.new_len;
     p->q_head += plan.total_pop;

@@ -28,6 +28,7 @@
 #include <vector>
 
 #include "leyline_internal.h"
+#include "leyline_pool_state.h"
 
 namespace leyline {
 const char* last_error_cstr();
@@ -269,6 +270,8 @@ int leyline_pool_destroy(leyline_pool_t* p)
     if (p->d_stage) cudaFree(p->d_stage);
     if (p->d_pending) cudaFree(p->d_pending);
     if (p->d_theta_j) cudaFree(p->d_theta_j);
+    if (p->d_ckpt_queue) cudaFree(p->d_ckpt_queue);
+    if (p->d_ckpt_pending) cudaFree(p->d_ckpt_pending);
     delete p;
     return LEYLINE_OK;
 }
@@ -517,6 +520,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     }
     rc = mark_done(p, stream);
     if (rc != LEYLINE_OK) return rc;
+    if (plan.reindex && !p->d_pending) p->ckpt_turned = true;  // bands turned in place
     if (chainable) {
         if (!overlap) {  // this call waited for everything before it: a new window opens
             p->window_open = true;
@@ -613,6 +617,7 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
                                      p->d_status, stream);
         if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
         launched = true;
+        p->ckpt_turned = true;  // stored bands turned in place
     }
     return launched ? mark_done(p, stream) : LEYLINE_OK;
 }
@@ -649,6 +654,73 @@ int leyline_sync_status(leyline_pool_t* p)
         snprintf(msg, sizeof msg, "device check failed (status bits 0x%x)", st);
         return set_error(LEYLINE_ERR_DEVICE_CHECK, msg);
     }
+    return LEYLINE_OK;
+}
+
+int leyline_pool_checkpoint(leyline_pool_t* p, void* stream_v)
+{
+    clear_error();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
+    const size_t slots = (size_t)p->g.num_pages * (size_t)p->g.block_size;
+    cudaError_t e = cudaSuccess;
+    if (!p->d_ckpt_queue) e = cudaMalloc(&p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap);
+    if (e == cudaSuccess && p->d_pending && !p->d_ckpt_pending)
+        e = cudaMalloc(&p->d_ckpt_pending, sizeof(int32_t) * slots);
+    if (e != cudaSuccess) return cuda_error(e, "allocating the checkpoint");
+    int rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    e = cudaMemcpyAsync(p->d_ckpt_queue, p->d_queue, sizeof(int32_t) * (size_t)p->q_cap, cudaMemcpyDeviceToDevice,
+                        stream);
+    if (e == cudaSuccess && p->d_pending)
+        e = cudaMemcpyAsync(p->d_ckpt_pending, p->d_pending, sizeof(int32_t) * slots, cudaMemcpyDeviceToDevice,
+                            stream);
+    if (e != cudaSuccess) return cuda_error(e, "copying the page accounting");
+    rc = mark_done(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    p->has_ckpt = true;
+    p->ckpt_head = p->q_head;
+    p->ckpt_tail = p->q_tail;
+    p->ckpt_turned = false;
+    return LEYLINE_OK;
+}
+
+int leyline_pool_rollback(leyline_pool_t* p, int32_t flags, void* stream_v)
+{
+    clear_error();
+    if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    p->window_open = false;  // other work on the pool ends the window of overlapping splices
+    if ((flags & ~LEYLINE_ROLLBACK_ACCEPT_TURNED) != 0) return set_error(LEYLINE_ERR_INVALID_ARG, "unknown flags");
+    if (!p->has_ckpt) return set_error(LEYLINE_ERR_INVALID_ARG, "the pool has no checkpoint");
+    // Pages returned since the checkpoint sit at ring positions from ckpt_tail on: once the
+    // head passed that point, one of them was taken again and may have been written.
+    if (p->q_head > p->ckpt_tail)
+        return set_error(LEYLINE_ERR_INVALID_ARG,
+                         "pages returned since the checkpoint have been taken again: their rows may be overwritten");
+    if (p->ckpt_turned && !(flags & LEYLINE_ROLLBACK_ACCEPT_TURNED))
+        return set_error(LEYLINE_ERR_INVALID_ARG,
+                         "stored rope bands were turned in place since the checkpoint (re-index splice of an eager "
+                         "pool, or materialize); a rollback would not undo that");
+    cudaStream_t stream = (cudaStream_t)stream_v;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
+    int rc = order_after_previous(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    const size_t slots = (size_t)p->g.num_pages * (size_t)p->g.block_size;
+    cudaError_t e = cudaMemcpyAsync(p->d_queue, p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap,
+                                    cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && p->d_pending)
+        e = cudaMemcpyAsync(p->d_pending, p->d_ckpt_pending, sizeof(int32_t) * slots, cudaMemcpyDeviceToDevice,
+                            stream);
+    if (e != cudaSuccess) return cuda_error(e, "restoring the page accounting");
+    rc = mark_done(p, stream);
+    if (rc != LEYLINE_OK) return rc;
+    p->q_head = p->ckpt_head;
+    p->q_tail = p->ckpt_tail;
+    p->ckpt_turned = false;
     return LEYLINE_OK;
 }
 

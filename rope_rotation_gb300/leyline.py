@@ -39,6 +39,7 @@ LEYLINE_EVICT = 2
 LEYLINE_POOL_REINDEX = 1
 LEYLINE_POOL_LAZY = 2
 LEYLINE_POOL_SPLIT_ROPE = 4
+LEYLINE_ROLLBACK_ACCEPT_TURNED = 1
 
 
 class LeylineError(RuntimeError):
@@ -89,6 +90,8 @@ _SIGNATURES = {
     "leyline_alloc_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "leyline_free_pages": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]),
     "leyline_free_page_count": (ctypes.c_int64, [_vp]),
+    "leyline_pool_checkpoint": (ctypes.c_int, [_vp, _vp]),
+    "leyline_pool_rollback": (ctypes.c_int, [_vp, ctypes.c_int32, _vp]),
     # the directives go in as a plain address: a ctypes array of Directive or a
     # DIRECTIVE_DTYPE record array (its data pointer)
     "leyline_splice": (ctypes.c_int, [_vp, ctypes.POINTER(BlockTable), _vp, ctypes.c_int32, _vp]),
@@ -205,6 +208,16 @@ def leyline_free_page_count(pool) -> int:
     n = load().leyline_free_page_count(pool)
     _check(int(n) if n < 0 else 0)
     return int(n)
+
+
+def leyline_pool_checkpoint(pool, stream=None) -> None:
+    """Save the pool's page accounting (free-page list, positions, lazy counts) on the device."""
+    _check(load().leyline_pool_checkpoint(pool, _stream_ptr(stream)))
+
+
+def leyline_pool_rollback(pool, flags: int = 0, stream=None) -> None:
+    """Restore the accounting saved by the last checkpoint; the caller restores its tables."""
+    _check(load().leyline_pool_rollback(pool, flags, _stream_ptr(stream)))
 
 
 # ----------------------------------------------------------- block table ----

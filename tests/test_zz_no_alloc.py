@@ -177,3 +177,45 @@ def test_noalloc_matches_splice_when_runs_shift_by_whole_blocks():
         del keep_ref, keep_new
     ref.close()
     new.close()
+
+
+def test_noalloc_calls_on_two_streams_of_one_pool():
+    """Consecutive no-alloc calls of one pool issued on two streams share the static scratch;
+    the pool orders the second after the first (it waits for the first's completion event),
+    so the results equal, bit for bit, leyline_splice's on one stream.  With kernel timing on,
+    both calls are timed as leyline_splice's would be."""
+    from rope_rotation_gb300 import leyline
+    steps = [[Dir(0, 40, 130, 9, 0), Dir(1, 5, 700, 3, 1), Dir(2, 76, 77, 1, 3)],
+             [Dir(0, 0, 3, 0, 4), Dir(1, 100, 101, 30, 5), Dir(2, 10, 50, 2, 6)]]
+    w = Workload("noalloc-streams", 3, 16, [300, 1000, 77], steps, seed=25)
+    ref = H.make_cache(w, slack_pages=16)
+    new = H.make_cache(w, slack_pages=16)
+    keep = []
+    for step in w.steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        leyline.leyline_splice(ref.pool, ref.tables, dirs)
+    calls = []
+    for step in w.steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        calls.append(dirs)
+    torch.cuda.synchronize()  # the caches and rows of R are written on the default stream
+    leyline.leyline_kernel_timing_enable(new.pool, True)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for dirs, s in zip(calls, streams):
+        leyline.leyline_splice_noalloc(new.pool, new.tables, dirs, s)
+    ms, n = leyline.leyline_kernel_timing_read(new.pool)
+    leyline.leyline_kernel_timing_enable(new.pool, False)
+    assert n == 2 and ms > 0
+    torch.cuda.synchronize()
+    ref.check_status()
+    new.check_status()
+    assert np.array_equal(ref.seq_lens_host, new.seq_lens_host)
+    assert ref.free_pages() == new.free_pages()
+    for r in range(w.num_reqs):
+        n_r = int(ref.seq_lens_host[r])
+        assert np.array_equal(H.logical_rows(ref, r, n_r), H.logical_rows(new, r, n_r)), f"request {r} differs"
+    del keep
+    ref.close()
+    new.close()
