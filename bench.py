@@ -1,17 +1,25 @@
 """Benchmark of the GB300 Leyline AMORTIZE splice.
 
-Workload (default): the DeepSeek-V2-Lite-shaped paged MLA cache -- 27 layers,
-32768 tokens, block size 16, latent 512 + rope 64 bf16 -- and one directive that
-replaces [20000, 26000) by 12 rows (Delta = -5988): 6768 downstream slots, each
-moved and rotated in all 27 layers.  A step is one leyline_splice call (plan,
-move+rotate, commit kernels) on one request.  Each timed step splices a
-different, pre-filled request, so every step reads 0.42 GB that no earlier step
-touched (inputs larger than L2; no reset inside the timed region).
+Workload (default): the largest synthetic configuration, a concurrency sweep of
+C = 16 requests sharing one 61-layer paged MLA pool (block size 16, latent 512 +
+rope 64 bf16, lengths lognormal with median 24000 clipped to [2048, 131072]) and
+1-3 directives per request: 36 directives, about 153k rewritten slots in every
+layer, 21.5 GB of algorithmic bytes per call.  A step is one leyline_splice call
+over all 16 requests (plan, move+rotate, commit kernels).
+
+The requests stay resident: a rewrite splice only reads its source pages, so
+between steps the caller's tables and lengths are put back from a saved copy and
+the pool's page accounting is rolled back (leyline_pool_checkpoint /
+leyline_pool_rollback); the next step splices the same 29.6 GB of rows again.
+Those restores are a few device copies of tables and the free-page ring, and
+they lie inside the timed region.  Smaller workloads keep as many copies as the
+memory budget holds and restore only when all have been used.
 
 Metric: downstream slots spliced per second (each slot covers all layers), plus
-HBM GB/s of the move+rotate kernel against the measured copy bandwidth.
+HBM GB/s of the move+rotate kernel against the measured copy bandwidth and the
+8 TB/s nominal.
 
-    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference] [--workload cfg2]
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl reference] [--workload cfg5-C16-B16]
 """
 from __future__ import annotations
 
@@ -34,18 +42,14 @@ if ROOT not in sys.path:
 
 METRIC = "downstream slots spliced/sec (all layers) and HBM GB/s vs 8 TB/s on 1 GB300"
 FALLBACK_HBM_GBS = 6800.0
-# Per-launch DRAM traffic (read + write bytes) of a kernel on a workload, from an ncu
-# capture, valid only for the kernel code it was taken on (kernel_sha)
-# (profiles/move_rotate_dsv2lite_27L_32k_B16_full.md: read 210.9 MB + write 160.8 MB; the
-# rest of the 210.9 MB written was still in L2 when the single captured launch ended).
+NOMINAL_HBM_GBS = 8000.0  # the GB300 HBM3e figure the metric names
+# Resident copies of a workload's requests are kept within this many bytes of pool.
+DEFAULT_MEM_GB = 96.0
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel on a
+# workload, from one ncu capture of that kernel, valid only for the kernel code it was
+# taken on (kernel_sha).  "scale": the capture ran on fewer layers and its traffic is
+# multiplied by the ratio of the units (tile x layer) the full launch processes.
 NCU_TRAFFIC = {
-    ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
-        "kernel_sha256": "cb5ffd94aae258a0a13a19b61dad06767e0bff66acc83ae01ddca7f255930f65",
-        "bytes": 210919168 + 160825344},
-    # profiles/rotate_in_place_sweep_C4_B1_16L_full.md (the rotate kernel alone)
-    ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "2d7517d189d93b0a50478fd95ba3c605c4f05540a7e8e380a390b1ef1cf6ff2b",
-        "bytes": 130889984 + 75299584},
 }
 
 
@@ -55,7 +59,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--workload", default="cfg5-C16-B16")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--reindex", action="store_true",
                     help="block size 1 pools: keep survivors in their pages (LEYLINE_POOL_REINDEX)")
@@ -72,7 +76,10 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the workload's layer count (small cases for profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="wall-time budget of each CPU-baseline sample (single core, then all cores)")
+    ap.add_argument("--mem-gb", type=float, default=DEFAULT_MEM_GB,
+                    help="device memory for resident copies of the workload's requests (at least one copy)")
     return ap.parse_args()
 
 
@@ -183,6 +190,7 @@ class ClockSampler:
 def workload(name: str, layers: int = 0, chain_ok: bool = False):
     from synth import configs
     w = configs.by_name(name)
+    w.key, w.layers_override = name, layers  # how a spawned worker rebuilds the same workload
     if len(w.steps) != 1 and not chain_ok:
         raise SystemExit(f"workload {name} is a multi-step chain; bench runs single-call workloads")
     if layers > 0:
@@ -191,13 +199,23 @@ def workload(name: str, layers: int = 0, chain_ok: bool = False):
     return w
 
 
-def per_request_counts(w):
-    """Downstream and replacement slots of one call of the workload (oracle-free: planner dry run)."""
+def _dry_directives(w, step):
+    """The workload's directives for a host-only dry run: a 16-byte aligned stand-in for each
+    directive's rows of R (the planner never reads them)."""
     from rope_rotation_gb300 import leyline
-    desc = leyline.pool_desc(w.num_layers, w.block_size, 1, w.latent_dim, w.rope_dim, w.theta)
-    dirs = [leyline.directive(d.req, d.s_start, d.s_end, None, n_repl=0) for d in w.steps[0]]
+    fake = 1 << 40
+    return [leyline.Directive(d.req, d.mode, d.s_start, d.s_end, d.n_repl, 0, fake if d.n_repl else None)
+            for d in step]
+
+
+def plan_stats(w, flags: int = 0):
+    """The work accounting of one call of the workload (leyline_splice_plan: host planner, no
+    device): downstream and replacement slots, algorithmic bytes, fresh pages taken."""
+    from rope_rotation_gb300 import leyline
+    desc = leyline.pool_desc(w.num_layers, w.block_size, 1, w.latent_dim, w.rope_dim, w.theta, flags=flags,
+                             rope_heads=w.rope_heads)
     nb = max(-(-(L + 64 * 3) // w.block_size) for L in w.lengths)
-    st, _ = leyline.leyline_splice_plan(desc, np.array(w.lengths, dtype=np.int64), nb, dirs)
+    st, _ = leyline.leyline_splice_plan(desc, np.array(w.lengths, dtype=np.int64), nb, _dry_directives(w, w.steps[0]))
     return st
 
 
@@ -205,9 +223,7 @@ def host_plan_us(w, flags: int, reps: int = 50) -> float:
     """Median time of the host planner alone (leyline_splice_plan, C, no device) for one call."""
     from rope_rotation_gb300 import leyline
     desc = leyline.pool_desc(w.num_layers, w.block_size, 1, w.latent_dim, w.rope_dim, w.theta, flags=flags)
-    fake = 1 << 40  # a 16-byte aligned stand-in for the rows of R: the dry run never reads them
-    dirs = [leyline.Directive(d.req, d.mode, d.s_start, d.s_end, d.n_repl, 0, fake if d.n_repl else None)
-            for d in w.steps[0]]
+    dirs = _dry_directives(w, w.steps[0])
     nb = max(-(-(L + 64 * 3) // w.block_size) for L in w.lengths)
     lens = np.array(w.lengths, dtype=np.int64)
     times = []
@@ -216,6 +232,13 @@ def host_plan_us(w, flags: int, reps: int = 50) -> float:
         leyline.leyline_splice_plan(desc, lens, nb, dirs)
         times.append((time.perf_counter() - t) * 1e6)
     return float(statistics.median(times))
+
+
+def resident_copies(copy_bytes: int, wanted: int, mem_gb: float) -> int:
+    """How many copies of the workload's requests stay resident: at most `wanted` (one per
+    step of a leg), at least one, within mem_gb of pool."""
+    fit = int(mem_gb * 1e9 // max(copy_bytes, 1))
+    return max(1, min(wanted, fit))
 
 
 # ---------------------------------------------------------------- our arm ---
@@ -229,6 +252,50 @@ HEAD_START_CYCLES = 2_000_000  # about 1 ms at 2 GHz
 
 def hold_stream(torch):
     torch.cuda._sleep(HEAD_START_CYCLES)
+
+
+class Resident:
+    """`copies` copies of the workload's requests in one pool, and the state to put them back.
+
+    Copy g holds requests g*C .. g*C + C - 1.  After filling, the caller's table and lengths
+    are saved and the pool's page accounting is checkpointed.  next_group() hands out the
+    copies in turn; once all have been spliced it first restores the table, the lengths and
+    the accounting (device copies on the stream, so they order after the last splice and
+    before the next one), which makes every copy splice-able again: a rewrite splice only
+    reads its source pages, and the rollback is refused if any of them was taken again."""
+
+    def __init__(self, torch, cache, copies: int, C: int, flags: int, stream):
+        from rope_rotation_gb300 import leyline
+        self.torch, self.cache, self.copies, self.C = torch, cache, copies, C
+        self.leyline = leyline
+        self.stream = stream
+        # bands turned in place (eager re-index) stay turned across a rollback: the work of
+        # the repeated call is the same, its values are not compared
+        self.flags = (leyline.LEYLINE_ROLLBACK_ACCEPT_TURNED
+                      if (flags & leyline.LEYLINE_POOL_REINDEX) and not (flags & leyline.LEYLINE_POOL_LAZY)
+                      else 0)
+        self.table = cache.table.clone()
+        self.lens_dev = cache.seq_lens_dev.clone()
+        self.lens_host = cache.seq_lens_host.copy()
+        leyline.leyline_pool_checkpoint(cache.pool, stream)
+        self.used = 0
+        self.restores = 0
+
+    def restore(self):
+        c = self.cache
+        c.table.copy_(self.table, non_blocking=True)
+        c.seq_lens_dev.copy_(self.lens_dev, non_blocking=True)
+        c.seq_lens_host[:] = self.lens_host
+        self.leyline.leyline_pool_rollback(c.pool, self.flags, self.stream)
+        self.used = 0
+        self.restores += 1
+
+    def next_group(self) -> int:
+        if self.used == self.copies:
+            self.restore()
+        g = self.used
+        self.used += 1
+        return g
 
 
 def run_ours(args, rank, world, local):
@@ -247,26 +314,25 @@ def run_ours(args, rank, world, local):
     w = workload(args.workload, args.layers)
     K, W = args.steps, args.warmup
     C = w.num_reqs
-    # legs: value (plain steps), kernel (the same steps with CUDA events around the
-    # move+rotate kernel, for the roofline), e2e (host buffers); each step and warm-up
-    # of each leg splices its own copy of the workload's requests
+    B = w.block_size
+    flags = ((leyline.LEYLINE_POOL_REINDEX if args.reindex else 0) | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)
+             | (leyline.LEYLINE_POOL_SPLIT_ROPE if args.split else 0))
     if args.single_leg:
         args.no_e2e = True
-    legs = 1 if args.single_leg else (2 if args.no_e2e else 3)
-    groups = (W + K) * legs
-    B = w.block_size
+    plan = plan_stats(w, flags)
     max_blocks = max(-(-(L + 64 * 3) // B) for L in w.lengths)
-    pages = groups * sum(-(-L // B) for L in w.lengths) + sum(-(-L // B) + 1 for L in w.lengths)
-    cache = PagedCache(w.num_layers, B, pages, groups * C, max_blocks, w.latent_dim, w.rope_dim, w.theta,
-                       flags=(leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
-                       | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)
-                       | (leyline.LEYLINE_POOL_SPLIT_ROPE if args.split else 0))
+    # pages of one copy: its requests, plus the fresh pages one call takes
+    copy_pages = sum(-(-L // B) for L in w.lengths) + plan.pages_popped + C
+    page_bytes = w.num_layers * B * w.row_elems * 2
+    copies = resident_copies(copy_pages * page_bytes, W + K, args.mem_gb)
+    cache = PagedCache(w.num_layers, B, copies * copy_pages, copies * C, max_blocks, w.latent_dim, w.rope_dim,
+                       w.theta, flags=flags)
     seed = rank_seed(w.seed, rank)
-    for g in range(groups):
+    for g in range(copies):
         for r, L in enumerate(w.lengths):
             cache.add_request(g * C + r, L)
             fill.fill_request(cache, seed, g * C + r, L)
-    # replacement rows: device copies (value leg) and pinned host copies (e2e leg)
+    # replacement rows: device copies (value and kernel legs) and pinned host copies (e2e leg)
     repl_dev, repl_host = {}, {}
     for d in w.steps[0]:
         if d.n_repl:
@@ -291,17 +357,26 @@ def run_ours(args, rank, world, local):
 
     stream = torch.cuda.current_stream()
     stream_ptr = stream.cuda_stream
-    # warm-up
-    for g in range(W):
-        cache.splice(dirs_for(g, repl_dev))
     torch.cuda.synchronize()
-    cache.check_status()
-    st = cache.last_stats()
+    res = Resident(torch, cache, copies, C, flags, stream_ptr)
+
+    def step(repl_map):
+        g = res.next_group()
+        cache.splice(dirs_for(g, repl_map), stream_ptr)
+        return g
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
+
+    # warm-up
+    for _ in range(W):
+        step(repl_dev)
+    torch.cuda.synchronize()
+    cache.check_status()
+    st = cache.last_stats()
+    assert st["downstream_slots"] == plan.downstream_slots and st["algorithmic_bytes"] == plan.algorithmic_bytes
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -309,36 +384,37 @@ def run_ours(args, rank, world, local):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.single_leg:
         leyline.leyline_kernel_timing_enable(cache.pool, True)
+    restores0 = res.restores
     barrier()
     torch.cuda.synchronize()
     hold_stream(torch)
     ev0.record(stream)
     t_host = time.perf_counter()
-    for k in range(K):
-        cache.splice(dirs_for(W + k, repl_dev), stream_ptr)
+    for _ in range(K):
+        step(repl_dev)
     enqueue_us = (time.perf_counter() - t_host) * 1e6 / K
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
     elapsed_ms = ev0.elapsed_time(ev1)
+    value_restores = res.restores - restores0
     cache.check_status()
     last = cache.last_stats()
 
     kernel_leg_ms = elapsed_ms  # --single-leg: the value leg carries the kernel events
     kl0, kl1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if not args.single_leg:
-        # kernel leg: the same steps on fresh requests, with events around move+rotate
-        base = W + K
-        for g in range(W):
-            cache.splice(dirs_for(base + g, repl_dev))
+        # kernel leg: the same steps with events around each move (or rotate) kernel
+        for _ in range(W):
+            step(repl_dev)
         torch.cuda.synchronize()
         leyline.leyline_kernel_timing_enable(cache.pool, True)
         barrier()
         torch.cuda.synchronize()
         hold_stream(torch)
         kl0.record(stream)
-        for k in range(K):
-            cache.splice(dirs_for(base + W + k, repl_dev))
+        for _ in range(K):
+            step(repl_dev)
         kl1.record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -349,20 +425,20 @@ def run_ours(args, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        # End to end through the public API: each step copies its replacement rows from
-        # pinned host memory, splices, and reads back the request's new lengths and table row.
-        base = 2 * (W + K)
+        # End to end through the public API: each step's rows of R come from pinned host
+        # memory, and the step's new lengths and table rows are read back to the host.
         rbuf = {k: torch.empty_like(v) for k, v in repl_dev.items()}
         out_tab = torch.empty((K, C, max_blocks), dtype=torch.int32).pin_memory()
         out_len = torch.empty((K, C), dtype=torch.int32).pin_memory()
+        exp_len = np.zeros((K, C), dtype=np.int64)
         # rows of R: by default the splice is given the pinned host rows and its move kernel
         # reads them in place over the host link; --e2e-copy stages them on the device first
         src = rbuf if args.e2e_copy else repl_host
-        for g in range(W):  # warm the copy path
+        for _ in range(W):  # warm the copy path
             if args.e2e_copy:
                 for k2, v in repl_host.items():
                     rbuf[k2].copy_(v, non_blocking=True)
-            cache.splice(dirs_for(base + g, src))
+            step(src)
         torch.cuda.synchronize()
         h2d = sum(v.numel() * v.element_size() for v in repl_host.values())
         d2h = C * max_blocks * 4 + C * 4
@@ -371,28 +447,31 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         e0.record(stream)
         for k in range(K):
-            g = base + W + k
             if args.e2e_copy:
                 for k2, v in repl_host.items():
                     rbuf[k2].copy_(v, non_blocking=True)
-            cache.splice(dirs_for(g, src), stream_ptr)
+            g = step(src)
             out_tab[k].copy_(cache.table[g * C:(g + 1) * C], non_blocking=True)
             out_len[k].copy_(cache.seq_lens_dev[g * C:(g + 1) * C], non_blocking=True)
+            exp_len[k] = cache.seq_lens_host[g * C:(g + 1) * C]
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
         e2e_ms = e0.elapsed_time(e1)
         cache.check_status()
-        exp_len = cache.seq_lens_host[(base + W) * C:(base + W + K) * C].reshape(K, C)
         assert np.array_equal(out_len.numpy(), exp_len), "e2e read-back lengths differ"
         e2e = {"ms": e2e_ms, "h2d": h2d, "d2h": d2h,
                "inputs": "rows of R copied to device buffers, then spliced" if args.e2e_copy
                else "rows of R read in place from pinned host memory by the move kernel"}
     lazy_read = None
     if args.lazy and args.read:
-        # the cost a lazy pool defers to its reads: materialize each request of the value
-        # leg's timed steps (every pending band turned in place once, counts cleared)
-        reqs = [g * C + r for g in range(W, W + K) for r in range(C)]
+        # the cost a lazy pool defers to its reads: splice every resident copy once, then
+        # materialize all their requests (every pending band turned in place once, counts
+        # cleared)
+        res.restore()
+        for _ in range(copies):
+            step(repl_dev)
+        reqs = list(range(copies * C))
         pend = cache.pending().view(-1)
         turned = 0
         for q in reqs:
@@ -425,11 +504,9 @@ def run_ours(args, rank, world, local):
     k2_avg_s = (k2_ms / max(k2_n, 1)) / 1e3
     achieved = st["algorithmic_bytes"] / k2_avg_s / 1e9
     kernel_name = "rotate_in_place" if reindexed else "move_rotate_" + os.environ.get("LEYLINE_MOVE_KERNEL", "vector")
-    traffic = None
-    stored = NCU_TRAFFIC.get((w.name, kernel_name))
-    if stored and not args.lazy and not args.split and stored["kernel_sha256"] == kernel_sha(
-            "rotate_in_place" if reindexed else "move_rotate"):
-        traffic = stored["bytes"]
+    traffic = stored_traffic(w, kernel_name, "rotate_in_place" if reindexed else "move_rotate",
+                             eligible=not args.lazy and not args.split)
+    step_achieved = st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -443,12 +520,20 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "layers": w.num_layers, "tokens": w.lengths if C > 1 else w.lengths[0],
+        "config": {"workload": w.name, "layers": w.num_layers, "requests": C,
+                   "tokens": w.lengths if C > 1 else w.lengths[0],
                    "block_size": B, "latent_dim": w.latent_dim, "rope_dim": w.rope_dim, "storage": "bf16",
-                   "directives": [[d.s_start, d.s_end, d.n_repl] for d in w.steps[0]],
+                   "directives": [[d.req, d.s_start, d.s_end, d.n_repl] for d in w.steps[0]],
                    "downstream_slots_per_step": st["downstream_slots"], "repl_slots_per_step": st["repl_slots"],
                    "algorithmic_bytes_per_step": st["algorithmic_bytes"],
-                   "l2": "inputs larger than L2: each step splices its own pre-filled request",
+                   "resident_copies": copies,
+                   "restores_in_value_leg": value_restores,
+                   "l2": "inputs larger than L2: each step splices "
+                         + (f"{st['algorithmic_bytes'] / 2e9:.2f} GB of source rows" if copies == 1
+                            else f"one of {copies} resident copies of the requests in turn"),
+                   "repeat": "between steps the caller's table and lengths are copied back and the pool's page "
+                             "accounting is rolled back (leyline_pool_rollback), once all resident copies have "
+                             "been spliced; these restores run inside the timed region",
                    "timing": "value: CUDA events around K steps queued behind a ~1 ms spin on the stream "
                              "(device time of the steps); e2e: events around the steps with no head start",
                    "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
@@ -458,8 +543,7 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "gbps_step": st["algorithmic_bytes"] * K * world / (elapsed_ms / 1e3) / 1e9,
         "slot_layers_per_s": value * w.num_layers,
-        "host_plan_us": host_plan_us(w, (leyline.LEYLINE_POOL_REINDEX if args.reindex else 0)
-                                     | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)),
+        "host_plan_us": host_plan_us(w, flags & (leyline.LEYLINE_POOL_REINDEX | leyline.LEYLINE_POOL_LAZY)),
         # host side of the timed steps: the Python loop per step, and the library's own
         # account of its last call (leyline_stats_t host_ns, resolve_ns, plan_ns)
         "host": {"enqueue_us_per_step": enqueue_us, "splice_call_us": last["host_ns"] / 1e3,
@@ -470,12 +554,13 @@ def run_ours(args, rank, world, local):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
                      "launch_ms": k2_avg_s * 1e3, "launches_timed": k2_n,
                      "algorithmic_bytes_per_launch": st["algorithmic_bytes"],
-                     # the value leg's steps: consecutive calls overlap there, which the
-                     # per-launch events of the kernel leg rule out
-                     "step_achieved": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9,
-                     "step_frac": st["algorithmic_bytes"] / (elapsed_ms / K / 1e3) / 1e9 / peak,
+                     # the value leg's steps (with their restores), against the same peaks
+                     "step_achieved": step_achieved,
+                     "step_frac": step_achieved / peak,
+                     "step_frac_nominal": step_achieved / NOMINAL_HBM_GBS,
                      # the kernel's share of the kernel leg's own steps (serialised like an ncu
                      # launch list, so the two shares compare)
                      "launch_share": k2_ms / kernel_leg_ms if kernel_leg_ms > 0 else None},
@@ -490,7 +575,14 @@ def run_ours(args, rank, world, local):
     return line, w
 
 
-# -------------------------------------------------------------- CPU oracle --
+def stored_traffic(w, kernel_name: str, kernel_src: str, eligible: bool = True):
+    """Per-launch DRAM bytes of the timed kernel on this workload from the stored ncu capture,
+    or None when there is none or the kernel's code changed since it was taken."""
+    stored = NCU_TRAFFIC.get((w.name, kernel_name))
+    if not eligible or not stored or stored["kernel_sha256"] != kernel_sha(kernel_src):
+        return None
+    return stored["bytes"] * stored.get("scale", 1.0)
+
 
 def run_chain(args, rank, world, local):
     """A workload of successive splices of one request (the 64-splice chain): a step is the
@@ -625,62 +717,158 @@ def run_chain(args, rank, world, local):
     return line, w
 
 
-def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
-    """Time the fp64 oracle (single thread, as it stands) on whole calls of the workload,
-    repeated until about budget_s seconds of CPU work."""
+# -------------------------------------------------------------- CPU oracle --
+#
+# The oracle (fp64 C, as it stands) timed on the host cores.  A call's work is cut into
+# units of one request's splice in one layer (layers are independent: the same plan turns
+# every layer).  A unit's rows are generated first and only the oracle call is timed.  The
+# single-core figure runs units one after another in this process; the all-core figure
+# runs them in a pool of spawned processes (spawned, not forked: this process may hold a
+# CUDA context), one per core, and divides their slots by the longest summed oracle time
+# of any process.  Slots are counted as the metric counts them: a unit of request r in one
+# layer is worth downstream(r) / layers slots.
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_units(w):
+    """[(request, layer, slot worth)] of one call, layer-major, and the call's downstream slots."""
+    import oracle
+    per_req = {}
+    for r in range(w.num_reqs):
+        ds = [d for d in w.steps[0] if d.req == r]
+        if not ds:
+            continue
+        _, kind, idx, _ = oracle.splice_map(w.lengths[r], [(d.s_start, d.s_end, d.n_repl) for d in ds])
+        first_end = min(d.s_end for d in ds)
+        per_req[r] = int(np.count_nonzero((kind == 0) & (idx >= first_end)))
+    units = [(r, layer, per_req[r] / w.num_layers) for layer in range(w.num_layers) for r in sorted(per_req)]
+    return units, sum(per_req.values())
+
+
+def _oracle_unit(job):
+    """One unit in a worker: generate the request's rows of one layer, time the oracle's splice."""
     import oracle
     import synth
-    st = per_request_counts(w)
-    caches = [synth.cache_request(seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)]
-    reps = {d.key: synth.repl_rows(seed, d.req, d.key, w.num_layers, d.n_repl, w.row_elems) for d in w.steps[0]}
-    calls, t_total = 0, 0.0
-    while t_total < budget_s or calls == 0:
+    seed, key, layers, r, layer = job
+    w = workload(key, layers)
+    ds = [d for d in w.steps[0] if d.req == r]
+    cache = synth.cache_rows(seed, r, layer, np.arange(w.lengths[r]), w.row_elems)[None]
+    reps = [synth.repl_rows(seed, r, d.key, w.num_layers, d.n_repl, w.row_elems)[layer:layer + 1] for d in ds]
+    t0 = time.perf_counter()
+    oracle.splice_request(cache, [(d.s_start, d.s_end, d.n_repl) for d in ds], reps, w.latent_dim, w.theta)
+    return time.perf_counter() - t0, os.getpid()
+
+
+class OraclePool:
+    """Spawned worker processes, one per host core, that run oracle units."""
+
+    def __init__(self, procs: int):
+        import multiprocessing as mp
+        import oracle
+        oracle.build()  # once, here; the workers load the built library
+        self.procs = procs
+        self.pool = mp.get_context("spawn").Pool(procs)
+
+    def run(self, seed: int, w, units) -> tuple[float, float]:
+        """(longest summed oracle seconds of any worker, wall seconds) over the units."""
+        per_pid = {}
         t0 = time.perf_counter()
-        for r in range(w.num_reqs):
-            ds = [d for d in w.steps[0] if d.req == r]
-            if ds:
-                oracle.splice_request(caches[r], [(d.s_start, d.s_end, d.n_repl) for d in ds],
-                                      [reps[d.key] for d in ds], w.latent_dim, w.theta)
-        t_total += time.perf_counter() - t0
-        calls += 1
-    value = st.downstream_slots * calls / t_total
-    return {"value": value, "unit": "slots/s", "cores": 1, "kind": "oracle",
-            "sample": f"{calls} whole call(s) of {w.name} ({w.num_layers} layers) through the fp64 C oracle, "
-                      f"single thread, {t_total:.1f} s"}, t_total / calls
+        jobs = [(seed, w.key, w.layers_override, r, l) for r, l, _ in units]
+        for dt, pid in self.pool.imap_unordered(_oracle_unit, jobs):
+            per_pid[pid] = per_pid.get(pid, 0.0) + dt
+        return max(per_pid.values()), time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def single_core_sample(w, units, budget_s: float, seed: int):
+    """Units one after another in this process until budget_s of oracle time: (slots, seconds, units)."""
+    slots, spent, n = 0.0, 0.0, 0
+    for r, layer, worth in units:
+        dt, _ = _oracle_unit((seed, w.key, w.layers_override, r, layer))
+        slots += worth
+        spent += dt
+        n += 1
+        if spent >= budget_s:
+            break
+    return slots, spent, n
+
+
+def parallel_units(units, rate_1: float, budget_core_s: float):
+    """The first units (layer-major, so every request is in the sample) whose single-core
+    estimate fits budget_core_s core-seconds; at least one layer of every request."""
+    per_layer = len({r for r, _, _ in units})
+    out, est = [], 0.0
+    for i, u in enumerate(units):
+        est += u[2] / rate_1
+        if est > budget_core_s and i >= per_layer:
+            break
+        out.append(u)
+    return out
+
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
+    """The oracle on the host cores: a single-core sample, then a sample on all cores."""
+    units, _ = oracle_units(w)
+    s1, t1, n1 = single_core_sample(w, units, budget_s / 2, seed)
+    rate_1 = s1 / t1
+    procs = host_cores()
+    pool = OraclePool(procs)
+    try:
+        pu = parallel_units(units, rate_1, budget_s * procs)
+        busy, wall = pool.run(seed, w, pu)
+    finally:
+        pool.close()
+    slots_n = sum(u[2] for u in pu)
+    whole = len(pu) == len(units)
+    return {"value": slots_n / busy, "unit": "slots/s", "cores": procs, "kind": "oracle",
+            "single_core_value": rate_1,
+            "sample": f"{'one whole call' if whole else f'{len(pu)} of {len(units)} (request, layer) units of a call'}"
+                      f" of {w.name} ({w.num_layers} layers) through the fp64 C oracle in {procs} spawned "
+                      f"processes: {slots_n:.0f} slots over the longest per-process oracle time {busy:.2f} s "
+                      f"({wall:.2f} s wall with row generation); single core: {n1} units, {s1:.0f} slots in "
+                      f"{t1:.2f} s"}
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the fp64 CPU oracle timed as it stands on the same workload."""
+    """The reference arm: the fp64 CPU oracle, as it stands, on all host cores.  A step is a
+    bounded sample of one call of the same workload: (request, layer) units, layer-major,
+    every request in it, sized from a single-core calibration to about cpu_seconds of wall
+    time on the host's cores."""
     if rank != 0:
         return None
     w = workload(args.workload, args.layers)
-    import oracle
-    import synth
-    st = per_request_counts(w)
     seed = w.seed
-    caches = [synth.cache_request(seed, r, w.num_layers, L, w.row_elems) for r, L in enumerate(w.lengths)]
-    reps = {d.key: synth.repl_rows(seed, d.req, d.key, w.num_layers, d.n_repl, w.row_elems) for d in w.steps[0]}
-
-    def one_call():
-        for r in range(w.num_reqs):
-            ds = [d for d in w.steps[0] if d.req == r]
-            if ds:
-                oracle.splice_request(caches[r], [(d.s_start, d.s_end, d.n_repl) for d in ds],
-                                      [reps[d.key] for d in ds], w.latent_dim, w.theta)
-    for _ in range(args.warmup):
-        one_call()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        one_call()
-    dt = time.perf_counter() - t0
-    value = st.downstream_slots * args.steps / dt
+    units, _ = oracle_units(w)
+    s1, t1, _ = single_core_sample(w, units, 1.0, seed)
+    procs = host_cores()
+    pu = parallel_units(units, s1 / t1, args.cpu_seconds * procs / 4)
+    slots = sum(u[2] for u in pu)
+    pool = OraclePool(procs)
+    try:
+        for _ in range(args.warmup):
+            pool.run(seed, w, pu)
+        busy = [pool.run(seed, w, pu)[0] for _ in range(args.steps)]
+    finally:
+        pool.close()
+    dt = sum(busy)
+    value = slots * args.steps / dt
+    sample = (f"{len(pu)} of {len(units)} (request, layer) units of one call of {w.name} per step "
+              f"({slots:.0f} slots), fp64 C oracle in {procs} spawned processes; a step's time is the longest "
+              f"per-process oracle time")
     return {"metric": METRIC, "value": value, "unit": "slots/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "layers": w.num_layers, "block_size": w.block_size, "storage": "bf16"},
-            "cpu_baseline": {"value": value, "unit": "slots/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} timed whole call(s) of {w.name} through the fp64 C oracle, "
-                                       "single thread"},
+            "cpu_baseline": {"value": value, "unit": "slots/s", "cores": procs, "kind": "oracle",
+                             "single_core_value": s1 / t1, "sample": sample},
             "e2e": {"value": value, "unit": "slots/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -697,7 +885,7 @@ def main():
     line, w = (run_chain if is_chain else run_ours)(args, rank, world, local)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1 and not is_chain:
-            cb, _ = cpu_oracle_sample(w, args.cpu_seconds)
+            cb = cpu_oracle_sample(w, args.cpu_seconds)
             line["cpu_baseline"] = cb
         print(json.dumps(line), flush=True)
     if world > 1:

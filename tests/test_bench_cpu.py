@@ -38,12 +38,29 @@ def test_kernel_hash_follows_code_not_comments(tmp_path, monkeypatch):
 
 
 def test_stored_traffic_names_real_workloads_and_kernels():
+    layers = {w.name: w.num_layers for w in (configs.by_name(n) for n in (
+        "cfg1", "cfg2", "cfg3", "cfg5-C4-B1", "cfg5-C16-B1", "cfg5-C16-B16"))}
     for (workload, kernel), entry in bench.NCU_TRAFFIC.items():
         base = workload.split("-as-")[0]
-        names = {configs.by_name(n).name for n in ("cfg1", "cfg2", "cfg3", "cfg5-C4-B1", "cfg5-C16-B1")}
-        assert base in names, workload
-        assert kernel in ("move_rotate_vector", "rotate_in_place"), kernel
+        assert base in layers, workload
+        assert kernel in ("move_rotate_vector", "rotate_in_place", "materialize"), kernel
         assert len(entry["kernel_sha256"]) == 64 and entry["bytes"] > 0
+        if "scale" in entry:  # captured on fewer layers: scaled by the units of a full launch
+            assert entry["scale"] == pytest.approx(layers[base] / entry["captured_layers"])
+
+
+def test_resident_copies_and_units():
+    # copies: one per step of a leg when they fit, at least one
+    assert bench.resident_copies(10 ** 9, 25, 96.0) == 25
+    assert bench.resident_copies(40 * 10 ** 9, 25, 96.0) == 2
+    assert bench.resident_copies(200 * 10 ** 9, 25, 96.0) == 1
+    # the CPU baseline's sample: layer-major units, every request in it, within the budget
+    w = configs.by_name("cfg5-C4-B16")
+    units, down = bench.oracle_units(w)
+    assert len(units) == 4 * w.num_layers and sum(u[2] for u in units) == pytest.approx(down)
+    pick = bench.parallel_units(units, rate_1=1e5, budget_core_s=0.0)
+    assert len(pick) == 4 and {u[0] for u in pick} == {0, 1, 2, 3} and {u[1] for u in pick} == {0}
+    assert len(bench.parallel_units(units, rate_1=1e12, budget_core_s=1.0)) == len(units)
 
 
 def test_job_value_is_all_ranks_over_the_slowest():
