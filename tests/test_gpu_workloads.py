@@ -9,8 +9,11 @@
 
 At these sizes every row is checked on the device for the properties that hold at
 any size (latents and unmoved rows bit-exact through the oracle's slot map, rows of
-R bit-exact, RoPE pair norms preserved), and sampled rows -- every segment
-boundary plus random ones -- are compared element by element with the oracle.
+R bit-exact, RoPE pair norms preserved); every row of four layers (the first, the
+last and two drawn at random) is compared element by element with the oracle's
+splice, and so are sampled rows -- every segment boundary plus random ones -- of
+all layers.  Every splice of the chain is compared with the oracle applied to the
+GPU's own cache before it, in two full layers per splice (all 61 in turn).
 """
 import json
 import os
@@ -61,10 +64,13 @@ def _single_call(w, seed=0):
     cache.check_status()
     stats = cache.last_stats()
     rng = np.random.default_rng(seed)
+    full = H.check_full_layers(w, cache, w.steps[0], before, H.check_layers(w.num_layers, rng))
+    assert full["moved"] > 0
     samp = H.check_sampled_single_call(w, cache, w.steps[0], before, rng)
     rows = H.check_properties_all_rows(w, cache, w.steps[0], before)
     del keep
     _release(cache)
+    samp["full_layers"] = full
     return stats, samp, rows
 
 
@@ -98,7 +104,51 @@ def _trace_back(maps, p_final):
     return ("old", p), pos[::-1]
 
 
+def _gather_layers(cache, req: int, layers, length: int) -> np.ndarray:
+    """uint16 [len(layers)][length][row] of one request, read through the C ABI gather."""
+    out = np.empty((len(layers), length, cache.row), dtype=np.uint16)
+    buf = torch.empty((max(length, 1), cache.row), dtype=torch.bfloat16, device=cache.device)
+    for i, layer in enumerate(layers):
+        cache.gather(req, int(layer), 0, length, buf[:length])
+        out[i] = buf[:length].view(torch.int16).cpu().numpy().view(np.uint16)
+    return out
+
+
+def _check_chain_step(w, d, before, after, layers, precision):
+    """One splice of the chain in the given layers: the oracle applied to the GPU's cache
+    before it (`before`, uint16 [layers][L][row]) against the GPU's cache after it."""
+    lat = w.latent_dim
+    L0 = before.shape[1]
+    newlen, kind, idx, _ = oracle.splice_map(L0, [(d.s_start, d.s_end, d.n_repl)])
+    assert after.shape[1] == newlen
+    reps = synth.repl_rows(w.seed, 0, d.key, w.num_layers, d.n_repl)[list(layers)]
+    if precision == 0:
+        want = oracle.splice_request(before, [(d.s_start, d.s_end, d.n_repl)], [reps], lat, w.theta)
+    else:
+        want = np.empty_like(after)
+        pos = np.arange(newlen)
+        surv = kind == 0
+        want[:, ~surv] = reps[:, idx[~surv]]
+        want[:, surv] = before[:, idx[surv]]
+        sh = surv & (idx != pos)
+        if sh.any():
+            delta = np.broadcast_to((pos - idx)[sh][None, :], (len(layers), int(sh.sum()))).reshape(-1)
+            want[:, sh, lat:] = oracle.rotate_bf16only(before[:, idx[sh], lat:].reshape(-1, w.rope_dim), delta,
+                                                       w.theta).reshape(len(layers), -1, w.rope_dim)
+    turned = (kind == 0) & (idx != np.arange(newlen))
+    assert np.array_equal(after[:, :, :lat], want[:, :, :lat]), "latent bits differ"
+    assert np.array_equal(after[:, ~turned], want[:, ~turned]), "prefix / R rows differ"
+    return H.compare_kpe(after[:, turned, lat:].reshape(-1, w.rope_dim), want[:, turned, lat:].reshape(-1, w.rope_dim),
+                         0, exact=precision != 0)
+
+
 def test_chain_64_drift():
+    """The 64-splice chain, twice: fp32 rotation and the naive bf16 arm.  Every splice is
+    checked against the oracle applied to the GPU's own cache before it (the per-splice
+    tolerance, no allowance for earlier splices; the bf16 arm bit-exact), in two full layers
+    that change from splice to splice.  The drift of the final rows against a from-scratch
+    encoding at their final positions is reported beside the oracle's own chain (section 4.3
+    of the Leyline page prints about 4.7e-3 for a workload it does not state)."""
     w = configs.chain_64()
     lat = w.latent_dim
     maps, L = [], w.lengths[0]
@@ -115,17 +165,25 @@ def test_chain_64_drift():
     gpu_vals = {}
     for precision, name in ((0, "fp32"), (1, "bf16")):
         cache = H.make_cache(w, precision=precision)
-        keep = []
-        for step in w.steps:
-            dirs, k = H.gpu_directives(w, step)
-            keep.append(k)
+        per_step = {"moved": 0, "floor_used": 0, "rel_l2_max": 0.0}
+        for k, step in enumerate(w.steps):
+            d = step[0]
+            check = sorted({k % w.num_layers, (k + w.num_layers // 2) % w.num_layers})
+            before = _gather_layers(cache, 0, check, int(cache.seq_lens_host[0]))
+            dirs, keep = H.gpu_directives(w, step)
             cache.splice(dirs)
-        torch.cuda.synchronize()
-        cache.check_status()
+            torch.cuda.synchronize()
+            cache.check_status()
+            after = _gather_layers(cache, 0, check, int(cache.seq_lens_host[0]))
+            del keep
+            c = _check_chain_step(w, d, before, after, check, precision)
+            per_step["moved"] += c["n"]
+            per_step["floor_used"] += c["floor_used"]
+            per_step["rel_l2_max"] = max(per_step["rel_l2_max"], c["rel_l2"])
         assert int(cache.seq_lens_host[0]) == final_len
+        report[f"{name}_per_splice"] = per_step
         got = H.fetch_rows(cache, 0, layers, pos)
         _release(cache)
-        del keep
         chain_rows, truth_rows, moves = [], [], []
         for i, ((origin, path), layer) in enumerate(zip(traces, layers)):
             if origin[0] == "old":
@@ -154,15 +212,10 @@ def test_chain_64_drift():
         c = oracle.bf16_value(chain)
         t = oracle.bf16_value(truth)
         if precision == 1:
+            # each splice bit-exact on its own input, from the same first input: the whole chain
             assert np.array_equal(got[:, lat:], chain), "bf16-only arm differs from the oracle's bf16-only chain"
         else:
-            # Each step may round one element one bf16 step apart from the oracle's chain; the
-            # difference of a pair then grows by at most 2^-6 of the pair norm per move.
-            d = g - c
-            dn = np.hypot(d[:, :32], d[:, 32:])
-            pn = np.hypot(c[:, :32], c[:, 32:])
-            assert np.all(dn <= moves[:, None] * 2.0 ** -6 * pn + 1e-30)
-            report["fp32_vs_oracle_chain_rel_l2"] = float(np.linalg.norm(d) / np.linalg.norm(c))
+            report["fp32_vs_oracle_chain_rel_l2"] = float(np.linalg.norm(g - c) / np.linalg.norm(c))
         drift = float(np.linalg.norm(g - t) / np.linalg.norm(t))
         report[f"{name}_drift_rel_l2"] = drift
         report[f"{name}_oracle_chain_drift_rel_l2"] = float(np.linalg.norm(c - t) / np.linalg.norm(t))
