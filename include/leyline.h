@@ -211,8 +211,11 @@ typedef struct {
  * [num_layers][num_pages][block_size][row], row = latent_dim + rope_heads * rope_dim,
  * 16-byte aligned; with LEYLINE_POOL_SPLIT_ROPE the latent array then the rope array).
  * All pages start free.  The library allocates the free-page list (a ring of
- * 2 * num_pages ids) and small plan and staging buffers on the current device.
- * Synchronous.
+ * 2 * num_pages ids) and small plan and staging buffers on the current device;
+ * a LEYLINE_POOL_LAZY pool also its pending counts (4 bytes per slot), the
+ * readers' turn table (32 * rope_dim KiB) and, when a row's rope bands span 128
+ * bytes (rope_heads * rope_dim == 64), the lists materialize works from (12 bytes
+ * per slot).  Synchronous.
  * Errors: INVALID_ARG (bad descriptor, null/misaligned kv_dev), CUDA. */
 int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_pool_t** out);
 

@@ -120,6 +120,47 @@ __device__ __forceinline__ void rotate_interleaved(uint4& v, const float* c, con
     }
 }
 
+// A 16-byte vector from lane ^ m (every lane of the warp takes part).
+__device__ __forceinline__ uint4 shfl_xor_vec(uint4 v, int m)
+{
+    v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
+    v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
+    v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
+    v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
+    return v;
+}
+
+// Half-split pairs, one half only: the lane holding x (pairs j0..j0+7) returns
+// x' = x c - y s, the lane holding y returns y' = x s + y c, each with the arithmetic of
+// rotate_half_split (fp32: one FMA per output; bf16 arm: products and sum rounded).
+template <bool kBf16>
+__device__ __forceinline__ uint4 turn_own_half(const uint4& mine, const uint4& other, bool y_half, const float* c,
+                                               const float* s)
+{
+    const uint32_t* mw = reinterpret_cast<const uint32_t*>(&mine);
+    const uint32_t* ow = reinterpret_cast<const uint32_t*>(&other);
+    uint4 out;
+    uint32_t* rw = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        float r[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float m = h ? bf16_hi(mw[w]) : bf16_lo(mw[w]);
+            const float o = h ? bf16_hi(ow[w]) : bf16_lo(ow[w]);
+            const float x = y_half ? o : m, y = y_half ? m : o;
+            const float cc = c[2 * w + h], ss = s[2 * w + h];
+            if (kBf16) {
+                r[h] = y_half ? round_bf16(x * ss) + round_bf16(y * cc) : round_bf16(x * cc) - round_bf16(y * ss);
+            } else {
+                r[h] = y_half ? fmaf(x, ss, y * cc) : fmaf(x, cc, -(y * ss));
+            }
+        }
+        rw[w] = pack_bf16x2(r[0], r[1]);
+    }
+    return out;
+}
+
 // ------------------------------------------------------------- plan access --
 // The plan is either a __grid_constant__ kernel parameter (small plans) or in
 // device memory; both are read through the same three pointers.

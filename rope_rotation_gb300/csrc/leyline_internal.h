@@ -124,10 +124,21 @@ struct MaterializeSet {
     int32_t req[kMaterializeReqs];
     int64_t row_end[kMaterializeReqs];
 };
+// Device lists of the rows a materialize launch turns (pool-owned, grown to the set's rows):
+// slot and count of each listed row, and the number listed.
+struct MaterializeScratch {
+    long long* slot;
+    int32_t* pend;
+    unsigned long long* n;
+};
+// Whether launch_materialize lists the rows first (and so needs MaterializeScratch of the
+// set's row count): rows whose rope bands fill 8 vectors.
+inline bool materialize_uses_list(const Geometry& g) { return g.rope_heads * g.head_vecs == 8; }
 // Lazy pools: turn every row of the set's requests by its pending count, in place, and
 // clear the counts; table is the block table [num_reqs][max_blocks].
 int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const MaterializeSet& set,
-                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status, void* stream);
+                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status,
+                       const MaterializeScratch& scratch, void* stream);
 // Lazy pools: set the pending counts of n pages (device ids) to 0.
 int launch_clear_pending(int32_t* pending, const int32_t* page_ids, int64_t n, int32_t block_size, void* stream);
 // Device access to a caller buffer.  Memory of `device` and managed memory are

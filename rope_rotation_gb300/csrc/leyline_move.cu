@@ -23,16 +23,6 @@
 namespace leyline {
 namespace {
 
-// A 16-byte value from lane ^ m of the warp (every lane must take part).
-__device__ __forceinline__ uint4 shfl_xor_vec(uint4 v, int m)
-{
-    v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
-    v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
-    v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
-    v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
-    return v;
-}
-
 // -------------------------------------------------------------------------
 // Move+rotate, MLA shape (latent 512 = 64 vectors, rope 64 = 8 vectors).
 // Work unit = (16-row tile, layer); a CTA takes a contiguous run of units, so it

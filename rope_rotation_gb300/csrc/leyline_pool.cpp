@@ -217,6 +217,12 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         if (e == cudaSuccess) e = cudaMalloc(&p->d_theta_j, sizeof(double) * tt.size());
         if (e == cudaSuccess)
             e = cudaMemcpy(p->d_theta_j, tt.data(), sizeof(double) * tt.size(), cudaMemcpyHostToDevice);
+        // materialize's row lists: a launch lists rows of live requests, at most one per slot
+        if (e == cudaSuccess && materialize_uses_list(g)) {
+            e = cudaMalloc(&p->d_mat_slot, sizeof(long long) * slots);
+            if (e == cudaSuccess) e = cudaMalloc(&p->d_mat_pend, sizeof(int32_t) * slots);
+            if (e == cudaSuccess) e = cudaMalloc(&p->d_mat_n, sizeof(unsigned long long));
+        }
     }
     if (e == cudaSuccess) e = (cudaError_t)launch_init_queue(p->d_queue, g.num_pages, nullptr);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -270,6 +276,9 @@ int leyline_pool_destroy(leyline_pool_t* p)
     if (p->d_stage) cudaFree(p->d_stage);
     if (p->d_pending) cudaFree(p->d_pending);
     if (p->d_theta_j) cudaFree(p->d_theta_j);
+    if (p->d_mat_slot) cudaFree(p->d_mat_slot);
+    if (p->d_mat_pend) cudaFree(p->d_mat_pend);
+    if (p->d_mat_n) cudaFree(p->d_mat_n);
     if (p->d_ckpt_queue) cudaFree(p->d_ckpt_queue);
     if (p->d_ckpt_pending) cudaFree(p->d_ckpt_pending);
     delete p;
@@ -598,6 +607,7 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
     }
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
+    const MaterializeScratch scratch{p->d_mat_slot, p->d_mat_pend, p->d_mat_n};
     int rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
     bool launched = false;
@@ -614,7 +624,7 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
         }
         if (set.n == 0) continue;
         int err = launch_materialize(p->kv, bt->table, bt->max_blocks, set, p->g, p->d_pending, p->d_theta_j,
-                                     p->d_status, stream);
+                                     p->d_status, scratch, stream);
         if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
         launched = true;
         p->ckpt_turned = true;  // stored bands turned in place

@@ -56,6 +56,10 @@ struct leyline_pool {
     int window_calls = 0;
     int64_t window_tail = 0;           // ring tail when the window's first call was planned
     std::vector<int32_t> window_reqs;  // requests the window's calls rewrite
+    // lazy pools: the lists of rows a materialize launch turns (one entry per slot of the pool)
+    long long* d_mat_slot = nullptr;
+    int32_t* d_mat_pend = nullptr;
+    unsigned long long* d_mat_n = nullptr;
     // Checkpoint of the page accounting (leyline_pool_checkpoint / leyline_pool_rollback):
     // copies of the ring and, in lazy pools, of the pending counts, with the ring positions.
     int32_t* d_ckpt_queue = nullptr;

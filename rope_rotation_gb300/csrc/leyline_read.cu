@@ -285,6 +285,223 @@ __global__ void materialize_kernel(uint4* kv, const int32_t* table, int max_bloc
     }
 }
 
+// -------------------------------------------------------------------------
+// Materialize, rows whose rope bands fill 8 vectors (MLA: one 64-wide band; GQA: 2 bands
+// of 32 or 4 of 16), in two kernels.  compact_pending_kernel lists the set's rows whose
+// count is not 0 (slot and count; the order of rows is kept within each block of 256), so
+// that the band pass splits only rows with work among its CTAs: after a splice the turned
+// rows of a request are one contiguous stretch, and an even split of all rows would leave
+// most CTAs idle.  materialize_band8_kernel cuts the list into tiles of 32 rows, and a unit
+// is (tile, kMatLayers layers); the CTAs take contiguous runs of units.  In a unit each
+// row's band is moved by 8 lanes, one 16-byte chunk each (a warp instruction covers four
+// whole 128-byte bands; half-split: the partner half comes from lane ^ head_vecs/2), with
+// the loads of all kMatLayers layers issued before any store.
+//
+// A prologue per chunk of up to 8 tiles reads the list (warp w: tile w of the chunk) and
+// clears the rows' counts (the band pass reads counts from the list only).  Consecutive
+// rows mostly share their count (a splice's survivors of one segment), so each warp forms
+// the cos / sin once per run of equal counts in its tile, for the first kMatRuns runs;
+// rows of later runs (more than kMatRuns distinct counts in 32 rows) form their own.
+constexpr int kMatThreads = 256;
+constexpr int kMatTileRows = 32;  // 8 lanes per row
+#ifndef LEYLINE_MAT_LAYERS
+#define LEYLINE_MAT_LAYERS 4
+#endif
+#ifndef LEYLINE_MAT_MIN_CTAS
+#define LEYLINE_MAT_MIN_CTAS 3
+#endif
+constexpr int kMatLayers = LEYLINE_MAT_LAYERS;  // layers in flight per unit
+constexpr int kMatChunkTiles = kMatThreads / 32;
+constexpr int kMatRuns = 4;
+
+// (cos, sin) of pair j of one count, out of line: the rare path of rows whose count has
+// no shared slot (returned by value, so the caller keeps its arrays in registers).
+__device__ __noinline__ float2 pair_trig(int pend, const double* turn, int half, int j, bool bf16)
+{
+    float c, s;
+    pending_trig(pend, turn, half, j, bf16, c, s);
+    return make_float2(c, s);
+}
+
+// Slot of flat row f of the set (-1 with the status bit raised when its page is bad).
+__device__ __forceinline__ long long set_row_slot(const MaterializeSet& set, const int32_t* table, int max_blocks,
+                                                  const Geometry& g, long long f, int32_t* status)
+{
+    int lo = 0, hi = set.n - 1;  // first request whose rows end after f
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (set.row_end[mid] > f) hi = mid;
+        else lo = mid + 1;
+    }
+    const long long t = f - (lo ? set.row_end[lo - 1] : 0);
+    const long long B = g.block_size;
+    const int page = table[(long long)set.req[lo] * max_blocks + t / B];
+    if (page < 0 || page >= g.num_pages) {
+        raise_status(status, ST_BAD_PAGE);
+        return -1;
+    }
+    return (long long)page * B + t % B;
+}
+
+// The set's rows with a count other than 0, appended to (slot, count) lists at *n.
+__global__ void __launch_bounds__(kMatThreads) compact_pending_kernel(const int32_t* table, int max_blocks,
+                                                                      const __grid_constant__ MaterializeSet set,
+                                                                      const Geometry g, const int32_t* pending,
+                                                                      long long* out_slot, int32_t* out_pend,
+                                                                      unsigned long long* n, int32_t* status)
+{
+    __shared__ int warp_n[kMatThreads / 32];
+    __shared__ unsigned long long base;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long rows = set.row_end[set.n - 1];
+    // every CTA runs the same number of rounds, so that all its threads reach the barriers
+    for (long long f0 = (long long)blockIdx.x * kMatThreads; f0 < rows; f0 += (long long)gridDim.x * kMatThreads) {
+        const long long f = f0 + threadIdx.x;
+        long long slot = -1;
+        int pend = 0;
+        if (f < rows) {
+            slot = set_row_slot(set, table, max_blocks, g, f, status);
+            if (slot >= 0) pend = pending[slot];
+        }
+        const unsigned has = __ballot_sync(0xffffffffu, pend != 0);
+        if (lane == 0) warp_n[warp] = __popc(has);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int total = 0;
+            for (int w = 0; w < kMatThreads / 32; ++w) {
+                const int c = warp_n[w];
+                warp_n[w] = total;  // exclusive prefix
+                total += c;
+            }
+            base = total ? atomicAdd(n, (unsigned long long)total) : 0ull;
+        }
+        __syncthreads();
+        if (pend != 0) {
+            const unsigned long long at = base + warp_n[warp] + __popc(has & ((1u << lane) - 1u));
+            out_slot[at] = slot;
+            out_pend[at] = pend;
+        }
+        __syncthreads();  // warp_n and base are rewritten in the next round
+    }
+    allow_next_grid();  // the band pass may launch; it waits for this grid before reading the lists
+}
+
+template <int kLayout, bool kBf16>
+__global__ void __launch_bounds__(kMatThreads, LEYLINE_MAT_MIN_CTAS) materialize_band8_kernel(uint4* kv, const Geometry g,
+                                                                        const long long* list_slot,
+                                                                        const int32_t* list_pend,
+                                                                        const unsigned long long* list_n,
+                                                                        int32_t* pending, const double* turn)
+{
+    __shared__ long long slot_s[kMatChunkTiles][kMatTileRows];  // -1: nothing to turn
+    __shared__ int cnt_s[kMatChunkTiles][kMatTileRows];         // the row's count
+    __shared__ int run_s[kMatChunkTiles][kMatTileRows];         // its run among the tile's counts
+    __shared__ float2 cs_s[kMatChunkTiles][kMatRuns][32];        // (cos, sin) per pair of the first runs
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hv = g.head_vecs;
+    const int half = g.rope_dim / 2;  // <= 32: the row's bands fill 8 vectors
+    const int row = threadIdx.x >> 3, c = threadIdx.x & 7;  // this thread's row of a tile and chunk of it
+    const int q = c & (hv - 1);                              // chunk within its band
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;
+    const int j0 = kLayout == 0 ? kPairs * (q & (hv / 2 - 1)) : kPairs * q;  // first pair of the chunk
+    const bool y_half = kLayout == 0 && q >= hv / 2;
+    const long long L = g.num_layers;
+    const long long groups = (L + kMatLayers - 1) / kMatLayers;
+    wait_for_previous_grid();  // the lists are complete
+    const long long rows = (long long)*list_n;
+    const long long tiles = (rows + kMatTileRows - 1) / kMatTileRows;
+    long long u0, u1;
+    my_units(tiles * groups, u0, u1);
+    long long u = u0;
+    while (u < u1) {
+        // prologue of a chunk: the tiles from the current unit's on
+        const long long t0 = u / groups;
+        const long long t_end = (u1 - 1) / groups + 1 < t0 + kMatChunkTiles ? (u1 - 1) / groups + 1 : t0 + kMatChunkTiles;
+        __syncthreads();  // the previous chunk's shared values are no longer read
+        {
+            const long long tile = t0 + warp;
+            const long long f = tile * kMatTileRows + lane;
+            long long slot = -1;
+            int pend = 0;
+            if (tile < t_end && f < rows) {
+                slot = list_slot[f];
+                pend = list_pend[f];
+                pending[slot] = 0;  // a slot is listed once; the band pass reads counts from the list
+            }
+            const int prev = __shfl_up_sync(0xffffffffu, pend, 1);
+            const bool start = pend != 0 && (lane == 0 || prev != pend);
+            const unsigned starts = __ballot_sync(0xffffffffu, start);
+            const int run = pend != 0 ? __popc(starts & (0xffffffffu >> (31 - lane))) - 1 : -1;
+            slot_s[warp][lane] = pend != 0 ? slot : -1;
+            cnt_s[warp][lane] = pend;
+            run_s[warp][lane] = run;
+            const int runs = __popc(starts);
+            unsigned rest = starts;
+            for (int r = 0; r < runs && r < kMatRuns; ++r) {
+                const int src = __ffs(rest) - 1;  // lane where run r starts
+                rest &= rest - 1;
+                const int cnt = __shfl_sync(0xffffffffu, pend, src);
+                if (lane < half) {
+                    float cc, ss;
+                    pending_trig(cnt, turn, half, lane, kBf16, cc, ss);
+                    cs_s[warp][r][lane] = make_float2(cc, ss);
+                }
+            }
+        }
+        __syncthreads();
+        // the chunk's units
+        const long long u_end = t_end * groups < u1 ? t_end * groups : u1;
+        long long cur_tile = -1;
+        long long slot = -1;
+        float cs[8], sn[8];
+        for (; u < u_end; ++u) {
+            const long long tile = u / groups;
+            const long long layer0 = (u - tile * groups) * kMatLayers;
+            if (tile != cur_tile) {
+                cur_tile = tile;
+                const int ti = (int)(tile - t0);
+                slot = slot_s[ti][row];
+                if (slot >= 0) {
+                    const int run = run_s[ti][row];
+                    if (run < kMatRuns) {
+#pragma unroll
+                        for (int w = 0; w < kPairs; ++w) {
+                            const float2 v = cs_s[ti][run][j0 + w];
+                            cs[w] = v.x;
+                            sn[w] = v.y;
+                        }
+                    } else {  // more distinct counts in this tile than the shared slots hold
+#pragma unroll
+                        for (int w = 0; w < kPairs; ++w) {
+                            const float2 t = pair_trig(cnt_s[ti][row], turn, half, j0 + w, kBf16);
+                            cs[w] = t.x;
+                            sn[w] = t.y;
+                        }
+                    }
+                }
+            }
+            uint4 v[kMatLayers];
+            uint4* p[kMatLayers];
+#pragma unroll
+            for (int k = 0; k < kMatLayers; ++k) {
+                v[k] = make_uint4(0u, 0u, 0u, 0u);
+                p[k] = kv + band_off(g, layer0 + k, slot < 0 ? 0 : slot) + c;
+                if (slot >= 0 && layer0 + k < L) v[k] = ld_rw(p[k]);
+            }
+#pragma unroll
+            for (int k = 0; k < kMatLayers; ++k) {
+                if (kLayout == 0) {
+                    const uint4 o = shfl_xor_vec(v[k], hv / 2);  // every lane takes part
+                    if (slot >= 0 && layer0 + k < L) st_stream(p[k], turn_own_half<kBf16>(v[k], o, y_half, cs, sn));
+                } else if (slot >= 0 && layer0 + k < L) {
+                    rotate_interleaved<kBf16>(v[k], cs, sn);
+                    st_stream(p[k], v[k]);
+                }
+            }
+        }
+    }
+}
+
 __global__ void clear_pending_kernel(int32_t* pending, const int32_t* page_ids, long long n, int block_size)
 {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n * block_size;
@@ -324,10 +541,32 @@ int launch_gather_lazy(const void* kv, const int32_t* table_row, const Geometry&
 }
 
 int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const MaterializeSet& set,
-                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status, void* stream)
+                       const Geometry& g, int32_t* pending, const double* turn, int32_t* status,
+                       const MaterializeScratch& scratch, void* stream)
 {
     if (set.n <= 0 || set.row_end[set.n - 1] <= 0) return 0;
     const long long rows = set.row_end[set.n - 1];
+    if (materialize_uses_list(g)) {  // the row's bands fill 8 vectors: the listed rows in tiles of 32
+        const cudaStream_t s = (cudaStream_t)stream;
+        const bool split = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
+        const bool bf16 = g.precision == LEYLINE_ROTATE_BF16_NAIVE;
+        auto k = split ? (bf16 ? materialize_band8_kernel<0, true> : materialize_band8_kernel<0, false>)
+                       : (bf16 ? materialize_band8_kernel<1, true> : materialize_band8_kernel<1, false>);
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMatThreads, 0);
+        if (e == cudaSuccess) e = cudaMemsetAsync(scratch.n, 0, sizeof(unsigned long long), s);
+        if (e != cudaSuccess) return (int)e;
+        compact_pending_kernel<<<grid_for(rows, kMatThreads, 4096), kMatThreads, 0, s>>>(
+            table, max_blocks, set, g, pending, scratch.slot, scratch.pend, scratch.n, status);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = launch_dependent(k, sms * std::max(per_sm, 1), kMatThreads, s, static_cast<uint4*>(kv), g,
+                                 static_cast<const long long*>(scratch.slot), static_cast<const int32_t*>(scratch.pend),
+                                 static_cast<const unsigned long long*>(scratch.n), pending, turn);
+        return (int)e;
+    }
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;
     k<<<grid_for(rows * 32, kReadThreads, 8192), kReadThreads, 0, (cudaStream_t)stream>>>(
         static_cast<uint4*>(kv), table, max_blocks, set, g, pending, turn, status);

@@ -496,6 +496,105 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 5 : 2) rotate_in_p
     }
 }
 
+// In-place rotation of rows whose rope bands fill 8 vectors (MLA: one 64-wide band; GQA:
+// 2 bands of 32 or 4 of 16).  Each band is turned by 8 lanes, one 16-byte chunk each, so
+// that a warp instruction covers four whole 128-byte bands (half-split: the partner half
+// comes from lane ^ head_vecs / 2).  The CTA's 256 threads cover 16 rows x 8 chunks x 2
+// layers, and each thread issues the loads of kRotPasses layers (2 apart) before any
+// store: a unit is (16-row tile, 2 * kRotPasses layers).  Tiles, their lookup and the
+// cos / sin of their segment are as in rotate_in_place.
+constexpr int kRotPasses = 4;
+constexpr int kRotUnitLayers = 2 * kRotPasses;
+
+template <int kLayout, bool kBf16, class PlanSrc>
+__global__ void __launch_bounds__(kMoveThreads, 4) rotate_in_place_lines(const __grid_constant__ SpliceArgs a,
+                                                                         const __grid_constant__ PlanSrc plan)
+{
+    __shared__ uint4* band_s[kTileRows];                  // the tile's rows' bands (layer 0); nullptr: none
+    __shared__ __align__(16) float trig_s[kMaxRopeDim];  // (cos, sin) per pair of the tile's segment
+    wait_for_previous_grid();
+    allow_next_grid();
+    const PlanView pv = plan_view(a, plan);
+    const long long L = a.g.num_layers;
+    const long long rope_layer = a.g.rope_layer_vecs;
+    const int hv = a.g.head_vecs;
+    const int rope_dim = a.g.rope_dim;
+    constexpr int kPairs = kLayout == 0 ? 8 : 4;
+    const int row = (threadIdx.x >> 3) & (kTileRows - 1);  // this thread's row of a tile
+    const int c = threadIdx.x & 7;                         // its chunk of the row's bands
+    const int lo = threadIdx.x / (8 * kTileRows);          // its layer of each pair of layers
+    const int q = c & (hv - 1);                            // chunk within its band
+    const int j0 = kLayout == 0 ? kPairs * (q & (hv / 2 - 1)) : kPairs * q;  // first pair of the chunk
+    const bool y_half = kLayout == 0 && q >= hv / 2;
+    const long long groups = (L + kRotUnitLayers - 1) / kRotUnitLayers;
+    long long u0, u1;
+    my_units(a.total_tiles * groups, u0, u1);
+    long long tile = u0 / groups, grp = u0 - (u0 / groups) * groups;
+    long long cur_tile = -1;
+    float cs[8], sn[8];
+    for (long long u = u0; u < u1; ++u) {
+        if (tile != cur_tile) {
+            __syncthreads();
+            if (threadIdx.x < kTileRows) {
+                uint4* band = nullptr;
+                const ReqPlan& rp = pv.reqs[find_req(pv.reqs, a.n_reqs, tile, BY_TILE)];
+                const long long lt = tile - rp.tile_begin;
+                const Seg* sg = pv.segs + rp.seg_begin;
+                int k = 0;
+                for (int qq = 0; qq < rp.seg_count; ++qq)
+                    if (sg[qq].tile_off >= 0 && sg[qq].tile_off <= lt) k = qq;
+                const Seg sgk = sg[k];
+                const long long B0 = a.g.block_size;
+                const long long seg_end = k + 1 < rp.seg_count ? sg[k + 1].new_start : rp.new_len;
+                const long long kept_end = (long long)sgk.kb1 * B0 < seg_end ? (long long)sgk.kb1 * B0 : seg_end;
+                const long long p = (long long)sgk.kb0 * B0 + (lt - sgk.tile_off) * kTileRows + threadIdx.x;
+                if (p < kept_end) {  // rows and block sizes fit 32 bits (the planner checks lengths)
+                    const unsigned B = (unsigned)a.g.block_size, pb = (unsigned)p / B;
+                    const int page = a.stage[rp.stage_begin + ((long long)pb - rp.b0)];
+                    if (page >= 0 && page < a.g.num_pages)
+                        band = static_cast<uint4*>(a.kv) + band_off(a.g, 0, (long long)page * B + ((unsigned)p - pb * B));
+                }
+                band_s[threadIdx.x] = band;
+                for (int e = threadIdx.x; e < rope_dim; e += kTileRows)  // the segment's cos/sin
+                    trig_s[e] = pv.trig[(long long)sgk.trig * rope_dim + e];
+            }
+            __syncthreads();
+            cur_tile = tile;
+#pragma unroll
+            for (int w = 0; w < kPairs; ++w) {
+                cs[w] = trig_s[2 * (j0 + w)];
+                sn[w] = trig_s[2 * (j0 + w) + 1];
+            }
+        }
+        uint4* band = band_s[row];
+        const long long layer0 = grp * kRotUnitLayers + lo;
+        uint4 v[kRotPasses];
+        uint4* ptr[kRotPasses];
+#pragma unroll
+        for (int k = 0; k < kRotPasses; ++k) {
+            const long long layer = layer0 + 2 * k;
+            ptr[k] = band + layer * rope_layer + c;
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (band && layer < L) v[k] = ld_rw(ptr[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kRotPasses; ++k) {
+            const bool ok = band && layer0 + 2 * k < L;
+            if (kLayout == 0) {
+                const uint4 o = shfl_xor_vec(v[k], hv / 2);  // every lane takes part
+                if (ok) st_stream(ptr[k], turn_own_half<kBf16>(v[k], o, y_half, cs, sn));
+            } else if (ok) {
+                rotate_interleaved<kBf16>(v[k], cs, sn);
+                st_stream(ptr[k], v[k]);
+            }
+        }
+        if (++grp == groups) {
+            grp = 0;
+            ++tile;
+        }
+    }
+}
+
 // Commit of a re-indexed call: staged entries into the new blocks [b0, new end),
 // -1 into the blocks past the new end, the new length, and (lazy pools) pending
 // counts of 0 on the returned pages.  The staged values are final before the
@@ -561,8 +660,9 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
     const int ipr = a.g.rope_heads * (split ? a.g.head_vecs / 2 : a.g.head_vecs);
     const int per_layer = kTileRows * ipr;
-    const bool mla = per_layer <= kMoveThreads;  // one item per thread; else kMaxItems
-    const int lpu = reindex_layers_per_unit(per_layer, mla ? 1 : kMaxItems);
+    const bool lines = a.g.rope_heads * a.g.head_vecs == 8;  // bands of 8 vectors: whole-line kernel
+    const bool mla = per_layer <= kMoveThreads;               // one item per thread; else kMaxItems
+    const int lpu = lines ? kRotUnitLayers : reindex_layers_per_unit(per_layer, mla ? 1 : kMaxItems);
     const long long units = a.total_tiles * ((a.g.num_layers + lpu - 1) / lpu);
     if (grid > units) grid = (int)std::max<long long>(units, 1);
     if (e == cudaSuccess && a.total_fresh > 0) {  // other fresh rows: items of (row, kFreshLayers layers)
@@ -572,7 +672,12 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
                        : (bf16 ? copy_fresh_reindex<1, true, PlanSrc> : copy_fresh_reindex<1, false, PlanSrc>);
         e = launch_dependent(k, fgrid, kMoveThreads, s, a, plan);
     }
-    if (e == cudaSuccess && units > 0) {
+    if (e == cudaSuccess && units > 0 && lines) {
+        e = split ? (bf16 ? launch_dependent(rotate_in_place_lines<0, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                          : launch_dependent(rotate_in_place_lines<0, false, PlanSrc>, grid, kMoveThreads, s, a, plan))
+                  : (bf16 ? launch_dependent(rotate_in_place_lines<1, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
+                          : launch_dependent(rotate_in_place_lines<1, false, PlanSrc>, grid, kMoveThreads, s, a, plan));
+    } else if (e == cudaSuccess && units > 0) {
         if (split)
             e = bf16 ? (mla ? launch_dependent(rotate_in_place<0, true, 1, PlanSrc>, grid, kMoveThreads, s, a, plan)
                             : launch_dependent(rotate_in_place<0, true, kMaxItems, PlanSrc>, grid, kMoveThreads, s, a,
@@ -608,8 +713,14 @@ int launch_reindex_call(const SpliceArgs& a, const ParamPlan* pp, int grid, void
 
 int rotate_in_place_blocks_per_sm(int* blocks)
 {
-    return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, rotate_in_place<0, false, 1, ParamPlan>,
-                                                              kMoveThreads, 0);
+    int a = 0, b = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, rotate_in_place<0, false, 1, ParamPlan>,
+                                                                  kMoveThreads, 0);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, rotate_in_place_lines<0, false, ParamPlan>, kMoveThreads,
+                                                          0);
+    *blocks = a < b ? a : b;  // a grid that both rotate kernels hold at once
+    return (int)e;
 }
 
 }  // namespace leyline
