@@ -124,12 +124,15 @@ struct MaterializeSet {
     int32_t req[kMaterializeReqs];
     int64_t row_end[kMaterializeReqs];
 };
-// Device lists of the rows a materialize launch turns (pool-owned, grown to the set's rows):
-// slot and count of each listed row, and the number listed.
+// Device lists of the rows a materialize launch turns (pool-owned, one entry per slot of
+// the pool): slot and count of each listed row, and the number listed.  Launches use two
+// counters in turn: n (0 when the launch starts) and n_next, which the launch's band pass
+// sets to 0 for the next launch.
 struct MaterializeScratch {
     long long* slot;
     int32_t* pend;
     unsigned long long* n;
+    unsigned long long* n_next;
 };
 // Whether launch_materialize lists the rows first (and so needs MaterializeScratch of the
 // set's row count): rows whose rope bands fill 8 vectors.

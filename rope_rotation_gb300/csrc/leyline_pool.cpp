@@ -221,7 +221,8 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
         if (e == cudaSuccess && materialize_uses_list(g)) {
             e = cudaMalloc(&p->d_mat_slot, sizeof(long long) * slots);
             if (e == cudaSuccess) e = cudaMalloc(&p->d_mat_pend, sizeof(int32_t) * slots);
-            if (e == cudaSuccess) e = cudaMalloc(&p->d_mat_n, sizeof(unsigned long long));
+            if (e == cudaSuccess) e = cudaMalloc(&p->d_mat_n, 2 * sizeof(unsigned long long));
+            if (e == cudaSuccess) e = cudaMemset(p->d_mat_n, 0, 2 * sizeof(unsigned long long));
         }
     }
     if (e == cudaSuccess) e = (cudaError_t)launch_init_queue(p->d_queue, g.num_pages, nullptr);
@@ -607,7 +608,7 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
     }
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
-    const MaterializeScratch scratch{p->d_mat_slot, p->d_mat_pend, p->d_mat_n};
+
     int rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
     bool launched = false;
@@ -623,8 +624,11 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
             ++set.n;
         }
         if (set.n == 0) continue;
+        const MaterializeScratch scratch{p->d_mat_slot, p->d_mat_pend, p->d_mat_n ? p->d_mat_n + p->mat_turn : nullptr,
+                                         p->d_mat_n ? p->d_mat_n + (1 - p->mat_turn) : nullptr};
         int err = launch_materialize(p->kv, bt->table, bt->max_blocks, set, p->g, p->d_pending, p->d_theta_j,
                                      p->d_status, scratch, stream);
+        if (err == 0 && materialize_uses_list(p->g)) p->mat_turn = 1 - p->mat_turn;
         if (err != 0) return cuda_error((cudaError_t)err, "launching the materialize kernel");
         launched = true;
         p->ckpt_turned = true;  // stored bands turned in place

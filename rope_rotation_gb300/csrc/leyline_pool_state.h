@@ -59,7 +59,8 @@ struct leyline_pool {
     // lazy pools: the lists of rows a materialize launch turns (one entry per slot of the pool)
     long long* d_mat_slot = nullptr;
     int32_t* d_mat_pend = nullptr;
-    unsigned long long* d_mat_n = nullptr;
+    unsigned long long* d_mat_n = nullptr;  // two counters, used by launches in turn
+    int mat_turn = 0;                        // the counter the next launch uses
     // Checkpoint of the page accounting (leyline_pool_checkpoint / leyline_pool_rollback):
     // copies of the ring and, in lazy pools, of the pending counts, with the ring positions.
     int32_t* d_ckpt_queue = nullptr;

@@ -391,7 +391,8 @@ __global__ void __launch_bounds__(kMatThreads, LEYLINE_MAT_MIN_CTAS) materialize
                                                                         const long long* list_slot,
                                                                         const int32_t* list_pend,
                                                                         const unsigned long long* list_n,
-                                                                        int32_t* pending, const double* turn)
+                                                                        unsigned long long* next_n, int32_t* pending,
+                                                                        const double* turn)
 {
     __shared__ long long slot_s[kMatChunkTiles][kMatTileRows];  // -1: nothing to turn
     __shared__ int cnt_s[kMatChunkTiles][kMatTileRows];         // the row's count
@@ -409,6 +410,7 @@ __global__ void __launch_bounds__(kMatThreads, LEYLINE_MAT_MIN_CTAS) materialize
     const long long groups = (L + kMatLayers - 1) / kMatLayers;
     wait_for_previous_grid();  // the lists are complete
     const long long rows = (long long)*list_n;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *next_n = 0;  // the next launch's counter (its lists are not in use)
     const long long tiles = (rows + kMatTileRows - 1) / kMatTileRows;
     long long u0, u1;
     my_units(tiles * groups, u0, u1);
@@ -556,7 +558,6 @@ int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMatThreads, 0);
-        if (e == cudaSuccess) e = cudaMemsetAsync(scratch.n, 0, sizeof(unsigned long long), s);
         if (e != cudaSuccess) return (int)e;
         compact_pending_kernel<<<grid_for(rows, kMatThreads, 4096), kMatThreads, 0, s>>>(
             table, max_blocks, set, g, pending, scratch.slot, scratch.pend, scratch.n, status);
@@ -564,7 +565,7 @@ int launch_materialize(void* kv, const int32_t* table, int32_t max_blocks, const
         if (e == cudaSuccess)
             e = launch_dependent(k, sms * std::max(per_sm, 1), kMatThreads, s, static_cast<uint4*>(kv), g,
                                  static_cast<const long long*>(scratch.slot), static_cast<const int32_t*>(scratch.pend),
-                                 static_cast<const unsigned long long*>(scratch.n), pending, turn);
+                                 static_cast<const unsigned long long*>(scratch.n), scratch.n_next, pending, turn);
         return (int)e;
     }
     auto k = g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT ? materialize_kernel<0> : materialize_kernel<1>;

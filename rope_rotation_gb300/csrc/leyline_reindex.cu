@@ -504,10 +504,13 @@ __global__ void __launch_bounds__(kMoveThreads, kItems == 1 ? 5 : 2) rotate_in_p
 // store: a unit is (16-row tile, 2 * kRotPasses layers).  Tiles, their lookup and the
 // cos / sin of their segment are as in rotate_in_place.
 constexpr int kRotPasses = 4;
+#ifndef LEYLINE_LINES_MIN_CTAS
+#define LEYLINE_LINES_MIN_CTAS 4
+#endif
 constexpr int kRotUnitLayers = 2 * kRotPasses;
 
 template <int kLayout, bool kBf16, class PlanSrc>
-__global__ void __launch_bounds__(kMoveThreads, 4) rotate_in_place_lines(const __grid_constant__ SpliceArgs a,
+__global__ void __launch_bounds__(kMoveThreads, LEYLINE_LINES_MIN_CTAS) rotate_in_place_lines(const __grid_constant__ SpliceArgs a,
                                                                          const __grid_constant__ PlanSrc plan)
 {
     __shared__ uint4* band_s[kTileRows];                  // the tile's rows' bands (layer 0); nullptr: none
