@@ -50,6 +50,15 @@ DEFAULT_MEM_GB = 96.0
 # taken on (kernel_sha).  "scale": the capture ran on fewer layers and its traffic is
 # multiplied by the ratio of the units (tile x layer) the full launch processes.
 NCU_TRAFFIC = {
+    # the move kernel on the largest workload, captured on 4 of its 61 layers (DRAM read
+    # 704.28 MB = the algorithmic read; write 654.66 MB, the rest still in L2 at kernel end)
+    ("sweep-C16-61L-B16", "move_rotate_vector"): {
+        "kernel_sha256": "967501961471016e1b33072f77b0d17734d1b9327554969529aa8e61f2ad88c5",
+        "bytes": 704279552 + 654659840, "captured_layers": 4, "scale": 61 / 4},
+    # the whole-line rotate kernel of a re-index call, block-1 sweep of 4 requests on 16 layers
+    ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
+        "kernel_sha256": "b506a2d0be3f9ee795dc5a365b5e2ce25e3f8b6f33424563e701196b2e0e0c85",
+        "bytes": 130888192 + 71854592},
 }
 
 
@@ -252,6 +261,26 @@ HEAD_START_CYCLES = 2_000_000  # about 1 ms at 2 GHz
 
 def hold_stream(torch):
     torch.cuda._sleep(HEAD_START_CYCLES)
+
+
+def copy_gbps_now(torch, gib: float = 2.0, reps: int = 5) -> float:
+    """A plain device copy (torch) of gib GiB on this GPU now, read + write bytes over the best of
+    reps CUDA-event timings: context for the kernel fractions, beside the stored peak."""
+    n = int(gib * (1 << 30)) // 2
+    a = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    best = float("inf")
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del a, b
+    torch.cuda.empty_cache()
+    return 2 * n * 2 / (best / 1e3) / 1e9
 
 
 class Resident:
@@ -491,6 +520,7 @@ def run_ours(args, rank, world, local):
         lazy_read = {"op": "leyline_materialize_requests", "requests": len(reqs), "turned_slots": turned,
                      "ms": read_ms, "slots_per_s": turned / (read_ms / 1e3),
                      "algorithmic_gbps": turned * band_bytes / (read_ms / 1e3) / 1e9}
+    copy_now = copy_gbps_now(torch)
     clocks = sampler.stop()
 
     # max over ranks
@@ -555,6 +585,9 @@ def run_ours(args, rank, world, local):
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
+                     # a plain torch copy timed in this run, on this GPU: boxes differ by a few
+                     # per cent, and this puts the fraction above in the run's own terms
+                     "copy_gbps_this_run": copy_now, "frac_of_copy_this_run": achieved / copy_now,
                      "launch_ms": k2_avg_s * 1e3, "launches_timed": k2_n,
                      "algorithmic_bytes_per_launch": st["algorithmic_bytes"],
                      # the value leg's steps (with their restores), against the same peaks
