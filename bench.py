@@ -55,6 +55,10 @@ NCU_TRAFFIC = {
     ("sweep-C16-61L-B16", "move_rotate_vector"): {
         "kernel_sha256": "967501961471016e1b33072f77b0d17734d1b9327554969529aa8e61f2ad88c5",
         "bytes": 704279552 + 654659840, "captured_layers": 4, "scale": 61 / 4},
+    # the move kernel on the DeepSeek-V2-Lite shape (one call, 27 layers)
+    ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
+        "kernel_sha256": "967501961471016e1b33072f77b0d17734d1b9327554969529aa8e61f2ad88c5",
+        "bytes": 210924288 + 161260288},
     # the whole-line rotate kernel of a re-index call, block-1 sweep of 4 requests on 16 layers
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
         "kernel_sha256": "b506a2d0be3f9ee795dc5a365b5e2ce25e3f8b6f33424563e701196b2e0e0c85",
