@@ -203,6 +203,11 @@ typedef struct {
     int64_t host_ns;           /* the whole call, from entry to return (kernels are enqueued, not waited for) */
     int64_t resolve_ns;        /* classifying the directives' pointers to rows of R */
     int64_t plan_ns;           /* the host planner */
+    int64_t timed_kernel_bytes; /* algorithmic bytes of the kernel that kernel timing brackets: the
+                                   move+rotate kernel (all of algorithmic_bytes) for a rewrite, the
+                                   in-place rotation (2 * rope_bytes per turned slot and layer) for
+                                   a re-index call that turns bands, else the launches before the
+                                   commit (all of algorithmic_bytes) */
 } leyline_stats_t;
 
 /* -------------------------------------------------------------- pool ---- */
@@ -371,7 +376,9 @@ int32_t* leyline_pending_ptr(leyline_pool_t* pool);
 int leyline_sync_status(leyline_pool_t* pool);
 
 /* Kernel timing for benchmarks.  While enabled, each splice records CUDA events
- * on its stream around its move+rotate kernel.  leyline_kernel_timing_read waits
+ * on its stream around its dominant kernel (stats: timed_kernel_bytes): the
+ * move+rotate kernel, a re-index call's in-place rotation, or the launches before
+ * a lazy re-index call's commit.  leyline_kernel_timing_read waits
  * for them and returns the summed kernel time (ms) and the number of timed
  * launches since the last enable, then keeps timing.  Enabling creates the events
  * of the first 256 timed calls at once, so that those calls create none. */

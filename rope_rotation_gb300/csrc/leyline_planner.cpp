@@ -453,18 +453,22 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
         st.algorithmic_bytes = lazy ? L2 * row_bytes * fresh_alg + 8 * (counts.kept_turned_rows + fresh_alg)
                                     : L2 * (rope_bytes * counts.kept_turned_rows + row_bytes * fresh_alg);
         st.moved_bytes = st.algorithmic_bytes + L2 * row_bytes * counts.fresh_head_rows;
+        st.timed_kernel_bytes =
+            plan->total_tiles > 0 ? L2 * rope_bytes * counts.kept_turned_rows : st.algorithmic_bytes;
     } else {
         st.algorithmic_bytes = L2 * row_bytes * (st.downstream_slots + st.repl_slots);
         st.moved_bytes = L2 * row_bytes * (st.downstream_slots + st.repl_slots + st.head_slots);
+        st.timed_kernel_bytes = st.algorithmic_bytes;
     }
     st.pages_popped = plan->total_pop;
     st.pages_pushed = plan->total_push;
     st.requests_touched = (int32_t)plan->reqs.size();
-    // re-index: prep, rows of R, other fresh rows, the in-place rotation (each if any), commit
-    st.kernels_launched =
-        plan->reqs.empty() ? 0
-        : reindex          ? 2 + (plan->total_repl > 0) + (plan->total_fresh > 0) + (plan->total_tiles > 0)
-                           : 2;
+    // re-index: prep with the rows of R (one launch), other fresh rows, the in-place rotation,
+    // commit (each if any)
+    st.kernels_launched = plan->reqs.empty() ? 0
+                          : reindex ? (plan->total_prep + plan->total_repl > 0) + (plan->total_fresh > 0) +
+                                          (plan->total_tiles > 0) + (plan->total_commit > 0)
+                                    : 2;
     st.reindexed = (!plan->reqs.empty() && reindex) ? 1 : 0;
     return LEYLINE_OK;
 }

@@ -456,9 +456,9 @@ __global__ void __launch_bounds__(kMatThreads, LEYLINE_MAT_MIN_CTAS) materialize
         long long cur_tile = -1;
         long long slot = -1;
         float cs[8], sn[8];
+        long long tile = t0, grp = u - t0 * groups;  // advanced by counters, not divisions
         for (; u < u_end; ++u) {
-            const long long tile = u / groups;
-            const long long layer0 = (u - tile * groups) * kMatLayers;
+            const long long layer0 = grp * kMatLayers;
             if (tile != cur_tile) {
                 cur_tile = tile;
                 const int ti = (int)(tile - t0);
@@ -499,6 +499,10 @@ __global__ void __launch_bounds__(kMatThreads, LEYLINE_MAT_MIN_CTAS) materialize
                     rotate_interleaved<kBf16>(v[k], cs, sn);
                     st_stream(p[k], v[k]);
                 }
+            }
+            if (++grp == groups) {
+                grp = 0;
+                ++tile;
             }
         }
     }

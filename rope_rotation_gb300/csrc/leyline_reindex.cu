@@ -653,7 +653,10 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     const int prep_ctas = a.total_prep > 0 ? grid_for(a.total_prep, kMoveThreads, 8192) : 0;
     const long long repl_items = a.total_repl * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
     const int repl_ctas = repl_items > 0 ? grid_for(repl_items * 32, kMoveThreads, 8192) : 0;
-    if (t0) e = cudaEventRecord(t0, s);
+    // Timing events bracket the in-place rotation when there is one (the call's dominant
+    // kernel), else the launches before the commit.
+    const bool rotates = a.total_tiles > 0;
+    if (t0 && !rotates) e = cudaEventRecord(t0, s);
     if (e == cudaSuccess && prep_ctas + repl_ctas > 0) {
         SpliceArgs b = a;
         b.prep_ctas = prep_ctas;
@@ -675,6 +678,7 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
                        : (bf16 ? copy_fresh_reindex<1, true, PlanSrc> : copy_fresh_reindex<1, false, PlanSrc>);
         e = launch_dependent(k, fgrid, kMoveThreads, s, a, plan);
     }
+    if (e == cudaSuccess && t0 && rotates) e = cudaEventRecord(t0, s);
     if (e == cudaSuccess && units > 0 && lines) {
         e = split ? (bf16 ? launch_dependent(rotate_in_place_lines<0, true, PlanSrc>, grid, kMoveThreads, s, a, plan)
                           : launch_dependent(rotate_in_place_lines<0, false, PlanSrc>, grid, kMoveThreads, s, a, plan))

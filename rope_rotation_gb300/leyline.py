@@ -77,7 +77,7 @@ class Stats(ctypes.Structure):
                 ("pages_pushed", ctypes.c_int64), ("requests_touched", ctypes.c_int32),
                 ("kernels_launched", ctypes.c_int32), ("reindexed", ctypes.c_int32),
                 ("overlapped", ctypes.c_int32), ("host_ns", ctypes.c_int64), ("resolve_ns", ctypes.c_int64),
-                ("plan_ns", ctypes.c_int64)]
+                ("plan_ns", ctypes.c_int64), ("timed_kernel_bytes", ctypes.c_int64)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

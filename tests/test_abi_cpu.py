@@ -191,9 +191,17 @@ def test_reindex_keeps_pages_of_runs_shifted_by_whole_blocks(L):
         st, new = _plan(L, lens, dirs, desc=desc)
         got = (st.reindexed, st.pages_popped, st.pages_pushed)
         assert got == (reindexed, pops, pushes), [(d.s_start, d.s_end, d.n_repl) for d in dirs]
-    # block size 1: every row of R gets a fresh page, every dropped token returns one
+    # block size 1: every row of R gets a fresh page, every dropped token returns one; three
+    # launches (prep with the rows of R, the in-place rotation, commit)
     st, _ = _plan(L, [100], [_d(L, 0, 3, 50, 7)], B=1, desc=L.pool_desc(4, 1, 1 << 20, flags=L.LEYLINE_POOL_REINDEX))
-    assert (st.reindexed, st.kernels_launched, st.pages_popped, st.pages_pushed) == (1, 4, 7, 47)
+    assert (st.reindexed, st.kernels_launched, st.pages_popped, st.pages_pushed) == (1, 3, 7, 47)
+    # bytes: the 50 survivors' bands turned in place (2 x 128 bytes per layer) and 7 whole rows of
+    # R written (2 x 1152 bytes per layer), 4 layers; the timed kernel is the rotation alone
+    assert st.algorithmic_bytes == 2 * 4 * (128 * 50 + 1152 * 7)
+    assert st.timed_kernel_bytes == 2 * 4 * 128 * 50
+    # a rewrite times its move+rotate kernel, which moves all of the call's bytes
+    st, _ = _plan(L, [100], [_d(L, 0, 3, 50, 7)], B=1, desc=L.pool_desc(4, 1, 1 << 20))
+    assert st.kernels_launched == 2 and st.timed_kernel_bytes == st.algorithmic_bytes == 2 * 4 * 1152 * (50 + 7)
 
 
 def test_binding_refuses_tensors_it_cannot_pass_as_rows(L):
