@@ -99,6 +99,14 @@ __device__ __forceinline__ void prep_item(const SpliceArgs& a, const PlanView& p
 constexpr int kMaxRopeDim = 256;
 constexpr int kMaxItems = 4;    // work items per thread: rope_heads * rope_dim <= 512
 constexpr int kFreshLayers = 8;  // layers per item of the fresh-rows kernel
+#ifndef LEYLINE_REPL_VECS
+#define LEYLINE_REPL_VECS 4
+#endif
+constexpr int kReplVecs = LEYLINE_REPL_VECS;  // vectors per lane in flight in a row-of-R item
+#ifndef LEYLINE_REPL_LAYERS
+#define LEYLINE_REPL_LAYERS 8
+#endif
+constexpr int kReplLayers = LEYLINE_REPL_LAYERS;  // layers per row-of-R item
 
 // Layers per work unit of the re-index rotate kernel: as many as give each of the
 // CTA's threads kItems work items (at least one layer).
@@ -108,7 +116,7 @@ __host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, i
     return l > 0 ? l : 1;
 }
 
-// One row-of-R item: row rrow of the call's rows of R, layers [l0, l0 + kFreshLayers),
+// One row-of-R item: row rrow of the call's rows of R, layers [l0, l0 + kReplLayers),
 // moved by one warp into the row's fresh page.  The page is the one prep stages for
 // the row's block (a block holding a row of R is never kept): the block's position
 // among its request's fresh blocks, read from the ring's pop region.
@@ -145,22 +153,27 @@ __device__ __forceinline__ void repl_item(const SpliceArgs& a, const PlanView& p
     if (a.pending && l0 == 0 && lane == 0) a.pending[slot] = 0;  // R is encoded at its final position
     const long long rstride = (long long)s.n_repl * row_vecs;
     const uint4* src = static_cast<const uint4*>(s.repl) + j * row_vecs;
-    const long long l1 = l0 + kFreshLayers < L ? l0 + kFreshLayers : L;
-    for (long long layer = l0; layer < l1; ++layer) {
-        for (int c0 = 0; c0 < row_vecs; c0 += 4 * 32) {
-            uint4 v[4];
+    const long long l1 = l0 + kReplLayers < L ? l0 + kReplLayers : L;
+    // the item's (layer, vector) pairs as one list, kReplVecs vectors per lane in flight
+    // before any store (a warp moves up to 32 * kReplVecs * 16 bytes at a time)
+    const int n = (int)(l1 - l0) * row_vecs;
+    for (int e0 = 0; e0 < n; e0 += 32 * kReplVecs) {
+        uint4 v[kReplVecs];
+        int dl[kReplVecs], dc[kReplVecs];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c = c0 + 32 * q + lane;
-                if (c < row_vecs) v[q] = ld_stream(src + layer * rstride + c);
-            }
+        for (int q = 0; q < kReplVecs; ++q) {
+            const int e = e0 + 32 * q + lane;
+            dl[q] = e / row_vecs;
+            dc[q] = e - dl[q] * row_vecs;
+            if (e < n) v[q] = ld_stream(src + (l0 + dl[q]) * rstride + dc[q]);
+        }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int c = c0 + 32 * q + lane;
-                if (c < row_vecs)
-                    st_stream(kv + (c < lv ? lat_off(a.g, layer, slot) + c : band_off(a.g, layer, slot) + (c - lv)),
-                              v[q]);
-            }
+        for (int q = 0; q < kReplVecs; ++q) {
+            const int e = e0 + 32 * q + lane;
+            const long long layer = l0 + dl[q];
+            const int c = dc[q];
+            if (e < n)
+                st_stream(kv + (c < lv ? lat_off(a.g, layer, slot) + c : band_off(a.g, layer, slot) + (c - lv)), v[q]);
         }
     }
 }
@@ -186,10 +199,10 @@ __global__ void __launch_bounds__(kMoveThreads) prep_repl_reindex(const __grid_c
     const int lane = threadIdx.x & 31;
     const long long gw = (((long long)blockIdx.x - prep_ctas) * blockDim.x + threadIdx.x) >> 5;
     const long long nw = (((long long)gridDim.x - prep_ctas) * blockDim.x) >> 5;
-    const long long chunks = (a.g.num_layers + kFreshLayers - 1) / kFreshLayers;
+    const long long chunks = (a.g.num_layers + kReplLayers - 1) / kReplLayers;
     for (long long w = gw; w < a.total_repl * chunks; w += nw) {
         const long long rrow = w / chunks;
-        repl_item(a, pv, rrow, (w - rrow * chunks) * kFreshLayers, lane);
+        repl_item(a, pv, rrow, (w - rrow * chunks) * kReplLayers, lane);
     }
 }
 
@@ -651,7 +664,7 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     cudaError_t e = cudaSuccess;
     // prep and the rows of R: one launch, prep CTAs first
     const int prep_ctas = a.total_prep > 0 ? grid_for(a.total_prep, kMoveThreads, 8192) : 0;
-    const long long repl_items = a.total_repl * ((a.g.num_layers + kFreshLayers - 1) / kFreshLayers);
+    const long long repl_items = a.total_repl * ((a.g.num_layers + kReplLayers - 1) / kReplLayers);
     const int repl_ctas = repl_items > 0 ? grid_for(repl_items * 32, kMoveThreads, 8192) : 0;
     // Timing events bracket the in-place rotation when there is one (the call's dominant
     // kernel), else the launches before the commit.
