@@ -61,8 +61,8 @@ NCU_TRAFFIC = {
         "bytes": 210924288 + 161260288},
     # the whole-line rotate kernel of a re-index call, block-1 sweep of 4 requests on 16 layers
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "b506a2d0be3f9ee795dc5a365b5e2ce25e3f8b6f33424563e701196b2e0e0c85",
-        "bytes": 130888192 + 71854592},
+        "kernel_sha256": "e997ad4a0142701f446491ca07b2b6cf59ecdc54dd7be24ba07cc0968f9c415f",
+        "bytes": 130884608 + 71590144},
 }
 
 
