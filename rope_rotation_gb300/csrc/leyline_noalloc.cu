@@ -74,6 +74,7 @@ int scratch_address(int device, void** out)
 extern "C" int leyline_splice_noalloc(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_directive_t* dirs,
                                       int32_t n, void* stream_v)
 {
+    NvtxRange range("leyline_splice_noalloc");
     clear_error();
     const HostClock t_enter = host_now();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");

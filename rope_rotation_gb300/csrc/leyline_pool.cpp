@@ -368,6 +368,7 @@ int leyline_splice_plan(const leyline_pool_desc_t* desc, const int64_t* seq_lens
 int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_directive_t* dirs, int32_t n,
                    void* stream_v)
 {
+    NvtxRange range("leyline_splice");
     clear_error();
     const HostClock t_enter = host_now();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
@@ -384,7 +385,10 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     const HostClock t_resolved = host_now();
     Plan plan;
     const int64_t free_now = p->q_tail - p->q_head;
-    rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
+    {
+        NvtxRange plan_range("leyline_splice: plan");
+        rc = build_plan(p->g, bt->seq_lens_host, bt->num_reqs, bt->max_blocks, use, n, free_now, &plan);
+    }
     if (rc != LEYLINE_OK) return rc;
     const HostClock t_planned = host_now();
     if (plan.reqs.empty()) {
@@ -563,6 +567,7 @@ int leyline_last_stats(const leyline_pool_t* p, leyline_stats_t* out)
 int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t req, int32_t layer, int64_t t0,
                    int64_t t1, void* out, void* stream_v)
 {
+    NvtxRange range("leyline_gather");
     clear_error();
     if (!p || !bt || !bt->table || !bt->seq_lens_host) return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
     p->window_open = false;  // other work on the pool ends the window of overlapping splices
@@ -591,6 +596,7 @@ int leyline_gather(leyline_pool_t* p, const leyline_block_table_t* bt, int32_t r
 int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t* bt, const int32_t* reqs, int32_t n,
                                  void* stream_v)
 {
+    NvtxRange range("leyline_materialize_requests");
     clear_error();
     if (!p || !bt || !bt->table || !bt->seq_lens_host || n < 0 || (n > 0 && !reqs))
         return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
@@ -673,6 +679,7 @@ int leyline_sync_status(leyline_pool_t* p)
 
 int leyline_pool_checkpoint(leyline_pool_t* p, void* stream_v)
 {
+    NvtxRange range("leyline_pool_checkpoint");
     clear_error();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
     p->window_open = false;  // other work on the pool ends the window of overlapping splices
@@ -704,6 +711,7 @@ int leyline_pool_checkpoint(leyline_pool_t* p, void* stream_v)
 
 int leyline_pool_rollback(leyline_pool_t* p, int32_t flags, void* stream_v)
 {
+    NvtxRange range("leyline_pool_rollback");
     clear_error();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
     p->window_open = false;  // other work on the pool ends the window of overlapping splices

@@ -9,7 +9,20 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "leyline_internal.h"
+
+namespace leyline {
+// A named NVTX range for the host side of an entry point (shown by profilers that record
+// NVTX, such as ncu --nvtx; close to free when no tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace leyline
 
 // State of one pool (opaque to callers as leyline_pool_t).
 struct leyline_pool {

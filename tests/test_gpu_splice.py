@@ -121,6 +121,61 @@ def test_delta_zero_leaves_logical_cache_unchanged():
     cache.close()
 
 
+@pytest.mark.parametrize("B", [16, 1])
+def test_two_splices_equal_one_composed_splice(B):
+    """Closure through the kernels ("Leyline: KV Cache Directives for Agentic Inference",
+    section 2.2: R(a) R(b) = R(a + b)).  One call holding two directives turns the rows past
+    both once by Delta_1 + Delta_2; the same edit as two calls (the right directive first, so
+    the left one's coordinates hold) turns them by Delta_2 and then by Delta_1, rounding to
+    bf16 in between.  Rows turned once (by Delta_1, with the same cos/sin) and every copied
+    row must agree bit for bit; rows turned twice differ at most by the two outputs' own
+    roundings (half a bf16 step each) plus the intermediate rounding turned once more:
+    each element of it is at most 2^-8 of the pair norm, so at most sqrt(2) 2^-8 of the
+    pair norm after the turn, plus fp32 noise."""
+    import oracle
+    left, right = (100, 300, 20), (500, 600, 7)
+    L = 900
+    # the right directive's rows of R sit at their final position in the one-call edit, and
+    # one call earlier (before the left directive moves them) in the two-call edit: different
+    # encodings, so they are compared with the oracle, not with each other
+    one = Workload(f"closure-one-B{B}", 2, B, [L], [[Dir(0, *left, 0), Dir(0, *right, 1)]], seed=33)
+    two = Workload(f"closure-two-B{B}", 2, B, [L], [[Dir(0, *right, 1)], [Dir(0, *left, 0)]], seed=33)
+    ca, cb = H.make_cache(one), H.make_cache(two)
+    keep = []
+    for w, cache in ((one, ca), (two, cb)):
+        for step in w.steps:
+            dirs, k = H.gpu_directives(w, step)
+            keep.append(k)
+            cache.splice(dirs)
+            torch.cuda.synchronize()
+            cache.check_status()
+    newlen, kind, idx, which = oracle.splice_map(L, [left, right])
+    assert int(ca.seq_lens_host[0]) == int(cb.seq_lens_host[0]) == newlen
+    a = H.logical_rows(ca, 0, newlen)
+    b = H.logical_rows(cb, 0, newlen)
+    lat = one.latent_dim
+    assert np.array_equal(a[:, :, :lat], b[:, :, :lat]), "latent bits differ"
+    right_r = (kind == 1) & (which == 1)
+    twice = (kind == 0) & (idx >= right[1])
+    same = ~right_r & ~twice  # prefix, the left directive's rows of R, rows turned once
+    assert np.array_equal(a[:, same], b[:, same]), "rows copied or turned once differ"
+    # the right directive's rows of R in the two-call edit: written, then turned by Delta_1
+    d1 = left[2] - (left[1] - left[0])
+    rr = b[:, right_r, lat:].reshape(-1, one.rope_dim)
+    want = oracle.rerotate(a[:, right_r, lat:].reshape(-1, one.rope_dim), 0, d1, one.theta)
+    H.compare_kpe(rr, want, 0)
+    ga = oracle.bf16_value(a[:, twice, lat:].reshape(-1, one.rope_dim))
+    gb = oracle.bf16_value(b[:, twice, lat:].reshape(-1, one.rope_dim))
+    pn = H.pair_norms(ga, 0)
+    bound = 0.5 * H.bf16_step(ga) + 0.5 * H.bf16_step(gb) + (np.sqrt(2.0) * 2.0 ** -8 + 2.0 ** -16) * pn
+    diff = np.abs(ga - gb)
+    assert np.all(diff <= bound), f"{int((diff > bound).sum())} elements beyond the two-rounding bound"
+    assert np.any(diff > 0), "two roundings should leave some elements apart"
+    del keep
+    ca.close()
+    cb.close()
+
+
 def test_contiguous_4k_workload():
     w = configs.contiguous_4k()
     cache = H.make_cache(w)
