@@ -4,6 +4,8 @@
 //
 // "Leyline: KV Cache Directives for Agentic Inference", sections 2.2-2.3 (the rotation
 // and re-index of every downstream slot) and 3 (block-level storage).
+#include <type_traits>
+
 #include "leyline_device.cuh"
 
 namespace leyline {
@@ -83,9 +85,10 @@ __device__ __forceinline__ void prep_item(const SpliceArgs& a, const PlanView& p
 
 // Re-index mode writes fresh rows and turns kept bands.
 //   prep_repl_reindex (its row-of-R part): the call's rows of R form one list; items
-//   of (row, 8 layers) are spread over every warp of its CTAs, a lane moving every
-//   32nd vector of the row with four loads in flight.  A row of R moves 9 times the
-//   bytes of a turned band, so rows of R are not tied to one CTA's share of the tiles.
+//   of (row, 8 layers) are spread over every warp of its CTAs, the warp moving the
+//   item's (layer, vector) list with kReplVecs vectors per lane in flight.  A row of R
+//   moves 9 times the bytes of a turned band, so rows of R are not tied to one CTA's
+//   share of the tiles.
 //   copy_fresh_reindex: the other rows of blocks that get fresh pages (survivors and
 //   prefix rows of boundary blocks), likewise spread over warps, read through the old
 //   table and turned by their segment's cos/sin.
@@ -114,6 +117,46 @@ __host__ __device__ __forceinline__ int reindex_layers_per_unit(int per_layer, i
 {
     const int l = items * kMoveThreads / per_layer;
     return l > 0 ? l : 1;
+}
+
+// An uploaded plan's requests and segments in shared memory, for the kernels that look up a
+// request and a segment per work item (prep, rows of R, fresh rows, commit).  They are
+// contiguous in the upload (requests, segments, then the cos / sin), so a CTA copies them
+// once and its lookups then read shared memory instead of a chain of global loads.  The
+// launch passes their bytes as dynamic shared memory, or 0 when they exceed
+// kStagedPlanMax (the lookups then read global memory); a plan that travels as a kernel
+// parameter is read where it is.
+constexpr unsigned kStagedPlanMax = 48u << 10;
+extern __shared__ uint4 staged_plan_smem[];
+
+__device__ __forceinline__ PlanView staged_plan_view(const SpliceArgs& a, const ParamPlan& plan)
+{
+    return plan_view(a, plan);
+}
+
+__device__ __forceinline__ PlanView staged_plan_view(const SpliceArgs& a, const NoParamPlan& plan)
+{
+    unsigned bytes;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(bytes));
+    if (bytes == 0) return plan_view(a, plan);
+    const uint4* src = reinterpret_cast<const uint4*>(a.reqs);
+    for (unsigned v = threadIdx.x; v < bytes / 16; v += blockDim.x) staged_plan_smem[v] = src[v];
+    __syncthreads();
+    const char* base = reinterpret_cast<const char*>(staged_plan_smem);
+    return PlanView{reinterpret_cast<const ReqPlan*>(base),
+                    reinterpret_cast<const Seg*>(base + (reinterpret_cast<const char*>(a.segs) -
+                                                         reinterpret_cast<const char*>(a.reqs))),
+                    a.trig};
+}
+
+// Dynamic shared memory of a launch that stages the plan: the bytes of its requests and
+// segments when the plan is uploaded and they fit, else 0.
+template <class PlanSrc>
+unsigned staged_plan_bytes(const SpliceArgs& a)
+{
+    if (std::is_same<PlanSrc, ParamPlan>::value) return 0;
+    const size_t bytes = (size_t)(reinterpret_cast<const char*>(a.trig) - reinterpret_cast<const char*>(a.reqs));
+    return bytes <= kStagedPlanMax && bytes % 16 == 0 ? (unsigned)bytes : 0u;
 }
 
 // One row-of-R item: row rrow of the call's rows of R, layers [l0, l0 + kReplLayers),
@@ -188,7 +231,7 @@ __global__ void __launch_bounds__(kMoveThreads) prep_repl_reindex(const __grid_c
 {
     wait_for_previous_grid();
     allow_next_grid();
-    const PlanView pv = plan_view(a, plan);
+    const PlanView pv = staged_plan_view(a, plan);
     const long long prep_ctas = a.prep_ctas;
     if ((long long)blockIdx.x < prep_ctas) {
         const long long stride = prep_ctas * blockDim.x;
@@ -252,7 +295,7 @@ __global__ void __launch_bounds__(kMoveThreads, 3) copy_fresh_reindex(const __gr
 {
     wait_for_previous_grid();
     allow_next_grid();
-    const PlanView pv = plan_view(a, plan);
+    const PlanView pv = staged_plan_view(a, plan);
     const int lane = threadIdx.x & 31;
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -620,7 +663,7 @@ template <class PlanSrc>
 __global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_constant__ SpliceArgs a,
                                                                  const __grid_constant__ PlanSrc plan)
 {
-    const PlanView pv = plan_view(a, plan);
+    const PlanView pv = staged_plan_view(a, plan);  // the plan is final before the previous kernel
     const long long stride = (long long)gridDim.x * blockDim.x;
     long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     int val = -1;
@@ -673,7 +716,8 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     if (e == cudaSuccess && prep_ctas + repl_ctas > 0) {
         SpliceArgs b = a;
         b.prep_ctas = prep_ctas;
-        e = launch_dependent(prep_repl_reindex<PlanSrc>, prep_ctas + repl_ctas, kMoveThreads, s, b, plan);
+        e = launch_dependent_smem(prep_repl_reindex<PlanSrc>, prep_ctas + repl_ctas, kMoveThreads,
+                                  staged_plan_bytes<PlanSrc>(a), s, b, plan);
     }
     const bool bf16 = a.g.precision == LEYLINE_ROTATE_BF16_NAIVE;
     const bool split = a.g.pair_layout == LEYLINE_PAIRS_HALF_SPLIT;
@@ -689,7 +733,7 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
         const int fgrid = grid_for(items * 32, kMoveThreads, 8192);
         auto k = split ? (bf16 ? copy_fresh_reindex<0, true, PlanSrc> : copy_fresh_reindex<0, false, PlanSrc>)
                        : (bf16 ? copy_fresh_reindex<1, true, PlanSrc> : copy_fresh_reindex<1, false, PlanSrc>);
-        e = launch_dependent(k, fgrid, kMoveThreads, s, a, plan);
+        e = launch_dependent_smem(k, fgrid, kMoveThreads, staged_plan_bytes<PlanSrc>(a), s, a, plan);
     }
     if (e == cudaSuccess && t0 && rotates) e = cudaEventRecord(t0, s);
     if (e == cudaSuccess && units > 0 && lines) {
@@ -715,8 +759,8 @@ int launch_reindex(const SpliceArgs& a, const PlanSrc& plan, int grid, cudaStrea
     }
     if (e == cudaSuccess && t1) e = cudaEventRecord(t1, s);
     if (e == cudaSuccess && a.total_commit > 0)
-        e = launch_dependent(commit_reindex<PlanSrc>, grid_for(a.total_commit, kCommitThreads, 8192), kCommitThreads, s,
-                             a, plan);
+        e = launch_dependent_smem(commit_reindex<PlanSrc>, grid_for(a.total_commit, kCommitThreads, 8192),
+                                  kCommitThreads, staged_plan_bytes<PlanSrc>(a), s, a, plan);
     if (e == cudaSuccess) e = cudaGetLastError();
     return (int)e;
 }
