@@ -656,9 +656,11 @@ __global__ void __launch_bounds__(kMoveThreads, LEYLINE_LINES_MIN_CTAS) rotate_i
 
 // Commit of a re-indexed call: staged entries into the new blocks [b0, new end),
 // -1 into the blocks past the new end, the new length, and (lazy pools) pending
-// counts of 0 on the returned pages.  The staged values are final before the
-// rotate kernel starts and it never writes them, so they are loaded before
-// griddepcontrol.wait.
+// counts of 0 on the returned pages.  The staged values are final once prep has
+// finished.  When a fresh-rows or rotate kernel runs between prep and this one, that
+// kernel waited for prep before it let this one launch, so the values are loaded before
+// griddepcontrol.wait; when prep itself is the previous kernel (a call that turns no
+// band and writes no other fresh rows: every lazy block-1 call), they are loaded after.
 template <class PlanSrc>
 __global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_constant__ SpliceArgs a,
                                                                  const __grid_constant__ PlanSrc plan)
@@ -670,13 +672,15 @@ __global__ void __launch_bounds__(kCommitThreads) commit_reindex(const __grid_co
     const ReqPlan* rp = nullptr;
     long long k = 0;
     const long long B = a.g.block_size;
+    const bool early = a.total_fresh > 0 || a.total_tiles > 0;  // a kernel between prep and this one
     if (i < a.total_commit) {
         rp = &pv.reqs[find_req(pv.reqs, a.n_reqs, i, BY_COMMIT)];
         k = i - rp->commit_begin;
-        if (k < (rp->new_len + B - 1) / B - rp->b0) val = a.stage[rp->stage_begin + k];
+        if (early && k < (rp->new_len + B - 1) / B - rp->b0) val = a.stage[rp->stage_begin + k];
     }
     wait_for_previous_grid();
     allow_next_grid();
+    if (!early && i < a.total_commit && k < (rp->new_len + B - 1) / B - rp->b0) val = a.stage[rp->stage_begin + k];
     while (i < a.total_commit) {
         int32_t* trow = a.table_w + (long long)rp->req * a.max_blocks;
         const long long nb_new = (rp->new_len + B - 1) / B, nb_old = (rp->old_len + B - 1) / B;

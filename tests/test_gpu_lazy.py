@@ -312,6 +312,42 @@ def test_materialize_band_shapes(rope_dim, heads, layout, B):
     cache.close()
 
 
+@pytest.mark.parametrize("B", [1, 16])
+def test_lazy_reindex_calls_in_flight_equal_calls_one_at_a_time(B):
+    """Lazy re-index calls enqueued back to back with no synchronisation (each call's commit
+    follows its prep directly: no band is turned, and at block size 1 no other fresh rows are
+    written) leave exactly the stored bits, counts and tables of the same calls made one at a
+    time with a synchronisation after each; those are checked against the oracle elsewhere."""
+    import torch
+    steps = _chain(97, 24, 1200, n_reqs=3)
+    w = Workload(f"lazy-inflight-B{B}", 2, B, [1200] * 3, steps, seed=98)
+    a = H.make_cache(w, flags=LAZY | REINDEX, slack_pages=64)
+    b = H.make_cache(w, flags=LAZY | REINDEX, slack_pages=64)
+    keep = []
+    for step in steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        a.splice(dirs)  # no synchronisation
+    for step in steps:
+        dirs, k = H.gpu_directives(w, step)
+        keep.append(k)
+        b.splice(dirs)
+        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    a.check_status()
+    b.check_status()
+    for r in range(w.num_reqs):
+        n = int(a.seq_lens_host[r])
+        assert n == int(b.seq_lens_host[r])
+        assert np.array_equal(_raw_rows(a, r, n), _raw_rows(b, r, n)), f"request {r}: stored bits differ"
+        assert np.array_equal(_pending_of(a, r, n), _pending_of(b, r, n)), f"request {r}: counts differ"
+    assert np.array_equal(a.table.cpu().numpy(), b.table.cpu().numpy())
+    _check_free_pages_clear(a)
+    del keep
+    a.close()
+    b.close()
+
+
 def test_free_pages_clears_pending():
     import torch
     from rope_rotation_gb300 import leyline
