@@ -61,8 +61,8 @@ NCU_TRAFFIC = {
         "bytes": 210924288 + 161260288},
     # the whole-line rotate kernel of a re-index call, block-1 sweep of 4 requests on 16 layers
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "e997ad4a0142701f446491ca07b2b6cf59ecdc54dd7be24ba07cc0968f9c415f",
-        "bytes": 130884608 + 71590144},
+        "kernel_sha256": "e891b396426e082616a96fd1efcf231d9f41109133cdec2511c21a8370e11773",
+        "bytes": 130883584 + 72365568},
 }
 
 
