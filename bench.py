@@ -840,9 +840,11 @@ def single_core_sample(w, units, budget_s: float, seed: int):
     return slots, spent, n
 
 
-def parallel_units(units, rate_1: float, budget_core_s: float):
+def parallel_units(units, rate_1: float, budget_core_s: float, procs: int = 1):
     """The first units (layer-major, so every request is in the sample) whose single-core
-    estimate fits budget_core_s core-seconds; at least one layer of every request."""
+    estimate fits budget_core_s core-seconds; at least one layer of every request.  When the
+    sample holds at least `procs` units it is cut to a multiple of procs, so that no process
+    runs one unit more than the others."""
     per_layer = len({r for r, _, _ in units})
     out, est = [], 0.0
     for i, u in enumerate(units):
@@ -850,6 +852,8 @@ def parallel_units(units, rate_1: float, budget_core_s: float):
         if est > budget_core_s and i >= per_layer:
             break
         out.append(u)
+    if procs > 1 and len(out) >= procs:
+        out = out[:len(out) // procs * procs]
     return out
 
 
@@ -861,7 +865,7 @@ def cpu_oracle_sample(w, budget_s: float, seed: int = 0):
     procs = host_cores()
     pool = OraclePool(procs)
     try:
-        pu = parallel_units(units, rate_1, budget_s * procs)
+        pu = parallel_units(units, rate_1, budget_s * procs, procs)
         busy, wall = pool.run(seed, w, pu)
     finally:
         pool.close()
@@ -888,7 +892,7 @@ def run_reference(args, rank, world):
     units, _ = oracle_units(w)
     s1, t1, _ = single_core_sample(w, units, 1.0, seed)
     procs = host_cores()
-    pu = parallel_units(units, s1 / t1, args.cpu_seconds * procs / 4)
+    pu = parallel_units(units, s1 / t1, args.cpu_seconds * procs / 4, procs)
     slots = sum(u[2] for u in pu)
     pool = OraclePool(procs)
     try:

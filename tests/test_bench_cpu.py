@@ -61,6 +61,9 @@ def test_resident_copies_and_units():
     pick = bench.parallel_units(units, rate_1=1e5, budget_core_s=0.0)
     assert len(pick) == 4 and {u[0] for u in pick} == {0, 1, 2, 3} and {u[1] for u in pick} == {0}
     assert len(bench.parallel_units(units, rate_1=1e12, budget_core_s=1.0)) == len(units)
+    # cut to a multiple of the processes: 244 units over 16 processes -> 240
+    assert len(bench.parallel_units(units, rate_1=1e12, budget_core_s=1.0, procs=16)) == 240
+    assert len(bench.parallel_units(units, rate_1=1e5, budget_core_s=0.0, procs=16)) == 4  # fewer units than procs
 
 
 def test_job_value_is_all_ranks_over_the_slowest():
