@@ -157,3 +157,38 @@ def test_rollback_after_turning_in_place_needs_the_flag():
     leyline.leyline_pool_rollback(lazy.pool)
     del saved
     lazy.close()
+
+
+def test_rollback_after_noalloc_splices():
+    """leyline_splice_noalloc keeps the same page accounting as leyline_splice: a checkpoint
+    before two no-alloc calls and a rollback after them give the rows back, and repeating the
+    calls gives the same result bit for bit."""
+    from rope_rotation_gb300 import leyline
+    steps = [[Dir(0, 40, 130, 9, 0), Dir(1, 5, 300, 3, 1)], [Dir(0, 0, 3, 0, 2), Dir(1, 100, 101, 30, 3)]]
+    w = Workload("rollback-noalloc", 2, 16, [600, 700], steps, seed=8)
+    cache = H.make_cache(w, slack_pages=80)
+    before = _all_rows(cache, w)
+    saved = _saved(cache)
+    leyline.leyline_pool_checkpoint(cache.pool)
+    keep = []
+
+    def run_steps():
+        for step in steps:
+            dirs, k = H.gpu_directives(w, step)
+            keep.append(k)
+            leyline.leyline_splice_noalloc(cache.pool, cache.tables, dirs)
+        torch.cuda.synchronize()
+        cache.check_status()
+        return _all_rows(cache, w)
+
+    first = run_steps()
+    leyline.leyline_pool_rollback(cache.pool)
+    _restore(cache, saved)
+    torch.cuda.synchronize()
+    for r, rows in enumerate(_all_rows(cache, w)):
+        assert np.array_equal(rows, before[r]), f"request {r}: rollback did not restore the cache"
+    again = run_steps()
+    for r in range(w.num_reqs):
+        assert np.array_equal(again[r], first[r]), f"request {r}: the repeat differs"
+    del keep
+    cache.close()
