@@ -263,8 +263,8 @@ def resident_copies(copy_bytes: int, wanted: int, mem_gb: float) -> int:
 HEAD_START_CYCLES = 2_000_000  # about 1 ms at 2 GHz
 
 
-def hold_stream(torch):
-    torch.cuda._sleep(HEAD_START_CYCLES)
+def hold_stream(torch, cycles: int = HEAD_START_CYCLES):
+    torch.cuda._sleep(cycles)
 
 
 def copy_gbps_now(torch, gib: float = 2.0, reps: int = 5) -> float:
@@ -644,15 +644,32 @@ def run_chain(args, rank, world, local):
     assert w.num_reqs == 1 and all(len(step) == 1 for step in w.steps), "one request, one directive per splice"
     L0, B = w.lengths[0], w.block_size
     nb = -(-max(L0, max(d.s_start + d.n_repl for step in w.steps for d in step)) // B) + 1
-    groups = W + K
     flags = ((leyline.LEYLINE_POOL_REINDEX if args.reindex else 0) | (leyline.LEYLINE_POOL_LAZY if args.lazy else 0)
              | (leyline.LEYLINE_POOL_SPLIT_ROPE if args.split else 0))
+    # As many copies of the request as the memory budget holds.  A chain's splices recycle the
+    # pages they return, so a spent copy cannot be rolled back: between chains (outside the
+    # timed events) its pages are returned and the request is written afresh.
+    copies = resident_copies(nb * w.num_layers * B * w.row_elems * 2, W + K, args.mem_gb)
     # every chain copy's pages, plus one request's worth for the fresh pages a rewrite takes
-    cache = PagedCache(w.num_layers, B, (groups + 1) * nb, groups, nb, w.latent_dim, w.rope_dim, w.theta, flags=flags)
+    cache = PagedCache(w.num_layers, B, (copies + 1) * nb, copies, nb, w.latent_dim, w.rope_dim, w.theta, flags=flags)
     seed = rank_seed(w.seed, rank)
-    for g in range(groups):
+    for g in range(copies):
         cache.add_request(g, L0)
         fill.fill_request(cache, seed, g, L0)
+    spent = [False] * copies
+
+    def fresh_copy(k):
+        """The copy chain k runs on, written afresh first if an earlier chain spent it."""
+        g = k % copies
+        if spent[g]:
+            n_old = -(-int(cache.seq_lens_host[g]) // B)
+            leyline.leyline_free_pages(cache.pool, cache.table[g, :n_old].cpu().numpy())
+            cache.table[g].fill_(-1)
+            cache.add_request(g, L0)
+            fill.fill_request(cache, seed, g, L0)
+            torch.cuda.synchronize()
+        spent[g] = True
+        return g
     tmpl = []
     for step in w.steps:
         d = step[0]
@@ -672,11 +689,11 @@ def run_chain(args, rank, world, local):
                     stats[k] = stats.get(k, 0) + v
 
     per_chain = {}
-    for g in range(W):
-        chain(g, per_chain if g == 0 else None)
+    for k in range(W):
+        chain(fresh_copy(k), per_chain if k == 0 else None)
+        torch.cuda.synchronize()
     if W == 0:
         raise SystemExit("a chain needs at least one warm-up chain (its work counts come from it)")
-    torch.cuda.synchronize()
     cache.check_status()
     n_splices = len(tmpl)
 
@@ -684,22 +701,27 @@ def run_chain(args, rank, world, local):
     sampler.start()
     time.sleep(0.2)
     leyline.leyline_kernel_timing_enable(cache.pool, True)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    hold_stream(torch)
-    ev0.record(stream)
-    t_host = time.perf_counter()
-    for g in range(W, W + K):
+    # each chain has its own events, behind a spin long enough for the host to queue the
+    # whole chain; a copy written afresh between chains lies outside them
+    elapsed_ms, enqueue_s = 0.0, 0.0
+    for k in range(W, W + K):
+        g = fresh_copy(k)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(torch, 4 * HEAD_START_CYCLES)
+        ev0.record(stream)
+        t_host = time.perf_counter()
         chain(g)
-    enqueue_us = (time.perf_counter() - t_host) * 1e6 / K
-    ev1.record(stream)
-    torch.cuda.synchronize()
+        enqueue_s += time.perf_counter() - t_host
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms += ev0.elapsed_time(ev1)
+    enqueue_us = enqueue_s * 1e6 / K
     if world > 1:
         dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
     cache.check_status()
     k2_ms, k2_n = leyline.leyline_kernel_timing_read(cache.pool)
     leyline.leyline_kernel_timing_enable(cache.pool, False)
@@ -732,7 +754,9 @@ def run_chain(args, rank, world, local):
                    "algorithmic_bytes_per_step": per_chain["algorithmic_bytes"],
                    "reindexed_splices": per_chain["reindexed"],
                    "l2": "inputs larger than L2: each chain splices its own pre-filled request",
-                   "timing": "CUDA events around K chains queued behind a ~1 ms spin on the stream",
+                   "resident_copies": copies,
+                   "timing": "CUDA events around each of the K chains, each queued behind a ~4 ms spin on the "
+                             "stream; a copy spent by an earlier chain is written afresh outside the events",
                    "pool": ("lazy (pending turns, rotation on read)" if args.lazy else "eager")
                    + (", re-index" if args.reindex else "") + (", split rope" if args.split else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
