@@ -269,6 +269,8 @@ int64_t leyline_free_page_count(const leyline_pool_t* pool);
  *     LEYLINE_ROLLBACK_ACCEPT_TURNED: the accounting is then restored but those
  *     bands stay turned (benchmark repeats, where the work and not the values
  *     matters).
+ * Both refuse a `stream` under graph capture (INVALID_ARG): the ring positions
+ * they save and restore are host state at enqueue time.
  * Errors: INVALID_ARG, CUDA. */
 #define LEYLINE_ROLLBACK_ACCEPT_TURNED 1
 int leyline_pool_checkpoint(leyline_pool_t* pool, void* stream);
@@ -295,8 +297,10 @@ int leyline_pool_rollback(leyline_pool_t* pool, int32_t flags, void* stream);
  * stream between two calls, or a call on another stream, orders them fully.
  * Errors (nothing is enqueued or changed): INVALID_ARG, INVALID_DIRECTIVE,
  * OVERLAP, UNSUPPORTED_MODE (FORGET: the caller re-prefills, section 2.1),
- * CAPACITY, NO_PAGES.  CUDA: a launch failed after validation; the pool must
- * then be considered inconsistent. */
+ * CAPACITY, NO_PAGES.  INVALID_ARG also when `stream` is being captured into a
+ * CUDA graph: the call is planned on the host for the cache as it stands, and a
+ * replay would apply that plan to a cache that has moved on.  CUDA: a launch
+ * failed after validation; the pool must then be considered inconsistent. */
 int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leyline_directive_t* dirs,
                    int32_t n, void* stream);
 
@@ -352,12 +356,14 @@ int leyline_gather(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_
 /* LEYLINE_POOL_LAZY pools: turn the stored rope bands of rows [0, seq_len) of
  * request `req` (all layers) by their pending counts, in fp32, storing bf16, and
  * set the counts to 0.  Asynchronous on `stream`.  Errors: INVALID_ARG (not a lazy
- * pool, bad request). */
+ * pool, bad request, `stream` under graph capture). */
 int leyline_materialize(leyline_pool_t* pool, const leyline_block_table_t* bt, int32_t req, void* stream);
 
 /* leyline_materialize for the n requests reqs[0..n) (host array, distinct ids), in one
  * launch per 64 requests: their rows form one list, so the launches are few and full.
- * Errors: INVALID_ARG (not a lazy pool, a request out of range or listed twice). */
+ * Errors: INVALID_ARG (not a lazy pool, a request out of range or listed twice, or
+ * `stream` under graph capture: the launches are sized from seq_lens_host as it
+ * stands). */
 int leyline_materialize_requests(leyline_pool_t* pool, const leyline_block_table_t* bt, const int32_t* reqs,
                                  int32_t n, void* stream);
 

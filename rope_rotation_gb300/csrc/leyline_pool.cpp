@@ -74,6 +74,23 @@ int wait_pool(leyline_pool_t* p)
     return LEYLINE_OK;
 }
 
+// Entry points whose work depends on host-side state at enqueue time (a plan made for the
+// cache as it stands, ring positions, lengths) refuse a stream under graph capture: a replay
+// would apply that state to a cache that has moved on.
+int refuse_capture(cudaStream_t stream, const char* what)
+{
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &st);
+    if (e != cudaSuccess) return cuda_error(e, "querying the stream's capture status");
+    if (st != cudaStreamCaptureStatusNone) {
+        char msg[160];
+        snprintf(msg, sizeof msg, "%s cannot be captured in a CUDA graph: it is planned on the host for the cache as "
+                 "it stands", what);
+        return set_error(LEYLINE_ERR_INVALID_ARG, msg);
+    }
+    return LEYLINE_OK;
+}
+
 // Make `stream` wait for the pool's previous work when it came from another stream.
 int order_after_previous(leyline_pool_t* p, cudaStream_t stream)
 {
@@ -372,6 +389,11 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
     clear_error();
     const HostClock t_enter = host_now();
     if (!p) return set_error(LEYLINE_ERR_INVALID_ARG, "null pool");
+    {
+        DeviceGuard capture_guard(p->device);
+        int rc0 = refuse_capture((cudaStream_t)stream_v, "leyline_splice");
+        if (rc0 != LEYLINE_OK) return rc0;
+    }
     if (!bt || !bt->table || !bt->seq_lens_dev || !bt->seq_lens_host || bt->num_reqs < 0 || bt->max_blocks < 0)
         return set_error(LEYLINE_ERR_INVALID_ARG, "incomplete block table");
     for (int32_t r = 0; r < bt->num_reqs; ++r)
@@ -600,6 +622,11 @@ int leyline_materialize_requests(leyline_pool_t* p, const leyline_block_table_t*
     clear_error();
     if (!p || !bt || !bt->table || !bt->seq_lens_host || n < 0 || (n > 0 && !reqs))
         return set_error(LEYLINE_ERR_INVALID_ARG, "null argument");
+    {
+        DeviceGuard capture_guard(p->device);
+        int rc0 = refuse_capture((cudaStream_t)stream_v, "leyline_materialize_requests");
+        if (rc0 != LEYLINE_OK) return rc0;
+    }
     p->window_open = false;  // other work on the pool ends the window of overlapping splices
     if (!p->d_pending) return set_error(LEYLINE_ERR_INVALID_ARG, "the pool was not created with LEYLINE_POOL_LAZY");
     std::vector<int32_t> seen(reqs, reqs + n);
@@ -686,6 +713,8 @@ int leyline_pool_checkpoint(leyline_pool_t* p, void* stream_v)
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
     if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
+    int rc_cap = refuse_capture(stream, "leyline_pool_checkpoint");
+    if (rc_cap != LEYLINE_OK) return rc_cap;
     const size_t slots = (size_t)p->g.num_pages * (size_t)p->g.block_size;
     cudaError_t e = cudaSuccess;
     if (!p->d_ckpt_queue) e = cudaMalloc(&p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap);
@@ -729,7 +758,9 @@ int leyline_pool_rollback(leyline_pool_t* p, int32_t flags, void* stream_v)
     cudaStream_t stream = (cudaStream_t)stream_v;
     DeviceGuard guard(p->device);
     if (!guard.ok) return set_error(LEYLINE_ERR_CUDA, "cannot select the pool's device");
-    int rc = order_after_previous(p, stream);
+    int rc = refuse_capture(stream, "leyline_pool_rollback");
+    if (rc != LEYLINE_OK) return rc;
+    rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
     const size_t slots = (size_t)p->g.num_pages * (size_t)p->g.block_size;
     cudaError_t e = cudaMemcpyAsync(p->d_queue, p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap,

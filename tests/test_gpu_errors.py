@@ -144,3 +144,39 @@ def test_splices_on_two_streams_are_ordered():
     with torch.cuda.stream(s2):
         H.splice_step_and_check(w, cache, state, w.steps[1], guard=False)
     cache.close()
+
+
+def test_host_planned_calls_refuse_graph_capture():
+    """A splice, a materialize and a checkpoint or rollback are planned on the host for the
+    cache as it stands, so a CUDA graph that replayed them would apply stale plans: each
+    refuses a stream under capture, before anything is enqueued or changed."""
+    import torch
+    from rope_rotation_gb300 import leyline
+    w = Workload("capture", 1, 16, [300], [[Dir(0, 10, 40, 3, 0)]], seed=3)
+    cache = H.make_cache(w, slack_pages=8)
+    lazy = H.make_cache(w, slack_pages=8, flags=leyline.LEYLINE_POOL_LAZY)
+    dirs, keep = H.gpu_directives(w, w.steps[0])
+    leyline.leyline_pool_checkpoint(cache.pool)
+    torch.cuda.synchronize()
+    free, lens = cache.free_pages(), cache.seq_lens_host.copy()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    codes = []
+    calls = [lambda: cache.splice(dirs, s), lambda: leyline.leyline_pool_checkpoint(cache.pool, s),
+             lambda: leyline.leyline_pool_rollback(cache.pool, 0, s), lambda: lazy.materialize(0, s)]
+    with torch.cuda.graph(graph, stream=s):
+        for call in calls:
+            try:
+                call()
+                codes.append(0)
+            except leyline.LeylineError as e:
+                codes.append(e.code)
+    assert codes == [leyline.LEYLINE_ERR_INVALID_ARG] * len(calls)
+    assert cache.free_pages() == free and np.array_equal(cache.seq_lens_host, lens)
+    cache.splice(dirs)  # outside the capture the same call proceeds
+    torch.cuda.synchronize()
+    cache.check_status()
+    assert int(cache.seq_lens_host[0]) == 300 - 30 + 3
+    del keep
+    cache.close()
+    lazy.close()
