@@ -313,8 +313,8 @@ int leyline_splice(leyline_pool_t* pool, leyline_block_table_t* bt, const leylin
  * scratch is a static 4 MiB device array that every GPU which loads the library
  * holds until the process exits, and the plan is staged through a static host
  * array (the host-side planning itself uses ordinary C++ containers).  The
- * array's device address is looked up on the first call on each device; make
- * that first call before any stream capture.  All calls share the array:
+ * array's device address is looked up on the first call on each device.  All
+ * calls share the array:
  * calls that overlap on the GPU without ordering (different streams, different
  * pools) race on it.  Copying the plan from pageable memory may make the call
  * wait for earlier work on `stream`.  Same arguments, results and error codes

@@ -15,7 +15,7 @@
 // on which this library's device code is loaded, from then until the process
 // exits.  Its device address is looked up once per device with
 // cudaGetSymbolAddress on the first call made on that device (with the device
-// current); make that first call before any stream capture.  Every call shares
+// current).  Every call shares
 // the array: calls that overlap on the GPU (on different streams, or from
 // different pools, without ordering between them) race on it.  Calls on one pool
 // are ordered by the pool, as for leyline_splice.  Each call writes every byte
