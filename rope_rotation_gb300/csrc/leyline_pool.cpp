@@ -81,7 +81,13 @@ int refuse_capture(cudaStream_t stream, const char* what)
 {
     cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
     cudaError_t e = cudaStreamIsCapturing(stream, &st);
-    if (e != cudaSuccess) return cuda_error(e, "querying the stream's capture status");
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // not left for a later launch check to find
+        if (e == cudaErrorStreamCaptureImplicit)  // the legacy stream while another stream captures
+            return set_error(LEYLINE_ERR_INVALID_ARG, "the legacy default stream cannot be used while another "
+                                                      "stream is being captured");
+        return cuda_error(e, "querying the stream's capture status");
+    }
     if (st != cudaStreamCaptureStatusNone) {
         char msg[160];
         snprintf(msg, sizeof msg, "%s cannot be captured in a CUDA graph: it is planned on the host for the cache as "
