@@ -32,6 +32,10 @@
  *     kv[layer][page][slot][latent_dim + rope_heads * rope_dim]      (bf16, row-major)
  * and one block table, shared by all layers, maps block b of request r to a page:
  *     table[r * max_blocks + b] = page id, for b < ceil(seq_len[r] / block_size).
+ * A page belongs to one request: no two live table entries may name the same
+ * page (a splice returns a request's old pages to the free list, and a lazy read
+ * turns each listed row once).  The device checks that page ids are in range,
+ * not that they are distinct.
  *
  * How a splice is carried out.  Every block from floor(s_min / block_size) on
  * (s_min = the smallest s_start of the request's directives) is rewritten into
