@@ -99,6 +99,9 @@ struct SpliceArgs {
 // Launchers (leyline_move.cu, leyline_reindex.cu, leyline_read.cu).  Each returns the
 // cudaError_t of the launches as int.
 int launch_init_queue(int32_t* q, int64_t num_pages, void* stream);
+// Copy an uploaded plan (bytes a multiple of 16) from pinned host memory into device
+// memory by a dependent launch on `stream`.
+int launch_upload_plan(const void* host_src, void* dev_dst, size_t bytes, void* stream);
 // Enqueue a re-indexed call's kernels (prep, rows of R, fresh rows, rotation, commit):
 // leyline_reindex.cu.  launch_splice calls it for plans with reindex set.
 int launch_reindex_call(const SpliceArgs& a, const ParamPlan* pp, int grid, void* stream, cudaEvent_t t0,

@@ -209,11 +209,13 @@ int leyline_pool_create(const leyline_pool_desc_t* desc, void* kv_dev, leyline_p
     if (e == cudaSuccess) e = cudaMalloc(&p->d_queue, sizeof(int32_t) * (size_t)p->q_cap);
     if (e == cudaSuccess) e = cudaMalloc(&p->d_status, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(p->d_status, 0, sizeof(int32_t));
-    // the staging slots are allocated now: cudaHostAlloc during a call would wait for the GPU
+    // the plan slots are allocated now: cudaHostAlloc during a call would wait for the GPU
     for (int i = 0; i < leyline_pool::kPlanSlots && e == cudaSuccess; ++i) {
         e = cudaEventCreateWithFlags(&p->plan_uploaded[i], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaHostAlloc((void**)&p->h_plan[i], kPlanSlotBytes, cudaHostAllocDefault);
         if (e == cudaSuccess) p->h_plan_cap[i] = kPlanSlotBytes;
+        if (e == cudaSuccess) e = cudaMalloc(&p->d_plan[i], kPlanSlotBytes);
+        if (e == cudaSuccess) p->d_plan_cap[i] = kPlanSlotBytes;
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
     if (e == cudaSuccess && (g.flags & LEYLINE_POOL_LAZY)) {
@@ -292,9 +294,9 @@ int leyline_pool_destroy(leyline_pool_t* p)
     for (int i = 0; i < leyline_pool::kPlanSlots; ++i) {
         if (p->plan_uploaded[i]) cudaEventDestroy(p->plan_uploaded[i]);
         if (p->h_plan[i]) cudaFreeHost(p->h_plan[i]);
+        if (p->d_plan[i]) cudaFree(p->d_plan[i]);
     }
     if (p->done) cudaEventDestroy(p->done);
-    if (p->d_plan) cudaFree(p->d_plan);
     if (p->d_status) cudaFree(p->d_status);
     if (p->d_queue) cudaFree(p->d_queue);
     if (p->d_stage) cudaFree(p->d_stage);
@@ -480,18 +482,18 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         const size_t off_segs = align_up(sizeof(ReqPlan) * plan.reqs.size(), 16);
         const size_t off_trig = align_up(off_segs + sizeof(Seg) * plan.segs.size(), 16);
         const size_t total = align_up(off_trig + sizeof(float) * plan.trig.size(), 256);
-        if (total > p->d_plan_cap) {
+        const int slot = p->next_slot;
+        if (total > p->d_plan_cap[slot]) {  // a larger device buffer: no kernel may still read it
             rc = wait_pool(p);
             if (rc != LEYLINE_OK) return rc;
-            if (p->d_plan) cudaFree(p->d_plan);
-            p->d_plan = nullptr;
-            p->d_plan_cap = 0;
+            if (p->d_plan[slot]) cudaFree(p->d_plan[slot]);
+            p->d_plan[slot] = nullptr;
+            p->d_plan_cap[slot] = 0;
             const size_t cap = std::max<size_t>(total * 2, 1 << 16);
-            e = cudaMalloc(&p->d_plan, cap);
+            e = cudaMalloc(&p->d_plan[slot], cap);
             if (e != cudaSuccess) return cuda_error(e, "allocating the plan buffer");
-            p->d_plan_cap = cap;
+            p->d_plan_cap[slot] = cap;
         }
-        const int slot = p->next_slot;
         p->next_slot = (slot + 1) % leyline_pool::kPlanSlots;
         if (p->slot_used[slot]) {  // the slot's last upload may still be in flight
             e = cudaEventSynchronize(p->plan_uploaded[slot]);
@@ -510,15 +512,15 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         memcpy(h, plan.reqs.data(), sizeof(ReqPlan) * plan.reqs.size());
         memcpy(h + off_segs, plan.segs.data(), sizeof(Seg) * plan.segs.size());
         if (!plan.trig.empty()) memcpy(h + off_trig, plan.trig.data(), sizeof(float) * plan.trig.size());
-        // the device buffer is reused: this copy is stream-ordered after the previous call's kernels
-        e = cudaMemcpyAsync(p->d_plan, h, total, cudaMemcpyHostToDevice, stream);
+        // copied by a kernel in the chain of dependent launches (see launch_upload_plan)
+        e = (cudaError_t)launch_upload_plan(h, p->d_plan[slot], total, stream);
         if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
         e = cudaEventRecord(p->plan_uploaded[slot], stream);
         if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
         p->slot_used[slot] = true;
-        a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan);
-        a.segs = reinterpret_cast<const Seg*>(p->d_plan + off_segs);
-        a.trig = reinterpret_cast<const float*>(p->d_plan + off_trig);
+        a.reqs = reinterpret_cast<const ReqPlan*>(p->d_plan[slot]);
+        a.segs = reinterpret_cast<const Seg*>(p->d_plan[slot] + off_segs);
+        a.trig = reinterpret_cast<const float*>(p->d_plan[slot] + off_trig);
     }
 
     cudaEvent_t t0 = nullptr, t1 = nullptr;

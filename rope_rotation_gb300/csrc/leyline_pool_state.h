@@ -44,11 +44,13 @@ struct leyline_pool {
     int64_t q_head = 0;          // monotonic: next page to take is d_queue[q_head % q_cap]
     int64_t q_tail = 0;          // monotonic: next free slot is d_queue[q_tail % q_cap]
     int32_t* d_status = nullptr;
-    char* d_plan = nullptr;
-    size_t d_plan_cap = 0;
-    // pinned staging of uploaded plans: a ring of slots, so the host can plan several calls
-    // ahead of the GPU; a slot is reused once its upload event has completed
+    // uploaded plans: a ring of slots, each a pinned host staging buffer and a device
+    // buffer, so the host can plan several calls ahead of the GPU and a call's upload may
+    // run beside the previous call's last kernel; a slot is reused once its upload event
+    // has completed (its device buffer was then last read by a call that has ended)
     static constexpr int kPlanSlots = 8;
+    char* d_plan[kPlanSlots] = {};
+    size_t d_plan_cap[kPlanSlots] = {};
     char* h_plan[kPlanSlots] = {};
     size_t h_plan_cap[kPlanSlots] = {};
     cudaEvent_t plan_uploaded[kPlanSlots] = {};

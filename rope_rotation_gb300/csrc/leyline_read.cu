@@ -517,6 +517,31 @@ __global__ void clear_pending_kernel(int32_t* pending, const int32_t* page_ids, 
 
 }  // namespace
 
+// A plan too large for a kernel parameter, copied from its pinned host staging slot into
+// the slot's device buffer by a kernel that reads host memory directly.  As a dependent
+// launch it keeps the call in the chain of dependent launches, where a copy-engine
+// transfer would break it: the copy would start only once the kernel before it had ended,
+// and the next kernel could launch only once the copy had.  The copy may run beside the
+// previous call's last kernel, since the slot's buffer was last read by a call that has
+// ended (slots are used in turn).  It then waits for that kernel before the next kernel
+// may launch, so every kernel after it starts after all earlier calls have ended, as
+// after a stream-ordered copy; the next kernel reads the plan only after its own wait.
+__global__ void upload_plan_kernel(const uint4* src, uint4* dst, long long n)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+    wait_for_previous_grid();
+    allow_next_grid();
+}
+
+int launch_upload_plan(const void* host_src, void* dev_dst, size_t bytes, void* stream)
+{
+    if (bytes == 0 || bytes % 16 != 0) return (int)cudaErrorInvalidValue;
+    const long long n = (long long)(bytes / 16);
+    return (int)launch_dependent(upload_plan_kernel, grid_for(n, 256, 64), 256, (cudaStream_t)stream,
+                                 static_cast<const uint4*>(host_src), static_cast<uint4*>(dev_dst), n);
+}
+
 int launch_init_queue(int32_t* q, int64_t num_pages, void* stream)
 {
     init_queue_kernel<<<grid_for(2 * num_pages, 256, 4096), 256, 0, (cudaStream_t)stream>>>(q, num_pages);
