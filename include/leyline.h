@@ -198,7 +198,8 @@ typedef struct {
     int64_t pages_popped;      /* fresh pages taken for the rewritten blocks */
     int64_t pages_pushed;      /* old pages returned to the free-page list */
     int32_t requests_touched;
-    int32_t kernels_launched;  /* kernels this call enqueued */
+    int32_t kernels_launched;  /* kernels this call enqueued (leyline_splice_plan: without the copy
+                                  kernel that leyline_splice adds for a plan it uploads) */
     int32_t reindexed;         /* 1: the call kept survivors in their pages (LEYLINE_POOL_REINDEX) */
     int32_t overlapped;        /* 1: the call's move kernel may start before the previous call's work
                                   on the stream ends (see leyline_splice) */

@@ -463,12 +463,13 @@ int build_plan(const Geometry& g, const int64_t* seq_lens_host, int32_t num_reqs
     st.pages_popped = plan->total_pop;
     st.pages_pushed = plan->total_push;
     st.requests_touched = (int32_t)plan->reqs.size();
-    // re-index: prep with the rows of R (one launch), other fresh rows, the in-place rotation,
-    // commit (each if any)
+    // rewrite: move+rotate and commit; re-index: prep with the rows of R (one launch), other
+    // fresh rows, the in-place rotation, commit (each if any).  A plan that leyline_splice
+    // uploads adds its copy kernel (counted there).
     st.kernels_launched = plan->reqs.empty() ? 0
                           : reindex ? (plan->total_prep + plan->total_repl > 0) + (plan->total_fresh > 0) +
                                           (plan->total_tiles > 0) + (plan->total_commit > 0)
-                                    : 2;
+                                    : (plan->total_tiles > 0) + (plan->total_commit > 0);
     st.reindexed = (!plan->reqs.empty() && reindex) ? 1 : 0;
     return LEYLINE_OK;
 }

@@ -515,6 +515,7 @@ int leyline_splice(leyline_pool_t* p, leyline_block_table_t* bt, const leyline_d
         // copied by a kernel in the chain of dependent launches (see launch_upload_plan)
         e = (cudaError_t)launch_upload_plan(h, p->d_plan[slot], total, stream);
         if (e != cudaSuccess) return cuda_error(e, "uploading the plan");
+        ++plan.stats.kernels_launched;
         e = cudaEventRecord(p->plan_uploaded[slot], stream);
         if (e != cudaSuccess) return cuda_error(e, "recording the plan upload");
         p->slot_used[slot] = true;
