@@ -261,7 +261,9 @@ int64_t leyline_free_page_count(const leyline_pool_t* pool);
  *
  * leyline_pool_rollback puts the saved accounting back (enqueued on `stream`):
  * pages taken since the checkpoint are free again and pages returned since are
- * owned again.  The block table and the lengths are the caller's: the caller
+ * owned again.  It copies back only the free-list entries written since the
+ * checkpoint (4 bytes per page returned since) and, in lazy pools, all pending
+ * counts.  The block table and the lengths are the caller's: the caller
  * restores them too (table, seq_lens_dev and seq_lens_host as they were at the
  * checkpoint), after the pool's work on the stream.  Refused, with nothing
  * changed (INVALID_ARG), when

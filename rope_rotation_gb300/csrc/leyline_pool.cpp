@@ -772,8 +772,22 @@ int leyline_pool_rollback(leyline_pool_t* p, int32_t flags, void* stream_v)
     rc = order_after_previous(p, stream);
     if (rc != LEYLINE_OK) return rc;
     const size_t slots = (size_t)p->g.num_pages * (size_t)p->g.block_size;
-    cudaError_t e = cudaMemcpyAsync(p->d_queue, p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap,
-                                    cudaMemcpyDeviceToDevice, stream);
+    // Only the ring entries written since the checkpoint differ from its copy: returned pages
+    // are written at positions [ckpt_tail, q_tail), while taking pages only moves the head.
+    const int64_t pushed = p->q_tail - p->ckpt_tail;
+    cudaError_t e = cudaSuccess;
+    if (pushed >= p->q_cap) {
+        e = cudaMemcpyAsync(p->d_queue, p->d_ckpt_queue, sizeof(int32_t) * (size_t)p->q_cap, cudaMemcpyDeviceToDevice,
+                            stream);
+    } else if (pushed > 0) {
+        const int64_t at = p->ckpt_tail % p->q_cap;
+        const int64_t first = std::min(pushed, p->q_cap - at);  // up to the ring's end, then from its start
+        e = cudaMemcpyAsync(p->d_queue + at, p->d_ckpt_queue + at, sizeof(int32_t) * (size_t)first,
+                            cudaMemcpyDeviceToDevice, stream);
+        if (e == cudaSuccess && pushed > first)
+            e = cudaMemcpyAsync(p->d_queue, p->d_ckpt_queue, sizeof(int32_t) * (size_t)(pushed - first),
+                                cudaMemcpyDeviceToDevice, stream);
+    }
     if (e == cudaSuccess && p->d_pending)
         e = cudaMemcpyAsync(p->d_pending, p->d_ckpt_pending, sizeof(int32_t) * slots, cudaMemcpyDeviceToDevice,
                             stream);

@@ -192,3 +192,46 @@ def test_rollback_after_noalloc_splices():
         assert np.array_equal(again[r], first[r]), f"request {r}: the repeat differs"
     del keep
     cache.close()
+
+
+def test_rollback_restores_the_free_list_across_the_ring_end():
+    """A rollback copies back only the free-list entries written since the checkpoint.  The
+    free list is a ring of 2 * num_pages entries whose positions only grow, so the returned
+    pages' region wraps past the ring's end once its positions do.  Against a twin pool that
+    skips the splice and its rollback, the free list must come out identical, page for page
+    in the order the pool hands pages out, at every checkpoint position tried."""
+    from rope_rotation_gb300 import leyline
+    step = [Dir(0, 100, 116, 16, 0)]  # rewrites blocks 6..9: takes 4 pages and returns 4
+    w = Workload("rollback-ring", 2, 16, [160], [step], seed=10)
+    cache = H.make_cache(w)
+    twin = H.make_cache(w)
+    num_pages = cache.num_pages
+    free = cache.free_pages()
+    assert free == twin.free_pages() and free > 4
+    q_cap, tail = 2 * num_pages, num_pages  # every page was returned once at creation
+    wrapped = False
+    for k, advance in enumerate([free, 7, free, 3, free, 9, free, 1, free, free - 2, free, 5]):
+        wrapped |= tail % q_cap + 4 > q_cap
+        saved = _saved(cache)
+        leyline.leyline_pool_checkpoint(cache.pool)
+        _splice(cache, w, step)
+        assert cache.last_stats()["pages_pushed"] == 4
+        leyline.leyline_pool_rollback(cache.pool)
+        _restore(cache, saved)
+        torch.cuda.synchronize()
+        assert cache.free_pages() == twin.free_pages() == free
+        assert np.array_equal(cache.table.cpu().numpy(), twin.table.cpu().numpy())
+        assert np.array_equal(H.logical_rows(cache, 0, 160), H.logical_rows(twin, 0, 160)), f"step {k}"
+        # take `advance` pages from both and give them back in another order: the positions move on
+        a = leyline.leyline_alloc_pages(cache.pool, advance)
+        b = leyline.leyline_alloc_pages(twin.pool, advance)
+        assert list(a) == list(b), f"step {k}: the free lists differ after the rollback"
+        leyline.leyline_free_pages(cache.pool, a[::-1])
+        leyline.leyline_free_pages(twin.pool, b[::-1])
+        tail += advance
+    assert wrapped, "no checkpoint put the returned pages' region across the ring's end"
+    rest_a = leyline.leyline_alloc_pages(cache.pool, free)
+    rest_b = leyline.leyline_alloc_pages(twin.pool, free)
+    assert list(rest_a) == list(rest_b)
+    cache.close()
+    twin.close()
