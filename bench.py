@@ -51,18 +51,18 @@ DEFAULT_MEM_GB = 96.0
 # multiplied by the ratio of the units (tile x layer) the full launch processes.
 NCU_TRAFFIC = {
     # the move kernel on the largest workload, captured on 4 of its 61 layers (DRAM read
-    # 704.28 MB = the algorithmic read; write 654.66 MB, the rest still in L2 at kernel end)
+    # 704.28 MB = the algorithmic read; write 654.73 MB, the rest still in L2 at kernel end)
     ("sweep-C16-61L-B16", "move_rotate_vector"): {
-        "kernel_sha256": "967501961471016e1b33072f77b0d17734d1b9327554969529aa8e61f2ad88c5",
-        "bytes": 704279552 + 654659840, "captured_layers": 4, "scale": 61 / 4},
+        "kernel_sha256": "2ef00ccd9feaf4b162dd17472d88bf800b50479db73ede0fe9b44c6d14c453a3",
+        "bytes": 704278016 + 654730752, "captured_layers": 4, "scale": 61 / 4},
     # the move kernel on the DeepSeek-V2-Lite shape (one call, 27 layers)
     ("dsv2lite-27L-32k-B16", "move_rotate_vector"): {
-        "kernel_sha256": "967501961471016e1b33072f77b0d17734d1b9327554969529aa8e61f2ad88c5",
-        "bytes": 210924288 + 161260288},
+        "kernel_sha256": "2ef00ccd9feaf4b162dd17472d88bf800b50479db73ede0fe9b44c6d14c453a3",
+        "bytes": 210919424 + 161249024},
     # the whole-line rotate kernel of a re-index call, block-1 sweep of 4 requests on 16 layers
     ("sweep-C4-61L-B1-as-16L", "rotate_in_place"): {
-        "kernel_sha256": "e891b396426e082616a96fd1efcf231d9f41109133cdec2511c21a8370e11773",
-        "bytes": 130883584 + 72365568},
+        "kernel_sha256": "e18d01e54a2418d387cdd03ae681b8d1df59b8c6e2830fe101411272b97dfcbb",
+        "bytes": 130887680 + 71868672},
 }
 
 
