@@ -335,13 +335,16 @@ def test_gqa_rows(layout, B, flags):
 
 
 # ------------------------------------------------------------------------------
-# Many calls in flight: plans too large for a kernel parameter are staged through a
-# ring of pinned slots, so the host enqueues call after call without waiting; the
-# final caches must equal, bit for bit, those of the same calls made one at a time,
-# each of which is checked against the oracle at the per-splice tolerance.
-@pytest.mark.parametrize("flags,batch", [(0, False), (REINDEX, False), (0, True), (REINDEX, True)])
-def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
-    """batch: the directives go in as one directive_batch() record array per call."""
+# Many calls in flight: plans too large for a kernel parameter go through a ring of plan
+# slots (a pinned staging buffer and a device buffer each; a kernel copies one to the
+# other), so the host enqueues call after call without waiting; the final caches must
+# equal, bit for bit, those of the same calls made one at a time, each of which is checked
+# against the oracle at the per-splice tolerance.
+@pytest.mark.parametrize("flags,batch,streams", [(0, False, 1), (REINDEX, False, 1), (0, True, 1), (REINDEX, True, 1),
+                                                 (0, False, 2), (REINDEX, True, 2)])
+def test_many_calls_in_flight_with_uploaded_plans(flags, batch, streams):
+    """batch: the directives go in as one directive_batch() record array per call.  streams=2:
+    the calls alternate between two streams (the pool orders each after the one before)."""
     import torch
     from rope_rotation_gb300 import leyline
     rng = np.random.default_rng(77)
@@ -364,17 +367,22 @@ def test_many_calls_in_flight_with_uploaded_plans(flags, batch):
         steps.append(step)
     w = Workload(f"in-flight-f{flags}", 2, B, lengths, steps, seed=78)
     cache = H.make_cache(w, slack_pages=64, flags=flags)
-    keep = []
-    for step in steps:  # no synchronisation between calls
+    keep, calls = [], []
+    for step in steps:
         dirs, k = H.gpu_directives(w, step)
         keep.append(k)
         if batch:
             dirs = leyline.directive_batch([d.req for d in step], [d.s_start for d in step],
                                            [d.s_end for d in step], k, n_repl=[d.n_repl for d in step],
                                            mode=[d.mode for d in step])
-        cache.splice(dirs)
+        calls.append(dirs)
+    torch.cuda.synchronize()  # the rows of R and the cache are written on the default stream
+    pick = [torch.cuda.current_stream()] if streams == 1 else [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i, dirs in enumerate(calls):  # no synchronisation between calls
+        cache.splice(dirs, pick[i % len(pick)])
         st = cache.last_stats()  # the library's account of its host time for this call
         assert st["host_ns"] >= st["resolve_ns"] + st["plan_ns"] and st["plan_ns"] > 0
+        assert st["kernels_launched"] >= 3  # the plan copy, then the splice's own kernels
     torch.cuda.synchronize()
     cache.check_status()
     # the same calls one at a time, each checked against the oracle on its own input
