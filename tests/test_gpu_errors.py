@@ -146,6 +146,7 @@ def test_splices_on_two_streams_are_ordered():
     cache.close()
 
 
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # every call was refused: nothing captured
 def test_host_planned_calls_refuse_graph_capture():
     """A splice, a materialize and a checkpoint or rollback are planned on the host for the
     cache as it stands, so a CUDA graph that replayed them would apply stale plans: each
@@ -180,3 +181,27 @@ def test_host_planned_calls_refuse_graph_capture():
     del keep
     cache.close()
     lazy.close()
+
+
+def test_plans_larger_than_a_plan_slot():
+    """300 one-token deletions in one call: 300 rotated segments, each with its own cos / sin,
+    make a plan of about 100 KB, more than the 64 KB a plan slot starts with.  The slot's
+    pinned and device buffers grow (after the pool's earlier work has ended), and the call is
+    checked against the oracle like any other; later calls take the slots in turn, one of
+    them the grown slot again."""
+    from rope_rotation_gb300 import leyline
+    L = 2000
+    big = [Dir(0, 5 * k + 2, 5 * k + 3, 0, k) for k in range(300)]
+    big2 = [Dir(0, 4 * k + 1, 4 * k + 2, 1 if k % 3 == 0 else 0, 300 + k) for k in range(300)]
+    # 30 one-token replacements: 60 segments, more than a kernel parameter holds, so these
+    # plans are uploaded too and the calls walk through all 8 slots, reusing the grown one
+    mid = [Dir(0, 3 * k + 1, 3 * k + 2, 1, 700 + k) for k in range(30)]
+    last = [Dir(0, 5 * k + 2, 5 * k + 3, 0, 1000 + k) for k in range(280)]  # within the shorter length
+    steps = [big] + [mid] * 7 + [big2, mid, last]
+    w = Workload("big-plan", 2, 16, [L], steps, seed=12)
+    cache = H.make_cache(w, slack_pages=8)
+    state = H.oracle_state(w)
+    for step in w.steps:
+        H.splice_step_and_check(w, cache, state, step)
+        assert cache.last_stats()["kernels_launched"] == 3  # the plan copy, move and commit
+    cache.close()
