@@ -293,9 +293,11 @@ int leyline_pool_rollback(leyline_pool_t* pool, int32_t flags, void* stream);
  * n_repl == 0 are no-ops.  On return the work is enqueued on `stream`, the
  * seq_lens_host entries hold the new lengths and the pages are accounted; the
  * table and seq_lens_dev change when the enqueued work runs.  Enqueues two
- * kernels (move+rotate, then commit).  The plan travels as a kernel parameter
- * when it has at most 8 requests, 24 segments and 10 rotated segments;
- * otherwise it is uploaded first with one host-to-device copy.
+ * kernels (move+rotate, then commit; a re-index call up to four).  The plan
+ * travels as a kernel parameter when it has at most 8 requests, 24 segments and
+ * 10 rotated segments; otherwise it is staged in one of 8 pinned host slots and
+ * a first kernel copies it to the device (the call then waits on the host only
+ * when all 8 slots are still in flight).
  * Calls enqueued back to back on one stream keep stream order for everything
  * the caller can observe, but the library may let a call's kernels start
  * before the previous calls' kernels end: only for a rewrite whose plan is a
