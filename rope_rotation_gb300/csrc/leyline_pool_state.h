@@ -46,8 +46,12 @@ struct leyline_pool {
     int32_t* d_status = nullptr;
     // uploaded plans: a ring of slots, each a pinned host staging buffer and a device
     // buffer, so the host can plan several calls ahead of the GPU and a call's upload may
-    // run beside the previous call's last kernel; a slot is reused once its upload event
-    // has completed (its device buffer was then last read by a call that has ended)
+    // run beside the previous call's last kernel.  The host rewrites a slot's staging
+    // buffer once the slot's last upload event has completed.  The device buffer is
+    // rewritten by the slot's next copy kernel, which may start before the previous call
+    // has ended, but not before the call that last read the buffer has: that call is 8
+    // uploaded calls back, and the copy kernel of the uploaded call after it waited for
+    // every earlier kernel before any later kernel could launch.
     static constexpr int kPlanSlots = 8;
     char* d_plan[kPlanSlots] = {};
     size_t d_plan_cap[kPlanSlots] = {};

@@ -522,10 +522,12 @@ __global__ void clear_pending_kernel(int32_t* pending, const int32_t* page_ids, 
 // launch it keeps the call in the chain of dependent launches, where a copy-engine
 // transfer would break it: the copy would start only once the kernel before it had ended,
 // and the next kernel could launch only once the copy had.  The copy may run beside the
-// previous call's last kernel, since the slot's buffer was last read by a call that has
-// ended (slots are used in turn).  It then waits for that kernel before the next kernel
-// may launch, so every kernel after it starts after all earlier calls have ended, as
-// after a stream-ordered copy; the next kernel reads the plan only after its own wait.
+// previous call's last kernel: the slot's buffer was last read by the call that used the
+// slot 8 uploaded calls back, and that call has ended, since the copy kernel of the
+// uploaded call after it waited for every earlier kernel before any later one launched.
+// It then waits for the previous kernel before the next kernel may launch, so every
+// kernel after it starts after all earlier calls have ended, as after a stream-ordered
+// copy; the next kernel reads the plan only after its own wait.
 __global__ void upload_plan_kernel(const uint4* src, uint4* dst, long long n)
 {
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
